@@ -1,0 +1,195 @@
+"""fp64 CPU oracle for the LTX-2.5 attention hot path -- TEST INFRASTRUCTURE ONLY.
+
+Only the test suite, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  The GPU library never calls it and the
+two share no code.  The arithmetic lives in ``oracle.c`` (plain C, double
+precision); this module compiles it with gcc, loads it with ctypes and
+marshals numpy arrays.  See the header of ``oracle.c`` for the definitions
+and the sources they follow.
+
+Parity status: dense attention, split-KV partials, the LSE merge, pooling,
+proxy scores, mu/sigma/tau and the selection are pinned by closed forms,
+library routines and invariants in ``tests/test_oracle_pins.py``.  The Taylor
+aggregates (W, T) and the Taylor-corrected sparse output follow this build's
+reading of the Sol-Attn page (first order about the row-mean proxy score,
+applied per block with pooled V); they are pinned only against a
+hand-derived closed form of that reading: parity unpinned with respect to the
+pages.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_LIB_PATH = os.path.join(_HERE, "_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+_D = ctypes.POINTER(ctypes.c_double)
+_I64 = ctypes.POINTER(ctypes.c_int64)
+_U8 = ctypes.POINTER(ctypes.c_uint8)
+_i64 = ctypes.c_int64
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.c into _oracle.so next to it (gcc, OpenMP)."""
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp", "-fno-fast-math",
+           "-ffp-contract=off", _SRC, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        lib = ctypes.CDLL(build())
+        lib.oracle_attend_rows.argtypes = [_D, _D, _D, _i64, _i64, _i64, _i64, ctypes.c_double, _I64, _i64, _D, _D]
+        lib.oracle_split_partials.argtypes = [_D, _D, _D, _i64, _i64, _i64, _i64, ctypes.c_double, _i64, _D, _D]
+        lib.oracle_lse_merge.argtypes = [_D, _D, _i64, _i64, _i64, _D, _D]
+        lib.oracle_block_pool.argtypes = [_D, _i64, _i64, _i64, _i64, _D]
+        lib.oracle_route.argtypes = [_D, _D, _D, _i64, _i64, _i64, _i64, _I64, ctypes.c_double, ctypes.c_double,
+                                     ctypes.c_int, _D, _U8, _I64, _D, _D, _D, _D, _D, _I64]
+        lib.oracle_sparse_rows.argtypes = [_D, _D, _D, _i64, _i64, _i64, _i64, _i64, _U8, _D, _D, _D,
+                                           ctypes.c_double, _I64, _i64, _D, _D]
+        for f in (lib.oracle_attend_rows, lib.oracle_split_partials, lib.oracle_lse_merge, lib.oracle_block_pool,
+                  lib.oracle_route, lib.oracle_sparse_rows):
+            f.restype = None
+        _lib = lib
+        return lib
+
+
+def _f64(a) -> np.ndarray:
+    return np.ascontiguousarray(np.asarray(a, dtype=np.float64))
+
+
+def _p(a: np.ndarray, t):
+    return a.ctypes.data_as(t)
+
+
+def _bhsd(x):
+    x = _f64(x)
+    if x.ndim != 4:
+        raise ValueError("expected a [B, H, S, d] array")
+    return x
+
+
+def attention(q, k, v, scale: float, rows=None):
+    """Dense softmax attention.  q: [B,H,Sq,d], k/v: [B,H,Skv,d].
+
+    rows=None evaluates every row and returns (out [B,H,Sq,d], lse [B,H,Sq]);
+    otherwise ``rows`` holds flat row indices (b*H + h)*Sq + i and the result
+    is (out [n, d], lse [n])."""
+    q, k, v = _bhsd(q), _bhsd(k), _bhsd(v)
+    B, H, Sq, d = q.shape
+    Skv = k.shape[2]
+    full = rows is None
+    r = np.arange(B * H * Sq, dtype=np.int64) if full else np.ascontiguousarray(rows, dtype=np.int64)
+    out = np.empty((r.size, d))
+    lse = np.empty(r.size)
+    _load().oracle_attend_rows(_p(q, _D), _p(k, _D), _p(v, _D), B * H, Sq, Skv, d, float(scale), _p(r, _I64),
+                               r.size, _p(out, _D), _p(lse, _D))
+    if full:
+        return out.reshape(B, H, Sq, d), lse.reshape(B, H, Sq)
+    return out, lse
+
+
+def split_partials(q, k, v, scale: float, n_split: int):
+    """Per-chunk partial answers: (o_part [n,B,H,Sq,d], lse_part [n,B,H,Sq])."""
+    q, k, v = _bhsd(q), _bhsd(k), _bhsd(v)
+    B, H, Sq, d = q.shape
+    Skv = k.shape[2]
+    o = np.empty((n_split, B, H, Sq, d))
+    lse = np.empty((n_split, B, H, Sq))
+    _load().oracle_split_partials(_p(q, _D), _p(k, _D), _p(v, _D), B * H, Sq, Skv, d, float(scale), n_split,
+                                  _p(o, _D), _p(lse, _D))
+    return o, lse
+
+
+def lse_merge(o_part, lse_part):
+    """Exact merge of partials: o_part [n,...,d], lse_part [n,...] -> (out, lse)."""
+    o_part, lse_part = _f64(o_part), _f64(lse_part)
+    n = o_part.shape[0]
+    d = o_part.shape[-1]
+    rows = int(np.prod(lse_part.shape[1:]))
+    out = np.empty(lse_part.shape[1:] + (d,))
+    lse = np.empty(lse_part.shape[1:])
+    _load().oracle_lse_merge(_p(o_part, _D), _p(lse_part, _D), n, rows, d, _p(out, _D), _p(lse, _D))
+    return out, lse
+
+
+def block_pool(x, block: int):
+    """Block mean-pool along S: [B,H,S,d] -> [B,H,ceil(S/block),d]."""
+    x = _bhsd(x)
+    B, H, S, d = x.shape
+    nb = (S + block - 1) // block
+    xp = np.empty((B, H, nb, d))
+    _load().oracle_block_pool(_p(x, _D), B * H, S, d, block, _p(xp, _D))
+    return xp
+
+
+def route(qp, kp, vp, S: int, block_k: int, scale: float, beta: float, clamp: bool = True):
+    """Sol-Attn routing from pooled tensors qp [B,H,NQB,d], kp/vp [B,H,NKB,d].
+
+    Returns a dict with proxy, sel (bool), sel_cnt, mu, sigma, tau, W, T and
+    n_clamped."""
+    qp, kp, vp = _bhsd(qp), _bhsd(kp), _bhsd(vp)
+    B, H, NQB, d = qp.shape
+    NKB = kp.shape[2]
+    nk = np.array([min(block_k, S - j * block_k) for j in range(NKB)], dtype=np.int64)
+    proxy = np.empty((B, H, NQB, NKB))
+    sel = np.empty((B, H, NQB, NKB), dtype=np.uint8)
+    cnt = np.empty((B, H, NQB), dtype=np.int64)
+    mu, sigma, tau, W = (np.empty((B, H, NQB)) for _ in range(4))
+    T = np.empty((B, H, NQB, d))
+    ncl = np.zeros(1, dtype=np.int64)
+    _load().oracle_route(_p(qp, _D), _p(kp, _D), _p(vp, _D), B * H, NQB, NKB, d, _p(nk, _I64), float(scale),
+                         float(beta), 1 if clamp else 0, _p(proxy, _D), _p(sel, _U8), _p(cnt, _I64), _p(mu, _D),
+                         _p(sigma, _D), _p(tau, _D), _p(W, _D), _p(T, _D), _p(ncl, _I64))
+    return dict(proxy=proxy, sel=sel.astype(bool), sel_cnt=cnt, mu=mu, sigma=sigma, tau=tau, W=W, T=T,
+                n_clamped=int(ncl[0]))
+
+
+def sparse_attention(q, k, v, block_q: int, block_k: int, sel, mu, W, T, scale: float, rows=None):
+    """Block-sparse attention with the Taylor term (self-attention, Sq = Skv = S).
+
+    sel [B,H,NQB,NKB] bool, mu/W [B,H,NQB], T [B,H,NQB,d].  ``rows`` as in
+    :func:`attention`."""
+    q, k, v = _bhsd(q), _bhsd(k), _bhsd(v)
+    B, H, S, d = q.shape
+    sel8 = np.ascontiguousarray(sel, dtype=np.uint8)
+    mu, W, T = _f64(mu), _f64(W), _f64(T)
+    full = rows is None
+    r = np.arange(B * H * S, dtype=np.int64) if full else np.ascontiguousarray(rows, dtype=np.int64)
+    out = np.empty((r.size, d))
+    lse = np.empty(r.size)
+    _load().oracle_sparse_rows(_p(q, _D), _p(k, _D), _p(v, _D), B * H, S, d, block_q, block_k, _p(sel8, _U8),
+                               _p(mu, _D), _p(W, _D), _p(T, _D), float(scale), _p(r, _I64), r.size, _p(out, _D),
+                               _p(lse, _D))
+    if full:
+        return out.reshape(B, H, S, d), lse.reshape(B, H, S)
+    return out, lse
+
+
+def sparse_route_attention(q, k, v, block_q: int, block_k: int, scale: float, beta: float, rows=None):
+    """The whole Sol-Attn path in the oracle: pool, route, sparse attention.
+
+    Returns (out, lse, route_dict, pooled (qp, kp, vp))."""
+    q, k, v = _bhsd(q), _bhsd(k), _bhsd(v)
+    S = q.shape[2]
+    qp, kp, vp = block_pool(q, block_q), block_pool(k, block_k), block_pool(v, block_k)
+    rt = route(qp, kp, vp, S, block_k, scale, beta)
+    out, lse = sparse_attention(q, k, v, block_q, block_k, rt["sel"], rt["mu"], rt["W"], rt["T"], scale, rows)
+    return out, lse, rt, (qp, kp, vp)

@@ -1,0 +1,362 @@
+"""Pins for the fp64 oracle: closed forms, library routines and invariants.
+
+Each test checks the oracle against something other than itself, chosen so
+that a plausible slip (a dropped term, a wrong sign or index, a transposed
+operand, an off-by-one chunk bound) fails at least one of them.  CPU only.
+"""
+import math
+import os
+
+import numpy as np
+import pytest
+import scipy.special
+import torch
+
+import oracle
+
+RNG = np.random.default_rng(1234)
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def rand(*shape, scale=1.0):
+    return RNG.standard_normal(shape) * scale
+
+
+def sdpa64(q, k, v, scale, mask=None):
+    """torch's own attention routine in float64 on the CPU (a library routine the oracle does not use)."""
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a))
+    out = torch.nn.functional.scaled_dot_product_attention(t(q), t(k), t(v), attn_mask=None if mask is None else t(mask),
+                                                           scale=scale)
+    return out.numpy()
+
+
+# ---------------------------------------------------------------- dense attention
+
+@pytest.mark.parametrize("B,H,Sq,Skv,d", [(1, 2, 33, 57, 64), (2, 1, 128, 256, 128), (1, 1, 1, 1, 64), (1, 3, 200, 7, 16)])
+def test_dense_matches_library_sdpa(B, H, Sq, Skv, d):
+    q, k, v = rand(B, H, Sq, d), rand(B, H, Skv, d), rand(B, H, Skv, d)
+    scale = 1 / math.sqrt(d)
+    out, lse = oracle.attention(q, k, v, scale)
+    ref = sdpa64(q, k, v, scale)
+    np.testing.assert_allclose(out, ref, rtol=0, atol=1e-12)
+    # lse against scipy's logsumexp of the explicit score matrix
+    scores = scale * np.einsum("bhqd,bhkd->bhqk", q, k)
+    np.testing.assert_allclose(lse, scipy.special.logsumexp(scores, axis=-1), rtol=0, atol=1e-12)
+
+
+def test_dense_two_keys_closed_form():
+    # with two keys the softmax is a logistic function of the score difference
+    d = 4
+    q = rand(1, 1, 5, d)
+    k = rand(1, 1, 2, d)
+    v = rand(1, 1, 2, d)
+    scale = 0.7
+    out, lse = oracle.attention(q, k, v, scale)
+    x = scale * q[0, 0] @ k[0, 0].T                      # [5, 2]
+    s1 = 1.0 / (1.0 + np.exp(-(x[:, 0] - x[:, 1])))
+    expect = s1[:, None] * v[0, 0, 0] + (1 - s1)[:, None] * v[0, 0, 1]
+    np.testing.assert_allclose(out[0, 0], expect, atol=1e-13)
+    np.testing.assert_allclose(lse[0, 0], np.logaddexp(x[:, 0], x[:, 1]), atol=1e-13)
+
+
+def test_dense_identical_keys_give_mean_value():
+    d, Skv = 8, 37
+    q = rand(1, 1, 3, d)
+    k = np.repeat(rand(1, 1, 1, d), Skv, axis=2)
+    v = rand(1, 1, Skv, d)
+    out, lse = oracle.attention(q, k, v, 0.5)
+    np.testing.assert_allclose(out[0, 0], np.broadcast_to(v[0, 0].mean(0), (3, d)), atol=1e-13)
+    x = 0.5 * q[0, 0] @ k[0, 0, 0]
+    np.testing.assert_allclose(lse[0, 0], x + math.log(Skv), atol=1e-12)
+
+
+def test_dense_large_scores_are_stable_and_one_hot():
+    d = 4
+    k = np.zeros((1, 1, 5, d))
+    k[0, 0, :, 0] = [-3, 1, 7, 2, 0]
+    q = np.zeros((1, 1, 1, d))
+    q[0, 0, 0, 0] = 400.0                               # scores up to 2800: exp overflows without the max shift
+    v = rand(1, 1, 5, d)
+    out, lse = oracle.attention(q, k, v, 1.0)
+    assert np.all(np.isfinite(out)) and np.isfinite(lse).all()
+    np.testing.assert_allclose(out[0, 0, 0], v[0, 0, 2], atol=1e-12)
+    np.testing.assert_allclose(lse[0, 0, 0], 2800.0, atol=1e-9)
+
+
+def test_dense_rows_sum_to_one_before_v():
+    q, k = rand(1, 2, 40, 16), rand(1, 2, 90, 16)
+    out, _ = oracle.attention(q, k, np.ones((1, 2, 90, 16)), 0.25)
+    np.testing.assert_allclose(out, 1.0, atol=1e-14)
+    # one-hot value columns expose the weights themselves: each row of weights sums to 1
+    v = np.zeros((1, 2, 90, 90))
+    v[0, :, np.arange(90), np.arange(90)] = 1.0
+    w, _ = oracle.attention(np.pad(q, ((0, 0), (0, 0), (0, 0), (0, 74))), np.pad(k, ((0, 0), (0, 0), (0, 0), (0, 74))),
+                            v, 0.25)
+    np.testing.assert_allclose(w.sum(-1), 1.0, atol=1e-13)
+    assert (w >= 0).all()
+
+
+def test_dense_key_permutation_invariance_and_row_subset():
+    q, k, v = rand(1, 1, 20, 8), rand(1, 1, 50, 8), rand(1, 1, 50, 8)
+    perm = RNG.permutation(50)
+    a, la = oracle.attention(q, k, v, 0.3)
+    b, lb = oracle.attention(q, k[:, :, perm], v[:, :, perm], 0.3)
+    np.testing.assert_allclose(a, b, atol=1e-13)
+    np.testing.assert_allclose(la, lb, atol=1e-13)
+    rows = np.array([19, 0, 7])
+    c, lc = oracle.attention(q, k, v, 0.3, rows=rows)
+    np.testing.assert_array_equal(c, a[0, 0, rows])
+    np.testing.assert_array_equal(lc, la[0, 0, rows])
+
+
+# ---------------------------------------------------------------- split-KV + merge
+
+@pytest.mark.parametrize("Skv,n", [(257, 1), (257, 2), (257, 3), (257, 8), (32769 // 64, 8), (5, 5), (3, 7)])
+def test_split_merge_equals_unsplit(Skv, n):
+    q, k, v = rand(1, 2, 9, 16), rand(1, 2, Skv, 16), rand(1, 2, Skv, 16)
+    full, lfull = oracle.attention(q, k, v, 0.25)
+    op, lp = oracle.split_partials(q, k, v, 0.25, n)
+    out, lse = oracle.lse_merge(op, lp)
+    np.testing.assert_allclose(out, full, atol=1e-12)
+    np.testing.assert_allclose(lse, lfull, atol=1e-12)
+    # every chunk is plain attention over its balanced, unpadded key range
+    for c in range(n):
+        lo, hi = (c * Skv) // n, ((c + 1) * Skv) // n
+        if hi == lo:
+            assert np.all(lp[c] == -np.inf) and np.all(op[c] == 0)
+            continue
+        np.testing.assert_allclose(op[c], sdpa64(q, k[:, :, lo:hi], v[:, :, lo:hi], 0.25), atol=1e-12)
+
+
+def test_split_single_chunk_is_identity():
+    q, k, v = rand(1, 1, 4, 8), rand(1, 1, 31, 8), rand(1, 1, 31, 8)
+    op, lp = oracle.split_partials(q, k, v, 0.5, 1)
+    full, lfull = oracle.attention(q, k, v, 0.5)
+    np.testing.assert_array_equal(op[0], full)
+    np.testing.assert_array_equal(lp[0], lfull)
+
+
+def test_unpadded_odd_length_equals_padded_and_masked():
+    # the padded key, masked out, changes nothing: attention over the odd-length sequence is the same
+    Skv = 65
+    q, k, v = rand(1, 2, 6, 8), rand(1, 2, Skv, 8), rand(1, 2, Skv, 8)
+    kp = np.concatenate([k, rand(1, 2, 1, 8)], axis=2)
+    vp = np.concatenate([v, rand(1, 2, 1, 8)], axis=2)
+    mask = np.ones((6, Skv + 1), dtype=bool)
+    mask[:, -1] = False
+    padded = sdpa64(q, kp, vp, 0.4, mask=mask)
+    out, _ = oracle.attention(q, k, v, 0.4)
+    np.testing.assert_allclose(out, padded, atol=1e-12)
+
+
+def test_merge_closed_form_two_partials():
+    # two partials with lse a, b: weights are the logistic function of a - b
+    o1, o2 = rand(3, 4), rand(3, 4)
+    a, b = np.array([0.0, 3.0, -700.0]), np.array([1.0, -2.0, -701.0])
+    out, lse = oracle.lse_merge(np.stack([o1, o2]), np.stack([a, b]))
+    w1 = 1.0 / (1.0 + np.exp(b - a))
+    np.testing.assert_allclose(out, w1[:, None] * o1 + (1 - w1)[:, None] * o2, atol=1e-13)
+    np.testing.assert_allclose(lse, np.logaddexp(a, b), atol=1e-12)
+
+
+def test_merge_all_empty_and_one_empty():
+    o = rand(2, 3, 4)
+    out, lse = oracle.lse_merge(np.zeros((2, 3, 4)), np.full((2, 3), -np.inf))
+    assert np.all(out == 0) and np.all(lse == -np.inf)
+    out, lse = oracle.lse_merge(np.stack([o[0], np.zeros((3, 4))]), np.stack([np.array([0.5, 1.0, 2.0]), np.full(3, -np.inf)]))
+    np.testing.assert_allclose(out, o[0], atol=1e-15)
+    np.testing.assert_allclose(lse, [0.5, 1.0, 2.0], atol=1e-15)
+
+
+# ---------------------------------------------------------------- pooling
+
+@pytest.mark.parametrize("S,block", [(256, 64), (300, 64), (129, 128), (1, 64), (1024, 128)])
+def test_pool_matches_numpy_mean(S, block):
+    x = rand(2, 3, S, 16)
+    xp = oracle.block_pool(x, block)
+    nb = -(-S // block)
+    assert xp.shape == (2, 3, nb, 16)
+    for i in range(nb):
+        np.testing.assert_allclose(xp[:, :, i], x[:, :, i * block:(i + 1) * block].mean(axis=2), atol=1e-14)
+
+
+def test_pool_constant_blocks():
+    x = np.repeat(np.arange(5.0)[None, None, :, None], 64, axis=2).reshape(1, 1, 320, 1) * np.ones((1, 1, 1, 4))
+    xp = oracle.block_pool(x, 64)
+    np.testing.assert_array_equal(xp[0, 0, :, 0], np.arange(5.0))
+
+
+# ---------------------------------------------------------------- routing
+
+def brute_route(q, k, v, block_q, block_k, scale, beta, clamp=True):
+    """Direct enumeration from raw tokens: proxy = mean token-pair score of each block pair."""
+    B, H, S, d = q.shape
+    nq, nk = -(-S // block_q), -(-S // block_k)
+    out = {}
+    scores = scale * np.einsum("bhqd,bhkd->bhqk", q, k)
+    proxy = np.zeros((B, H, nq, nk))
+    for i in range(nq):
+        for j in range(nk):
+            proxy[:, :, i, j] = scores[:, :, i * block_q:(i + 1) * block_q, j * block_k:(j + 1) * block_k].mean(axis=(2, 3))
+    mu = proxy.mean(-1)
+    sigma = proxy.std(-1)
+    tau = np.full_like(mu, -np.inf) if beta == -np.inf else mu + beta * sigma
+    sel = proxy >= tau[..., None]
+    am = proxy.argmax(-1)
+    for b in range(B):
+        for h in range(H):
+            for i in range(nq):
+                sel[b, h, i, am[b, h, i]] = True
+    sizes = np.array([min(block_k, S - j * block_k) for j in range(nk)], dtype=float)
+    w = sizes * (1 + proxy - mu[..., None])
+    if clamp:
+        w = np.maximum(w, 0)
+    w = np.where(sel, 0.0, w)
+    vbar = np.stack([v[:, :, j * block_k:(j + 1) * block_k].mean(axis=2) for j in range(nk)], axis=2)
+    out.update(proxy=proxy, mu=mu, sigma=sigma, tau=tau, sel=sel, W=w.sum(-1), T=np.einsum("bhij,bhjd->bhid", w, vbar))
+    return out
+
+
+@pytest.mark.parametrize("S,bq,bk,beta", [(256, 64, 64, 0.5), (300, 64, 128, 0.0), (512, 128, 64, 1.3), (256, 64, 64, -0.7)])
+def test_route_matches_brute_force_enumeration(S, bq, bk, beta):
+    d = 16
+    q, k, v = rand(1, 2, S, d), rand(1, 2, S, d), rand(1, 2, S, d)
+    scale = 1 / math.sqrt(d)
+    _, _, rt, _ = oracle.sparse_route_attention(q, k, v, bq, bk, scale, beta, rows=np.arange(2))
+    ref = brute_route(q, k, v, bq, bk, scale, beta)
+    np.testing.assert_allclose(rt["proxy"], ref["proxy"], atol=1e-12)
+    np.testing.assert_allclose(rt["mu"], ref["mu"], atol=1e-12)
+    np.testing.assert_allclose(rt["sigma"], ref["sigma"], atol=1e-12)
+    np.testing.assert_allclose(rt["tau"], ref["tau"], atol=1e-12)
+    # selection must agree exactly away from the threshold
+    near = np.abs(ref["proxy"] - ref["tau"][..., None]) < 1e-9
+    assert np.array_equal(rt["sel"] | near, ref["sel"] | near)
+    np.testing.assert_array_equal(rt["sel_cnt"], rt["sel"].sum(-1))
+    np.testing.assert_allclose(rt["W"], ref["W"], atol=1e-10)
+    np.testing.assert_allclose(rt["T"], ref["T"], atol=1e-10)
+
+
+def test_route_beta_minus_inf_selects_all():
+    q, k, v = rand(1, 1, 256, 8), rand(1, 1, 256, 8), rand(1, 1, 256, 8)
+    _, _, rt, _ = oracle.sparse_route_attention(q, k, v, 64, 64, 0.3, -np.inf, rows=np.arange(1))
+    assert rt["sel"].all()
+    assert np.all(rt["tau"] == -np.inf)
+    assert np.all(rt["W"] == 0) and np.all(rt["T"] == 0)
+
+
+def test_route_constant_keys_zero_sigma_selects_all():
+    # identical pooled keys (dyadic values, exact mean) -> sigma = 0 -> every block meets tau = mu
+    q = rand(1, 1, 256, 8)
+    k = np.tile(np.array([0.5, -0.25, 1.0, 0.0, 0.125, 2.0, -1.0, 0.75]), (1, 1, 256, 1))
+    v = rand(1, 1, 256, 8)
+    qp, kp, vp = oracle.block_pool(q, 64), oracle.block_pool(k, 64), oracle.block_pool(v, 64)
+    rt = oracle.route(qp, kp, vp, 256, 64, 1.0, 2.0)
+    assert np.all(rt["sigma"] == 0)
+    assert rt["sel"].all()
+
+
+def test_route_density_monotone_in_beta_and_argmax_kept():
+    q, k, v = rand(1, 2, 512, 16), rand(1, 2, 512, 16), rand(1, 2, 512, 16)
+    qp, kp, vp = oracle.block_pool(q, 64), oracle.block_pool(k, 64), oracle.block_pool(v, 64)
+    prev = None
+    for beta in [-np.inf, -2, -1, 0, 0.5, 1, 2, 5, 1e9]:
+        rt = oracle.route(qp, kp, vp, 512, 64, 0.25, beta)
+        dens = rt["sel"].sum()
+        if prev is not None:
+            assert dens <= prev
+        prev = dens
+        am = rt["proxy"].argmax(-1)
+        assert np.take_along_axis(rt["sel"], am[..., None], -1).all()
+    assert prev == 2 * 8                                 # beta -> inf keeps only the argmax block of each row
+
+
+# ---------------------------------------------------------------- sparse attention + Taylor term
+
+def test_sparse_beta_minus_inf_equals_dense_bitwise():
+    q, k, v = rand(1, 2, 300, 16), rand(1, 2, 300, 16), rand(1, 2, 300, 16)
+    out, lse, rt, _ = oracle.sparse_route_attention(q, k, v, 64, 64, 0.25, -np.inf)
+    dense, ldense = oracle.attention(q, k, v, 0.25)
+    assert np.array_equal(out, dense)
+    assert np.array_equal(lse, ldense)
+
+
+def test_sparse_without_taylor_equals_masked_library_attention():
+    # zero Taylor aggregates: the output is softmax attention restricted to the selected blocks
+    S, b = 256, 64
+    q, k, v = rand(1, 1, S, 8), rand(1, 1, S, 8), rand(1, 1, S, 8)
+    qp, kp, vp = oracle.block_pool(q, b), oracle.block_pool(k, b), oracle.block_pool(v, b)
+    rt = oracle.route(qp, kp, vp, S, b, 0.5, 0.8)
+    assert not rt["sel"].all()
+    out, _ = oracle.sparse_attention(q, k, v, b, b, rt["sel"], rt["mu"], np.zeros_like(rt["W"]),
+                                     np.zeros_like(rt["T"]), 0.5)
+    mask = np.repeat(np.repeat(rt["sel"][0, 0], b, axis=0), b, axis=1)
+    np.testing.assert_allclose(out, sdpa64(q, k, v, 0.5, mask=mask), atol=1e-12)
+
+
+def load_taylor_fixture():
+    path = os.path.join(GOLDEN, "taylor_closed_form.txt")
+    vals = {}
+    with open(path) as f:
+        for line in f:
+            line = line.split("#", 1)[0].strip()
+            if line:
+                key, rhs = line.split("=", 1)
+                vals[key.strip()] = np.array([float(t) for t in rhs.split()])
+    return vals
+
+
+def test_taylor_hand_derived_closed_form():
+    """Two query blocks x two key blocks with identical tokens inside each block.
+
+    Every token score then equals its block proxy, so the Taylor-corrected
+    row has a two-term closed form (derivation in the fixture file)."""
+    g = load_taylor_fixture()
+    a, bq = g["q_block0"], g["q_block1"]
+    alpha, gamma = g["k_block0"], g["k_block1"]
+    vA, vB = g["v_block0"], g["v_block1"]
+    beta, scale = float(g["beta"][0]), float(g["scale"][0])
+    q = np.array([a, a, bq, bq])[None, None]
+    k = np.array([alpha, alpha, gamma, gamma])[None, None]
+    v = np.array([vA, vA, vB, vB])[None, None]
+    out, lse, rt, _ = oracle.sparse_route_attention(q, k, v, 2, 2, scale, beta)
+    # row block 0: s00 = 0.6, s01 = 0.2 -> mu = 0.4, sigma = 0.2, only block 0 kept
+    # row block 1: s10 = 0.2, s11 = 0.4 -> mu = 0.3, sigma = 0.1, only block 1 kept
+    np.testing.assert_allclose(rt["mu"][0, 0], [0.4, 0.3], atol=1e-14)
+    np.testing.assert_allclose(rt["sigma"][0, 0], [0.2, 0.1], atol=1e-14)
+    assert rt["sel"][0, 0].tolist() == [[True, False], [False, True]]
+    np.testing.assert_allclose(rt["W"][0, 0], [2 * 0.8, 2 * 0.9], atol=1e-14)
+    r0 = math.exp(-0.2) * 0.8
+    r1 = math.exp(-0.1) * 0.9
+    exp0 = (vA + r0 * vB) / (1 + r0)
+    exp1 = (vB + r1 * vA) / (1 + r1)
+    np.testing.assert_allclose(out[0, 0, 0], exp0, atol=1e-14)
+    np.testing.assert_allclose(out[0, 0, 1], exp0, atol=1e-14)
+    np.testing.assert_allclose(out[0, 0, 2], exp1, atol=1e-14)
+    np.testing.assert_allclose(lse[0, 0, 0], 0.6 + math.log(2 + 2 * r0), atol=1e-14)
+    np.testing.assert_allclose(lse[0, 0, 3], 0.4 + math.log(2 + 2 * r1), atol=1e-14)
+
+
+def test_taylor_constant_v_and_unit_mass():
+    # with V constant, num = c * den exactly in exact arithmetic: the output is that constant,
+    # i.e. the selected probabilities plus the Taylor mass sum to one
+    S = 320
+    q, k = rand(1, 2, S, 16, scale=0.5), rand(1, 2, S, 16, scale=0.5)
+    cst = rand(16)
+    v = np.tile(cst, (1, 2, S, 1))
+    out, _, rt, _ = oracle.sparse_route_attention(q, k, v, 64, 64, 0.25, 0.5)
+    assert not rt["sel"].all()
+    np.testing.assert_allclose(out, np.broadcast_to(cst, out.shape), atol=1e-13)
+    out1, _, _, _ = oracle.sparse_route_attention(q, k, np.ones((1, 2, S, 16)), 64, 64, 0.25, 0.5)
+    np.testing.assert_allclose(out1, 1.0, atol=1e-14)
+
+
+def test_taylor_unclamped_switch_and_clamp_count():
+    # strongly peaked rows: some rejected blocks fall below mu - 1 and get clamped
+    S, b, d = 512, 64, 16
+    q, k, v = rand(1, 1, S, d, scale=3), rand(1, 1, S, d, scale=3), rand(1, 1, S, d)
+    qp, kp, vp = oracle.block_pool(q, b), oracle.block_pool(k, b), oracle.block_pool(v, b)
+    rc = oracle.route(qp, kp, vp, S, b, 1.0, 0.5, clamp=True)
+    ru = oracle.route(qp, kp, vp, S, b, 1.0, 0.5, clamp=False)
+    low = (~rc["sel"]) & (rc["proxy"] < rc["mu"][..., None] - 1)
+    assert rc["n_clamped"] == int(low.sum()) > 0
+    assert np.all(rc["W"] >= ru["W"])
