@@ -1,0 +1,435 @@
+#!/usr/bin/env python3
+"""Benchmark of the LTX-2.5 Stage-2 attention hot path on GB300.
+
+One step = the attention of one Stage-2 transformer block on synthetic data:
+  1. Sol-Attn routing of the 65664-token video+audio sequence (pool + route),
+  2. block-sparse self-attention with the Taylor term (H=32, d=128, block 128, beta=1),
+  3. audio->video cross attention: 128 audio queries against 65536 video keys
+     as 8 split-KV partial answers,
+  4. the exact log-sum-exp merge of those partials.
+Metric: executed attention TFLOP/s of the whole step (dense-equivalent
+TFLOP/s and the fraction of the measured bf16 tensor peak are reported too).
+
+Usage: python bench.py [--gpus N --steps K --warmup W] [--impl reference]
+Under torchrun every rank runs its own copy of the step (weak scaling, no
+data-path collective); rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from workloads import WORKLOADS, Workload, make_qkv, to_f64  # noqa: E402
+
+METRIC = "attention TFLOP/s (executed & dense-equiv) and % bf16 tensor peak, S=64K, d=128"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+CROSS_N_SPLIT = 8
+CROSS_SKV = 65536
+CROSS_SQ = 128
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_fingerprint() -> str:
+    h = hashlib.sha256()
+    for name in ("attn_fwd.cuh", "ptx.cuh", "attn_fwd_d128.cu"):
+        with open(os.path.join(ROOT, "video_diffusion_transformer_block_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload: str):
+    """Per-launch DRAM bytes of the sparse forward from the committed ncu summary, if it was
+    taken on the current kernel source."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        t = json.load(f)
+    ent = t.get(workload)
+    if not ent or ent.get("kernel_fingerprint") != kernel_fingerprint():
+        return None
+    return ent.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.15)
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self):
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in getattr(self, "lines", []):
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax = float(parts[2])
+            except ValueError:
+                continue
+            for n, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": smax, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(local)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def executed_sparse_flops(sel_idx: torch.Tensor, sel_cnt: torch.Tensor, S: int, block: int, d: int) -> float:
+    """sum over (b, h, query block i, selected j) of 4 * m_i * n_j * d."""
+    idx = sel_idx.cpu().numpy()
+    cnt = sel_cnt.cpu().numpy()
+    nb = idx.shape[-1]
+    sizes = np.array([min(block, S - j * block) for j in range(nb)], dtype=np.float64)
+    total = 0.0
+    flat_idx = idx.reshape(-1, nb)
+    flat_cnt = cnt.reshape(-1)
+    for r in range(flat_cnt.size):
+        i = r % nb
+        keys = sizes[flat_idx[r, :flat_cnt[r]]].sum()
+        total += sizes[i] * keys
+    return 4.0 * d * total
+
+
+# ============================================================ native arm
+
+def make_inputs(rank: int, beta: float):
+    w = WORKLOADS["sparse64k"]
+    wr = Workload(w.name, B=w.B, H=w.H, Sq=w.Sq, Skv=w.Skv, d=w.d, seed=w.seed + 1000 * rank, q_std=w.q_std,
+                  k_std=w.k_std, grid=w.grid, audio_per_frame=w.audio_per_frame, pe=True, block=w.block, beta=beta)
+    q, k, v = make_qkv(wr, device="cuda")
+    wc = Workload("cross_stage2", B=1, H=w.H, Sq=CROSS_SQ, Skv=CROSS_SKV, d=w.d, seed=3 + 1000 * rank)
+    qa, kx, vx = make_qkv(wc, device="cuda")
+    return wr, (q, k, v), (qa, kx, vx)
+
+
+def run_native(args, world, rank, local):
+    import video_diffusion_transformer_block_gb300 as vd
+    from video_diffusion_transformer_block_gb300 import build as vbuild
+
+    vbuild.build()
+    vd.load_library()
+    peaks, peaks_src = load_peaks()
+    w, (q, k, v), (qa, kx, vx) = make_inputs(rank, args.beta)
+    B, H, S, d, block = w.B, w.H, w.Sq, w.d, w.block
+    dev = q.device
+    ws = torch.empty(vd.attn_sparse_workspace_bytes(B, H, S, d, block, block), dtype=torch.uint8, device=dev)
+    rt = vd.sparse_route_buffers(B, H, S, d, block, dev)
+    out = torch.empty_like(q)
+    lse = torch.empty((B, H, S), dtype=torch.float32, device=dev)
+    op = torch.empty((CROSS_N_SPLIT, B, H, CROSS_SQ, d), dtype=torch.float32, device=dev)
+    lp = torch.empty((CROSS_N_SPLIT, B, H, CROSS_SQ), dtype=torch.float32, device=dev)
+    oa = torch.empty((B, H, CROSS_SQ, d), dtype=torch.bfloat16, device=dev)
+    la = torch.empty((B, H, CROSS_SQ), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+    kernels_per_step = 5  # pool, route, sparse forward, split-KV forward, merge
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        vd.attn_sparse_route(q, k, v, args.beta, block=block, route=rt, workspace=ws)
+        if ev is not None:
+            ev[1].record(stream)
+        vd.attn_sparse_fwd(q, k, v, rt, block=block, out=out, lse=lse)
+        if ev is not None:
+            ev[2].record(stream)
+        vd.attn_cross_splitkv_fwd(qa, kx, vx, CROSS_N_SPLIT, out_part=op, lse_part=lp)
+        vd.attn_lse_merge(op, lp, out=oa, lse=la)
+        if ev is not None:
+            ev[3].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    status = vd.attn_last_device_status()
+    if status != 0:
+        raise RuntimeError(f"device status after warm-up: {vd.attn_status_string(status)}")
+    sparse_flops = executed_sparse_flops(rt["sel_idx"], rt["sel_cnt"], S, block, d)
+    dense_eq = 4.0 * B * H * S * S * d
+    cross_flops = 4.0 * B * H * CROSS_SQ * CROSS_SKV * d
+    density = sparse_flops / dense_eq
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        for i in range(args.steps):
+            step(evs[i])
+        torch.cuda.synchronize()
+    barrier(world)
+    status = vd.attn_last_device_status()
+    if status != 0:
+        raise RuntimeError(f"device status after timed region: {vd.attn_status_string(status)}")
+    total_ms = evs[0][0].elapsed_time(evs[-1][3])
+    route_ms = sum(e[0].elapsed_time(e[1]) for e in evs) / args.steps
+    fwd_ms = sum(e[1].elapsed_time(e[2]) for e in evs) / args.steps
+    cross_ms = sum(e[2].elapsed_time(e[3]) for e in evs) / args.steps
+    total_ms = max_over_ranks(total_ms, world)
+    ms_per_step = total_ms / args.steps
+    step_flops = sparse_flops + cross_flops
+    value = world * step_flops * args.steps / (total_ms * 1e-3) / 1e12
+    dense_equiv = world * (dense_eq + cross_flops) * args.steps / (total_ms * 1e-3) / 1e12
+
+    peak_sus = peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
+    peak_burst = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
+    fwd_tflops = sparse_flops / (fwd_ms * 1e-3) / 1e12
+    traffic = profiled_traffic("sparse64k")
+    result = {
+        "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded noise + 3D sinusoidal position code)",
+        "config": {"workload": "sparse64k: Stage-2 block-sparse self-attention B=1 H=32 S=65664 (16x64x64 video + "
+                               "8 audio tokens per frame) d=128 block 128 beta=1.0, plus audio->video cross "
+                               "attention 128 x 65536 split into 8 KV chunks and LSE-merged",
+                   "global_batch": world, "seq_len": S, "parallelism": f"replicas x{world} (heads/batches shard "
+                   "with no exchange)", "l2": "inputs (3.2 GB per step) larger than L2; no flush"},
+        "dense_equiv_tflops": round(dense_equiv, 2),
+        "density": round(density, 5),
+        "pct_bf16_peak_executed": round(100 * value / world / peak_sus, 2),
+        "breakdown_ms": {"pool_route": round(route_ms, 4), "sparse_fwd": round(fwd_ms, 4),
+                         "cross_splitkv_merge": round(cross_ms, 4)},
+        "roofline": {"bound": "tensor", "kernel": "attn_fwd_kernel (sparse, d=128, block 128)",
+                     "achieved": round(fwd_tflops, 2), "peak": peak_sus, "unit": "TFLOP/s",
+                     "frac": round(fwd_tflops / peak_sus, 4), "frac_of_burst_peak": round(fwd_tflops / peak_burst, 4),
+                     "peak_source": f"{peaks_src} bf16_tflops_sustained (kernel timed inside a long step)",
+                     "traffic": traffic},
+        "gpu_launches": kernels_per_step * args.steps,
+        "clocks": clocks.summary(),
+    }
+    if not args.no_e2e:
+        result["e2e"] = run_e2e(args, vd, w, (q, k, v), (qa, kx, vx), rt, ws, step_flops, world)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(q, k, v, w, budget_s=args.cpu_seconds)
+    return result
+
+
+def run_e2e(args, vd, w, qkv, cross, rt, ws, step_flops, world):
+    """Same step through the public API with the inputs in pinned host memory: every step
+    copies its inputs host->device and reads its outputs back, inside the timed region."""
+    q, k, v = qkv
+    qa, kx, vx = cross
+    hin = [t.cpu().pin_memory() for t in (q, k, v, qa, kx, vx)]
+    din = [torch.empty_like(t) for t in (q, k, v, qa, kx, vx)]
+    B, H, S, d, block = w.B, w.H, w.Sq, w.d, w.block
+    out = torch.empty_like(q)
+    lse = torch.empty((B, H, S), dtype=torch.float32, device=q.device)
+    op = torch.empty((CROSS_N_SPLIT, B, H, CROSS_SQ, d), dtype=torch.float32, device=q.device)
+    lp = torch.empty((CROSS_N_SPLIT, B, H, CROSS_SQ), dtype=torch.float32, device=q.device)
+    oa = torch.empty((B, H, CROSS_SQ, d), dtype=torch.bfloat16, device=q.device)
+    la = torch.empty((B, H, CROSS_SQ), dtype=torch.float32, device=q.device)
+    hout = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in (out, lse, oa, la)]
+    h2d = sum(t.numel() * t.element_size() for t in hin)
+    d2h = sum(t.numel() * t.element_size() for t in hout)
+
+    def step():
+        for dst, src in zip(din, hin):
+            dst.copy_(src, non_blocking=True)
+        vd.attn_sparse_route(din[0], din[1], din[2], args.beta, block=block, route=rt, workspace=ws)
+        vd.attn_sparse_fwd(din[0], din[1], din[2], rt, block=block, out=out, lse=lse)
+        vd.attn_cross_splitkv_fwd(din[3], din[4], din[5], CROSS_N_SPLIT, out_part=op, lse_part=lp)
+        vd.attn_lse_merge(op, lp, out=oa, lse=la)
+        for dst, src in zip(hout, (out, lse, oa, la)):
+            dst.copy_(src, non_blocking=True)
+
+    step()
+    torch.cuda.synchronize()
+    steps = max(3, args.steps // 2)
+    barrier(world)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        step()
+    e1.record()
+    torch.cuda.synchronize()
+    barrier(world)
+    ms = max_over_ranks(e0.elapsed_time(e1), world) / steps
+    return {"value": round(world * step_flops / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s", "ms_per_step": round(ms, 4),
+            "steps": steps, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+
+
+# ============================================================ oracle (CPU baseline / reference arm)
+
+def oracle_sample(qh, kh, vh, w, n_rows, rng):
+    """Oracle work on a bounded sample of the Stage-2 workload: pool + route of one head and
+    block-sparse attention of n_rows sampled query rows of it.  Returns (seconds, executed FLOPs)."""
+    import oracle
+    S, d, block = w.Sq, w.d, w.block
+    rows = np.sort(rng.choice(S, size=n_rows, replace=False)).astype(np.int64)
+    t0 = time.perf_counter()
+    qp, kp, vp = oracle.block_pool(qh, block), oracle.block_pool(kh, block), oracle.block_pool(vh, block)
+    rt = oracle.route(qp, kp, vp, S, block, w.scale, w.beta)
+    oracle.sparse_attention(qh, kh, vh, block, block, rt["sel"], rt["mu"], rt["W"], rt["T"], w.scale, rows=rows)
+    dt = time.perf_counter() - t0
+    nb = rt["sel"].shape[-1]
+    sizes = np.array([min(block, S - j * block) for j in range(nb)], dtype=np.float64)
+    keys_per_block = rt["sel"][0, 0].astype(np.float64) @ sizes
+    flops = 4.0 * d * keys_per_block[rows // block].sum()
+    return dt, flops
+
+
+def host_head0(q, k, v):
+    return [to_f64(x[:, :1].contiguous()) for x in (q, k, v)]
+
+
+def cpu_baseline(q, k, v, w, budget_s=15.0):
+    import oracle
+    oracle.build()
+    qh, kh, vh = host_head0(q, k, v)
+    rng = np.random.default_rng(0)
+    dt0, _ = oracle_sample(qh, kh, vh, w, 64, rng)                     # calibration
+    per_row = max(dt0 / 64, 1e-6)
+    n_rows = int(min(w.Sq, max(256, budget_s / per_row)))
+    dt, flops = oracle_sample(qh, kh, vh, w, n_rows, rng)
+    cores = len(os.sched_getaffinity(0))
+    return {"value": round(flops / dt / 1e12, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+            "seconds": round(dt, 3),
+            "sample": f"head 0 of the sparse64k workload: block pool + route of the head and block-sparse attention "
+                      f"of {n_rows} seeded sampled query rows (fp64 C oracle, OpenMP on {cores} threads)"}
+
+
+def run_reference(args, world, rank):
+    """Reference arm: the fp64 CPU oracle timed on bounded samples of the same workload."""
+    if rank != 0:
+        return None
+    import oracle
+    oracle.build()
+    w = WORKLOADS["sparse64k"]
+    q, k, v = make_qkv(Workload(w.name, B=1, H=1, Sq=w.Sq, Skv=w.Skv, d=w.d, seed=w.seed, q_std=w.q_std,
+                                k_std=w.k_std, grid=w.grid, audio_per_frame=w.audio_per_frame, pe=True,
+                                block=w.block, beta=args.beta), device="cpu")
+    w = Workload(w.name, B=1, H=1, Sq=w.Sq, Skv=w.Skv, d=w.d, seed=w.seed, block=w.block, beta=args.beta)
+    qh, kh, vh = to_f64(q), to_f64(k), to_f64(v)
+    rng = np.random.default_rng(1)
+    dt0, _ = oracle_sample(qh, kh, vh, w, 32, rng)
+    per_row = max(dt0 / 32, 1e-6)
+    budget = max(2.0, args.cpu_seconds * 4 / max(1, args.steps + args.warmup))
+    n_rows = int(min(w.Sq, max(64, budget / per_row)))
+    for _ in range(args.warmup):
+        oracle_sample(qh, kh, vh, w, n_rows, rng)
+    tot_t, tot_f = 0.0, 0.0
+    for _ in range(args.steps):
+        dt, fl = oracle_sample(qh, kh, vh, w, n_rows, rng)
+        tot_t += dt
+        tot_f += fl
+    val = tot_f / tot_t / 1e12
+    cores = len(os.sched_getaffinity(0))
+    sample = (f"per step: head 0 of the sparse64k workload, block pool + route of the head and block-sparse "
+              f"attention of {n_rows} seeded sampled query rows (fp64 C oracle, {cores} threads)")
+    return {"metric": METRIC, "value": round(val, 6), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(1e3 * tot_t / args.steps, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": "sparse64k (bounded sample, see cpu_baseline.sample)", "seq_len": w.Sq},
+            "impl": "reference",
+            "cpu_baseline": {"value": round(val, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(val, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["native", "reference"], default="native")
+    ap.add_argument("--beta", type=float, default=1.0)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        res = run_reference(args, world, rank)
+    else:
+        res = run_native(args, world, rank, local)
+    if rank == 0 and res is not None:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,205 @@
+/*
+ * attn_api.h -- C ABI of the GB300 (sm_103a) attention hot path of an
+ * LTX-2.5-style video+audio diffusion transformer block.
+ *
+ * Three operations, each a hand-written CUDA kernel path:
+ *   - dense bf16 softmax attention over long video token sequences;
+ *   - audio->video cross attention as split-KV partial answers plus an exact
+ *     log-sum-exp merge;
+ *   - Sol-Attn-style training-free block-sparse attention (pool, route,
+ *     block-sparse forward with a Taylor term for rejected blocks).
+ *
+ * Conventions shared by every entry point
+ *   Layout      q, k, v and out are [B][H][S][d] row-major (d innermost,
+ *               contiguous), bf16 passed as raw 16-bit patterns (attn_bf16).
+ *               d is 64 or 128.  Every device pointer must be 16-byte aligned.
+ *   Ownership   All pointers are device pointers owned by the caller.  The
+ *               library never allocates or frees device memory and keeps no
+ *               pointer past the call.  Its only state is one device status
+ *               word per device (see attn_last_device_status).
+ *   Streams     Every call is asynchronous on `stream` (0 = legacy default
+ *               stream) and does not synchronise the host, except
+ *               attn_last_device_status.
+ *   Errors      Arguments are validated on the host before anything is
+ *               launched; an invalid call returns an error and launches
+ *               nothing.  A launch failure returns ATTN_ERR_CUDA.  A device
+ *               barrier wait that exceeds its time limit (about 2 s) makes
+ *               the kernel return early and sets the device status word,
+ *               which attn_last_device_status reports as ATTN_ERR_TIMEOUT.
+ *               No exception or process exit crosses this ABI.
+ *   Lengths     There are no masks: ragged and odd lengths (S not a multiple
+ *               of any tile, odd key counts) are handled by in-kernel bounds,
+ *               the way the LTX-2.5 page drops the padded key instead of
+ *               masking it ("LTX-2.5 at 4K, in half the time", section
+ *               "Attention across two GPUs").
+ *   Numerics    bf16 inputs, fp32 accumulation and softmax, bf16 outputs
+ *               rounded to nearest even, lse in natural log (fp32).
+ */
+#ifndef ATTN_API_H
+#define ATTN_API_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t attn_bf16; /* raw bf16 bit pattern */
+
+typedef enum {
+  ATTN_OK = 0,
+  ATTN_ERR_INVALID_ARG = 1, /* null/misaligned pointer, bad size or value */
+  ATTN_ERR_UNSUPPORTED = 2, /* valid but outside what the kernels implement (d, block, length limits) */
+  ATTN_ERR_WORKSPACE = 3,   /* workspace missing or smaller than attn_sparse_workspace_bytes() */
+  ATTN_ERR_CUDA = 4,        /* a CUDA runtime/driver call or a launch failed */
+  ATTN_ERR_TIMEOUT = 5      /* a device barrier wait ran out (reported by attn_last_device_status) */
+} attn_status_t;
+
+/*
+ * Dense attention  O = softmax(scale * Q K^T) V, non-causal, and
+ * lse = log sum_k exp(scale * q.k) per query row.
+ *   q    [B][H][Sq][d]  bf16      k, v  [B][H][Skv][d]  bf16
+ *   out  [B][H][Sq][d]  bf16      lse   [B][H][Sq]      fp32 (nullable)
+ * Requires B, H, Sq, Skv >= 1, d in {64, 128}, scale finite.
+ * Source: "Accelerating LTX-2.5 with Sol Engine", section "Stage 2
+ * Optimization" (attention over long video sequences dominates Stage 2);
+ * "LTX-2.5 Optimization" (openltx.com), attention-backend paragraph.
+ */
+attn_status_t attn_dense_fwd(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v, attn_bf16* out, float* lse,
+                             int B, int H, int Sq, int Skv, int d, float scale, cudaStream_t stream);
+
+/*
+ * Split-KV partial answers for few-query cross attention (about a hundred
+ * audio queries against tens of thousands of video keys).  Chunk c of
+ * n_split covers keys [floor(c*Skv/n_split), floor((c+1)*Skv/n_split)):
+ * balanced bounds, nothing padded.  For each chunk and query row the kernel
+ * writes the chunk-normalised output and the chunk's log-sum-exp:
+ *   out_part [n_split][B][H][Sq][d] fp32,  lse_part [n_split][B][H][Sq] fp32.
+ * An empty chunk (possible only when n_split > Skv, which is rejected) would
+ * be o = 0, lse = -inf.  Requires 1 <= n_split <= Skv.
+ * Source: "LTX-2.5 at 4K, in half the time", section "Attention across two
+ * GPUs" (each partial answer carries its running maximum and sum of
+ * exponentials; the kernel splits the work along the keys).
+ */
+attn_status_t attn_cross_splitkv_fwd(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v, float* out_part,
+                                     float* lse_part, int B, int H, int Sq, int Skv, int d, int n_split, float scale,
+                                     cudaStream_t stream);
+
+/*
+ * Exact log-sum-exp merge of n_split partial answers:
+ *   L = log sum_c exp(lse_c),  o = sum_c exp(lse_c - L) o_c.
+ *   out_part [n_split][B][H][Sq][d] fp32, lse_part [n_split][B][H][Sq] fp32
+ *   out [B][H][Sq][d] bf16, lse [B][H][Sq] fp32 (nullable).
+ * A row whose partials are all empty (lse = -inf) gets o = 0, lse = -inf.
+ * Source: "LTX-2.5 at 4K, in half the time", section "Attention across two
+ * GPUs" (partial answers are merged exactly).
+ */
+attn_status_t attn_lse_merge(const float* out_part, const float* lse_part, attn_bf16* out, float* lse, int n_split,
+                             int B, int H, int Sq, int d, cudaStream_t stream);
+
+/*
+ * Block mean-pool along the sequence: x_pool[b][h][i] = mean of x[b][h][t]
+ * over the tokens t of block i = [i*block, min((i+1)*block, S)).
+ *   x [B][H][S][d] bf16  ->  x_pool [B][H][ceil(S/block)][d] fp32.
+ * block in {64, 128}.
+ * Source: "Accelerating LTX-2.5 with Sol Engine", section "Stage 2
+ * Optimization", bullet "On-the-fly routing" (pooled keys).
+ */
+attn_status_t attn_block_pool(const attn_bf16* x, float* x_pool, int B, int H, int S, int d, int block,
+                              cudaStream_t stream);
+
+/*
+ * Bytes of device workspace attn_sparse_route_fwd needs for these sizes
+ * (pooled Q/K/V, selected-block lists, per-block statistics, Taylor
+ * aggregates).  Returns 0 for sizes the library does not support.
+ */
+size_t attn_sparse_workspace_bytes(int B, int H, int S, int d, int block_q, int block_k);
+
+/*
+ * Sol-Attn block-sparse self-attention (Sq = Skv = S).
+ * Source: "Accelerating LTX-2.5 with Sol Engine", section "Stage 2
+ * Optimization - Core Technology: Sol-Attn", bullets "Query-dependent
+ * thresholding", "On-the-fly routing" and "Proxy-score reuse".
+ *
+ * With NQB = ceil(S/block_q), NKB = ceil(S/block_k), Qbar/Kbar/Vbar the block
+ * means (attn_block_pool), per head and query block i:
+ *   s_ij  = scale * Qbar_i . Kbar_j                  (block proxy score)
+ *   mu_i, sigma_i = mean and population std of s_ij over j
+ *   tau_i = mu_i + beta * sigma_i                    (beta = -INFINITY keeps every block)
+ *   Sel_i = { j : s_ij >= tau_i } plus the argmax block (lowest j on ties)
+ *   for rejected j: w_ij = n_j * max(0, 1 + s_ij - mu_i)   (n_j = keys in block j)
+ *   W_i = sum w_ij,  T_i = sum w_ij Vbar_j
+ * and for each query row q of block i, over the keys of the selected blocks,
+ *   M = max scale*q.k,  num = sum e^(x-M) v + e^(mu_i-M) T_i,
+ *   den = sum e^(x-M) + e^(mu_i-M) W_i,  out = num/den,  lse = M + ln den.
+ * (When Sel_i is every block the Taylor terms are skipped.)
+ * The proxy scores are recomputed on chip and never written to memory.
+ *
+ *   q, k, v, out [B][H][S][d] bf16,  lse [B][H][S] fp32 (nullable)
+ *   block_q == block_k, in {64, 128}
+ *   workspace  device buffer of at least attn_sparse_workspace_bytes(...)
+ *              bytes, 256-byte aligned, contents ignored on entry
+ *   sel_idx    [B][H][NQB][NKB] int32 (nullable): the first sel_cnt entries of
+ *              each row are the selected key blocks in ascending order; the
+ *              rest are left unspecified
+ *   sel_cnt    [B][H][NQB] int32 (nullable)
+ *   stats      [B][H][NQB][4] fp32 (nullable): mu, sigma, tau, W
+ *   taylor_t   [B][H][NQB][d] fp32 (nullable): T
+ * Null outputs are kept inside the workspace.  S is limited to NKB <= 8192.
+ */
+attn_status_t attn_sparse_route_fwd(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v, attn_bf16* out,
+                                    float* lse, int B, int H, int S, int d, float scale, float beta, int block_q,
+                                    int block_k, void* workspace, size_t workspace_bytes, int32_t* sel_idx,
+                                    int32_t* sel_cnt, float* stats, float* taylor_t, cudaStream_t stream);
+
+/*
+ * Routing half of attn_sparse_route_fwd: block mean-pool of Q, K, V and the
+ * Sol-Attn selection with its Taylor aggregates (same definitions as
+ * attn_sparse_route_fwd).  Here sel_idx, sel_cnt, stats and taylor_t are
+ * required (non-null); the workspace holds the pooled tensors.
+ */
+attn_status_t attn_sparse_route(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v, int B, int H, int S,
+                                int d, float scale, float beta, int block_q, int block_k, void* workspace,
+                                size_t workspace_bytes, int32_t* sel_idx, int32_t* sel_cnt, float* stats,
+                                float* taylor_t, cudaStream_t stream);
+
+/*
+ * Forward half of attn_sparse_route_fwd: block-sparse attention with the
+ * Taylor term, given a routing in the layout attn_sparse_route writes
+ * (sel_idx/sel_cnt ascending lists, stats[..][0] = mu, stats[..][3] = W,
+ * taylor_t = T).  Lets a caller reuse one routing for several calls.  A list
+ * entry outside [0, NKB) is clamped and reported by attn_last_device_status
+ * as ATTN_ERR_INVALID_ARG.
+ */
+attn_status_t attn_sparse_fwd(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v, attn_bf16* out, float* lse,
+                              int B, int H, int S, int d, float scale, int block_q, int block_k,
+                              const int32_t* sel_idx, const int32_t* sel_cnt, const float* stats,
+                              const float* taylor_t, cudaStream_t stream);
+
+/*
+ * Synchronises `stream`, reads and clears the current device's status word.
+ * Returns ATTN_OK, ATTN_ERR_TIMEOUT if a kernel gave up on a barrier wait,
+ * ATTN_ERR_INVALID_ARG if a kernel met a corrupt selected-block list, or
+ * ATTN_ERR_CUDA if the synchronisation itself failed.
+ */
+attn_status_t attn_last_device_status(cudaStream_t stream);
+
+/* Static, human-readable name of a status code. */
+const char* attn_status_string(attn_status_t status);
+
+/*
+ * Self-test of the bounded-wait path: launches one CTA that waits on a
+ * barrier nothing ever arrives on, with a limit of `limit_us` microseconds
+ * (1..1000000).  The kernel gives up, records the timeout in the status word
+ * and exits, so a following attn_last_device_status returns
+ * ATTN_ERR_TIMEOUT.  Leaves the context usable.
+ */
+attn_status_t attn_selftest_wait_timeout(int limit_us, cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_API_H */

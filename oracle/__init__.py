@@ -61,7 +61,7 @@ def _load():
         lib.oracle_lse_merge.argtypes = [_D, _D, _i64, _i64, _i64, _D, _D]
         lib.oracle_block_pool.argtypes = [_D, _i64, _i64, _i64, _i64, _D]
         lib.oracle_route.argtypes = [_D, _D, _D, _i64, _i64, _i64, _i64, _I64, ctypes.c_double, ctypes.c_double,
-                                     ctypes.c_int, _D, _U8, _I64, _D, _D, _D, _D, _D, _I64]
+                                     ctypes.c_int, _U8, _D, _U8, _I64, _D, _D, _D, _D, _D, _I64]
         lib.oracle_sparse_rows.argtypes = [_D, _D, _D, _i64, _i64, _i64, _i64, _i64, _U8, _D, _D, _D,
                                            ctypes.c_double, _I64, _i64, _D, _D]
         for f in (lib.oracle_attend_rows, lib.oracle_split_partials, lib.oracle_lse_merge, lib.oracle_block_pool,
@@ -140,11 +140,12 @@ def block_pool(x, block: int):
     return xp
 
 
-def route(qp, kp, vp, S: int, block_k: int, scale: float, beta: float, clamp: bool = True):
+def route(qp, kp, vp, S: int, block_k: int, scale: float, beta: float, clamp: bool = True, force_sel=None):
     """Sol-Attn routing from pooled tensors qp [B,H,NQB,d], kp/vp [B,H,NKB,d].
 
-    Returns a dict with proxy, sel (bool), sel_cnt, mu, sigma, tau, W, T and
-    n_clamped."""
+    ``force_sel`` (bool [B,H,NQB,NKB]) replaces the threshold rule as the
+    selection.  Returns a dict with proxy, sel (bool), sel_cnt, mu, sigma,
+    tau, W, T and n_clamped."""
     qp, kp, vp = _bhsd(qp), _bhsd(kp), _bhsd(vp)
     B, H, NQB, d = qp.shape
     NKB = kp.shape[2]
@@ -155,8 +156,14 @@ def route(qp, kp, vp, S: int, block_k: int, scale: float, beta: float, clamp: bo
     mu, sigma, tau, W = (np.empty((B, H, NQB)) for _ in range(4))
     T = np.empty((B, H, NQB, d))
     ncl = np.zeros(1, dtype=np.int64)
+    fs = None
+    if force_sel is not None:
+        fs = np.ascontiguousarray(force_sel, dtype=np.uint8)
+        if fs.shape != (B, H, NQB, NKB):
+            raise ValueError("force_sel shape")
     _load().oracle_route(_p(qp, _D), _p(kp, _D), _p(vp, _D), B * H, NQB, NKB, d, _p(nk, _I64), float(scale),
-                         float(beta), 1 if clamp else 0, _p(proxy, _D), _p(sel, _U8), _p(cnt, _I64), _p(mu, _D),
+                         float(beta), 1 if clamp else 0, None if fs is None else _p(fs, _U8), _p(proxy, _D),
+                         _p(sel, _U8), _p(cnt, _I64), _p(mu, _D),
                          _p(sigma, _D), _p(tau, _D), _p(W, _D), _p(T, _D), _p(ncl, _I64))
     return dict(proxy=proxy, sel=sel.astype(bool), sel_cnt=cnt, mu=mu, sigma=sigma, tau=tau, W=W, T=T,
                 n_clamped=int(ncl[0]))

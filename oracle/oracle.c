@@ -169,13 +169,17 @@ void oracle_block_pool(const double* x, int64_t BH, int64_t S, int64_t d, int64_
  *   w_ij   = n_j * max(0, 1 + s_ij - mu_i)     (clamp: see `clamp`)
  *   W_i    = sum_{j rejected} w_ij
  *   T_i    = sum_{j rejected} w_ij * Vbar_j    (a common factor exp(mu_i) is left out)
+ * If `force_sel` is non-NULL, it replaces the threshold rule as the selection
+ * (used to evaluate the Taylor aggregates for another implementation's
+ * selection when a block's proxy lies within rounding distance of tau).
  * Outputs: proxy [BH][NQB][NKB] (may be NULL), sel [BH][NQB][NKB] (0/1),
  * sel_cnt [BH][NQB], mu, sigma, tau, W [BH][NQB], T [BH][NQB][d];
  * n_clamped[0] receives the number of rejected blocks whose weight was
  * clamped at zero.  With clamp == 0 the weights are left unclamped (study
  * switch; the library always clamps). */
 void oracle_route(const double* qp, const double* kp, const double* vp, int64_t BH, int64_t NQB, int64_t NKB, int64_t d,
-                  const int64_t* nk, double scale, double beta, int clamp, double* proxy, uint8_t* sel,
+                  const int64_t* nk, double scale, double beta, int clamp, const uint8_t* force_sel, double* proxy,
+                  uint8_t* sel,
                   int64_t* sel_cnt, double* mu, double* sigma, double* tau, double* W, double* T, int64_t* n_clamped) {
   int64_t clamped_total = 0;
 #pragma omp parallel reduction(+ : clamped_total)
@@ -207,7 +211,7 @@ void oracle_route(const double* qp, const double* kp, const double* vp, int64_t 
       double w_sum = 0.0;
       for (int64_t c = 0; c < d; ++c) T[t * d + c] = 0.0;
       for (int64_t j = 0; j < NKB; ++j) {
-        int keep = (s[j] >= th) || (j == jmax);
+        int keep = force_sel ? (force_sel[t * NKB + j] != 0) : ((s[j] >= th) || (j == jmax));
         sel[t * NKB + j] = (uint8_t)keep;
         if (keep) {
           ++cnt;

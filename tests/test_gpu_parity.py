@@ -1,0 +1,216 @@
+"""GPU parity: every kernel of the hot path against the fp64 oracle, through the C ABI.
+
+Small cases (seconds of oracle time) cover several tiles, ragged tails, odd
+key counts, d = 64/128, B > 1 and the degenerate cases; they compare every
+output element.  Tolerances: max-abs 2e-2 and relative L2 5e-3 on outputs
+(bf16 inputs, fp32 accumulation), selection lists exact outside the 1e-4
+band around tau.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import video_diffusion_transformer_block_gb300 as vd
+from workloads import WORKLOADS, Workload, make_qkv
+from parity_util import assert_close, compare_selection, gpu_selection, host
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+def rnd_qkv(B, H, Sq, Skv, d, seed, std=1.0):
+    w = Workload("t", B=B, H=H, Sq=Sq, Skv=Skv, d=d, seed=seed, q_std=std, k_std=std)
+    return make_qkv(w, device=DEV)
+
+
+@pytest.fixture(autouse=True)
+def _status_clean():
+    torch.cuda.synchronize()
+    yield
+    assert vd.attn_last_device_status() == 0, "device status word set (timeout or bad list)"
+
+
+# ---------------------------------------------------------------- pool
+
+@pytest.mark.parametrize("B,H,S,d,block", [(1, 2, 1024, 64, 64), (2, 3, 1000, 128, 128), (1, 1, 77, 128, 64),
+                                           (1, 2, 129, 64, 128)])
+def test_block_pool(B, H, S, d, block):
+    x, _, _ = rnd_qkv(B, H, S, S, d, seed=11)
+    xp = vd.attn_block_pool(x, block)
+    torch.cuda.synchronize()
+    ref = oracle.block_pool(host(x), block)
+    np.testing.assert_allclose(host(xp), ref, rtol=1e-5, atol=1e-6)
+
+
+# ---------------------------------------------------------------- merge
+
+@pytest.mark.parametrize("n,d", [(1, 128), (3, 64), (8, 128), (5, 128)])
+def test_lse_merge(n, d):
+    g = torch.Generator(device="cpu").manual_seed(5 + n)
+    B, H, Sq = 1, 3, 37
+    o = torch.randn((n, B, H, Sq, d), generator=g)
+    lse = torch.randn((n, B, H, Sq), generator=g) * 3
+    lse[:, 0, 0, 0] = -math.inf                      # a row whose partials are all empty
+    if n > 1:
+        lse[0, 0, 1, 2] = -math.inf                  # one empty partial
+        lse[1, 0, 2, 3] = 80.0                       # dominant partial
+    out, l = vd.attn_lse_merge(o.to(DEV), lse.to(DEV))
+    torch.cuda.synchronize()
+    ro, rl = oracle.lse_merge(o.double().numpy(), lse.double().numpy())
+    assert_close(host(out), ro, "merge out")
+    lg = host(l)
+    assert lg[0, 0, 0] == -np.inf and np.all(host(out)[0, 0, 0] == 0)
+    fin = np.isfinite(rl)
+    np.testing.assert_allclose(lg[fin], rl[fin], atol=1e-5, rtol=1e-6)
+
+
+# ---------------------------------------------------------------- dense
+
+@pytest.mark.parametrize("B,H,Sq,Skv,d", [
+    (1, 2, 256, 256, 128),      # exact tiles
+    (1, 2, 300, 517, 64),       # ragged query and key tails
+    (2, 1, 1, 1, 128),          # single token
+    (1, 1, 129, 1000, 128),     # one full + one 1-row query tile
+    (1, 3, 513, 255, 64),       # three query-tile pairs, odd keys
+    (1, 1, 640, 2049, 128),     # odd key count across many tiles
+])
+def test_dense(B, H, Sq, Skv, d):
+    q, k, v = rnd_qkv(B, H, Sq, Skv, d, seed=21 + Sq)
+    out, lse = vd.attn_dense_fwd(q, k, v)
+    torch.cuda.synchronize()
+    ro, rl = oracle.attention(host(q), host(k), host(v), 1 / math.sqrt(d))
+    assert_close(host(out), ro, "dense out")
+    assert_close(host(lse), rl, "dense lse")
+
+
+def test_dense_large_scores_rescale():
+    # peaked rows: the running max grows by far more than the lazy-rescale threshold across tiles
+    B, H, S, d = 1, 2, 1024, 128
+    q, k, v = rnd_qkv(B, H, S, S, d, seed=3, std=3.0)
+    out, lse = vd.attn_dense_fwd(q, k, v, scale=0.3)
+    torch.cuda.synchronize()
+    ro, rl = oracle.attention(host(q), host(k), host(v), 0.3)
+    assert_close(host(out), ro, "dense peaked out")
+    assert_close(host(lse), rl, "dense peaked lse", max_abs=2e-2 * max(1.0, float(np.abs(rl).max()) / 10))
+
+
+# ---------------------------------------------------------------- split-KV + merge
+
+@pytest.mark.parametrize("H,Sq,Skv,d,n", [(2, 128, 4096, 128, 8), (2, 128, 4097, 128, 3), (1, 100, 1000, 64, 7),
+                                          (2, 130, 2000, 128, 1), (1, 128, 5, 128, 5)])
+def test_splitkv_and_merge(H, Sq, Skv, d, n):
+    q, k, v = rnd_qkv(1, H, Sq, Skv, d, seed=31 + Skv)
+    scale = 1 / math.sqrt(d)
+    op, lp = vd.attn_cross_splitkv_fwd(q, k, v, n)
+    out, lse = vd.attn_lse_merge(op, lp)
+    torch.cuda.synchronize()
+    qh, kh, vh = host(q), host(k), host(v)
+    rop, rlp = oracle.split_partials(qh, kh, vh, scale, n)
+    assert_close(host(op), rop, "partials out")
+    assert_close(host(lp), rlp, "partials lse")
+    ro, rl = oracle.attention(qh, kh, vh, scale)
+    assert_close(host(out), ro, "merged out")
+    assert_close(host(lse), rl, "merged lse")
+
+
+# ---------------------------------------------------------------- block-sparse
+
+def sparse_check(q, k, v, block, beta, scale=None, rows=None, heads_idx=None):
+    """Runs the GPU path with route outputs and checks route + output against the oracle.
+
+    Returns (n_flips, density, errors)."""
+    B, H, S, d = q.shape
+    scale = 1 / math.sqrt(d) if scale is None else scale
+    out, lse, rt = vd.attn_sparse_route_fwd(q, k, v, beta, block=block, scale=scale, route=True)
+    torch.cuda.synchronize()
+    hs = list(range(H)) if heads_idx is None else list(heads_idx)
+    qh, kh, vh = (host(x[:, hs].contiguous()) for x in (q, k, v))
+    o_out, o_lse, ort, (qp, kp, vp) = oracle.sparse_route_attention(qh, kh, vh, block, block, scale, beta, rows=[0])
+    gsel = gpu_selection(rt["sel_idx"][:, hs], rt["sel_cnt"][:, hs])
+    flips = compare_selection(gsel, ort)
+    st = host(rt["stats"][:, hs])
+    np.testing.assert_allclose(st[..., 0], ort["mu"], atol=1e-4, rtol=1e-4)
+    np.testing.assert_allclose(st[..., 1], ort["sigma"], atol=1e-4, rtol=1e-4)
+    if beta != -math.inf:
+        np.testing.assert_allclose(st[..., 2], ort["tau"], atol=1e-4, rtol=1e-4)
+    # Taylor aggregates and outputs for the GPU's own selection (separates near-tau flips from arithmetic)
+    forced = oracle.route(qp, kp, vp, S, block, scale, beta, force_sel=gsel)
+    np.testing.assert_allclose(st[..., 3], forced["W"], atol=2e-3, rtol=1e-3)
+    np.testing.assert_allclose(host(rt["taylor_t"][:, hs]), forced["T"], atol=2e-3 * block, rtol=1e-3)
+    nsel = len(hs) * S
+    rws = np.arange(nsel) if rows is None else np.asarray(rows)
+    ro, rl = oracle.sparse_attention(qh, kh, vh, block, block, gsel, forced["mu"], forced["W"], forced["T"], scale,
+                                     rows=rws)
+    go = host(out[:, hs].contiguous()).reshape(-1, d)[rws]
+    gl = host(lse[:, hs].contiguous()).reshape(-1)[rws]
+    e1 = assert_close(go, ro, "sparse out")
+    assert_close(gl, rl, "sparse lse")
+    density = float(gsel.mean())
+    return flips, density, e1
+
+
+@pytest.mark.parametrize("beta", [0.5, -math.inf, 0.0, 3.0])
+def test_sparse_tiny_config(beta):
+    w = WORKLOADS["tiny"]
+    q, k, v = make_qkv(w, device=DEV)
+    flips, density, _ = sparse_check(q, k, v, w.block, beta)
+    if beta == -math.inf:
+        assert density == 1.0
+
+
+def test_sparse_beta_minus_inf_equals_dense():
+    for d, block in [(64, 64), (128, 128)]:
+        q, k, v = rnd_qkv(1, 2, 1000, 1000, d, seed=41)
+        out_s, lse_s = vd.attn_sparse_route_fwd(q, k, v, -math.inf, block=block)
+        out_d, lse_d = vd.attn_dense_fwd(q, k, v)
+        torch.cuda.synchronize()
+        if block == 128:
+            # same kernel main loop over the same tiles: bitwise equal
+            assert torch.equal(out_s, out_d) and torch.equal(lse_s, lse_d)
+        else:
+            assert_close(host(out_s), host(out_d), "sparse(-inf) vs dense")
+
+
+@pytest.mark.parametrize("d,block,beta", [(128, 128, 1.0), (128, 64, 0.5), (64, 128, 1.5)])
+def test_sparse_local_workload_ragged(d, block, beta):
+    # the Stage-2 generator (noise + 3D position code, interleaved audio) truncated to two frames: S = 8208
+    w = WORKLOADS["sparse64k"]
+    w2 = Workload("s2", B=1, H=2, Sq=8208, Skv=8208, d=d, seed=7, q_std=0.5, k_std=0.5, grid=w.grid,
+                  audio_per_frame=8, pe=True, block=block, beta=beta)
+    q, k, v = make_qkv(w2, device=DEV)
+    flips, density, _ = sparse_check(q, k, v, block, beta)
+    assert 0.0 < density < 1.0
+
+
+def test_sparse_batch_gt_one():
+    q, k, v = rnd_qkv(2, 2, 640, 640, 128, seed=43)
+    out, lse, rt = vd.attn_sparse_route_fwd(q, k, v, 0.7, block=128, route=True)
+    torch.cuda.synchronize()
+    for b in range(2):
+        qh, kh, vh = (host(x[b:b + 1]) for x in (q, k, v))
+        _, _, ort, (qp, kp, vp) = oracle.sparse_route_attention(qh, kh, vh, 128, 128, 1 / math.sqrt(128), 0.7,
+                                                                rows=[0])
+        gsel = gpu_selection(rt["sel_idx"][b:b + 1], rt["sel_cnt"][b:b + 1])
+        compare_selection(gsel, ort)
+        forced = oracle.route(qp, kp, vp, 640, 128, 1 / math.sqrt(128), 0.7, force_sel=gsel)
+        ro, rl = oracle.sparse_attention(qh, kh, vh, 128, 128, gsel, forced["mu"], forced["W"], forced["T"],
+                                         1 / math.sqrt(128))
+        assert_close(host(out[b:b + 1]), ro, f"batch {b} out")
+        assert_close(host(lse[b:b + 1]), rl, f"batch {b} lse")
+
+
+# ---------------------------------------------------------------- status word
+
+def test_bounded_wait_reports_timeout_and_context_survives():
+    vd.attn_selftest_wait_timeout(2000)
+    assert vd.attn_last_device_status() == 5
+    assert vd.attn_last_device_status() == 0          # cleared on read
+    q, k, v = rnd_qkv(1, 1, 128, 128, 64, seed=1)
+    out, _ = vd.attn_dense_fwd(q, k, v)
+    torch.cuda.synchronize()
+    ro, _ = oracle.attention(host(q), host(k), host(v), 1 / 8)
+    assert_close(host(out), ro, "dense after timeout self-test")

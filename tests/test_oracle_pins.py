@@ -360,3 +360,18 @@ def test_taylor_unclamped_switch_and_clamp_count():
     low = (~rc["sel"]) & (rc["proxy"] < rc["mu"][..., None] - 1)
     assert rc["n_clamped"] == int(low.sum()) > 0
     assert np.all(rc["W"] >= ru["W"])
+
+
+def test_route_forced_selection_matches_threshold_rule_on_its_own_selection():
+    # forcing the selection the threshold rule would take reproduces W and T exactly
+    q, k, v = rand(1, 2, 384, 16), rand(1, 2, 384, 16), rand(1, 2, 384, 16)
+    qp, kp, vp = oracle.block_pool(q, 64), oracle.block_pool(k, 64), oracle.block_pool(v, 64)
+    rt = oracle.route(qp, kp, vp, 384, 64, 0.25, 0.3)
+    rf = oracle.route(qp, kp, vp, 384, 64, 0.25, 0.3, force_sel=rt["sel"])
+    assert np.array_equal(rf["sel"], rt["sel"])
+    np.testing.assert_array_equal(rf["W"], rt["W"])
+    np.testing.assert_array_equal(rf["T"], rt["T"])
+    flip = rt["sel"].copy()
+    flip[0, 0, 0, 0] = ~flip[0, 0, 0, 0]
+    ff = oracle.route(qp, kp, vp, 384, 64, 0.25, 0.3, force_sel=flip)
+    assert ff["sel_cnt"][0, 0, 0] == rt["sel_cnt"][0, 0, 0] + (1 if flip[0, 0, 0, 0] else -1)

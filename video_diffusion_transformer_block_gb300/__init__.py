@@ -1,0 +1,241 @@
+"""GB300 (sm_103a) attention hot path of an LTX-2.5-style video+audio DiT block.
+
+Thin Python binding over the C ABI in ``include/attn_api.h`` (library
+``libvdtb_attn.so`` built in-tree by :mod:`.build`).  Every function here has
+the name of the C entry point it calls and only marshals arguments: torch
+provides device memory and the current CUDA stream, the kernels do all the
+work.  There is no fallback: if the library is missing or fails to load,
+every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+import torch
+
+__all__ = [
+    "AttnError", "load_library", "attn_dense_fwd", "attn_cross_splitkv_fwd", "attn_lse_merge", "attn_block_pool",
+    "attn_sparse_workspace_bytes", "attn_sparse_route_fwd", "attn_sparse_route", "attn_sparse_fwd",
+    "attn_last_device_status", "attn_status_string", "attn_selftest_wait_timeout", "EXPORTED_SYMBOLS",
+]
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_PKG, "libvdtb_attn.so")
+_lock = threading.Lock()
+_lib = None
+
+EXPORTED_SYMBOLS = (
+    "attn_dense_fwd", "attn_cross_splitkv_fwd", "attn_lse_merge", "attn_block_pool", "attn_sparse_workspace_bytes",
+    "attn_sparse_route_fwd", "attn_sparse_route", "attn_sparse_fwd", "attn_last_device_status", "attn_status_string",
+    "attn_selftest_wait_timeout",
+)
+
+_STATUS = {0: "ATTN_OK", 1: "ATTN_ERR_INVALID_ARG", 2: "ATTN_ERR_UNSUPPORTED", 3: "ATTN_ERR_WORKSPACE",
+           4: "ATTN_ERR_CUDA", 5: "ATTN_ERR_TIMEOUT"}
+
+
+class AttnError(RuntimeError):
+    def __init__(self, fn: str, code: int):
+        self.code = code
+        super().__init__(f"{fn} failed: {_STATUS.get(code, code)}")
+
+
+def load_library(path: str | None = None) -> ctypes.CDLL:
+    """Load libvdtb_attn.so (built by ``build()``); raises if it is missing."""
+    global _lib
+    with _lock:
+        if _lib is not None and path is None:
+            return _lib
+        p = path or _LIB_PATH
+        if not os.path.exists(p):
+            raise RuntimeError(f"{p} is missing: build the CUDA library first "
+                               "(python -m video_diffusion_transformer_block_gb300.build)")
+        lib = ctypes.CDLL(p)
+        vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+        lib.attn_dense_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, vp]
+        lib.attn_cross_splitkv_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, vp]
+        lib.attn_lse_merge.argtypes = [vp, vp, vp, vp, i, i, i, i, i, vp]
+        lib.attn_block_pool.argtypes = [vp, vp, i, i, i, i, i, vp]
+        lib.attn_sparse_workspace_bytes.argtypes = [i, i, i, i, i, i]
+        lib.attn_sparse_workspace_bytes.restype = sz
+        lib.attn_sparse_route_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, f, i, i, vp, sz, vp, vp, vp, vp, vp]
+        lib.attn_sparse_route.argtypes = [vp, vp, vp, i, i, i, i, f, f, i, i, vp, sz, vp, vp, vp, vp, vp]
+        lib.attn_sparse_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, i, vp, vp, vp, vp, vp]
+        lib.attn_last_device_status.argtypes = [vp]
+        lib.attn_status_string.argtypes = [i]
+        lib.attn_status_string.restype = ctypes.c_char_p
+        lib.attn_selftest_wait_timeout.argtypes = [i, vp]
+        for name in ("attn_dense_fwd", "attn_cross_splitkv_fwd", "attn_lse_merge", "attn_block_pool",
+                     "attn_sparse_route_fwd", "attn_sparse_route", "attn_sparse_fwd", "attn_last_device_status",
+                     "attn_selftest_wait_timeout"):
+            getattr(lib, name).restype = ctypes.c_int
+        if path is None:
+            _lib = lib
+        return lib
+
+
+def _check(fn: str, code: int):
+    if code != 0:
+        raise AttnError(fn, code)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _bhsd(x: torch.Tensor, name: str):
+    if x.dtype != torch.bfloat16 or not x.is_cuda or x.dim() != 4 or not x.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous CUDA bf16 tensor [B, H, S, d]")
+    return x.shape
+
+
+def attn_status_string(code: int) -> str:
+    return load_library().attn_status_string(int(code)).decode()
+
+
+def attn_dense_fwd(q, k, v, scale=None, out=None, lse=None, stream=None):
+    """Dense attention; returns (out bf16 [B,H,Sq,d], lse fp32 [B,H,Sq])."""
+    lib = load_library()
+    B, H, Sq, d = _bhsd(q, "q")
+    Skv = _bhsd(k, "k")[2]
+    _bhsd(v, "v")
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    out = torch.empty_like(q) if out is None else out
+    lse = torch.empty((B, H, Sq), dtype=torch.float32, device=q.device) if lse is None else lse
+    _check("attn_dense_fwd", lib.attn_dense_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, Sq, Skv, d,
+                                                scale, _stream(stream)))
+    return out, lse
+
+
+def attn_cross_splitkv_fwd(q, k, v, n_split, scale=None, out_part=None, lse_part=None, stream=None):
+    """Split-KV partials; returns (out_part fp32 [n,B,H,Sq,d], lse_part fp32 [n,B,H,Sq])."""
+    lib = load_library()
+    B, H, Sq, d = _bhsd(q, "q")
+    Skv = _bhsd(k, "k")[2]
+    _bhsd(v, "v")
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    if out_part is None:
+        out_part = torch.empty((n_split, B, H, Sq, d), dtype=torch.float32, device=q.device)
+    if lse_part is None:
+        lse_part = torch.empty((n_split, B, H, Sq), dtype=torch.float32, device=q.device)
+    _check("attn_cross_splitkv_fwd",
+           lib.attn_cross_splitkv_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out_part), _ptr(lse_part), B, H, Sq, Skv, d,
+                                      int(n_split), scale, _stream(stream)))
+    return out_part, lse_part
+
+
+def attn_lse_merge(out_part, lse_part, out=None, lse=None, stream=None):
+    """Merge partials; returns (out bf16 [B,H,Sq,d], lse fp32 [B,H,Sq])."""
+    lib = load_library()
+    n, B, H, Sq, d = out_part.shape
+    if out is None:
+        out = torch.empty((B, H, Sq, d), dtype=torch.bfloat16, device=out_part.device)
+    if lse is None:
+        lse = torch.empty((B, H, Sq), dtype=torch.float32, device=out_part.device)
+    _check("attn_lse_merge", lib.attn_lse_merge(_ptr(out_part), _ptr(lse_part), _ptr(out), _ptr(lse), n, B, H, Sq, d,
+                                                _stream(stream)))
+    return out, lse
+
+
+def attn_block_pool(x, block, x_pool=None, stream=None):
+    """Block mean-pool; returns fp32 [B,H,ceil(S/block),d]."""
+    lib = load_library()
+    B, H, S, d = _bhsd(x, "x")
+    nb = (S + block - 1) // block
+    if x_pool is None:
+        x_pool = torch.empty((B, H, nb, d), dtype=torch.float32, device=x.device)
+    _check("attn_block_pool", lib.attn_block_pool(_ptr(x), _ptr(x_pool), B, H, S, d, int(block), _stream(stream)))
+    return x_pool
+
+
+def attn_sparse_workspace_bytes(B, H, S, d, block_q, block_k) -> int:
+    return int(load_library().attn_sparse_workspace_bytes(B, H, S, d, block_q, block_k))
+
+
+def attn_sparse_route_fwd(q, k, v, beta, block=128, scale=None, out=None, lse=None, workspace=None, route=False,
+                          stream=None):
+    """Sol-Attn block-sparse attention (pool + route + sparse forward).
+
+    Returns (out, lse) or, with route=True, (out, lse, dict(sel_idx, sel_cnt,
+    stats, taylor_t)) with the routing results as device tensors."""
+    lib = load_library()
+    B, H, S, d = _bhsd(q, "q")
+    _bhsd(k, "k")
+    _bhsd(v, "v")
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    out = torch.empty_like(q) if out is None else out
+    lse = torch.empty((B, H, S), dtype=torch.float32, device=q.device) if lse is None else lse
+    nbytes = attn_sparse_workspace_bytes(B, H, S, d, block, block)
+    if nbytes == 0:
+        raise AttnError("attn_sparse_workspace_bytes", 2)
+    if workspace is None:
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
+    extra = sparse_route_buffers(B, H, S, d, block, q.device) if route else {}
+    _check("attn_sparse_route_fwd",
+           lib.attn_sparse_route_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, S, d, scale, float(beta),
+                                     block, block, _ptr(workspace), workspace.numel(), _ptr(extra.get("sel_idx")),
+                                     _ptr(extra.get("sel_cnt")), _ptr(extra.get("stats")),
+                                     _ptr(extra.get("taylor_t")), _stream(stream)))
+    return (out, lse, extra) if route else (out, lse)
+
+
+def sparse_route_buffers(B, H, S, d, block, device):
+    """Allocates (with torch) the routing outputs of attn_sparse_route for these sizes."""
+    nq = (S + block - 1) // block
+    return dict(sel_idx=torch.empty((B, H, nq, nq), dtype=torch.int32, device=device),
+                sel_cnt=torch.empty((B, H, nq), dtype=torch.int32, device=device),
+                stats=torch.empty((B, H, nq, 4), dtype=torch.float32, device=device),
+                taylor_t=torch.empty((B, H, nq, d), dtype=torch.float32, device=device))
+
+
+def attn_sparse_route(q, k, v, beta, block=128, scale=None, route=None, workspace=None, stream=None):
+    """Pool + route only; returns the routing dict (sel_idx, sel_cnt, stats, taylor_t)."""
+    lib = load_library()
+    B, H, S, d = _bhsd(q, "q")
+    _bhsd(k, "k")
+    _bhsd(v, "v")
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    route = sparse_route_buffers(B, H, S, d, block, q.device) if route is None else route
+    nbytes = attn_sparse_workspace_bytes(B, H, S, d, block, block)
+    if nbytes == 0:
+        raise AttnError("attn_sparse_workspace_bytes", 2)
+    if workspace is None:
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
+    _check("attn_sparse_route",
+           lib.attn_sparse_route(_ptr(q), _ptr(k), _ptr(v), B, H, S, d, scale, float(beta), block, block,
+                                 _ptr(workspace), workspace.numel(), _ptr(route["sel_idx"]), _ptr(route["sel_cnt"]),
+                                 _ptr(route["stats"]), _ptr(route["taylor_t"]), _stream(stream)))
+    return route
+
+
+def attn_sparse_fwd(q, k, v, route, block=128, scale=None, out=None, lse=None, stream=None):
+    """Block-sparse forward for a given routing; returns (out, lse)."""
+    lib = load_library()
+    B, H, S, d = _bhsd(q, "q")
+    _bhsd(k, "k")
+    _bhsd(v, "v")
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    out = torch.empty_like(q) if out is None else out
+    lse = torch.empty((B, H, S), dtype=torch.float32, device=q.device) if lse is None else lse
+    _check("attn_sparse_fwd",
+           lib.attn_sparse_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, S, d, scale, block, block,
+                               _ptr(route["sel_idx"]), _ptr(route["sel_cnt"]), _ptr(route["stats"]),
+                               _ptr(route["taylor_t"]), _stream(stream)))
+    return out, lse
+
+
+def attn_last_device_status(stream=None) -> int:
+    """Synchronise the stream and return (and clear) the device status code."""
+    return int(load_library().attn_last_device_status(_stream(stream)))
+
+
+def attn_selftest_wait_timeout(limit_us: int, stream=None):
+    _check("attn_selftest_wait_timeout", load_library().attn_selftest_wait_timeout(int(limit_us), _stream(stream)))

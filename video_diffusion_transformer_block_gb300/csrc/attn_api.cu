@@ -1,0 +1,351 @@
+// C ABI of the attention hot path (declarations and contracts in attn_api.h).
+// Host-side validation, TMA descriptor encoding, workspace carving and
+// kernel launches.  Nothing here allocates device memory.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+#include <math.h>
+#include <mutex>
+#include <stdint.h>
+#include <string.h>
+
+#include "attn_api.h"
+#include "launch.h"
+
+namespace vdtb {
+
+// One status word per device; kernels receive its address.
+__device__ int g_status_word;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::once_flag g_encode_once;
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::mutex g_status_mutex;
+int* g_status_ptr[kMaxDevices] = {nullptr};
+
+bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+attn_status_t status_ptr(int** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return ATTN_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_status_mutex);
+  if (g_status_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess || p == nullptr) return ATTN_ERR_CUDA;
+    g_status_ptr[dev] = (int*)p;
+  }
+  *out = g_status_ptr[dev];
+  return ATTN_OK;
+}
+
+attn_status_t get_encoder() {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = (PFN_cuTensorMapEncodeTiled_v12000)fn;
+  });
+  return g_encode ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+// 3-D map over a [BH][S][D] bf16 tensor: dims (D, S, BH), box (64, rows, 1),
+// 128-byte swizzle; rows past S read as zero.
+attn_status_t make_map(CUtensorMap* m, const void* ptr, int D, int S, int BH, int box_rows) {
+  if (get_encoder() != ATTN_OK) return ATTN_ERR_CUDA;
+  memset(m, 0, sizeof(*m));
+  cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)S, (cuuint64_t)BH};
+  cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)S * D * 2};
+  cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, es,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+attn_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA; }
+
+bool valid_d(int d) { return d == 64 || d == 128; }
+
+cudaError_t launch_fwd(int D, int BK, int mode, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                       const FwdParams& p, cudaStream_t stream) {
+  return D == 128 ? launch_attn_fwd_d128(BK, mode, tq, tk, tv, p, stream)
+                  : launch_attn_fwd_d64(BK, mode, tq, tk, tv, p, stream);
+}
+
+FwdParams base_params(int B, int H, int Sq, int Skv, float scale, int mode, int* status) {
+  FwdParams p;
+  memset(&p, 0, sizeof(p));
+  p.BH = B * H;
+  p.Sq = Sq;
+  p.Skv = Skv;
+  const int rows_per_cta = 128 * fwd_query_tiles(mode);
+  p.n_qg = (Sq + rows_per_cta - 1) / rows_per_cta;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.status = status;
+  return p;
+}
+
+// Sizes checked once: products that index memory must fit the kernels' ranges.
+bool sizes_ok(long long B, long long H, long long S) {
+  return B >= 1 && H >= 1 && S >= 1 && B * H <= 0x7fffffffLL && S <= 0x3fffffffLL;
+}
+
+struct SparseLayout {
+  size_t qp, kp, vp, sel_idx, sel_cnt, stats, taylor, total;
+};
+
+size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+bool sparse_layout(int B, int H, int S, int d, int block_q, int block_k, SparseLayout* L) {
+  if (!sizes_ok(B, H, S) || !valid_d(d) || block_q != block_k || (block_q != 64 && block_q != 128)) return false;
+  const size_t BH = (size_t)B * H;
+  const size_t NQB = (S + block_q - 1) / block_q, NKB = (S + block_k - 1) / block_k;
+  if (NKB > 8192) return false;
+  size_t off = 0;
+  L->qp = off;
+  off = align256(off + BH * NQB * d * 4);
+  L->kp = off;
+  off = align256(off + BH * NKB * d * 4);
+  L->vp = off;
+  off = align256(off + BH * NKB * d * 4);
+  L->sel_idx = off;
+  off = align256(off + BH * NQB * NKB * 4);
+  L->sel_cnt = off;
+  off = align256(off + BH * NQB * 4);
+  L->stats = off;
+  off = align256(off + BH * NQB * 4 * 4);
+  L->taylor = off;
+  off = align256(off + BH * NQB * d * 4);
+  L->total = off;
+  return true;
+}
+
+}  // namespace
+}  // namespace vdtb
+
+using namespace vdtb;
+
+extern "C" {
+
+const char* attn_status_string(attn_status_t status) {
+  switch (status) {
+    case ATTN_OK: return "ATTN_OK";
+    case ATTN_ERR_INVALID_ARG: return "ATTN_ERR_INVALID_ARG";
+    case ATTN_ERR_UNSUPPORTED: return "ATTN_ERR_UNSUPPORTED";
+    case ATTN_ERR_WORKSPACE: return "ATTN_ERR_WORKSPACE";
+    case ATTN_ERR_CUDA: return "ATTN_ERR_CUDA";
+    case ATTN_ERR_TIMEOUT: return "ATTN_ERR_TIMEOUT";
+  }
+  return "ATTN_ERR_UNKNOWN";
+}
+
+attn_status_t attn_dense_fwd(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v, attn_bf16* out, float* lse,
+                             int B, int H, int Sq, int Skv, int d, float scale, cudaStream_t stream) {
+  if (!q || !k || !v || !out) return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || (lse && ((uintptr_t)lse & 3u)))
+    return ATTN_ERR_INVALID_ARG;
+  if (!sizes_ok(B, H, Sq) || !sizes_ok(B, H, Skv) || !isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+  if (!valid_d(d)) return ATTN_ERR_UNSUPPORTED;
+  int* status = nullptr;
+  attn_status_t st = status_ptr(&status);
+  if (st != ATTN_OK) return st;
+  CUtensorMap tq, tk, tv;
+  if ((st = make_map(&tq, q, d, Sq, B * H, 128)) != ATTN_OK) return st;
+  if ((st = make_map(&tk, k, d, Skv, B * H, 128)) != ATTN_OK) return st;
+  if ((st = make_map(&tv, v, d, Skv, B * H, 128)) != ATTN_OK) return st;
+  FwdParams p = base_params(B, H, Sq, Skv, scale, kModeDense, status);
+  p.out = out;
+  p.lse = lse;
+  return cuda_status(launch_fwd(d, 128, kModeDense, tq, tk, tv, p, stream));
+}
+
+attn_status_t attn_cross_splitkv_fwd(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v, float* out_part,
+                                     float* lse_part, int B, int H, int Sq, int Skv, int d, int n_split, float scale,
+                                     cudaStream_t stream) {
+  if (!q || !k || !v || !out_part || !lse_part) return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out_part) || ((uintptr_t)lse_part & 3u))
+    return ATTN_ERR_INVALID_ARG;
+  if (!sizes_ok(B, H, Sq) || !sizes_ok(B, H, Skv) || !isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+  if (n_split < 1 || n_split > Skv) return ATTN_ERR_INVALID_ARG;
+  if (!valid_d(d)) return ATTN_ERR_UNSUPPORTED;
+  int* status = nullptr;
+  attn_status_t st = status_ptr(&status);
+  if (st != ATTN_OK) return st;
+  CUtensorMap tq, tk, tv;
+  if ((st = make_map(&tq, q, d, Sq, B * H, 128)) != ATTN_OK) return st;
+  if ((st = make_map(&tk, k, d, Skv, B * H, 128)) != ATTN_OK) return st;
+  if ((st = make_map(&tv, v, d, Skv, B * H, 128)) != ATTN_OK) return st;
+  FwdParams p = base_params(B, H, Sq, Skv, scale, kModeSplit, status);
+  p.out_part = out_part;
+  p.lse_part = lse_part;
+  p.n_split = n_split;
+  return cuda_status(launch_fwd(d, 128, kModeSplit, tq, tk, tv, p, stream));
+}
+
+attn_status_t attn_lse_merge(const float* out_part, const float* lse_part, attn_bf16* out, float* lse, int n_split,
+                             int B, int H, int Sq, int d, cudaStream_t stream) {
+  if (!out_part || !lse_part || !out) return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(out_part) || ((uintptr_t)lse_part & 3u) || !aligned16(out) || (lse && ((uintptr_t)lse & 3u)))
+    return ATTN_ERR_INVALID_ARG;
+  if (!sizes_ok(B, H, Sq) || n_split < 1) return ATTN_ERR_INVALID_ARG;
+  if (!valid_d(d)) return ATTN_ERR_UNSUPPORTED;
+  const long long rows = (long long)B * H * Sq;
+  return cuda_status(launch_merge(out_part, lse_part, out, lse, n_split, rows, d, stream));
+}
+
+attn_status_t attn_block_pool(const attn_bf16* x, float* x_pool, int B, int H, int S, int d, int block,
+                              cudaStream_t stream) {
+  if (!x || !x_pool || !aligned16(x) || !aligned16(x_pool)) return ATTN_ERR_INVALID_ARG;
+  if (!sizes_ok(B, H, S)) return ATTN_ERR_INVALID_ARG;
+  if (!valid_d(d) || (block != 64 && block != 128)) return ATTN_ERR_UNSUPPORTED;
+  return cuda_status(launch_pool(x, x, x, x_pool, x_pool, x_pool, 1, B * H, S, d, block, stream));
+}
+
+size_t attn_sparse_workspace_bytes(int B, int H, int S, int d, int block_q, int block_k) {
+  SparseLayout L;
+  if (!sparse_layout(B, H, S, d, block_q, block_k, &L)) return 0;
+  return L.total;
+}
+
+namespace {
+
+struct SparseArgs {
+  const attn_bf16 *q, *k, *v;
+  int B, H, S, d, block_q, block_k;
+  float scale;
+};
+
+attn_status_t sparse_common_checks(const SparseArgs& a) {
+  if (!a.q || !a.k || !a.v) return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(a.q) || !aligned16(a.k) || !aligned16(a.v)) return ATTN_ERR_INVALID_ARG;
+  if (!sizes_ok(a.B, a.H, a.S) || !isfinite(a.scale)) return ATTN_ERR_INVALID_ARG;
+  if (!valid_d(a.d) || a.block_q != a.block_k || (a.block_q != 64 && a.block_q != 128)) return ATTN_ERR_UNSUPPORTED;
+  SparseLayout L;
+  if (!sparse_layout(a.B, a.H, a.S, a.d, a.block_q, a.block_k, &L)) return ATTN_ERR_UNSUPPORTED;
+  return ATTN_OK;
+}
+
+attn_status_t run_route(const SparseArgs& a, float beta, void* workspace, size_t workspace_bytes, int32_t* si,
+                        int32_t* sc, float* stt, float* tt, cudaStream_t stream) {
+  SparseLayout L;
+  sparse_layout(a.B, a.H, a.S, a.d, a.block_q, a.block_k, &L);
+  if (!workspace || ((uintptr_t)workspace & 255u) || workspace_bytes < L.total) return ATTN_ERR_WORKSPACE;
+  uint8_t* ws = (uint8_t*)workspace;
+  float* qp = (float*)(ws + L.qp);
+  float* kp = (float*)(ws + L.kp);
+  float* vp = (float*)(ws + L.vp);
+  const int BH = a.B * a.H;
+  const int NQB = (a.S + a.block_q - 1) / a.block_q, NKB = (a.S + a.block_k - 1) / a.block_k;
+  if (launch_pool(a.q, a.k, a.v, qp, kp, vp, 3, BH, a.S, a.d, a.block_q, stream) != cudaSuccess) return ATTN_ERR_CUDA;
+  if (launch_route(qp, kp, vp, BH, NQB, NKB, a.S, a.d, a.block_k, a.scale, beta, si, sc, stt, tt, stream) !=
+      cudaSuccess)
+    return ATTN_ERR_CUDA;
+  return ATTN_OK;
+}
+
+attn_status_t run_sparse_fwd(const SparseArgs& a, attn_bf16* out, float* lse, const int32_t* si, const int32_t* sc,
+                             const float* stt, const float* tt, cudaStream_t stream) {
+  int* status = nullptr;
+  attn_status_t st = status_ptr(&status);
+  if (st != ATTN_OK) return st;
+  const int BH = a.B * a.H;
+  CUtensorMap tq, tk, tv;
+  if ((st = make_map(&tq, a.q, a.d, a.S, BH, 128)) != ATTN_OK) return st;
+  if ((st = make_map(&tk, a.k, a.d, a.S, BH, a.block_k)) != ATTN_OK) return st;
+  if ((st = make_map(&tv, a.v, a.d, a.S, BH, a.block_k)) != ATTN_OK) return st;
+  FwdParams p = base_params(a.B, a.H, a.S, a.S, a.scale, kModeSparse, status);
+  p.out = out;
+  p.lse = lse;
+  p.sel_idx = si;
+  p.sel_cnt = sc;
+  p.stats = stt;
+  p.taylor_t = tt;
+  p.NQB = (a.S + a.block_q - 1) / a.block_q;
+  p.NKB = (a.S + a.block_k - 1) / a.block_k;
+  return cuda_status(launch_fwd(a.d, a.block_k, kModeSparse, tq, tk, tv, p, stream));
+}
+
+bool bad_opt_ptrs(const int32_t* si, const int32_t* sc, const float* stt, const float* tt) {
+  return (si && ((uintptr_t)si & 3u)) || (sc && ((uintptr_t)sc & 3u)) || (stt && !aligned16(stt)) ||
+         (tt && !aligned16(tt));
+}
+
+}  // namespace
+
+attn_status_t attn_sparse_route(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v, int B, int H, int S,
+                                int d, float scale, float beta, int block_q, int block_k, void* workspace,
+                                size_t workspace_bytes, int32_t* sel_idx, int32_t* sel_cnt, float* stats,
+                                float* taylor_t, cudaStream_t stream) {
+  SparseArgs a{q, k, v, B, H, S, d, block_q, block_k, scale};
+  attn_status_t st = sparse_common_checks(a);
+  if (st != ATTN_OK) return st;
+  if (!sel_idx || !sel_cnt || !stats || !taylor_t || bad_opt_ptrs(sel_idx, sel_cnt, stats, taylor_t) || isnan(beta) ||
+      beta == INFINITY)
+    return ATTN_ERR_INVALID_ARG;
+  return run_route(a, beta, workspace, workspace_bytes, sel_idx, sel_cnt, stats, taylor_t, stream);
+}
+
+attn_status_t attn_sparse_fwd(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v, attn_bf16* out, float* lse,
+                              int B, int H, int S, int d, float scale, int block_q, int block_k,
+                              const int32_t* sel_idx, const int32_t* sel_cnt, const float* stats,
+                              const float* taylor_t, cudaStream_t stream) {
+  SparseArgs a{q, k, v, B, H, S, d, block_q, block_k, scale};
+  attn_status_t st = sparse_common_checks(a);
+  if (st != ATTN_OK) return st;
+  if (!out || !aligned16(out) || (lse && ((uintptr_t)lse & 3u))) return ATTN_ERR_INVALID_ARG;
+  if (!sel_idx || !sel_cnt || !stats || !taylor_t || bad_opt_ptrs(sel_idx, sel_cnt, stats, taylor_t))
+    return ATTN_ERR_INVALID_ARG;
+  return run_sparse_fwd(a, out, lse, sel_idx, sel_cnt, stats, taylor_t, stream);
+}
+
+attn_status_t attn_sparse_route_fwd(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v, attn_bf16* out,
+                                    float* lse, int B, int H, int S, int d, float scale, float beta, int block_q,
+                                    int block_k, void* workspace, size_t workspace_bytes, int32_t* sel_idx,
+                                    int32_t* sel_cnt, float* stats, float* taylor_t, cudaStream_t stream) {
+  SparseArgs a{q, k, v, B, H, S, d, block_q, block_k, scale};
+  attn_status_t st = sparse_common_checks(a);
+  if (st != ATTN_OK) return st;
+  if (!out || !aligned16(out) || (lse && ((uintptr_t)lse & 3u)) || bad_opt_ptrs(sel_idx, sel_cnt, stats, taylor_t))
+    return ATTN_ERR_INVALID_ARG;
+  if (isnan(beta) || beta == INFINITY) return ATTN_ERR_INVALID_ARG;
+  SparseLayout L;
+  sparse_layout(B, H, S, d, block_q, block_k, &L);
+  if (!workspace || ((uintptr_t)workspace & 255u) || workspace_bytes < L.total) return ATTN_ERR_WORKSPACE;
+  uint8_t* ws = (uint8_t*)workspace;
+  int32_t* si = sel_idx ? sel_idx : (int32_t*)(ws + L.sel_idx);
+  int32_t* sc = sel_cnt ? sel_cnt : (int32_t*)(ws + L.sel_cnt);
+  float* stt = stats ? stats : (float*)(ws + L.stats);
+  float* tt = taylor_t ? taylor_t : (float*)(ws + L.taylor);
+  if ((st = run_route(a, beta, workspace, workspace_bytes, si, sc, stt, tt, stream)) != ATTN_OK) return st;
+  return run_sparse_fwd(a, out, lse, si, sc, stt, tt, stream);
+}
+
+attn_status_t attn_last_device_status(cudaStream_t stream) {
+  int* status = nullptr;
+  attn_status_t st = status_ptr(&status);
+  if (st != ATTN_OK) return st;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return ATTN_ERR_CUDA;
+  int word = 0;
+  if (cudaMemcpy(&word, status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return ATTN_ERR_CUDA;
+  if (word != 0) {
+    const int zero = 0;
+    if (cudaMemcpy(status, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) return ATTN_ERR_CUDA;
+  }
+  if (word & ATTN_DEVICE_TIMEOUT) return ATTN_ERR_TIMEOUT;
+  if (word & ATTN_DEVICE_BAD_LIST) return ATTN_ERR_INVALID_ARG;
+  return ATTN_OK;
+}
+
+attn_status_t attn_selftest_wait_timeout(int limit_us, cudaStream_t stream) {
+  if (limit_us < 1 || limit_us > 1000000) return ATTN_ERR_INVALID_ARG;
+  int* status = nullptr;
+  attn_status_t st = status_ptr(&status);
+  if (st != ATTN_OK) return st;
+  return cuda_status(launch_wait_selftest(limit_us, status, stream));
+}
+
+}  // extern "C"

@@ -1,0 +1,528 @@
+// tcgen05 attention forward for sm_103a: dense, block-sparse (selected-block
+// lists + Taylor term) and split-KV (chunk partials) share one main loop.
+//
+// CTA = NQT query tiles of 128 rows that share every K/V tile load.
+//   warps 0..4*NQT-1 : softmax/epilogue, one warpgroup per query tile; thread
+//                      r of the warpgroup owns query row r = TMEM lane r
+//   warp  4*NQT      : TMA producer (Q once, then K_s, V_s for every step s
+//                      into a ring of NSTAGE slots)
+//   warp  4*NQT+1    : tcgen05 MMA issuer (one thread); allocates TMEM
+// TMEM, per query tile t: S_t at columns [256t, 256t+BK) in fp32; P_t (bf16
+// pairs) overwrites the first BK/2 columns of S_t; O_t at [256t+128, +D).
+// Per step s: S_t = Q_t K_s^T (SS MMA, both K-major, 128B swizzle), softmax
+// writes P_t, O_t += P_t V_s (TS MMA, P from TMEM, V MN-major).  The MMA
+// thread issues PV_t(s-1) immediately before S_t(s), so the tensor pipe
+// works on one tile while the other tile's softmax runs.
+// Online softmax in base 2 with a lazy rescale: the running max is only
+// moved (and O_t rescaled in TMEM) when a tile's max exceeds it by more than
+// kRescaleLog2, so P stays <= 2^kRescaleLog2 and the final normalisation by
+// the same stale max is exact.
+#pragma once
+#include <float.h>
+#include <limits.h>
+#include "ptx.cuh"
+
+namespace vdtb {
+
+enum FwdMode { kModeDense = 0, kModeSparse = 1, kModeSplit = 2 };
+
+constexpr float kRescaleLog2 = 8.0f;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+struct FwdParams {
+  int BH;             // B * H
+  int Sq, Skv;        // query rows, key rows (per head)
+  int n_qg;           // CTA query groups per head = ceil(Sq / (128 * NQT))
+  float scale_log2;   // softmax scale * log2(e)
+  uint16_t* out;      // dense/sparse: [BH][Sq][D] bf16
+  float* lse;         // dense/sparse: [BH][Sq] (nullable)
+  float* out_part;    // split: [n_split][BH][Sq][D]
+  float* lse_part;    // split: [n_split][BH][Sq]
+  int n_split;
+  const int32_t* sel_idx;  // sparse: [BH][NQB][NKB]
+  const int32_t* sel_cnt;  // sparse: [BH][NQB]
+  const float* stats;      // sparse: [BH][NQB][4] = mu, sigma, tau, W
+  const float* taylor_t;   // sparse: [BH][NQB][D]
+  int NQB, NKB;
+  int* status;             // device status word
+};
+
+// Walks the ascending union of up to 4 tile lists (one per query block the
+// CTA owns).  Each step yields the kv tile index and a bit per list that
+// contains it.  Dense/split lists are implicit ranges [0, n).
+struct TileMerge {
+  const int32_t* ptr[4];
+  int n[4];
+  int pos[4];
+  int nlists;
+  int limit;      // valid tile indices are [0, limit)
+  bool implicit;
+  int* status;
+
+  __device__ __forceinline__ int head(int l) const {
+    if (implicit) return pos[l];
+    int v = __ldg(ptr[l] + pos[l]);
+    if ((unsigned)v >= (unsigned)limit) {
+      atomicOr(status, ATTN_DEVICE_BAD_LIST);
+      v = v < 0 ? 0 : limit - 1;
+    }
+    return v;
+  }
+  // Returns the next tile index, or -1 when every list is exhausted.
+  __device__ __forceinline__ int next(uint32_t& flags) {
+    int u = INT_MAX;
+    int h[4];
+#pragma unroll
+    for (int l = 0; l < 4; ++l) {
+      h[l] = INT_MAX;
+      if (l < nlists && pos[l] < n[l]) h[l] = head(l);
+      u = min(u, h[l]);
+    }
+    if (u == INT_MAX) return -1;
+    flags = 0;
+#pragma unroll
+    for (int l = 0; l < 4; ++l)
+      if (h[l] == u) {
+        flags |= 1u << l;
+        ++pos[l];
+      }
+    return u;
+  }
+};
+
+template <int D, int BK, int MODE, int NQT, int NSTAGE>
+struct FwdCfg {
+  static constexpr int QB = (MODE == kModeSparse) ? 128 / BK : 1;   // query blocks per 128-row tile
+  static constexpr int kThreads = NQT * 128 + 64;
+  static constexpr int kProducerWarp = NQT * 4;
+  static constexpr int kMmaWarp = NQT * 4 + 1;
+  static constexpr int kQTileBytes = 128 * D * 2;
+  static constexpr int kSlotBytes = BK * D * 2;
+  // A two-tile CTA takes all 512 TMEM columns: its shared-memory request is
+  // padded past half of the SM's 228 KB so that two such CTAs never share an
+  // SM (the second would stall in tcgen05.alloc until the first exits).
+  static constexpr int kSmemRaw = 1024 + NQT * kQTileBytes + NSTAGE * kSlotBytes;
+  static constexpr int kSmemBytes = (NQT == 2 && kSmemRaw < 120 * 1024) ? 120 * 1024 : kSmemRaw;
+  static constexpr uint32_t kTmemCols = NQT == 2 ? 512 : 256;
+  static constexpr uint32_t kIdescS = idesc_bf16_f32(128, BK, 0, 0);
+  static constexpr uint32_t kIdescPV = idesc_bf16_f32(128, D, 0, 1);
+  static_assert(D == 64 || D == 128, "head dim");
+  static_assert(BK == 64 || BK == 128, "kv tile");
+  static_assert(NQT == 1 || NQT == 2, "query tiles per CTA");
+  static_assert(NQT * QB <= 4, "lists per CTA");
+  static_assert(NSTAGE >= 2, "ring depth");
+};
+
+template <int D, int BK, int MODE, int NQT, int NSTAGE>
+__global__ void __launch_bounds__(NQT * 128 + 64, (NQT == 1) ? 2 : 1)
+    attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
+  using Cfg = FwdCfg<D, BK, MODE, NQT, NSTAGE>;
+  constexpr int QB = Cfg::QB;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  uint8_t* sQ = smem;
+  uint8_t* sKV = smem + NQT * Cfg::kQTileBytes;
+
+  __shared__ uint64_t bar_q;
+  __shared__ uint64_t bar_full[NSTAGE], bar_empty[NSTAGE];
+  __shared__ uint64_t bar_s[NQT], bar_p[NQT], bar_o[NQT];
+  __shared__ uint64_t bar_mma_done, bar_drain;
+  __shared__ uint32_t tmem_base_sh;
+  __shared__ volatile int abort_flag;
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5, lane = tid & 31;
+
+  // ---- work item
+  int linear = blockIdx.x;
+  const int qg = linear % p.n_qg;
+  linear /= p.n_qg;
+  const int bh = linear % p.BH;
+  const int chunk = (MODE == kModeSplit) ? linear / p.BH : 0;
+  const int q_row0 = qg * NQT * 128;
+  int kv_lo = 0, kv_hi = p.Skv;
+  if (MODE == kModeSplit) {
+    kv_lo = (int)(((long long)chunk * p.Skv) / p.n_split);
+    kv_hi = (int)(((long long)(chunk + 1) * p.Skv) / p.n_split);
+  }
+  int n_valid_tiles = 0;
+#pragma unroll
+  for (int t = 0; t < NQT; ++t)
+    if (q_row0 + t * 128 < p.Sq) n_valid_tiles = t + 1;
+
+  TileMerge merge;
+  merge.status = p.status;
+  if (MODE == kModeSparse) {
+    merge.implicit = false;
+    merge.nlists = NQT * QB;
+    merge.limit = p.NKB;
+#pragma unroll
+    for (int l = 0; l < 4; ++l) {
+      merge.pos[l] = 0;
+      merge.n[l] = 0;
+      merge.ptr[l] = p.sel_idx;
+      if (l < NQT * QB) {
+        long long i = (long long)(qg * NQT + l / QB) * QB + (l % QB);
+        if (i < p.NQB) {
+          long long row = (long long)bh * p.NQB + i;
+          int c = __ldg(p.sel_cnt + row);
+          merge.n[l] = c < 0 ? 0 : (c > p.NKB ? p.NKB : c);
+          merge.ptr[l] = p.sel_idx + row * p.NKB;
+        }
+      }
+    }
+  } else {
+    merge.implicit = true;
+    merge.nlists = n_valid_tiles;
+    int nt = (kv_hi - kv_lo + BK - 1) / BK;
+    merge.limit = nt;
+#pragma unroll
+    for (int l = 0; l < 4; ++l) {
+      merge.pos[l] = 0;
+      merge.n[l] = nt;
+      merge.ptr[l] = nullptr;
+    }
+  }
+
+  // ---- setup
+  if (tid == 0) {
+    mbar_init(&bar_q, 1);
+    for (int s = 0; s < NSTAGE; ++s) {
+      mbar_init(&bar_full[s], 1);
+      mbar_init(&bar_empty[s], 1);
+    }
+    for (int t = 0; t < NQT; ++t) {
+      mbar_init(&bar_s[t], 1);
+      mbar_init(&bar_p[t], 128);
+      mbar_init(&bar_o[t], 1);
+    }
+    mbar_init(&bar_mma_done, 1);
+    mbar_init(&bar_drain, 1);
+    abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == Cfg::kMmaWarp) tmem_alloc(&tmem_base_sh, Cfg::kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base_sh;
+
+  if (warp == Cfg::kProducerWarp) {
+    // ======================= TMA producer =======================
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      mbar_expect_tx(&bar_q, n_valid_tiles * Cfg::kQTileBytes);
+      for (int t = 0; t < n_valid_tiles; ++t)
+        for (int h = 0; h < D / 64; ++h)
+          tma_load_3d(sQ + t * Cfg::kQTileBytes + h * 16384, &tm_q, &bar_q, h * 64, q_row0 + t * 128, bh);
+      int ld = 0;
+      uint32_t flags;
+      int u;
+      bool ok = true;
+      while (ok && (u = merge.next(flags)) >= 0) {
+        const int row = kv_lo + u * BK;
+#pragma unroll
+        for (int kv = 0; kv < 2; ++kv) {
+          const int slot = ld % NSTAGE;
+          if (ld >= NSTAGE && !bounded_wait(&bar_empty[slot], ((ld / NSTAGE) - 1) & 1, &abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+          uint8_t* dst = sKV + slot * Cfg::kSlotBytes;
+          mbar_expect_tx(&bar_full[slot], Cfg::kSlotBytes);
+          for (int h = 0; h < D / 64; ++h)
+            tma_load_3d(dst + h * (BK * 128), kv == 0 ? &tm_k : &tm_v, &bar_full[slot], h * 64, row, bh);
+          ++ld;
+        }
+      }
+      // drain: make sure no copy is still landing when the CTA exits
+      bounded_wait(&bar_q, 0, nullptr, p.status);
+      for (int j = (ld > NSTAGE ? ld - NSTAGE : 0); j < ld; ++j) bounded_wait(&bar_full[j % NSTAGE], (j / NSTAGE) & 1, nullptr, p.status);
+    }
+  } else if (warp == Cfg::kMmaWarp) {
+    // ======================= MMA issuer =======================
+    if (lane == 0) {
+      bool ok = bounded_wait(&bar_q, 0, &abort_flag, p.status);
+      tc_fence_after();
+      const uint32_t q_base = smem_u32(sQ);
+      const uint32_t kv_base = smem_u32(sKV);
+      int ld = 0;
+      bool pending[NQT];
+      int pv_count[NQT];
+#pragma unroll
+      for (int t = 0; t < NQT; ++t) {
+        pending[t] = false;
+        pv_count[t] = 0;
+      }
+      int prev_vslot = -1, prev_vpar = 0;
+      uint32_t flags;
+      int u;
+      auto issue_pv = [&](int t, int vslot) {
+        const uint32_t v_addr = kv_base + vslot * Cfg::kSlotBytes;
+        const uint32_t d_tmem = tmem + t * 256 + 128;
+        const uint32_t p_tmem = tmem + t * 256;
+#pragma unroll
+        for (int kk = 0; kk < BK / 16; ++kk) {
+          uint64_t bdesc = smem_desc_sw128(v_addr + kk * 16 * 128, BK * 128, 1024);
+          mma_ts(d_tmem, p_tmem + kk * 8, bdesc, Cfg::kIdescPV, (pv_count[t] > 0 || kk > 0) ? 1u : 0u);
+        }
+        mma_commit(&bar_o[t]);
+        ++pv_count[t];
+        pending[t] = false;
+      };
+      while (ok && (u = merge.next(flags)) >= 0) {
+        const int kslot = ld % NSTAGE;
+        if (!bounded_wait(&bar_full[kslot], (ld / NSTAGE) & 1, &abort_flag, p.status)) break;
+        ++ld;
+        const int vslot = ld % NSTAGE;
+        const int vpar = (ld / NSTAGE) & 1;
+        ++ld;
+        tc_fence_after();
+        bool prev_v_ready = false, any_pv = false;
+#pragma unroll
+        for (int t = 0; t < NQT; ++t) {
+          if (pending[t]) {
+            if (!prev_v_ready) {
+              if (!bounded_wait(&bar_full[prev_vslot], prev_vpar, &abort_flag, p.status)) { ok = false; break; }
+              prev_v_ready = true;
+            }
+            if (!bounded_wait(&bar_p[t], pv_count[t] & 1, &abort_flag, p.status)) { ok = false; break; }
+            tc_fence_after();
+            issue_pv(t, prev_vslot);
+            any_pv = true;
+          }
+          if ((flags >> (t * QB)) & ((1u << QB) - 1u)) {
+            const uint32_t k_addr = kv_base + kslot * Cfg::kSlotBytes;
+            const uint32_t qa = q_base + t * Cfg::kQTileBytes;
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+              uint64_t adesc = smem_desc_sw128(qa + (kk / 4) * 16384 + (kk % 4) * 32, 16, 1024);
+              uint64_t bdesc = smem_desc_sw128(k_addr + (kk / 4) * (BK * 128) + (kk % 4) * 32, 16, 1024);
+              mma_ss(tmem + t * 256, adesc, bdesc, Cfg::kIdescS, kk > 0 ? 1u : 0u);
+            }
+            mma_commit(&bar_s[t]);
+            pending[t] = true;
+          }
+        }
+        if (!ok) break;
+        mma_commit(&bar_empty[kslot]);
+        if (any_pv) mma_commit(&bar_empty[prev_vslot]);
+        prev_vslot = vslot;
+        prev_vpar = vpar;
+      }
+      if (ok) {
+        bool any_pv = false, v_ready = false;
+#pragma unroll
+        for (int t = 0; t < NQT; ++t) {
+          if (!pending[t]) continue;
+          if (!v_ready) {
+            if (!bounded_wait(&bar_full[prev_vslot], prev_vpar, &abort_flag, p.status)) break;
+            v_ready = true;
+          }
+          if (!bounded_wait(&bar_p[t], pv_count[t] & 1, &abort_flag, p.status)) break;
+          tc_fence_after();
+          issue_pv(t, prev_vslot);
+          any_pv = true;
+        }
+        if (any_pv) mma_commit(&bar_empty[prev_vslot]);
+      }
+      // every MMA issued by this thread has completed before TMEM is released
+      mma_commit(&bar_mma_done);
+      bounded_wait(&bar_mma_done, 0, nullptr, p.status);
+    }
+  } else {
+    // ======================= softmax + epilogue =======================
+    const int t = warp >> 2;
+    const int w4 = warp & 3;
+    const int r = w4 * 32 + lane;                  // row within the tile = TMEM lane
+    const int grow = q_row0 + t * 128 + r;         // row within the head
+    const bool row_valid = grow < p.Sq;
+    const int qb = (QB == 2) ? (w4 >> 1) : 0;      // warp-uniform
+    const uint32_t my_bit = 1u << (t * QB + qb);
+    const uint32_t tile_mask = ((1u << QB) - 1u) << (t * QB);
+    const uint32_t lane_base = (uint32_t)(w4 * 32) << 16;
+    const uint32_t tS = tmem + lane_base + t * 256;
+    const uint32_t tO = tS + 128;
+    float m_run = -INFINITY;
+    float l_run = 0.f;
+    int it = 0;
+    uint32_t flags;
+    int u;
+    bool ok = t < n_valid_tiles;
+    while (ok && (u = merge.next(flags)) >= 0) {
+      if (!(flags & tile_mask)) continue;
+      if (!__all_sync(0xffffffffu, bounded_wait(&bar_s[t], it & 1, &abort_flag, p.status))) break;
+      tc_fence_after();
+      float x[BK];
+      {
+        uint32_t rr[BK / 32][32];
+#pragma unroll
+        for (int c = 0; c < BK / 32; ++c) tmem_ld32(tS + c * 32, rr[c]);
+        tmem_ld_wait();
+#pragma unroll
+        for (int c = 0; c < BK / 32; ++c) {
+          tmem_reg_fence(rr[c]);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) x[c * 32 + j] = __uint_as_float(rr[c][j]);
+        }
+      }
+      const int n_valid = min(BK, kv_hi - (kv_lo + u * BK));
+      const bool mine = (flags & my_bit) != 0;
+      float mt = -INFINITY;
+      if (mine && n_valid == BK) {
+#pragma unroll
+        for (int c = 0; c < BK; ++c) {
+          x[c] *= p.scale_log2;
+          mt = fmaxf(mt, x[c]);
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < BK; ++c) {
+          x[c] = (mine && c < n_valid) ? x[c] * p.scale_log2 : -INFINITY;
+          mt = fmaxf(mt, x[c]);
+        }
+      }
+      // lazy rescale of the running max
+      float alpha = 1.f;
+      bool need = mt > m_run + kRescaleLog2 || (m_run == -INFINITY && mt > -INFINITY);
+      if (need) {
+        alpha = (m_run == -INFINITY) ? 0.f : ex2_approx(m_run - mt);
+        l_run *= alpha;
+        m_run = mt;
+      }
+      if (__any_sync(0xffffffffu, need && alpha != 0.f && it > 0)) {
+        // O_t holds the sum over earlier steps: wait for the last PV, rescale in TMEM
+        if (!__all_sync(0xffffffffu, bounded_wait(&bar_o[t], (it - 1) & 1, &abort_flag, p.status))) break;
+        tc_fence_after();
+        const float a = (need && it > 0) ? alpha : 1.f;
+#pragma unroll
+        for (int c0 = 0; c0 < D; c0 += 32) {
+          uint32_t rr[32];
+          tmem_ld32(tO + c0, rr);
+          tmem_ld_wait();
+          tmem_reg_fence(rr);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) rr[j] = __float_as_uint(__uint_as_float(rr[j]) * a);
+          tmem_st32(tO + c0, rr);
+        }
+      }
+      const float base = (m_run == -INFINITY) ? 0.f : m_run;
+      float ls0 = 0.f, ls1 = 0.f;
+#pragma unroll
+      for (int c0 = 0; c0 < BK; c0 += 64) {
+        uint32_t pk[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          float p0 = ex2_approx(x[c0 + 2 * j] - base);
+          float p1 = ex2_approx(x[c0 + 2 * j + 1] - base);
+          ls0 += p0;
+          ls1 += p1;
+          pk[j] = pack_bf16x2(p0, p1);
+        }
+        tmem_st32(tS + c0 / 2, pk);
+      }
+      l_run += ls0 + ls1;
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&bar_p[t]);
+      ++it;
+    }
+    // ---- epilogue
+    if (t < n_valid_tiles && !abort_flag) {
+      bool have_o = it > 0;
+      if (have_o && !__all_sync(0xffffffffu, bounded_wait(&bar_o[t], (it - 1) & 1, &abort_flag, p.status))) have_o = false;
+      tc_fence_after();
+      if (MODE == kModeSplit) {
+        const bool empty = !have_o || l_run == 0.f;
+        const float inv = empty ? 0.f : 1.f / l_run;
+        const long long orow = ((long long)chunk * p.BH + bh) * p.Sq + grow;
+        float* dst = p.out_part + orow * D;
+#pragma unroll
+        for (int c0 = 0; c0 < D; c0 += 32) {
+          uint32_t rr[32];
+          if (have_o) {
+            tmem_ld32(tO + c0, rr);
+            tmem_ld_wait();
+            tmem_reg_fence(rr);
+          }
+          if (row_valid) {
+#pragma unroll
+            for (int j = 0; j < 32; j += 4) {
+              float4 o4;
+              o4.x = have_o ? __uint_as_float(rr[j]) * inv : 0.f;
+              o4.y = have_o ? __uint_as_float(rr[j + 1]) * inv : 0.f;
+              o4.z = have_o ? __uint_as_float(rr[j + 2]) * inv : 0.f;
+              o4.w = have_o ? __uint_as_float(rr[j + 3]) * inv : 0.f;
+              *reinterpret_cast<float4*>(dst + c0 + j) = o4;
+            }
+          }
+        }
+        if (row_valid) p.lse_part[orow] = empty ? -INFINITY : (m_run + __log2f(l_run)) * kLn2;
+      } else {
+        // Taylor term for the rejected blocks of this row's query block
+        float f = 0.f;
+        const float* tt = nullptr;
+        if (MODE == kModeSparse) {
+          const long long qbi = (long long)(qg * NQT + t) * QB + qb;
+          if (qbi < p.NQB) {
+            const long long srow = (long long)bh * p.NQB + qbi;
+            const int cnt = __ldg(p.sel_cnt + srow);
+            if (cnt < p.NKB) {
+              const float mu = __ldg(p.stats + srow * 4 + 0);
+              const float W = __ldg(p.stats + srow * 4 + 3);
+              f = ex2_approx(mu * kLog2e - m_run);
+              l_run += f * W;
+              tt = p.taylor_t + srow * D;
+            }
+          }
+        }
+        const bool empty = !have_o || !(l_run > 0.f);
+        if (empty && row_valid && it == 0 && MODE == kModeSparse) atomicOr(p.status, ATTN_DEVICE_BAD_LIST);
+        const float inv = empty ? 0.f : 1.f / l_run;
+        uint16_t* dst = p.out + ((long long)bh * p.Sq + grow) * D;
+#pragma unroll
+        for (int c0 = 0; c0 < D; c0 += 32) {
+          uint32_t rr[32];
+          if (have_o) {
+            tmem_ld32(tO + c0, rr);
+            tmem_ld_wait();
+            tmem_reg_fence(rr);
+          }
+          if (row_valid) {
+#pragma unroll
+            for (int j = 0; j < 32; j += 8) {
+              uint4 pk;
+              float o[8];
+#pragma unroll
+              for (int e = 0; e < 8; ++e) {
+                float val = have_o ? __uint_as_float(rr[j + e]) : 0.f;
+                if (tt != nullptr) val = fmaf(f, __ldg(tt + c0 + j + e), val);
+                o[e] = val * inv;
+              }
+              pk.x = pack_bf16x2(o[0], o[1]);
+              pk.y = pack_bf16x2(o[2], o[3]);
+              pk.z = pack_bf16x2(o[4], o[5]);
+              pk.w = pack_bf16x2(o[6], o[7]);
+              *reinterpret_cast<uint4*>(dst + c0 + j) = pk;
+            }
+          }
+        }
+        if (row_valid && p.lse != nullptr)
+          p.lse[(long long)bh * p.Sq + grow] = empty ? -INFINITY : (m_run + __log2f(l_run)) * kLn2;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == Cfg::kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem, Cfg::kTmemCols);
+  }
+}
+
+}  // namespace vdtb
