@@ -172,12 +172,12 @@ def executed_sparse_flops(sel_idx: torch.Tensor, sel_cnt: torch.Tensor, S: int, 
 
 # ============================================================ native arm
 
-def make_inputs(rank: int, beta: float):
+def make_inputs(rank: int, beta: float, heads: int):
     w = WORKLOADS["sparse64k"]
-    wr = Workload(w.name, B=w.B, H=w.H, Sq=w.Sq, Skv=w.Skv, d=w.d, seed=w.seed + 1000 * rank, q_std=w.q_std,
+    wr = Workload(w.name, B=w.B, H=heads, Sq=w.Sq, Skv=w.Skv, d=w.d, seed=w.seed + 1000 * rank, q_std=w.q_std,
                   k_std=w.k_std, grid=w.grid, audio_per_frame=w.audio_per_frame, pe=True, block=w.block, beta=beta)
     q, k, v = make_qkv(wr, device="cuda")
-    wc = Workload("cross_stage2", B=1, H=w.H, Sq=CROSS_SQ, Skv=CROSS_SKV, d=w.d, seed=3 + 1000 * rank)
+    wc = Workload("cross_stage2", B=1, H=heads, Sq=CROSS_SQ, Skv=CROSS_SKV, d=w.d, seed=3 + 1000 * rank)
     qa, kx, vx = make_qkv(wc, device="cuda")
     return wr, (q, k, v), (qa, kx, vx)
 
@@ -189,7 +189,7 @@ def run_native(args, world, rank, local):
     vbuild.build()
     vd.load_library()
     peaks, peaks_src = load_peaks()
-    w, (q, k, v), (qa, kx, vx) = make_inputs(rank, args.beta)
+    w, (q, k, v), (qa, kx, vx) = make_inputs(rank, args.beta, args.heads)
     B, H, S, d, block = w.B, w.H, w.Sq, w.d, w.block
     dev = q.device
     ws = torch.empty(vd.attn_sparse_workspace_bytes(B, H, S, d, block, block), dtype=torch.uint8, device=dev)
@@ -257,7 +257,7 @@ def run_native(args, world, rank, local):
         "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded noise + 3D sinusoidal position code)",
-        "config": {"workload": "sparse64k: Stage-2 block-sparse self-attention B=1 H=32 S=65664 (16x64x64 video + "
+        "config": {"workload": f"sparse64k: Stage-2 block-sparse self-attention B=1 H={H} S=65664 (16x64x64 video + "
                                "8 audio tokens per frame) d=128 block 128 beta=1.0, plus audio->video cross "
                                "attention 128 x 65536 split into 8 KV chunks and LSE-merged",
                    "global_batch": world, "seq_len": S, "parallelism": f"replicas x{world} (heads/batches shard "
@@ -413,6 +413,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
     ap.add_argument("--beta", type=float, default=1.0)
+    ap.add_argument("--heads", type=int, default=32, help="heads (32 = the benchmark; fewer only for profiling)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
