@@ -179,6 +179,48 @@ attn_status_t attn_sparse_fwd(const attn_bf16* q, const attn_bf16* k, const attn
                               const float* taylor_t, cudaStream_t stream);
 
 /*
+ * Size of the library-owned device scratch used by
+ * attn_sparse_route_fwd_noalloc (32 MiB on every device that loads the
+ * library, held until the process exits).
+ */
+#define ATTN_NOALLOC_WORKSPACE_BYTES ((size_t)32 << 20)
+
+/*
+ * attn_sparse_route_fwd for callers that must not allocate device memory.
+ * (No counterpart on the LTX-2.5 / Sol-Attn pages: this is a packaging
+ * variant, not part of the method.)
+ *
+ * Some callers cannot provide the scratch buffer attn_sparse_route_fwd asks
+ * for: code embedded in a host framework that owns every device allocation
+ * (a fixed memory arena handed out by an inference server or a plug-in host),
+ * or latency-critical threads where cudaMalloc may synchronise the device and
+ * stall other work.  This entry point computes exactly what
+ * attn_sparse_route_fwd computes, but keeps the pooled tensors and the
+ * routing (selected-block lists, statistics, Taylor aggregates) in one
+ * file-scope device array of ATTN_NOALLOC_WORKSPACE_BYTES owned by the
+ * library.  It calls no cudaMalloc, cudaFree or other allocating routine.
+ *
+ *   Arguments   as attn_sparse_route_fwd, without the workspace and the
+ *               optional routing outputs.
+ *   Limit       sizes whose attn_sparse_workspace_bytes(...) exceeds
+ *               ATTN_NOALLOC_WORKSPACE_BYTES are rejected with
+ *               ATTN_ERR_WORKSPACE before anything is launched (for H = 32,
+ *               d = 128, block 128 that is S up to about 32K tokens).
+ *   Set-up      the first call on a device looks up the device address of
+ *               the array (once per device, with that device current); make
+ *               that first call before any stream capture.
+ *   Sharing     every call on a device uses the same array and leaves its
+ *               contents behind; nothing in it has to start at zero (every
+ *               byte a call reads was written earlier in the same call), but
+ *               calls that overlap on the GPU (different streams, or
+ *               different host threads without ordering) race on it and must
+ *               be serialised by the caller.
+ */
+attn_status_t attn_sparse_route_fwd_noalloc(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v,
+                                            attn_bf16* out, float* lse, int B, int H, int S, int d, float scale,
+                                            float beta, int block_q, int block_k, cudaStream_t stream);
+
+/*
  * Synchronises `stream`, reads and clears the current device's status word.
  * Returns ATTN_OK, ATTN_ERR_TIMEOUT if a kernel gave up on a barrier wait,
  * ATTN_ERR_INVALID_ARG if a kernel met a corrupt selected-block list, or

@@ -19,7 +19,8 @@ import torch
 __all__ = [
     "AttnError", "load_library", "attn_dense_fwd", "attn_cross_splitkv_fwd", "attn_lse_merge", "attn_block_pool",
     "attn_sparse_workspace_bytes", "attn_sparse_route_fwd", "attn_sparse_route", "attn_sparse_fwd",
-    "attn_last_device_status", "attn_status_string", "attn_selftest_wait_timeout", "EXPORTED_SYMBOLS",
+    "attn_last_device_status", "attn_status_string", "attn_selftest_wait_timeout",
+    "attn_sparse_route_fwd_noalloc", "NOALLOC_WORKSPACE_BYTES", "EXPORTED_SYMBOLS",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -30,8 +31,11 @@ _lib = None
 EXPORTED_SYMBOLS = (
     "attn_dense_fwd", "attn_cross_splitkv_fwd", "attn_lse_merge", "attn_block_pool", "attn_sparse_workspace_bytes",
     "attn_sparse_route_fwd", "attn_sparse_route", "attn_sparse_fwd", "attn_last_device_status", "attn_status_string",
-    "attn_selftest_wait_timeout",
+    "attn_selftest_wait_timeout", "attn_sparse_route_fwd_noalloc",
 )
+
+# Size of the library-owned scratch of attn_sparse_route_fwd_noalloc (ATTN_NOALLOC_WORKSPACE_BYTES).
+NOALLOC_WORKSPACE_BYTES = 32 << 20
 
 _STATUS = {0: "ATTN_OK", 1: "ATTN_ERR_INVALID_ARG", 2: "ATTN_ERR_UNSUPPORTED", 3: "ATTN_ERR_WORKSPACE",
            4: "ATTN_ERR_CUDA", 5: "ATTN_ERR_TIMEOUT"}
@@ -64,13 +68,14 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         lib.attn_sparse_route_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, f, i, i, vp, sz, vp, vp, vp, vp, vp]
         lib.attn_sparse_route.argtypes = [vp, vp, vp, i, i, i, i, f, f, i, i, vp, sz, vp, vp, vp, vp, vp]
         lib.attn_sparse_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, i, vp, vp, vp, vp, vp]
+        lib.attn_sparse_route_fwd_noalloc.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, f, i, i, vp]
         lib.attn_last_device_status.argtypes = [vp]
         lib.attn_status_string.argtypes = [i]
         lib.attn_status_string.restype = ctypes.c_char_p
         lib.attn_selftest_wait_timeout.argtypes = [i, vp]
         for name in ("attn_dense_fwd", "attn_cross_splitkv_fwd", "attn_lse_merge", "attn_block_pool",
                      "attn_sparse_route_fwd", "attn_sparse_route", "attn_sparse_fwd", "attn_last_device_status",
-                     "attn_selftest_wait_timeout"):
+                     "attn_selftest_wait_timeout", "attn_sparse_route_fwd_noalloc"):
             getattr(lib, name).restype = ctypes.c_int
         if path is None:
             _lib = lib
@@ -229,6 +234,26 @@ def attn_sparse_fwd(q, k, v, route, block=128, scale=None, out=None, lse=None, s
            lib.attn_sparse_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, S, d, scale, block, block,
                                _ptr(route["sel_idx"]), _ptr(route["sel_cnt"]), _ptr(route["stats"]),
                                _ptr(route["taylor_t"]), _stream(stream)))
+    return out, lse
+
+
+def attn_sparse_route_fwd_noalloc(q, k, v, beta, block=128, scale=None, out=None, lse=None, stream=None):
+    """attn_sparse_route_fwd with the library's own fixed device scratch, for callers that may
+    not allocate device memory on this path (a host framework owning every allocation, or a
+    latency-critical thread that must not stall on cudaMalloc).  Sizes needing more than
+    NOALLOC_WORKSPACE_BYTES of scratch are rejected; calls that overlap on the GPU share the
+    scratch and must be serialised by the caller.  (Outputs may still be allocated here by
+    torch when not passed in; pass ``out``/``lse`` to allocate nothing at all.)"""
+    lib = load_library()
+    B, H, S, d = _bhsd(q, "q")
+    _bhsd(k, "k")
+    _bhsd(v, "v")
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    out = torch.empty_like(q) if out is None else out
+    lse = torch.empty((B, H, S), dtype=torch.float32, device=q.device) if lse is None else lse
+    _check("attn_sparse_route_fwd_noalloc",
+           lib.attn_sparse_route_fwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, S, d, scale,
+                                             float(beta), block, block, _stream(stream)))
     return out, lse
 
 

@@ -324,6 +324,47 @@ attn_status_t attn_sparse_route_fwd(const attn_bf16* q, const attn_bf16* k, cons
   return run_sparse_fwd(a, out, lse, si, sc, stt, tt, stream);
 }
 
+// ---------------------------------------------------------------- allocation-free variant
+// Scratch of attn_sparse_route_fwd_noalloc for callers that cannot allocate
+// device memory themselves (see attn_api.h).  It lives in the library's
+// module on each device and is shared by every call on that device.
+static __device__ __align__(256) uint8_t g_noalloc_workspace[ATTN_NOALLOC_WORKSPACE_BYTES];
+
+namespace {
+std::mutex g_noalloc_mutex;
+void* g_noalloc_ptr[kMaxDevices] = {nullptr};
+
+// Host code cannot use g_noalloc_workspace's name as a device address; look
+// the address up once per device, with that device current.
+attn_status_t noalloc_workspace(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return ATTN_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+  if (g_noalloc_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_workspace) != cudaSuccess || p == nullptr) return ATTN_ERR_CUDA;
+    g_noalloc_ptr[dev] = p;
+  }
+  *out = g_noalloc_ptr[dev];
+  return ATTN_OK;
+}
+}  // namespace
+
+attn_status_t attn_sparse_route_fwd_noalloc(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v,
+                                            attn_bf16* out, float* lse, int B, int H, int S, int d, float scale,
+                                            float beta, int block_q, int block_k, cudaStream_t stream) {
+  const size_t need = attn_sparse_workspace_bytes(B, H, S, d, block_q, block_k);
+  if (need > ATTN_NOALLOC_WORKSPACE_BYTES) return ATTN_ERR_WORKSPACE;
+  void* ws = nullptr;
+  if (need > 0) {
+    attn_status_t st = noalloc_workspace(&ws);
+    if (st != ATTN_OK) return st;
+  }
+  // need == 0 means unsupported sizes: the checks below report them without launching
+  return attn_sparse_route_fwd(q, k, v, out, lse, B, H, S, d, scale, beta, block_q, block_k, ws,
+                               ATTN_NOALLOC_WORKSPACE_BYTES, nullptr, nullptr, nullptr, nullptr, stream);
+}
+
 attn_status_t attn_last_device_status(cudaStream_t stream) {
   int* status = nullptr;
   attn_status_t st = status_ptr(&status);
