@@ -33,7 +33,8 @@
  *               masking it ("LTX-2.5 at 4K, in half the time", section
  *               "Attention across two GPUs").
  *   Numerics    bf16 inputs, fp32 accumulation and softmax, bf16 outputs
- *               rounded to nearest even, lse in natural log (fp32).
+ *               rounded to nearest even, lse in natural log (fp32).  The
+ *               softmax scale must be finite and positive.
  */
 #ifndef ATTN_API_H
 #define ATTN_API_H
@@ -62,7 +63,7 @@ typedef enum {
  * lse = log sum_k exp(scale * q.k) per query row.
  *   q    [B][H][Sq][d]  bf16      k, v  [B][H][Skv][d]  bf16
  *   out  [B][H][Sq][d]  bf16      lse   [B][H][Sq]      fp32 (nullable)
- * Requires B, H, Sq, Skv >= 1, d in {64, 128}, scale finite.
+ * Requires B, H, Sq, Skv >= 1, d in {64, 128}, scale finite and > 0.
  * Source: "Accelerating LTX-2.5 with Sol Engine", section "Stage 2
  * Optimization" (attention over long video sequences dominates Stage 2);
  * "LTX-2.5 Optimization" (openltx.com), attention-backend paragraph.

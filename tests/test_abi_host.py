@@ -56,6 +56,8 @@ NULL = None
     ((P, P, P, P, P, 1, 1, 0, 16, 128, 0.1), 1),                # Sq = 0
     ((P, P, P, P, P, 1, 1, 16, 16, 96, 0.1), 2),                # unsupported d
     ((P, P, P, P, P, 1, 1, 16, 16, 128, math.nan), 1),          # NaN scale
+    ((P, P, P, P, P, 1, 1, 16, 16, 128, 0.0), 1),               # non-positive scale
+    ((P, P, P, P, P, 1, 1, 16, 16, 128, -0.5), 1),
 ])
 def test_dense_rejects_bad_arguments(lib, args, code):
     assert lib.attn_dense_fwd(*args, None) == code

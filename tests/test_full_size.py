@@ -1,0 +1,110 @@
+"""Full-size parity: the benchmark-size workloads in the launch configuration bench.py times.
+
+The GPU runs each whole problem; the oracle recomputes sampled heads and
+sampled query rows one by one (seeded), plus the complete routing of the
+sampled heads.  Tolerances as in the small cases.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import video_diffusion_transformer_block_gb300 as vd
+from workloads import WORKLOADS, Workload, make_qkv
+from parity_util import assert_close, compare_selection, gpu_selection, host
+
+pytestmark = pytest.mark.gpu
+
+
+def sample_heads(H, rng, n=4):
+    extra = rng.choice(np.arange(1, H - 1), size=max(0, n - 2), replace=False)
+    return sorted({0, H - 1, *extra.tolist()})
+
+
+@pytest.fixture(autouse=True)
+def _free():
+    yield
+    torch.cuda.empty_cache()
+    assert vd.attn_last_device_status() == 0
+
+
+def test_dense16k_full_size_sampled_rows():
+    w = WORKLOADS["dense16k"]
+    q, k, v = make_qkv(w, device="cuda")
+    out, lse = vd.attn_dense_fwd(q, k, v)
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(102)
+    hs = sample_heads(w.H, rng)
+    qh, kh, vh = (host(x[:, hs].contiguous()) for x in (q, k, v))
+    rows = np.sort(rng.choice(len(hs) * w.Sq, size=512, replace=False))
+    ro, rl = oracle.attention(qh, kh, vh, w.scale, rows=rows)
+    go = host(out[:, hs].contiguous()).reshape(-1, w.d)[rows]
+    gl = host(lse[:, hs].contiguous()).reshape(-1)[rows]
+    assert_close(go, ro, "dense16k out")
+    assert_close(gl, rl, "dense16k lse")
+
+
+@pytest.mark.parametrize("Skv", [32768, 32769])
+def test_cross_full_size_split_merge(Skv):
+    w = WORKLOADS["cross"]
+    q, k, v = make_qkv(w, device="cuda", Skv=Skv)
+    op, lp = vd.attn_cross_splitkv_fwd(q, k, v, w.n_split)
+    out, lse = vd.attn_lse_merge(op, lp)
+    dense, dlse = vd.attn_dense_fwd(q, k, v)
+    torch.cuda.synchronize()
+    # merged partials against the GPU's own unsplit attention (every head, every row)
+    assert_close(host(out), host(dense), "merged vs unsplit (GPU)")
+    assert_close(host(lse), host(dlse), "merged lse vs unsplit (GPU)")
+    rng = np.random.default_rng(103 + Skv)
+    hs = sample_heads(w.H, rng)
+    qh, kh, vh = (host(x[:, hs].contiguous()) for x in (q, k, v))
+    rop, rlp = oracle.split_partials(qh, kh, vh, w.scale, w.n_split)
+    assert_close(host(op[:, :, hs].contiguous()), rop, "partials out")
+    assert_close(host(lp[:, :, hs].contiguous()), rlp, "partials lse")
+    ro, rl = oracle.attention(qh, kh, vh, w.scale)
+    assert_close(host(out[:, hs].contiguous()), ro, "merged out")
+    assert_close(host(lse[:, hs].contiguous()), rl, "merged lse")
+
+
+def sparse_full_size(w, beta, n_rows, n_heads, seed):
+    q, k, v = make_qkv(w, device="cuda")
+    out, lse, rt = vd.attn_sparse_route_fwd(q, k, v, beta, block=w.block, route=True)
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(seed)
+    hs = sample_heads(w.H, rng, n_heads)
+    qh, kh, vh = (host(x[:, hs].contiguous()) for x in (q, k, v))
+    del q, k, v
+    qp, kp, vp = (oracle.block_pool(x, w.block) for x in (qh, kh, vh))
+    ort = oracle.route(qp, kp, vp, w.Sq, w.block, w.scale, beta)
+    gsel = gpu_selection(rt["sel_idx"][:, hs], rt["sel_cnt"][:, hs])
+    flips = compare_selection(gsel, ort)
+    st = host(rt["stats"][:, hs])
+    np.testing.assert_allclose(st[..., 0], ort["mu"], atol=1e-4, rtol=1e-4)
+    np.testing.assert_allclose(st[..., 1], ort["sigma"], atol=1e-4, rtol=1e-4)
+    forced = oracle.route(qp, kp, vp, w.Sq, w.block, w.scale, beta, force_sel=gsel)
+    np.testing.assert_allclose(st[..., 3], forced["W"], atol=2e-3, rtol=1e-3)
+    np.testing.assert_allclose(host(rt["taylor_t"][:, hs]), forced["T"], atol=0.3, rtol=1e-3)
+    rows = np.sort(rng.choice(len(hs) * w.Sq, size=n_rows, replace=False))
+    ro, rl = oracle.sparse_attention(qh, kh, vh, w.block, w.block, gsel, forced["mu"], forced["W"], forced["T"],
+                                     w.scale, rows=rows)
+    go = host(out[:, hs].contiguous()).reshape(-1, w.d)[rows]
+    gl = host(lse[:, hs].contiguous()).reshape(-1)[rows]
+    assert_close(go, ro, f"{w.name} beta={beta} out")
+    assert_close(gl, rl, f"{w.name} beta={beta} lse")
+    return flips, float(gsel.mean())
+
+
+def test_sparse64k_full_size():
+    w = WORKLOADS["sparse64k"]
+    flips, density = sparse_full_size(w, w.beta, n_rows=4096, n_heads=4, seed=104)
+    assert 0.0 < density < 1.0
+
+
+@pytest.mark.parametrize("beta", [-math.inf, 0.0, 0.5, 1.0, 2.0])
+def test_sweep128k_full_size(beta):
+    w = WORKLOADS["sweep128k"]
+    flips, density = sparse_full_size(w, beta, n_rows=512, n_heads=2, seed=105)
+    if beta == -math.inf:
+        assert density == 1.0

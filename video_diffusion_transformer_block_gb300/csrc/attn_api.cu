@@ -148,7 +148,7 @@ attn_status_t attn_dense_fwd(const attn_bf16* q, const attn_bf16* k, const attn_
   if (!q || !k || !v || !out) return ATTN_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || (lse && ((uintptr_t)lse & 3u)))
     return ATTN_ERR_INVALID_ARG;
-  if (!sizes_ok(B, H, Sq) || !sizes_ok(B, H, Skv) || !isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+  if (!sizes_ok(B, H, Sq) || !sizes_ok(B, H, Skv) || !(isfinite(scale) && scale > 0.f)) return ATTN_ERR_INVALID_ARG;
   if (!valid_d(d)) return ATTN_ERR_UNSUPPORTED;
   int* status = nullptr;
   attn_status_t st = status_ptr(&status);
@@ -169,7 +169,7 @@ attn_status_t attn_cross_splitkv_fwd(const attn_bf16* q, const attn_bf16* k, con
   if (!q || !k || !v || !out_part || !lse_part) return ATTN_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out_part) || ((uintptr_t)lse_part & 3u))
     return ATTN_ERR_INVALID_ARG;
-  if (!sizes_ok(B, H, Sq) || !sizes_ok(B, H, Skv) || !isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+  if (!sizes_ok(B, H, Sq) || !sizes_ok(B, H, Skv) || !(isfinite(scale) && scale > 0.f)) return ATTN_ERR_INVALID_ARG;
   if (n_split < 1 || n_split > Skv) return ATTN_ERR_INVALID_ARG;
   if (!valid_d(d)) return ATTN_ERR_UNSUPPORTED;
   int* status = nullptr;
@@ -222,7 +222,7 @@ struct SparseArgs {
 attn_status_t sparse_common_checks(const SparseArgs& a) {
   if (!a.q || !a.k || !a.v) return ATTN_ERR_INVALID_ARG;
   if (!aligned16(a.q) || !aligned16(a.k) || !aligned16(a.v)) return ATTN_ERR_INVALID_ARG;
-  if (!sizes_ok(a.B, a.H, a.S) || !isfinite(a.scale)) return ATTN_ERR_INVALID_ARG;
+  if (!sizes_ok(a.B, a.H, a.S) || !(isfinite(a.scale) && a.scale > 0.f)) return ATTN_ERR_INVALID_ARG;
   if (!valid_d(a.d) || a.block_q != a.block_k || (a.block_q != 64 && a.block_q != 128)) return ATTN_ERR_UNSUPPORTED;
   SparseLayout L;
   if (!sparse_layout(a.B, a.H, a.S, a.d, a.block_q, a.block_k, &L)) return ATTN_ERR_UNSUPPORTED;

@@ -94,9 +94,20 @@ struct TileMerge {
 template <int D, int BK, int MODE, int NQT, int NSTAGE>
 struct FwdCfg {
   static constexpr int QB = (MODE == kModeSparse) ? 128 / BK : 1;   // query blocks per 128-row tile
-  static constexpr int kThreads = NQT * 128 + 64;
+  // NQT softmax warpgroups + one control warpgroup (TMA producer warp, MMA
+  // warp, two idle warps): whole warpgroups so that setmaxnreg can move
+  // registers from the control warpgroup to the softmax warpgroups.
+  static constexpr int kThreads = NQT * 128 + 128;
   static constexpr int kProducerWarp = NQT * 4;
   static constexpr int kMmaWarp = NQT * 4 + 1;
+  // Registers per thread: at launch (65536 / (threads * CTAs per SM), rounded
+  // down to 8), for the control warpgroup after setmaxnreg.dec, and for the
+  // softmax warpgroups after setmaxnreg.inc.  The split must add up to the
+  // launch allocation: NQT*128*kRegsSoftmax + 128*kRegsControl <= kThreads*kRegsLaunch.
+  static constexpr int kRegsLaunch = NQT == 2 ? 168 : 128;
+  static constexpr int kRegsControl = NQT == 2 ? 64 : 56;
+  static constexpr int kRegsSoftmax = NQT == 2 ? 216 : 200;
+  static_assert(NQT * 128 * kRegsSoftmax + 128 * kRegsControl <= kThreads * kRegsLaunch, "register split");
   static constexpr int kQTileBytes = 128 * D * 2;
   static constexpr int kSlotBytes = BK * D * 2;
   // A two-tile CTA takes all 512 TMEM columns: its shared-memory request is
@@ -115,7 +126,7 @@ struct FwdCfg {
 };
 
 template <int D, int BK, int MODE, int NQT, int NSTAGE>
-__global__ void __launch_bounds__(NQT * 128 + 64, (NQT == 1) ? 2 : 1)
+__global__ void __launch_bounds__(NQT * 128 + 128, (NQT == 1) ? 2 : 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
   using Cfg = FwdCfg<D, BK, MODE, NQT, NSTAGE>;
@@ -209,6 +220,8 @@ __global__ void __launch_bounds__(NQT * 128 + 64, (NQT == 1) ? 2 : 1)
   tc_fence_after();
   const uint32_t tmem = tmem_base_sh;
 
+  if (warp >= Cfg::kProducerWarp) {
+    setmaxnreg_dec<Cfg::kRegsControl>();
   if (warp == Cfg::kProducerWarp) {
     // ======================= TMA producer =======================
     if (lane == 0) {
@@ -334,7 +347,9 @@ __global__ void __launch_bounds__(NQT * 128 + 64, (NQT == 1) ? 2 : 1)
       mma_commit(&bar_mma_done);
       bounded_wait(&bar_mma_done, 0, nullptr, p.status);
     }
+  }
   } else {
+    setmaxnreg_inc<Cfg::kRegsSoftmax>();
     // ======================= softmax + epilogue =======================
     const int t = warp >> 2;
     const int w4 = warp & 3;
@@ -372,20 +387,20 @@ __global__ void __launch_bounds__(NQT * 128 + 64, (NQT == 1) ? 2 : 1)
       }
       const int n_valid = min(BK, kv_hi - (kv_lo + u * BK));
       const bool mine = (flags & my_bit) != 0;
-      float mt = -INFINITY;
-      if (mine && n_valid == BK) {
+      // raw scores stay unscaled: the softmax scale is positive, so the max
+      // commutes with it and the scaling folds into the exponent's FFMA
+      if (!(mine && n_valid == BK)) {
 #pragma unroll
-        for (int c = 0; c < BK; ++c) {
-          x[c] *= p.scale_log2;
-          mt = fmaxf(mt, x[c]);
-        }
-      } else {
-#pragma unroll
-        for (int c = 0; c < BK; ++c) {
-          x[c] = (mine && c < n_valid) ? x[c] * p.scale_log2 : -INFINITY;
-          mt = fmaxf(mt, x[c]);
-        }
+        for (int c = 0; c < BK; ++c)
+          if (!mine || c >= n_valid) x[c] = -INFINITY;
       }
+      float mx0 = x[0], mx1 = x[1];
+#pragma unroll
+      for (int c = 2; c < BK; c += 2) {
+        mx0 = fmaxf(mx0, x[c]);
+        mx1 = fmaxf(mx1, x[c + 1]);
+      }
+      const float mt = fmaxf(mx0, mx1) * p.scale_log2;
       // lazy rescale of the running max
       float alpha = 1.f;
       bool need = mt > m_run + kRescaleLog2 || (m_run == -INFINITY && mt > -INFINITY);
@@ -410,15 +425,15 @@ __global__ void __launch_bounds__(NQT * 128 + 64, (NQT == 1) ? 2 : 1)
           tmem_st32(tO + c0, rr);
         }
       }
-      const float base = (m_run == -INFINITY) ? 0.f : m_run;
+      const float nbase = (m_run == -INFINITY) ? 0.f : -m_run;
       float ls0 = 0.f, ls1 = 0.f;
 #pragma unroll
       for (int c0 = 0; c0 < BK; c0 += 64) {
         uint32_t pk[32];
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
-          float p0 = ex2_approx(x[c0 + 2 * j] - base);
-          float p1 = ex2_approx(x[c0 + 2 * j + 1] - base);
+          float p0 = ex2_approx(fmaf(x[c0 + 2 * j], p.scale_log2, nbase));
+          float p1 = ex2_approx(fmaf(x[c0 + 2 * j + 1], p.scale_log2, nbase));
           ls0 += p0;
           ls1 += p1;
           pk[j] = pack_bf16x2(p0, p1);

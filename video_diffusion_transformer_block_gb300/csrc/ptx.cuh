@@ -54,7 +54,7 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 // CTA has aborted.  Returns false on timeout/abort.  A null `abort_flag` is
 // used by the drain waits at the end of a kernel, which must not be cut
 // short by an abort.
-static __device__ __noinline__ bool bounded_wait_slow(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int* status,
+static __device__ __forceinline__ bool bounded_wait_slow(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int* status,
                                                unsigned long long limit_ns) {
   uint64_t t0 = global_timer_ns();
   while (true) {
@@ -161,6 +161,16 @@ __device__ __forceinline__ void tmem_reg_fence(uint32_t (&r)[32]) {
                  "+r"(r[30]), "+r"(r[31]));
 }
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// Per-warpgroup register reallocation (all four warps of a warpgroup execute it).
+template <int N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
 
 // ---------------------------------------------------------------- math helpers
 __device__ __forceinline__ float ex2_approx(float x) {
