@@ -282,6 +282,82 @@ def run_native(args, world, rank, local):
     return result
 
 
+def run_native_kernel(args, world, rank, local):
+    """Secondary workloads (not the benchmark line): one kernel path per step.
+      dense16k: attn_dense_fwd on B1 H32 S16384 d128 (tensor-bound)
+      cross:    attn_cross_splitkv_fwd + attn_lse_merge, 128 x 32768, 8 chunks (HBM-bound)"""
+    import video_diffusion_transformer_block_gb300 as vd
+    from video_diffusion_transformer_block_gb300 import build as vbuild
+
+    vbuild.build()
+    vd.load_library()
+    peaks, peaks_src = load_peaks()
+    w0 = WORKLOADS[args.workload]
+    w = Workload(w0.name, B=w0.B, H=args.heads, Sq=w0.Sq, Skv=w0.Skv, d=w0.d, seed=w0.seed + 1000 * rank,
+                 q_std=w0.q_std, k_std=w0.k_std, grid=w0.grid, audio_per_frame=w0.audio_per_frame, pe=w0.pe,
+                 n_split=w0.n_split)
+    q, k, v = make_qkv(w, device="cuda")
+    B, H, Sq, Skv, d = w.B, w.H, w.Sq, w.Skv, w.d
+    stream = torch.cuda.current_stream()
+    out = torch.empty_like(q)
+    lse = torch.empty((B, H, Sq), dtype=torch.float32, device=q.device)
+    if args.workload == "dense16k":
+        launches = 1
+        flops = 4.0 * B * H * Sq * Skv * d
+
+        def step():
+            vd.attn_dense_fwd(q, k, v, out=out, lse=lse)
+    else:
+        n = w.n_split
+        op = torch.empty((n, B, H, Sq, d), dtype=torch.float32, device=q.device)
+        lp = torch.empty((n, B, H, Sq), dtype=torch.float32, device=q.device)
+        launches = 2
+        flops = 4.0 * B * H * Sq * Skv * d
+        kv_bytes = 2.0 * B * H * Skv * d * 2 + B * H * Sq * d * 2 + n * B * H * Sq * (d + 1) * 4
+
+        def step():
+            vd.attn_cross_splitkv_fwd(q, k, v, n, out_part=op, lse_part=lp)
+            vd.attn_lse_merge(op, lp, out=out, lse=lse)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=q.device)   # 256 MB > L2, written between steps
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        for e0, e1 in evs:
+            flush.fill_(1)
+            e0.record(stream)
+            step()
+            e1.record(stream)
+        torch.cuda.synchronize()
+    barrier(world)
+    status = vd.attn_last_device_status()
+    if status != 0:
+        raise RuntimeError(f"device status after timed region: {vd.attn_status_string(status)}")
+    ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in evs) / args.steps, world)
+    value = world * flops / (ms * 1e-3) / 1e12
+    if args.workload == "dense16k":
+        peak = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
+        roof = {"bound": "tensor", "kernel": "attn_fwd_kernel (dense, d=128)", "achieved": round(value / world, 2),
+                "peak": peak, "unit": "TFLOP/s", "frac": round(value / world / peak, 4),
+                "peak_source": f"{peaks_src} bf16_tflops (burst: one kernel per timed step, L2 flushed between)",
+                "traffic": None}
+    else:
+        peak = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
+        gbs = kv_bytes / (ms * 1e-3) / 1e9
+        roof = {"bound": "hbm", "kernel": "attn_fwd_kernel (split-KV) + lse_merge_kernel", "achieved": round(gbs, 1),
+                "peak": peak, "unit": "GB/s", "frac": round(gbs / peak, 4), "peak_source": f"{peaks_src} hbm_gbs",
+                "traffic": None}
+    return {"metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": f"{args.workload}: B={B} H={H} Sq={Sq} Skv={Skv} d={d}", "seq_len": Skv,
+                       "l2": "256 MB buffer written between timed steps (L2 flush)"},
+            "roofline": roof, "gpu_launches": launches * args.steps, "clocks": clocks.summary()}
+
+
 def run_e2e(args, vd, w, qkv, cross, rt, ws, step_flops, world):
     """Same step through the public API with the inputs in pinned host memory: every step
     copies its inputs host->device and reads its outputs back, inside the timed region."""
@@ -414,6 +490,8 @@ def main():
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
     ap.add_argument("--beta", type=float, default=1.0)
     ap.add_argument("--heads", type=int, default=32, help="heads (32 = the benchmark; fewer only for profiling)")
+    ap.add_argument("--workload", choices=["sparse64k", "dense16k", "cross"], default="sparse64k",
+                    help="sparse64k = the benchmark step; dense16k / cross time one kernel path each")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
@@ -423,6 +501,8 @@ def main():
     world, rank, local = dist_setup()
     if args.impl == "reference":
         res = run_reference(args, world, rank)
+    elif args.workload != "sparse64k":
+        res = run_native_kernel(args, world, rank, local)
     else:
         res = run_native(args, world, rank, local)
     if rank == 0 and res is not None:
