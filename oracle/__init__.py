@@ -50,25 +50,38 @@ def build(force: bool = False) -> str:
     return _LIB_PATH
 
 
+def _configure(lib):
+    lib.oracle_attend_rows.argtypes = [_D, _D, _D, _i64, _i64, _i64, _i64, ctypes.c_double, _I64, _i64, _D, _D]
+    lib.oracle_split_partials.argtypes = [_D, _D, _D, _i64, _i64, _i64, _i64, ctypes.c_double, _i64, _D, _D]
+    lib.oracle_lse_merge.argtypes = [_D, _D, _i64, _i64, _i64, _D, _D]
+    lib.oracle_block_pool.argtypes = [_D, _i64, _i64, _i64, _i64, _D]
+    lib.oracle_route.argtypes = [_D, _D, _D, _i64, _i64, _i64, _i64, _I64, ctypes.c_double, ctypes.c_double,
+                                 ctypes.c_int, _U8, _D, _U8, _I64, _D, _D, _D, _D, _D, _I64]
+    lib.oracle_sparse_rows.argtypes = [_D, _D, _D, _i64, _i64, _i64, _i64, _i64, _U8, _D, _D, _D,
+                                       ctypes.c_double, _I64, _i64, _D, _D]
+    for f in (lib.oracle_attend_rows, lib.oracle_split_partials, lib.oracle_lse_merge, lib.oracle_block_pool,
+              lib.oracle_route, lib.oracle_sparse_rows):
+        f.restype = None
+    return lib
+
+
 def _load():
     global _lib
     with _lock:
-        if _lib is not None:
-            return _lib
-        lib = ctypes.CDLL(build())
-        lib.oracle_attend_rows.argtypes = [_D, _D, _D, _i64, _i64, _i64, _i64, ctypes.c_double, _I64, _i64, _D, _D]
-        lib.oracle_split_partials.argtypes = [_D, _D, _D, _i64, _i64, _i64, _i64, ctypes.c_double, _i64, _D, _D]
-        lib.oracle_lse_merge.argtypes = [_D, _D, _i64, _i64, _i64, _D, _D]
-        lib.oracle_block_pool.argtypes = [_D, _i64, _i64, _i64, _i64, _D]
-        lib.oracle_route.argtypes = [_D, _D, _D, _i64, _i64, _i64, _i64, _I64, ctypes.c_double, ctypes.c_double,
-                                     ctypes.c_int, _U8, _D, _U8, _I64, _D, _D, _D, _D, _D, _I64]
-        lib.oracle_sparse_rows.argtypes = [_D, _D, _D, _i64, _i64, _i64, _i64, _i64, _U8, _D, _D, _D,
-                                           ctypes.c_double, _I64, _i64, _D, _D]
-        for f in (lib.oracle_attend_rows, lib.oracle_split_partials, lib.oracle_lse_merge, lib.oracle_block_pool,
-                  lib.oracle_route, lib.oracle_sparse_rows):
-            f.restype = None
-        _lib = lib
-        return lib
+        if _lib is None:
+            _lib = _configure(ctypes.CDLL(build()))
+        return _lib
+
+
+def _swap_library(path):
+    """Test hook: route every oracle call through another build of oracle.c
+    (used by the mutation tests, which plant mistakes in a copy).  Returns the
+    previous library; pass None to restore the default build."""
+    global _lib
+    with _lock:
+        prev = _lib
+        _lib = None if path is None else _configure(ctypes.CDLL(path))
+        return prev
 
 
 def _f64(a) -> np.ndarray:
