@@ -180,6 +180,26 @@ attn_status_t attn_sparse_fwd(const attn_bf16* q, const attn_bf16* k, const attn
                               const float* taylor_t, cudaStream_t stream);
 
 /*
+ * attn_sparse_route_fwd with the routing folded into the forward kernel: after
+ * the block mean-pool, each CTA of the forward computes the proxy scores of
+ * its own query blocks against every pooled key block, their mean, standard
+ * deviation and threshold, the compacted selection and the Taylor aggregates
+ * in shared memory, and then runs the block-sparse main loop over those
+ * on-chip lists.  No routing launch, and neither the proxy map nor the lists
+ * are written to memory (unless the optional outputs are given).
+ * Source: "Accelerating LTX-2.5 with Sol Engine", section "Stage 2
+ * Optimization - Core Technology: Sol-Attn" (block selection folded into the
+ * online-softmax pass, no separate routing stage, no proxy map).
+ *   Arguments, definitions and optional outputs as attn_sparse_route_fwd;
+ *   the workspace (attn_sparse_workspace_bytes) holds the pooled tensors.
+ *   Limit: NKB = ceil(S/block_k) <= 1024 (ATTN_ERR_UNSUPPORTED beyond).
+ */
+attn_status_t attn_sparse_fused_fwd(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v, attn_bf16* out,
+                                    float* lse, int B, int H, int S, int d, float scale, float beta, int block_q,
+                                    int block_k, void* workspace, size_t workspace_bytes, int32_t* sel_idx,
+                                    int32_t* sel_cnt, float* stats, float* taylor_t, cudaStream_t stream);
+
+/*
  * Size of the library-owned device scratch used by
  * attn_sparse_route_fwd_noalloc (32 MiB on every device that loads the
  * library, held until the process exits).

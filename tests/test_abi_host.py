@@ -94,3 +94,15 @@ def test_sparse_workspace_and_rejections(lib):
 def test_selftest_rejects_bad_limit(lib):
     assert lib.attn_selftest_wait_timeout(0, None) == 1
     assert lib.attn_selftest_wait_timeout(2_000_000, None) == 1
+
+
+def test_fused_sparse_rejections(lib):
+    ws = ctypes.c_void_p(0x100000)
+    big = 1 << 40
+    # more than 1024 key blocks: the on-chip routing has no room for them
+    assert lib.attn_sparse_fused_fwd(P, P, P, P, P, 1, 1, 1025 * 128, 128, 0.088, 1.0, 128, 128, ws, big,
+                                     None, None, None, None, None) == 2
+    assert lib.attn_sparse_fused_fwd(P, P, P, P, P, 1, 1, 4096, 128, 0.088, 1.0, 128, 128, ws, 0,
+                                     None, None, None, None, None) == 3
+    assert lib.attn_sparse_fused_fwd(P, P, P, P, P, 1, 1, 4096, 128, 0.088, math.inf, 128, 128, ws, big,
+                                     None, None, None, None, None) == 1

@@ -68,9 +68,10 @@ def test_cross_full_size_split_merge(Skv):
     assert_close(host(lse[:, hs].contiguous()), rl, "merged lse")
 
 
-def sparse_full_size(w, beta, n_rows, n_heads, seed):
+def sparse_full_size(w, beta, n_rows, n_heads, seed, fn=None):
+    fn = vd.attn_sparse_route_fwd if fn is None else fn
     q, k, v = make_qkv(w, device="cuda")
-    out, lse, rt = vd.attn_sparse_route_fwd(q, k, v, beta, block=w.block, route=True)
+    out, lse, rt = fn(q, k, v, beta, block=w.block, route=True)
     torch.cuda.synchronize()
     rng = np.random.default_rng(seed)
     hs = sample_heads(w.H, rng, n_heads)
@@ -99,6 +100,12 @@ def sparse_full_size(w, beta, n_rows, n_heads, seed):
 def test_sparse64k_full_size():
     w = WORKLOADS["sparse64k"]
     flips, density = sparse_full_size(w, w.beta, n_rows=4096, n_heads=4, seed=104)
+    assert 0.0 < density < 1.0
+
+
+def test_sparse64k_full_size_fused_routing():
+    w = WORKLOADS["sparse64k"]
+    flips, density = sparse_full_size(w, w.beta, n_rows=4096, n_heads=4, seed=106, fn=vd.attn_sparse_fused_fwd)
     assert 0.0 < density < 1.0
 
 

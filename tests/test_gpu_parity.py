@@ -119,13 +119,13 @@ def test_splitkv_and_merge(H, Sq, Skv, d, n):
 
 # ---------------------------------------------------------------- block-sparse
 
-def sparse_check(q, k, v, block, beta, scale=None, rows=None, heads_idx=None):
-    """Runs the GPU path with route outputs and checks route + output against the oracle.
-
-    Returns (n_flips, density, errors)."""
+def sparse_check(q, k, v, block, beta, scale=None, rows=None, heads_idx=None, fn=None):
+    """Runs a GPU block-sparse path (two-kernel by default, or ``fn``) with route outputs and
+    checks route + output against the oracle.  Returns (n_flips, density, errors)."""
     B, H, S, d = q.shape
     scale = 1 / math.sqrt(d) if scale is None else scale
-    out, lse, rt = vd.attn_sparse_route_fwd(q, k, v, beta, block=block, scale=scale, route=True)
+    fn = vd.attn_sparse_route_fwd if fn is None else fn
+    out, lse, rt = fn(q, k, v, beta, block=block, scale=scale, route=True)
     torch.cuda.synchronize()
     hs = list(range(H)) if heads_idx is None else list(heads_idx)
     qh, kh, vh = (host(x[:, hs].contiguous()) for x in (q, k, v))
@@ -201,6 +201,45 @@ def test_sparse_batch_gt_one():
                                          1 / math.sqrt(128))
         assert_close(host(out[b:b + 1]), ro, f"batch {b} out")
         assert_close(host(lse[b:b + 1]), rl, f"batch {b} lse")
+
+
+# ---------------------------------------------------------------- routing folded into the forward
+
+@pytest.mark.parametrize("beta", [0.5, -math.inf, 3.0])
+def test_fused_tiny_config(beta):
+    w = WORKLOADS["tiny"]
+    q, k, v = make_qkv(w, device=DEV)
+    _, density, _ = sparse_check(q, k, v, w.block, beta, fn=vd.attn_sparse_fused_fwd)
+    if beta == -math.inf:
+        assert density == 1.0
+
+
+@pytest.mark.parametrize("d,block,beta", [(128, 128, 1.0), (128, 64, 0.5), (64, 128, 1.5), (64, 64, 0.0)])
+def test_fused_local_workload_ragged(d, block, beta):
+    w = WORKLOADS["sparse64k"]
+    w2 = Workload("s2", B=1, H=2, Sq=8208, Skv=8208, d=d, seed=8, q_std=0.5, k_std=0.5, grid=w.grid,
+                  audio_per_frame=8, pe=True, block=block, beta=beta)
+    q, k, v = make_qkv(w2, device=DEV)
+    _, density, _ = sparse_check(q, k, v, block, beta, fn=vd.attn_sparse_fused_fwd)
+    assert 0.0 < density < 1.0
+
+
+def test_fused_agrees_with_two_kernel_path_and_dense():
+    q, k, v = rnd_qkv(2, 2, 1000, 1000, 128, seed=47, std=1.0)
+    o1, l1, r1 = vd.attn_sparse_route_fwd(q, k, v, 0.6, block=128, route=True)
+    o2, l2, r2 = vd.attn_sparse_fused_fwd(q, k, v, 0.6, block=128, route=True)
+    torch.cuda.synchronize()
+    s1 = gpu_selection(r1["sel_idx"], r1["sel_cnt"])
+    s2 = gpu_selection(r2["sel_idx"], r2["sel_cnt"])
+    np.testing.assert_allclose(host(r1["stats"])[..., 0], host(r2["stats"])[..., 0], atol=1e-5, rtol=1e-5)
+    if np.array_equal(s1, s2):
+        assert_close(host(o2), host(o1), "fused vs two-kernel")
+        np.testing.assert_allclose(host(r2["taylor_t"]), host(r1["taylor_t"]), atol=1e-2, rtol=1e-4)
+    # with every block kept, the fused path runs exactly the dense arithmetic
+    od, ld = vd.attn_dense_fwd(q, k, v)
+    of, lf = vd.attn_sparse_fused_fwd(q, k, v, -math.inf, block=128)
+    torch.cuda.synchronize()
+    assert torch.equal(of, od) and torch.equal(lf, ld)
 
 
 # ---------------------------------------------------------------- status word

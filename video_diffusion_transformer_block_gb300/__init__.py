@@ -20,7 +20,7 @@ __all__ = [
     "AttnError", "load_library", "attn_dense_fwd", "attn_cross_splitkv_fwd", "attn_lse_merge", "attn_block_pool",
     "attn_sparse_workspace_bytes", "attn_sparse_route_fwd", "attn_sparse_route", "attn_sparse_fwd",
     "attn_last_device_status", "attn_status_string", "attn_selftest_wait_timeout",
-    "attn_sparse_route_fwd_noalloc", "NOALLOC_WORKSPACE_BYTES", "EXPORTED_SYMBOLS",
+    "attn_sparse_route_fwd_noalloc", "attn_sparse_fused_fwd", "NOALLOC_WORKSPACE_BYTES", "EXPORTED_SYMBOLS",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -31,7 +31,7 @@ _lib = None
 EXPORTED_SYMBOLS = (
     "attn_dense_fwd", "attn_cross_splitkv_fwd", "attn_lse_merge", "attn_block_pool", "attn_sparse_workspace_bytes",
     "attn_sparse_route_fwd", "attn_sparse_route", "attn_sparse_fwd", "attn_last_device_status", "attn_status_string",
-    "attn_selftest_wait_timeout", "attn_sparse_route_fwd_noalloc",
+    "attn_selftest_wait_timeout", "attn_sparse_route_fwd_noalloc", "attn_sparse_fused_fwd",
 )
 
 # Size of the library-owned scratch of attn_sparse_route_fwd_noalloc (ATTN_NOALLOC_WORKSPACE_BYTES).
@@ -69,13 +69,14 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         lib.attn_sparse_route.argtypes = [vp, vp, vp, i, i, i, i, f, f, i, i, vp, sz, vp, vp, vp, vp, vp]
         lib.attn_sparse_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, i, vp, vp, vp, vp, vp]
         lib.attn_sparse_route_fwd_noalloc.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, f, i, i, vp]
+        lib.attn_sparse_fused_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, f, i, i, vp, sz, vp, vp, vp, vp, vp]
         lib.attn_last_device_status.argtypes = [vp]
         lib.attn_status_string.argtypes = [i]
         lib.attn_status_string.restype = ctypes.c_char_p
         lib.attn_selftest_wait_timeout.argtypes = [i, vp]
         for name in ("attn_dense_fwd", "attn_cross_splitkv_fwd", "attn_lse_merge", "attn_block_pool",
                      "attn_sparse_route_fwd", "attn_sparse_route", "attn_sparse_fwd", "attn_last_device_status",
-                     "attn_selftest_wait_timeout", "attn_sparse_route_fwd_noalloc"):
+                     "attn_selftest_wait_timeout", "attn_sparse_route_fwd_noalloc", "attn_sparse_fused_fwd"):
             getattr(lib, name).restype = ctypes.c_int
         if path is None:
             _lib = lib
@@ -235,6 +236,33 @@ def attn_sparse_fwd(q, k, v, route, block=128, scale=None, out=None, lse=None, s
                                _ptr(route["sel_idx"]), _ptr(route["sel_cnt"]), _ptr(route["stats"]),
                                _ptr(route["taylor_t"]), _stream(stream)))
     return out, lse
+
+
+def attn_sparse_fused_fwd(q, k, v, beta, block=128, scale=None, out=None, lse=None, workspace=None, route=False,
+                          stream=None):
+    """Sol-Attn block-sparse attention with the routing folded into the forward kernel.
+
+    Same results as attn_sparse_route_fwd; with route=True the routing the
+    kernel computed on chip is also copied out (dict as attn_sparse_route)."""
+    lib = load_library()
+    B, H, S, d = _bhsd(q, "q")
+    _bhsd(k, "k")
+    _bhsd(v, "v")
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    out = torch.empty_like(q) if out is None else out
+    lse = torch.empty((B, H, S), dtype=torch.float32, device=q.device) if lse is None else lse
+    nbytes = attn_sparse_workspace_bytes(B, H, S, d, block, block)
+    if nbytes == 0:
+        raise AttnError("attn_sparse_workspace_bytes", 2)
+    if workspace is None:
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
+    extra = sparse_route_buffers(B, H, S, d, block, q.device) if route else {}
+    _check("attn_sparse_fused_fwd",
+           lib.attn_sparse_fused_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, S, d, scale, float(beta),
+                                     block, block, _ptr(workspace), workspace.numel(), _ptr(extra.get("sel_idx")),
+                                     _ptr(extra.get("sel_cnt")), _ptr(extra.get("stats")),
+                                     _ptr(extra.get("taylor_t")), _stream(stream)))
+    return (out, lse, extra) if route else (out, lse)
 
 
 def attn_sparse_route_fwd_noalloc(q, k, v, beta, block=128, scale=None, out=None, lse=None, stream=None):

@@ -324,6 +324,51 @@ attn_status_t attn_sparse_route_fwd(const attn_bf16* q, const attn_bf16* k, cons
   return run_sparse_fwd(a, out, lse, si, sc, stt, tt, stream);
 }
 
+attn_status_t attn_sparse_fused_fwd(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v, attn_bf16* out,
+                                    float* lse, int B, int H, int S, int d, float scale, float beta, int block_q,
+                                    int block_k, void* workspace, size_t workspace_bytes, int32_t* sel_idx,
+                                    int32_t* sel_cnt, float* stats, float* taylor_t, cudaStream_t stream) {
+  SparseArgs a{q, k, v, B, H, S, d, block_q, block_k, scale};
+  attn_status_t st = sparse_common_checks(a);
+  if (st != ATTN_OK) return st;
+  if (!out || !aligned16(out) || (lse && ((uintptr_t)lse & 3u)) || bad_opt_ptrs(sel_idx, sel_cnt, stats, taylor_t))
+    return ATTN_ERR_INVALID_ARG;
+  if (isnan(beta) || beta == INFINITY) return ATTN_ERR_INVALID_ARG;
+  const int NQB = (S + block_q - 1) / block_q, NKB = (S + block_k - 1) / block_k;
+  if (NKB > kFusedMaxNKB) return ATTN_ERR_UNSUPPORTED;
+  SparseLayout L;
+  sparse_layout(B, H, S, d, block_q, block_k, &L);
+  if (!workspace || ((uintptr_t)workspace & 255u) || workspace_bytes < L.total) return ATTN_ERR_WORKSPACE;
+  int* status = nullptr;
+  if ((st = status_ptr(&status)) != ATTN_OK) return st;
+  uint8_t* ws = (uint8_t*)workspace;
+  float* qp = (float*)(ws + L.qp);
+  float* kp = (float*)(ws + L.kp);
+  float* vp = (float*)(ws + L.vp);
+  const int BH = B * H;
+  CUtensorMap tq, tk, tv;
+  if ((st = make_map(&tq, q, d, S, BH, 128)) != ATTN_OK) return st;
+  if ((st = make_map(&tk, k, d, S, BH, block_k)) != ATTN_OK) return st;
+  if ((st = make_map(&tv, v, d, S, BH, block_k)) != ATTN_OK) return st;
+  if (launch_pool(q, k, v, qp, kp, vp, 3, BH, S, d, block_q, stream) != cudaSuccess) return ATTN_ERR_CUDA;
+  FwdParams p = base_params(B, H, S, S, scale, kModeSparseFused, status);
+  p.out = out;
+  p.lse = lse;
+  p.NQB = NQB;
+  p.NKB = NKB;
+  p.qbar = qp;
+  p.kbar = kp;
+  p.vbar = vp;
+  p.scale = scale;
+  p.beta = beta;
+  p.block_k = block_k;
+  p.out_sel_idx = sel_idx;
+  p.out_sel_cnt = sel_cnt;
+  p.out_stats = stats;
+  p.out_taylor = taylor_t;
+  return cuda_status(launch_fwd(d, block_k, kModeSparseFused, tq, tk, tv, p, stream));
+}
+
 // ---------------------------------------------------------------- allocation-free variant
 // Scratch of attn_sparse_route_fwd_noalloc for callers that cannot allocate
 // device memory themselves (see attn_api.h).  It lives in the library's

@@ -24,7 +24,7 @@
 
 namespace vdtb {
 
-enum FwdMode { kModeDense = 0, kModeSparse = 1, kModeSplit = 2 };
+enum FwdMode { kModeDense = 0, kModeSparse = 1, kModeSplit = 2, kModeSparseFused = 3 };
 
 constexpr float kRescaleLog2 = 8.0f;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -46,6 +46,18 @@ struct FwdParams {
   const float* taylor_t;   // sparse: [BH][NQB][D]
   int NQB, NKB;
   int* status;             // device status word
+  // fused routing (kModeSparseFused): pooled inputs, routing constants and
+  // optional copies of the routing the kernel computed on chip
+  const float* qbar;       // [BH][NQB][D]
+  const float* kbar;       // [BH][NKB][D]
+  const float* vbar;       // [BH][NKB][D]
+  float scale;             // softmax scale (natural units)
+  float beta;
+  int block_k;
+  int32_t* out_sel_idx;    // nullable, [BH][NQB][NKB]
+  int32_t* out_sel_cnt;    // nullable, [BH][NQB]
+  float* out_stats;        // nullable, [BH][NQB][4]
+  float* out_taylor;       // nullable, [BH][NQB][D]
 };
 
 // Walks the ascending union of up to 4 tile lists (one per query block the
@@ -53,6 +65,8 @@ struct FwdParams {
 // contains it.  Dense/split lists are implicit ranges [0, n).
 struct TileMerge {
   const int32_t* ptr[4];
+  const uint16_t* sptr[4];   // lists in shared memory (fused routing)
+  bool smem_lists;
   int n[4];
   int pos[4];
   int nlists;
@@ -62,6 +76,7 @@ struct TileMerge {
 
   __device__ __forceinline__ int head(int l) const {
     if (implicit) return pos[l];
+    if (smem_lists) return sptr[l][pos[l]];
     int v = __ldg(ptr[l] + pos[l]);
     if ((unsigned)v >= (unsigned)limit) {
       atomicOr(status, ATTN_DEVICE_BAD_LIST);
@@ -93,7 +108,15 @@ struct TileMerge {
 
 template <int D, int BK, int MODE, int NQT, int NSTAGE>
 struct FwdCfg {
-  static constexpr int QB = (MODE == kModeSparse) ? 128 / BK : 1;   // query blocks per 128-row tile
+  static constexpr bool kSparseLike = MODE == kModeSparse || MODE == kModeSparseFused;
+  static constexpr bool kFused = MODE == kModeSparseFused;
+  static constexpr int QB = kSparseLike ? 128 / BK : 1;   // query blocks per 128-row tile
+  // fused routing: query blocks per CTA, key-block capacity, staging chunk
+  static constexpr int kFusedR = NQT * QB;
+  static constexpr int kFusedMaxNKB = 1024;
+  static constexpr int kFusedCH = 128;
+  static constexpr int kFusedPersistBytes =
+      kFused ? ((kFusedR * kFusedMaxNKB * 2 + kFusedR * D * 4 + kFusedR * 16 + 15) / 16) * 16 : 0;
   // NQT softmax warpgroups + one control warpgroup (TMA producer warp, MMA
   // warp, two idle warps): whole warpgroups so that setmaxnreg can move
   // registers from the control warpgroup to the softmax warpgroups.
@@ -113,7 +136,7 @@ struct FwdCfg {
   // A two-tile CTA takes all 512 TMEM columns: its shared-memory request is
   // padded past half of the SM's 228 KB so that two such CTAs never share an
   // SM (the second would stall in tcgen05.alloc until the first exits).
-  static constexpr int kSmemRaw = 1024 + NQT * kQTileBytes + NSTAGE * kSlotBytes;
+  static constexpr int kSmemRaw = 1024 + NQT * kQTileBytes + NSTAGE * kSlotBytes + kFusedPersistBytes;
   static constexpr int kSmemBytes = (NQT == 2 && kSmemRaw < 120 * 1024) ? 120 * 1024 : kSmemRaw;
   static constexpr uint32_t kTmemCols = NQT == 2 ? 512 : 256;
   static constexpr uint32_t kIdescS = idesc_bf16_f32(128, BK, 0, 0);
@@ -123,7 +146,170 @@ struct FwdCfg {
   static_assert(NQT == 1 || NQT == 2, "query tiles per CTA");
   static_assert(NQT * QB <= 4, "lists per CTA");
   static_assert(NSTAGE >= 2, "ring depth");
+  static_assert(!kFused || kFusedCH * D * 4 + kFusedR * kFusedMaxNKB * 4 + kFusedR * D * 4 <= NSTAGE * kSlotBytes,
+                "fused routing scratch must fit in the K/V ring");
+  static_assert(!kFused || NQT == 2, "fused routing runs on the two-tile CTA");
 };
+
+__device__ __forceinline__ void named_sync(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// Sol-Attn routing of the CTA's R query blocks, computed on chip by the TH
+// softmax threads before the main loop (no routing launch, no lists in
+// memory).  Same definitions as route_kernel: proxy s_ij = scale Qbar_i.Kbar_j,
+// mu/sigma over j (two-pass), tau = mu + beta sigma, selection s >= tau or the
+// argmax (lowest j), ascending compaction with ballot/popc, Taylor weights
+// w = n_j max(0, 1 + s - mu) of rejected blocks, W = sum w, T = sum w Vbar_j.
+// chunk/prow/qs live in the (still idle) K/V ring; lists/cnts/mus/Ws/Ts persist.
+template <int D, int R, int CH, int KMAX, int TH>
+__device__ __forceinline__ void fused_route(const FwdParams& p, int bh, int qb0, int st, float* chunk, float* prow,
+                                            float* qs, uint16_t* lists, int* cnts, float* mus, float* Ws, float* Ts) {
+  const int NQB = p.NQB, NKB = p.NKB;
+  const int w = st >> 5, lane = st & 31;
+  for (int e = st; e < R * D; e += TH) {
+    const int r = e / D, c = e % D, i = qb0 + r;
+    qs[e] = (i < NQB) ? __ldg(p.qbar + ((long long)bh * NQB + i) * D + c) : 0.f;
+  }
+  // pass 1: proxy scores of every key block, staged through shared memory
+  for (int j0 = 0; j0 < NKB; j0 += CH) {
+    named_sync(1, TH);
+    for (int e = st; e < CH * (D / 4); e += TH) {
+      const int jj = e / (D / 4), c4 = e % (D / 4);
+      float4 v4 = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (j0 + jj < NKB) v4 = __ldg(reinterpret_cast<const float4*>(p.kbar + ((long long)bh * NKB + j0 + jj) * D) + c4);
+      reinterpret_cast<float4*>(chunk)[e] = v4;
+    }
+    named_sync(1, TH);
+    for (int e = st; e < R * CH; e += TH) {
+      const int r = e / CH, jj = e % CH, j = j0 + jj;
+      if (j >= NKB) continue;
+      const float* krow = chunk + jj * D;
+      const float* qrow = qs + r * D;
+      float acc = 0.f;
+#pragma unroll 8
+      for (int c = 0; c < D; ++c) {
+        const int cc = (c + jj) & (D - 1);   // rotated column: conflict-free across the warp
+        acc = fmaf(qrow[cc], krow[cc], acc);
+      }
+      prow[r * KMAX + j] = p.scale * acc;
+    }
+  }
+  named_sync(1, TH);
+  // statistics, selection and Taylor weights: warp w owns row w
+  if (w < R) {
+    float* row = prow + w * KMAX;
+    float sum = 0.f, best = -INFINITY;
+    int bidx = INT_MAX;
+    for (int j = lane; j < NKB; j += 32) {
+      const float v = row[j];
+      sum += v;
+      if (v > best) {
+        best = v;
+        bidx = j;
+      }
+    }
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) {
+      sum += __shfl_xor_sync(0xffffffffu, sum, off);
+      const float ob = __shfl_xor_sync(0xffffffffu, best, off);
+      const int oi = __shfl_xor_sync(0xffffffffu, bidx, off);
+      if (ob > best || (ob == best && oi < bidx)) {
+        best = ob;
+        bidx = oi;
+      }
+    }
+    const float mu = sum / (float)NKB;
+    float sq = 0.f;
+    for (int j = lane; j < NKB; j += 32) {
+      const float dv = row[j] - mu;
+      sq = fmaf(dv, dv, sq);
+    }
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, off);
+    const float sigma = sqrtf(sq / (float)NKB);
+    const float tau = (p.beta == -INFINITY) ? -INFINITY : fmaf(p.beta, sigma, mu);
+    int cnt = 0;
+    float wsum = 0.f;
+    for (int j0 = 0; j0 < NKB; j0 += 32) {
+      const int j = j0 + lane;
+      const bool in = j < NKB;
+      const float v = in ? row[j] : 0.f;
+      const bool keep = in && (v >= tau || j == bidx);
+      const unsigned m = __ballot_sync(0xffffffffu, keep);
+      if (keep) lists[w * KMAX + cnt + __popc(m & ((1u << lane) - 1u))] = (uint16_t)j;
+      cnt += __popc(m);
+      float wt = 0.f;
+      if (in && !keep) {
+        const int nj = min(p.block_k, p.Skv - j * p.block_k);
+        wt = (float)nj * fmaxf(0.f, 1.f + v - mu);
+      }
+      if (in) row[j] = wt;   // the proxy is no longer needed: keep the Taylor weight
+      wsum += wt;
+    }
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, off);
+    const int i = qb0 + w;
+    if (lane == 0) {
+      cnts[w] = (i < NQB) ? cnt : 0;
+      mus[w] = mu;
+      Ws[w] = wsum;
+    }
+    if (i < NQB) {
+      const long long rrow = (long long)bh * NQB + i;
+      if (p.out_sel_cnt != nullptr && lane == 0) p.out_sel_cnt[rrow] = cnt;
+      if (p.out_stats != nullptr && lane == 0) {
+        p.out_stats[rrow * 4 + 0] = mu;
+        p.out_stats[rrow * 4 + 1] = sigma;
+        p.out_stats[rrow * 4 + 2] = tau;
+        p.out_stats[rrow * 4 + 3] = wsum;
+      }
+      if (p.out_sel_idx != nullptr) {
+        __syncwarp();
+        for (int k = lane; k < cnt; k += 32) p.out_sel_idx[rrow * NKB + k] = lists[w * KMAX + k];
+      }
+    }
+  }
+  // T = sum_j w_j Vbar_j, V staged through shared memory
+  constexpr int PER = (R * D + TH - 1) / TH;
+  float acc[PER];
+#pragma unroll
+  for (int k = 0; k < PER; ++k) acc[k] = 0.f;
+  for (int j0 = 0; j0 < NKB; j0 += CH) {
+    named_sync(1, TH);
+    for (int e = st; e < CH * (D / 4); e += TH) {
+      const int jj = e / (D / 4), c4 = e % (D / 4);
+      float4 v4 = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (j0 + jj < NKB) v4 = __ldg(reinterpret_cast<const float4*>(p.vbar + ((long long)bh * NKB + j0 + jj) * D) + c4);
+      reinterpret_cast<float4*>(chunk)[e] = v4;
+    }
+    named_sync(1, TH);
+    const int jn = min(CH, NKB - j0);
+#pragma unroll
+    for (int k = 0; k < PER; ++k) {
+      const int e = st + k * TH;
+      if (e < R * D) {
+        const int r = e / D, c = e % D;
+        const float* wrow = prow + r * KMAX + j0;
+        float a = acc[k];
+        for (int jj = 0; jj < jn; ++jj) a = fmaf(wrow[jj], chunk[jj * D + c], a);
+        acc[k] = a;
+      }
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < PER; ++k) {
+    const int e = st + k * TH;
+    if (e < R * D) {
+      Ts[e] = acc[k];
+      const int r = e / D, i = qb0 + r;
+      if (p.out_taylor != nullptr && i < NQB) p.out_taylor[((long long)bh * NQB + i) * D + e % D] = acc[k];
+    }
+  }
+  // the ring is handed over to TMA (async proxy) after these generic accesses
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  named_sync(1, TH);
+}
 
 template <int D, int BK, int MODE, int NQT, int NSTAGE>
 __global__ void __launch_bounds__(NQT * 128 + 128, (NQT == 1) ? 2 : 1)
@@ -135,11 +321,20 @@ __global__ void __launch_bounds__(NQT * 128 + 128, (NQT == 1) ? 2 : 1)
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint8_t* sQ = smem;
   uint8_t* sKV = smem + NQT * Cfg::kQTileBytes;
+  // fused routing: persistent lists and aggregates after the ring; the
+  // prologue's scratch (chunk, proxy rows, pooled Q) lives in the idle ring
+  constexpr int FR = Cfg::kFusedR, FKMAX = Cfg::kFusedMaxNKB;
+  uint8_t* sFused = sKV + NSTAGE * Cfg::kSlotBytes;
+  uint16_t* f_lists = reinterpret_cast<uint16_t*>(sFused);
+  float* f_T = reinterpret_cast<float*>(sFused + FR * FKMAX * 2);
+  int* f_cnt = reinterpret_cast<int*>(f_T + FR * D);
+  float* f_mu = reinterpret_cast<float*>(f_cnt + FR);
+  float* f_W = f_mu + FR;
 
   __shared__ uint64_t bar_q;
   __shared__ uint64_t bar_full[NSTAGE], bar_empty[NSTAGE];
   __shared__ uint64_t bar_s[NQT], bar_p[NQT], bar_o[NQT];
-  __shared__ uint64_t bar_mma_done, bar_drain;
+  __shared__ uint64_t bar_mma_done, bar_drain, bar_route;
   __shared__ uint32_t tmem_base_sh;
   __shared__ volatile int abort_flag;
 
@@ -165,7 +360,23 @@ __global__ void __launch_bounds__(NQT * 128 + 128, (NQT == 1) ? 2 : 1)
 
   TileMerge merge;
   merge.status = p.status;
-  if (MODE == kModeSparse) {
+  merge.smem_lists = false;
+#pragma unroll
+  for (int l = 0; l < 4; ++l) merge.sptr[l] = f_lists;
+  if (MODE == kModeSparseFused) {
+    // counts are filled in once the on-chip routing is done (route_ready)
+    merge.implicit = false;
+    merge.smem_lists = true;
+    merge.nlists = FR;
+    merge.limit = p.NKB;
+#pragma unroll
+    for (int l = 0; l < 4; ++l) {
+      merge.pos[l] = 0;
+      merge.n[l] = 0;
+      merge.ptr[l] = nullptr;
+      merge.sptr[l] = f_lists + (l < FR ? l : 0) * FKMAX;
+    }
+  } else if (MODE == kModeSparse) {
     merge.implicit = false;
     merge.nlists = NQT * QB;
     merge.limit = p.NKB;
@@ -211,6 +422,7 @@ __global__ void __launch_bounds__(NQT * 128 + 128, (NQT == 1) ? 2 : 1)
     }
     mbar_init(&bar_mma_done, 1);
     mbar_init(&bar_drain, 1);
+    mbar_init(&bar_route, 1);
     abort_flag = 0;
     fence_barrier_init();
   }
@@ -219,6 +431,11 @@ __global__ void __launch_bounds__(NQT * 128 + 128, (NQT == 1) ? 2 : 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_base_sh;
+  // fused routing: lists are ready once the softmax threads arrive on bar_route
+  auto take_fused_lists = [&]() {
+#pragma unroll
+    for (int l = 0; l < 4; ++l) merge.n[l] = (l < FR) ? f_cnt[l] : 0;
+  };
 
   if (warp >= Cfg::kProducerWarp) {
     setmaxnreg_dec<Cfg::kRegsControl>();
@@ -236,6 +453,10 @@ __global__ void __launch_bounds__(NQT * 128 + 128, (NQT == 1) ? 2 : 1)
       uint32_t flags;
       int u;
       bool ok = true;
+      if (MODE == kModeSparseFused) {
+        ok = bounded_wait(&bar_route, 0, &abort_flag, p.status);   // the ring holds routing scratch until then
+        take_fused_lists();
+      }
       while (ok && (u = merge.next(flags)) >= 0) {
         const int row = kv_lo + u * BK;
 #pragma unroll
@@ -260,6 +481,10 @@ __global__ void __launch_bounds__(NQT * 128 + 128, (NQT == 1) ? 2 : 1)
     // ======================= MMA issuer =======================
     if (lane == 0) {
       bool ok = bounded_wait(&bar_q, 0, &abort_flag, p.status);
+      if (MODE == kModeSparseFused) {
+        ok = ok && bounded_wait(&bar_route, 0, &abort_flag, p.status);
+        take_fused_lists();
+      }
       tc_fence_after();
       const uint32_t q_base = smem_u32(sQ);
       const uint32_t kv_base = smem_u32(sKV);
@@ -362,6 +587,15 @@ __global__ void __launch_bounds__(NQT * 128 + 128, (NQT == 1) ? 2 : 1)
     const uint32_t lane_base = (uint32_t)(w4 * 32) << 16;
     const uint32_t tS = tmem + lane_base + t * 256;
     const uint32_t tO = tS + 128;
+    if (MODE == kModeSparseFused) {
+      float* chunk = reinterpret_cast<float*>(sKV);
+      float* prow = chunk + Cfg::kFusedCH * D;
+      float* qs = prow + FR * FKMAX;
+      fused_route<D, FR, Cfg::kFusedCH, FKMAX, NQT * 128>(p, bh, qg * NQT * QB, tid, chunk, prow, qs, f_lists, f_cnt,
+                                                         f_mu, f_W, f_T);
+      if (tid == 0) mbar_arrive(&bar_route);
+      take_fused_lists();
+    }
     float m_run = -INFINITY;
     float l_run = 0.f;
     int it = 0;
@@ -481,6 +715,14 @@ __global__ void __launch_bounds__(NQT * 128 + 128, (NQT == 1) ? 2 : 1)
         // Taylor term for the rejected blocks of this row's query block
         float f = 0.f;
         const float* tt = nullptr;
+        if (MODE == kModeSparseFused) {
+          const int l = t * QB + qb;
+          if (qg * NQT * QB + l < p.NQB && f_cnt[l] < p.NKB) {
+            f = ex2_approx(f_mu[l] * kLog2e - m_run);
+            l_run += f * f_W[l];
+            tt = f_T + l * D;
+          }
+        }
         if (MODE == kModeSparse) {
           const long long qbi = (long long)(qg * NQT + t) * QB + qb;
           if (qbi < p.NQB) {
@@ -496,7 +738,7 @@ __global__ void __launch_bounds__(NQT * 128 + 128, (NQT == 1) ? 2 : 1)
           }
         }
         const bool empty = !have_o || !(l_run > 0.f);
-        if (empty && row_valid && it == 0 && MODE == kModeSparse) atomicOr(p.status, ATTN_DEVICE_BAD_LIST);
+        if (empty && row_valid && it == 0 && Cfg::kSparseLike) atomicOr(p.status, ATTN_DEVICE_BAD_LIST);
         const float inv = empty ? 0.f : 1.f / l_run;
         uint16_t* dst = p.out + ((long long)bh * p.Sq + grow) * D;
 #pragma unroll
@@ -515,7 +757,7 @@ __global__ void __launch_bounds__(NQT * 128 + 128, (NQT == 1) ? 2 : 1)
 #pragma unroll
               for (int e = 0; e < 8; ++e) {
                 float val = have_o ? __uint_as_float(rr[j + e]) : 0.f;
-                if (tt != nullptr) val = fmaf(f, __ldg(tt + c0 + j + e), val);
+                if (tt != nullptr) val = fmaf(f, tt[c0 + j + e], val);
                 o[e] = val * inv;
               }
               pk.x = pack_bf16x2(o[0], o[1]);

@@ -30,6 +30,9 @@ cudaError_t launch_attn_fwd_d128(int BK, int mode, const CUtensorMap& tq, const 
 // Query tiles of 128 rows per CTA for a mode (the grid is BH * ceil(Sq / (128 * tiles)) [* n_split]).
 inline int fwd_query_tiles(int mode) { return mode == kModeSplit ? 1 : 2; }
 
+// Largest key-block count the fused (on-chip routing) forward accepts.
+constexpr int kFusedMaxNKB = 1024;
+
 // Bounded-wait self-test kernel.
 cudaError_t launch_wait_selftest(int limit_us, int* status, cudaStream_t stream);
 
