@@ -149,6 +149,30 @@ __device__ __forceinline__ void route_load_rows(float (*dst)[D + 4], const float
   }
 }
 
+// One chunk of pooled rows held in registers (D/32 float4 per thread of 256):
+// the next chunk is fetched while the current one is being used from shared
+// memory, so the L2 latency of the stream overlaps the arithmetic.
+template <int D>
+struct ChunkRegs {
+  float4 v[D / 32];
+  __device__ __forceinline__ void load(const float* __restrict__ src, int row0, int nrows_total) {
+#pragma unroll
+    for (int k = 0; k < D / 32; ++k) {
+      const int e = threadIdx.x + k * 256;
+      const int r = e / (D / 4), c = (e % (D / 4)) * 4;
+      v[k] = (row0 + r < nrows_total) ? __ldg(reinterpret_cast<const float4*>(src + (long long)(row0 + r) * D + c))
+                                      : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+  }
+  __device__ __forceinline__ void store(float (*dst)[D + 4]) const {
+#pragma unroll
+    for (int k = 0; k < D / 32; ++k) {
+      const int e = threadIdx.x + k * 256;
+      *reinterpret_cast<float4*>(&dst[e / (D / 4)][(e % (D / 4)) * 4]) = v[k];
+    }
+  }
+};
+
 template <int D>
 __global__ void __launch_bounds__(256) route_kernel(const float* __restrict__ qp, const float* __restrict__ kp,
                                                     const float* __restrict__ vp, int NQB, int NKB, int S,
@@ -171,9 +195,12 @@ __global__ void __launch_bounds__(256) route_kernel(const float* __restrict__ qp
   float wn[2] = {0.f, 0.f}, wmean[2] = {0.f, 0.f}, wm2[2] = {0.f, 0.f};
   float bmax[2] = {-INFINITY, -INFINITY};
   int bidx[2] = {INT_MAX, INT_MAX};
+  ChunkRegs<D> kreg;
+  kreg.load(kh, 0, NKB);
   for (int j0 = 0; j0 < NKB; j0 += kRouteChunk) {
     __syncthreads();
-    route_load_rows<D>(sm.k, kh, j0, NKB, kRouteChunk);
+    kreg.store(sm.k);
+    if (j0 + kRouteChunk < NKB) kreg.load(kh, j0 + kRouteChunk, NKB);
     __syncthreads();
     float s[2][2];
     route_scores<D>(sm, ti, tj, scale, s);
@@ -255,10 +282,17 @@ __global__ void __launch_bounds__(256) route_kernel(const float* __restrict__ qp
 #pragma unroll
   for (int m = 0; m < D / 32; ++m) tacc[m][0] = tacc[m][1] = tacc[m][2] = tacc[m][3] = 0.f;
   float wsum = 0.f;
+  ChunkRegs<D> vreg;
+  kreg.load(kh, 0, NKB);
+  vreg.load(vh, 0, NKB);
   for (int j0 = 0; j0 < NKB; j0 += kRouteChunk) {
     __syncthreads();
-    route_load_rows<D>(sm.k, kh, j0, NKB, kRouteChunk);
-    route_load_rows<D>(sm.v, vh, j0, NKB, kRouteChunk);
+    kreg.store(sm.k);
+    vreg.store(sm.v);
+    if (j0 + kRouteChunk < NKB) {
+      kreg.load(kh, j0 + kRouteChunk, NKB);
+      vreg.load(vh, j0 + kRouteChunk, NKB);
+    }
     __syncthreads();
     float s[2][2];
     route_scores<D>(sm, ti, tj, scale, s);
