@@ -14,7 +14,9 @@ aggregates (W, T) and the Taylor-corrected sparse output follow this build's
 reading of the Sol-Attn page (first order about the row-mean proxy score,
 applied per block with pooled V); they are pinned only against a
 hand-derived closed form of that reading: parity unpinned with respect to the
-pages.
+pages.  3D neighbourhood attention follows the published definition of
+neighbourhood attention (the pages name the kernel but do not define it) and
+is pinned by closed forms, an independent brute force and a mirror symmetry.
 """
 from __future__ import annotations
 
@@ -59,8 +61,10 @@ def _configure(lib):
                                  ctypes.c_int, _U8, _D, _U8, _I64, _D, _D, _D, _D, _D, _I64]
     lib.oracle_sparse_rows.argtypes = [_D, _D, _D, _i64, _i64, _i64, _i64, _i64, _U8, _D, _D, _D,
                                        ctypes.c_double, _I64, _i64, _D, _D]
+    lib.oracle_na3d_rows.argtypes = [_D, _D, _D, _i64, _i64, _i64, _i64, _i64, _i64, _i64, _i64, ctypes.c_double,
+                                     _I64, _i64, _D, _D]
     for f in (lib.oracle_attend_rows, lib.oracle_split_partials, lib.oracle_lse_merge, lib.oracle_block_pool,
-              lib.oracle_route, lib.oracle_sparse_rows):
+              lib.oracle_route, lib.oracle_sparse_rows, lib.oracle_na3d_rows):
         f.restype = None
     return lib
 
@@ -213,3 +217,30 @@ def sparse_route_attention(q, k, v, block_q: int, block_k: int, scale: float, be
     rt = route(qp, kp, vp, S, block_k, scale, beta)
     out, lse = sparse_attention(q, k, v, block_q, block_k, rt["sel"], rt["mu"], rt["W"], rt["T"], scale, rows)
     return out, lse, rt, (qp, kp, vp)
+
+
+def na3d_attention(q, k, v, grid, kernel, scale: float, rows=None):
+    """3D neighbourhood attention.  q, k, v: [B,H,S,d] with S = T*Y*X tokens in
+    raster order (t, y, x), x fastest; grid = (T, Y, X); kernel = (Kt, Ky, Kx)
+    with 1 <= K <= L per axis.
+
+    rows=None evaluates every row and returns (out [B,H,S,d], lse [B,H,S]);
+    otherwise ``rows`` holds flat row indices (b*H + h)*S + i and the result is
+    (out [n, d], lse [n])."""
+    q, k, v = _bhsd(q), _bhsd(k), _bhsd(v)
+    B, H, S, d = q.shape
+    T, Y, X = (int(g) for g in grid)
+    Kt, Ky, Kx = (int(g) for g in kernel)
+    if T * Y * X != S or k.shape != q.shape or v.shape != q.shape:
+        raise ValueError("grid does not match the tensors")
+    if not (1 <= Kt <= T and 1 <= Ky <= Y and 1 <= Kx <= X):
+        raise ValueError("window must satisfy 1 <= K <= L on every axis")
+    full = rows is None
+    r = np.arange(B * H * S, dtype=np.int64) if full else np.ascontiguousarray(rows, dtype=np.int64)
+    out = np.empty((r.size, d))
+    lse = np.empty(r.size)
+    _load().oracle_na3d_rows(_p(q, _D), _p(k, _D), _p(v, _D), B * H, T, Y, X, d, Kt, Ky, Kx, float(scale),
+                             _p(r, _I64), r.size, _p(out, _D), _p(lse, _D))
+    if full:
+        return out.reshape(B, H, S, d), lse.reshape(B, H, S)
+    return out, lse

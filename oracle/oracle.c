@@ -23,11 +23,21 @@
  *    tau_i = mu_i + beta*sigma_i over block proxy-score statistics, pooled
  *    keys, and a Taylor expansion around the row-wise mean score for rejected
  *    blocks.
+ *  - "LTX-2.5 at 4K, in half the time", section "Inside the decoder", and
+ *    "Optimization Tips" (LTX-2 pipelines documentation), section "Diffusion
+ *    VAE Decoder": the video decoder spends most of its time in a
+ *    neighbourhood-attention kernel over (frame, height, width) volumes.  The
+ *    pages do not define the window; oracle_na3d_rows uses the published
+ *    neighbourhood-attention definition (each query attends to the K keys per
+ *    axis nearest to it, the window shifted inward at the borders).
  *
  * Parity status per function (what pins it is listed in the test suite):
  *  - oracle_attend_rows, oracle_split_partials, oracle_lse_merge,
  *    oracle_block_pool, oracle_route (proxy, mu, sigma, tau, selection):
  *    pinned by closed forms, library routines and invariants.
+ *  - oracle_na3d_rows: pinned by closed forms (a window of one token, a
+ *    window covering the whole grid), a brute-force masked softmax with the
+ *    window found by a different construction, and a mirror symmetry.
  *  - oracle_route (Taylor aggregates W, T) and oracle_sparse_rows: the pages
  *    give no formula for the Taylor term.  The first-order block-level form
  *    used here is this build's reading; it is pinned by a hand-derived closed
@@ -302,6 +312,75 @@ void oracle_sparse_rows(const double* q, const double* k, const double* v, int64
       for (int64_t c = 0; c < d; ++c) o[c] /= den;
       lse[r] = M + log(den);
     }
+    free(xbuf);
+  }
+}
+
+/* First coordinate of the neighbourhood window along one axis of length L for
+ * a query at coordinate p and a window of K positions (1 <= K <= L): the
+ * window is centred on p, [p - floor(K/2), p - floor(K/2) + K), and moved
+ * inward when it would cross either border, so it always holds exactly K
+ * in-range positions and contains p. */
+static int64_t na_window_start(int64_t p, int64_t K, int64_t L) {
+  int64_t s = p - K / 2;
+  if (s < 0) s = 0;
+  if (s > L - K) s = L - K;
+  return s;
+}
+
+/* 3D neighbourhood attention over a T x Y x X token volume, evaluated on the
+ * listed rows.  Tokens of a head are stored in raster order (t, y, x), x
+ * fastest: token index i = (t*Y + y)*X + x.  q, k, v: [B*H][T*Y*X][d];
+ * rows[r] = (b*H + h)*S + i.  For the query at (t, y, x) the keys are the
+ * Kt x Ky x Kx tokens of the window whose per-axis start is
+ * na_window_start(coordinate, K, L); over them
+ *   x_k = scale <q, k_k>,  M = max x_k,  l = sum exp(x_k - M),
+ *   o = sum exp(x_k - M) v_k / l,  lse = M + ln l,
+ * visiting the keys in ascending token order. */
+void oracle_na3d_rows(const double* q, const double* k, const double* v, int64_t BH, int64_t T, int64_t Y, int64_t X,
+                      int64_t d, int64_t Kt, int64_t Ky, int64_t Kx, double scale, const int64_t* rows,
+                      int64_t n_rows, double* out, double* lse) {
+  (void)BH;
+  const int64_t S = T * Y * X;
+  const int64_t nwin = Kt * Ky * Kx;
+#pragma omp parallel
+  {
+    double* xbuf = (double*)malloc(sizeof(double) * (size_t)(nwin > 0 ? nwin : 1));
+    int64_t* kbuf = (int64_t*)malloc(sizeof(int64_t) * (size_t)(nwin > 0 ? nwin : 1));
+#pragma omp for schedule(dynamic, 4)
+    for (int64_t r = 0; r < n_rows; ++r) {
+      const int64_t flat = rows[r];
+      const int64_t bh = flat / S, i = flat % S;
+      const int64_t pt = i / (Y * X), py = (i / X) % Y, px = i % X;
+      const int64_t t0 = na_window_start(pt, Kt, T);
+      const int64_t y0 = na_window_start(py, Ky, Y);
+      const int64_t x0 = na_window_start(px, Kx, X);
+      const double* qrow = q + flat * d;
+      const double* kh = k + bh * S * d;
+      const double* vh = v + bh * S * d;
+      int64_t n = 0;
+      for (int64_t tt = t0; tt < t0 + Kt; ++tt)
+        for (int64_t yy = y0; yy < y0 + Ky; ++yy)
+          for (int64_t xx = x0; xx < x0 + Kx; ++xx) kbuf[n++] = (tt * Y + yy) * X + xx;
+      double M = -INFINITY;
+      for (int64_t j = 0; j < n; ++j) {
+        double dot = 0.0;
+        for (int64_t c = 0; c < d; ++c) dot += qrow[c] * kh[kbuf[j] * d + c];
+        xbuf[j] = scale * dot;
+        if (xbuf[j] > M) M = xbuf[j];
+      }
+      double* o = out + r * d;
+      for (int64_t c = 0; c < d; ++c) o[c] = 0.0;
+      double l = 0.0;
+      for (int64_t j = 0; j < n; ++j) {
+        double p = exp(xbuf[j] - M);
+        l += p;
+        for (int64_t c = 0; c < d; ++c) o[c] += p * vh[kbuf[j] * d + c];
+      }
+      for (int64_t c = 0; c < d; ++c) o[c] /= l;
+      lse[r] = M + log(l);
+    }
+    free(kbuf);
     free(xbuf);
   }
 }

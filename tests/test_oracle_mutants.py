@@ -16,7 +16,7 @@ MUTANTS = [
     ("dense: no max shift", "double p = exp(xbuf[j - lo] - M);", "double p = exp(xbuf[j - lo]);"),
     ("dense: score sign", "double x = scale * dot;\n    xbuf[j - lo] = x;", "double x = -scale * dot;\n    xbuf[j - lo] = x;"),
     ("dense: q.v instead of q.k", "dot += q[c] * k[j * d + c];", "dot += q[c] * v[j * d + c];"),
-    ("dense: no normalisation", "for (int64_t c = 0; c < d; ++c) o[c] /= l;", ""),
+    ("dense: no normalisation", "o[c] /= l;\n  *lse = M + log(l);", "\n  *lse = M + log(l);"),
     ("dense: lse without max", "*lse = M + log(l);", "*lse = log(l);"),
     ("split: overlapping chunks", "int64_t hi = ((c + 1) * Skv) / n_split;", "int64_t hi = ((c + 1) * Skv) / n_split + 1 < Skv ? ((c + 1) * Skv) / n_split + 1 : Skv;"),
     ("merge: weights against M", "double w = exp(lse_part[c * rows + r] - L);", "double w = exp(lse_part[c * rows + r] - M);"),
@@ -32,6 +32,14 @@ MUTANTS = [
     ("sparse: factor sign", "double f = exp(mu[t] - M);", "double f = exp(M - mu[t]);"),
     ("sparse: Taylor mass missing in den", "den += f * W[t];", ""),
     ("sparse: Taylor missing in num", "o[c] += f * T[t * d + c];", ";"),
+    ("na: window centred half a step late", "int64_t s = p - K / 2;", "int64_t s = p - (K - 1) / 2;"),
+    ("na: low border reflected", "if (s < 0) s = 0;", "if (s < 0) s = -s;"),
+    ("na: high border not shifted inward", "if (s > L - K) s = L - K;", "if (s > L - K) s = (L - K) / 2;"),
+    ("na: one frame short", "for (int64_t tt = t0; tt < t0 + Kt; ++tt)", "for (int64_t tt = t0; tt < t0 + Kt - 1; ++tt)"),
+    ("na: y-fastest raster order", "kbuf[n++] = (tt * Y + yy) * X + xx;", "kbuf[n++] = (tt * X + xx) * Y + yy;"),
+    ("na: q.v instead of q.k", "dot += qrow[c] * kh[kbuf[j] * d + c];", "dot += qrow[c] * vh[kbuf[j] * d + c];"),
+    ("na: lse without max", "lse[r] = M + log(l);", "lse[r] = log(l);"),
+    ("na: no normalisation", "o[c] /= l;\n      lse[r] = M + log(l);", "\n      lse[r] = M + log(l);"),
 ]
 
 PINS = [
@@ -50,6 +58,11 @@ PINS = [
     pins.test_sparse_without_taylor_equals_masked_library_attention,
     pins.test_taylor_hand_derived_closed_form,
     pins.test_taylor_constant_v_and_unit_mass,
+    lambda: pins.test_na3d_matches_masked_library_attention(*pins.NA_CASES[0]),
+    lambda: pins.test_na3d_matches_masked_library_attention(*pins.NA_CASES[1]),
+    lambda: pins.test_na3d_window_indicator(*pins.NA_CASES[0]),
+    pins.test_na3d_single_token_window_returns_own_value,
+    lambda: pins.test_na3d_mirror_symmetry_odd_window(0),
 ]
 
 

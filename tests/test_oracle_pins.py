@@ -375,3 +375,101 @@ def test_route_forced_selection_matches_threshold_rule_on_its_own_selection():
     flip[0, 0, 0, 0] = ~flip[0, 0, 0, 0]
     ff = oracle.route(qp, kp, vp, 384, 64, 0.25, 0.3, force_sel=flip)
     assert ff["sel_cnt"][0, 0, 0] == rt["sel_cnt"][0, 0, 0] + (1 if flip[0, 0, 0, 0] else -1)
+
+
+# ---------------------------------------------------------------- 3D neighbourhood attention
+
+def nearest_window(p, K, L):
+    """Start of the K-position window nearest to p: among all starts whose window
+    lies inside [0, L), the one whose centre p' = s + K//2 is closest to p
+    (a search over feasible windows, not the clamp formula)."""
+    starts = np.arange(L - K + 1)
+    return int(starts[np.argmin(np.abs(starts + K // 2 - p))])
+
+
+def na_mask(grid, kernel):
+    """Boolean [S, S] key mask of 3D neighbourhood attention, built token by token."""
+    T, Y, X = grid
+    S = T * Y * X
+    coords = [(t, y, x) for t in range(T) for y in range(Y) for x in range(X)]
+    mask = np.zeros((S, S), dtype=bool)
+    for i, c in enumerate(coords):
+        lo = [nearest_window(c[a], kernel[a], grid[a]) for a in range(3)]
+        for j, e in enumerate(coords):
+            mask[i, j] = all(lo[a] <= e[a] < lo[a] + kernel[a] for a in range(3))
+    return mask
+
+
+NA_CASES = [((3, 5, 6), (3, 3, 3)), ((4, 6, 5), (2, 4, 3)), ((1, 7, 9), (1, 5, 4)), ((5, 4, 4), (3, 4, 1)),
+            ((2, 3, 8), (2, 1, 8))]
+
+
+@pytest.mark.parametrize("grid,kernel", NA_CASES)
+def test_na3d_matches_masked_library_attention(grid, kernel):
+    S = int(np.prod(grid))
+    d = 8
+    q, k, v = rand(1, 2, S, d), rand(1, 2, S, d), rand(1, 2, S, d)
+    scale = 0.45
+    out, lse = oracle.na3d_attention(q, k, v, grid, kernel, scale)
+    mask = na_mask(grid, kernel)
+    add = np.where(mask, 0.0, -np.inf)[None, None]
+    np.testing.assert_allclose(out, sdpa64(q, k, v, scale, mask=add), rtol=0, atol=1e-12)
+    scores = scale * np.einsum("bhqd,bhkd->bhqk", q, k) + add
+    np.testing.assert_allclose(lse, scipy.special.logsumexp(scores, axis=-1), rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("grid,kernel", NA_CASES[:3])
+def test_na3d_window_indicator(grid, kernel):
+    # uniform scores and one-hot values: row i of the output is the window of
+    # query i divided by its size, so the exact key set is visible
+    S = int(np.prod(grid))
+    q = np.zeros((1, 1, S, S))
+    v = np.eye(S)[None, None]
+    out, lse = oracle.na3d_attention(q, q, v, grid, kernel, 1.0)
+    n = int(np.prod(kernel))
+    np.testing.assert_allclose(out[0, 0], na_mask(grid, kernel) / n, rtol=0, atol=1e-15)
+    np.testing.assert_array_equal((out[0, 0] > 0).sum(axis=1), n)
+    np.testing.assert_allclose(lse, math.log(n), atol=1e-14)
+
+
+def test_na3d_single_token_window_returns_own_value():
+    grid = (2, 3, 4)
+    S, d = 24, 16
+    q, k, v = rand(2, 1, S, d), rand(2, 1, S, d), rand(2, 1, S, d)
+    out, lse = oracle.na3d_attention(q, k, v, grid, (1, 1, 1), 0.3)
+    np.testing.assert_array_equal(out, v)
+    np.testing.assert_allclose(lse, 0.3 * np.einsum("bhsd,bhsd->bhs", q, k), rtol=0, atol=1e-13)
+
+
+def test_na3d_full_window_equals_library_dense():
+    grid = (3, 4, 5)
+    S, d = 60, 32
+    q, k, v = rand(1, 3, S, d), rand(1, 3, S, d), rand(1, 3, S, d)
+    out, lse = oracle.na3d_attention(q, k, v, grid, grid, 0.2)
+    np.testing.assert_allclose(out, sdpa64(q, k, v, 0.2), rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse, scipy.special.logsumexp(0.2 * np.einsum("bhqd,bhkd->bhqk", q, k), axis=-1),
+                               rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("axis", [0, 1, 2])
+def test_na3d_mirror_symmetry_odd_window(axis):
+    # an odd window is centred, so mirroring the volume along an axis mirrors the output
+    grid, kernel = (5, 6, 7), (3, 3, 5)
+    S, d = 210, 8
+    q, k, v = rand(1, 1, S, d), rand(1, 1, S, d), rand(1, 1, S, d)
+    flip = lambda a: np.flip(a.reshape(1, 1, *grid, -1), axis=2 + axis).reshape(1, 1, S, -1)
+    out, lse = oracle.na3d_attention(q, k, v, grid, kernel, 0.5)
+    fo, fl = oracle.na3d_attention(flip(q), flip(k), flip(v), grid, kernel, 0.5)
+    np.testing.assert_allclose(flip(fo), out, rtol=0, atol=1e-13)
+    np.testing.assert_allclose(flip(fl[..., None])[..., 0], lse, rtol=0, atol=1e-13)
+
+
+def test_na3d_row_subset_matches_full():
+    grid, kernel = (3, 5, 6), (2, 3, 3)
+    S, d = 90, 8
+    q, k, v = rand(2, 2, S, d), rand(2, 2, S, d), rand(2, 2, S, d)
+    out, lse = oracle.na3d_attention(q, k, v, grid, kernel, 0.4)
+    rows = np.array([0, 17, 89, 90, 200, 359])
+    ro, rl = oracle.na3d_attention(q, k, v, grid, kernel, 0.4, rows=rows)
+    np.testing.assert_array_equal(ro, out.reshape(-1, d)[rows])
+    np.testing.assert_array_equal(rl, lse.reshape(-1)[rows])

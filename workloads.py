@@ -7,7 +7,9 @@ in raster (t, y, x) order, with audio tokens interleaved per frame for the
 Stage-2 self-attention ("Accelerating LTX-2.5 with Sol Engine", section
 "Stage 2 Optimization") and ~100 audio queries against a video KV for the
 cross attention ("LTX-2.5 at 4K, in half the time", section "Attention
-across two GPUs").
+across two GPUs").  The neighbourhood-attention workload is a decoder tile of
+four latent frames ("LTX-2.5 at 4K, in half the time", section "Inside the
+decoder": each decoder tile holds four frames) over a 128 x 128 grid.
 
 Recipe: a ``torch.Generator`` on the requested device, seeded per workload,
 draws float32 noise for q, k, v in that order; a fixed 3D sinusoidal position
@@ -108,6 +110,9 @@ WORKLOADS = {
     # beta sweep at 32x64x64 (no audio)
     "sweep128k": Workload("sweep128k", B=1, H=32, Sq=131072, Skv=131072, d=128, seed=5, q_std=0.5, k_std=0.5,
                           grid=(32, 64, 64), pe=True, block=128, beta=1.0),
+    # 3D neighbourhood attention over a 4x128x128 decoder tile, window 3x7x7 (frames x rows x columns)
+    "na3d": Workload("na3d", B=1, H=32, Sq=65536, Skv=65536, d=128, seed=6, grid=(4, 128, 128), pe=True,
+                     extra={"kernel": (3, 7, 7)}),
 }
 
 
