@@ -200,6 +200,49 @@ attn_status_t attn_sparse_fused_fwd(const attn_bf16* q, const attn_bf16* k, cons
                                     int32_t* sel_cnt, float* stats, float* taylor_t, cudaStream_t stream);
 
 /*
+ * 3D neighbourhood attention over a (T, Y, X) token volume.
+ * ("LTX-2.5 at 4K, in half the time", section "Inside the decoder": the video
+ * decoder's time goes mostly to a neighbourhood-attention kernel; "Optimization
+ * Tips", section "Diffusion VAE Decoder": the decoder's neighbourhood-attention
+ * backends.  The window follows the published neighbourhood-attention
+ * definition, which the pages do not restate.)
+ *
+ *   For the query at (t, y, x) the keys are the Kt x Ky x Kx tokens whose
+ *   coordinate on each axis lies in [s, s + K) with s = clamp(p - floor(K/2),
+ *   0, L - K): the window is centred on the query and moved inward at the
+ *   borders, so every query sees exactly Kt*Ky*Kx keys, itself included.
+ *   Over them: O = softmax(scale * q k^T) V, lse = log of the denominator
+ *   (natural log, including the max).  Non-causal, dilation 1.
+ *
+ *   q, k, v, out  bf16 [B][H][S][d], S = T*Y*X tokens in raster order
+ *                 (t, y, x), x fastest; 16-byte aligned; d in {64, 128}.
+ *   lse           nullable, fp32 [B][H][S].
+ *   Kt, Ky, Kx    window per axis, 1 <= K <= L (T, Y, X).
+ *   scale         softmax scale, finite and > 0.
+ *   brick         query/key tile shape, frames x rows x columns of 128 tokens:
+ *                 1 = 1x8x16, 2 = 2x8x8, 3 = 4x4x8, 0 = chosen by the library.
+ *   pair_axis     axis along which a CTA's two query bricks are neighbours:
+ *                 0 = frames, 1 = rows, 2 = columns, -1 = chosen by the library.
+ *   The choice only changes speed, never results beyond fp32 rounding order.
+ *   Errors: ATTN_ERR_INVALID_ARG (null or misaligned pointer, a window outside
+ *   [1, L], S > 2^30, non-positive scale, bad brick/pair code),
+ *   ATTN_ERR_UNSUPPORTED (d), ATTN_ERR_CUDA (launch).  Asynchronous on stream.
+ */
+attn_status_t attn_na3d_fwd(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v, attn_bf16* out, float* lse,
+                            int B, int H, int T, int Y, int X, int d, int Kt, int Ky, int Kx, float scale, int brick,
+                            int pair_axis, cudaStream_t stream);
+
+/*
+ * The tile plan attn_na3d_fwd uses for a volume and window.  On entry *brick
+ * and *pair_axis hold the caller's request (0 / -1 = open); on return the
+ * plan.  *key_boxes (nullable) receives the number of 128-key boxes the query
+ * tiles of one head multiply: the executed work of one head is
+ * key_boxes * 4 * 128 * 128 * d floating-point operations.  Host only.
+ */
+attn_status_t attn_na3d_plan(int T, int Y, int X, int Kt, int Ky, int Kx, int* brick, int* pair_axis,
+                             long long* key_boxes);
+
+/*
  * Size of the library-owned device scratch used by
  * attn_sparse_route_fwd_noalloc (32 MiB on every device that loads the
  * library, held until the process exits).

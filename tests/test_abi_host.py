@@ -6,6 +6,7 @@ import math
 import os
 import re
 
+import numpy as np
 import pytest
 
 import video_diffusion_transformer_block_gb300 as vd
@@ -106,3 +107,114 @@ def test_fused_sparse_rejections(lib):
                                      None, None, None, None, None) == 3
     assert lib.attn_sparse_fused_fwd(P, P, P, P, P, 1, 1, 4096, 128, 0.088, math.inf, 128, 128, ws, big,
                                      None, None, None, None, None) == 1
+
+
+# ---------------------------------------------------------------- 3D neighbourhood attention (host logic)
+
+BRICKS = {1: (1, 8, 16), 2: (2, 8, 8), 3: (4, 4, 8)}
+
+
+def na_start(p, K, L):
+    return min(max(p - K // 2, 0), L - K)
+
+
+def na_walk(grid, kernel, brick, pair):
+    """Python restatement of the kernel's box walk: yields, per CTA, the two query
+    bricks (origin or None) and the boxes with their tile flags."""
+    B = BRICKS[brick]
+    nq = [-(-grid[a] // B[a]) for a in range(3)]
+    np_ = [(-(-nq[a] // 2) if a == pair else nq[a]) for a in range(3)]
+    for it in range(np_[0]):
+        for iy in range(np_[1]):
+            for ix in range(np_[2]):
+                idx = [it, iy, ix]
+                tiles = []
+                for t in range(2):
+                    ib = [2 * idx[a] + t if a == pair else idx[a] for a in range(3)]
+                    if ib[pair] >= nq[pair]:
+                        continue
+                    org = [ib[a] * B[a] for a in range(3)]
+                    lo = [na_start(org[a], kernel[a], grid[a]) for a in range(3)]
+                    hi = [na_start(min(org[a] + B[a], grid[a]) - 1, kernel[a], grid[a]) + kernel[a] for a in range(3)]
+                    tiles.append((org, lo, hi))
+                cu = [min(tl[1][a] for tl in tiles) for a in range(3)]
+                nk = [-(-(max(tl[2][a] for tl in tiles) - cu[a]) // B[a]) for a in range(3)]
+                boxes = []
+                for ut in range(nk[0]):
+                    for uy in range(nk[1]):
+                        for ux in range(nk[2]):
+                            box = [cu[0] + ut * B[0], cu[1] + uy * B[1], cu[2] + ux * B[2]]
+                            flags = [all(box[a] < tl[2][a] and box[a] + B[a] > tl[1][a] for a in range(3))
+                                     for tl in tiles]
+                            if any(flags):
+                                boxes.append((box, flags))
+                yield tiles, boxes
+
+
+@pytest.mark.parametrize("grid,kernel", [((3, 13, 21), (3, 5, 7)), ((5, 11, 19), (3, 5, 4)), ((1, 20, 24), (1, 9, 9)),
+                                         ((4, 16, 32), (2, 16, 1)), ((2, 5, 6), (2, 5, 6))])
+@pytest.mark.parametrize("brick", [1, 2, 3])
+@pytest.mark.parametrize("pair", [0, 1, 2])
+def test_na3d_walk_covers_every_window_and_plan_counts_it(lib, grid, kernel, brick, pair):
+    B = BRICKS[brick]
+    work = 0
+    for tiles, boxes in na_walk(grid, kernel, brick, pair):
+        for t, (org, lo, hi) in enumerate(tiles):
+            mine = [box for box, fl in boxes if fl[t]]
+            work += len(mine)
+            # every key of every query's window lies in a box flagged for this tile
+            for dt in range(B[0]):
+                for dy in range(B[1]):
+                    for dx in range(B[2]):
+                        c = (org[0] + dt, org[1] + dy, org[2] + dx)
+                        if any(c[a] >= grid[a] for a in range(3)):
+                            continue
+                        ws = [na_start(c[a], kernel[a], grid[a]) for a in range(3)]
+                        for a in range(3):
+                            covered = set()
+                            for box in mine:
+                                covered.update(range(box[a], box[a] + B[a]))
+                            assert set(range(ws[a], ws[a] + kernel[a])) <= covered
+                        corners = [(ws[0] + e0 * (kernel[0] - 1), ws[1] + e1 * (kernel[1] - 1), ws[2] + e2 * (kernel[2] - 1))
+                                   for e0 in (0, 1) for e1 in (0, 1) for e2 in (0, 1)]
+                        for kc in corners:
+                            assert any(all(box[a] <= kc[a] < box[a] + B[a] for a in range(3)) for box in mine)
+    b, pa, nb = ctypes.c_int(brick), ctypes.c_int(pair), ctypes.c_longlong(0)
+    assert lib.attn_na3d_plan(*grid, *kernel, ctypes.byref(b), ctypes.byref(pa), ctypes.byref(nb)) == 0
+    assert (b.value, pa.value) == (brick, pair)
+    assert nb.value == work
+
+
+def test_na3d_plan_picks_the_least_work(lib):
+    # cost of a plan = key boxes multiplied + 3 per CTA; the open plan is the minimum over all nine
+    for grid, kernel in [((4, 128, 128), (3, 7, 7)), ((4, 64, 64), (3, 31, 31)), ((1, 96, 160), (1, 13, 13))]:
+        costs = {}
+        for brick in (1, 2, 3):
+            for pair in (0, 1, 2):
+                _, _, nbox = vd.attn_na3d_plan(grid, kernel, brick, pair)
+                nq = [-(-grid[a] // BRICKS[brick][a]) for a in range(3)]
+                ctas = np.prod([(-(-nq[a] // 2) if a == pair else nq[a]) for a in range(3)])
+                costs[(brick, pair)] = nbox + 3 * ctas
+                assert nbox * 128 * 128 >= np.prod(grid) * np.prod(kernel)   # the boxes hold every window
+        b, pa, nb = vd.attn_na3d_plan(grid, kernel)
+        assert costs[(b, pa)] == min(costs.values())
+
+
+def test_na3d_rejections(lib):
+    base = [P, P, P, P, P, 1, 2, 4, 16, 16, 128, 3, 5, 5, 0.088, 0, -1, None]
+    for i, bad in [(11, 0), (11, 5), (12, 17), (13, 0), (7, 0), (14, 0.0), (14, math.nan), (15, 4), (15, -1),
+                   (16, 3), (16, -2)]:
+        args = list(base)
+        args[i] = bad
+        assert lib.attn_na3d_fwd(*args) == 1, (i, bad)
+    args = list(base)
+    args[10] = 96
+    assert lib.attn_na3d_fwd(*args) == 2
+    args = list(base)
+    args[0] = NULL
+    assert lib.attn_na3d_fwd(*args) == 1
+    args = list(base)
+    args[3] = MIS
+    assert lib.attn_na3d_fwd(*args) == 1
+    b, pa = ctypes.c_int(0), ctypes.c_int(-1)
+    assert lib.attn_na3d_plan(4, 16, 16, 5, 3, 3, ctypes.byref(b), ctypes.byref(pa), None) == 1   # Kt > T

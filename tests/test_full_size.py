@@ -115,3 +115,22 @@ def test_sweep128k_full_size(beta):
     flips, density = sparse_full_size(w, beta, n_rows=512, n_heads=2, seed=105)
     if beta == -math.inf:
         assert density == 1.0
+
+
+def test_na3d_full_size_sampled_rows():
+    w = WORKLOADS["na3d"]
+    q, k, v = make_qkv(w, device="cuda")
+    out, lse = vd.attn_na3d_fwd(q, k, v, w.grid, w.extra["kernel"])
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(107)
+    hs = sample_heads(w.H, rng)
+    qh, kh, vh = (host(x[:, hs].contiguous()) for x in (q, k, v))
+    # every row of the first and last sampled head, 4096 sampled rows of the others
+    rows = np.concatenate([np.arange(w.Sq), (len(hs) - 1) * w.Sq + np.arange(w.Sq),
+                           rng.choice(np.arange(w.Sq, (len(hs) - 1) * w.Sq), size=4096, replace=False)])
+    rows = np.sort(rows)
+    ro, rl = oracle.na3d_attention(qh, kh, vh, w.grid, w.extra["kernel"], w.scale, rows=rows)
+    go = host(out[:, hs].contiguous()).reshape(-1, w.d)[rows]
+    gl = host(lse[:, hs].contiguous()).reshape(-1)[rows]
+    assert_close(go, ro, "na3d out")
+    assert_close(gl, rl, "na3d lse")

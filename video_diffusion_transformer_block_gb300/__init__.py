@@ -20,7 +20,8 @@ __all__ = [
     "AttnError", "load_library", "attn_dense_fwd", "attn_cross_splitkv_fwd", "attn_lse_merge", "attn_block_pool",
     "attn_sparse_workspace_bytes", "attn_sparse_route_fwd", "attn_sparse_route", "attn_sparse_fwd",
     "attn_last_device_status", "attn_status_string", "attn_selftest_wait_timeout",
-    "attn_sparse_route_fwd_noalloc", "attn_sparse_fused_fwd", "NOALLOC_WORKSPACE_BYTES", "EXPORTED_SYMBOLS",
+    "attn_sparse_route_fwd_noalloc", "attn_sparse_fused_fwd", "attn_na3d_fwd", "attn_na3d_plan",
+    "NOALLOC_WORKSPACE_BYTES", "EXPORTED_SYMBOLS",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -31,7 +32,8 @@ _lib = None
 EXPORTED_SYMBOLS = (
     "attn_dense_fwd", "attn_cross_splitkv_fwd", "attn_lse_merge", "attn_block_pool", "attn_sparse_workspace_bytes",
     "attn_sparse_route_fwd", "attn_sparse_route", "attn_sparse_fwd", "attn_last_device_status", "attn_status_string",
-    "attn_selftest_wait_timeout", "attn_sparse_route_fwd_noalloc", "attn_sparse_fused_fwd",
+    "attn_selftest_wait_timeout", "attn_sparse_route_fwd_noalloc", "attn_sparse_fused_fwd", "attn_na3d_fwd",
+    "attn_na3d_plan",
 )
 
 # Size of the library-owned scratch of attn_sparse_route_fwd_noalloc (ATTN_NOALLOC_WORKSPACE_BYTES).
@@ -70,13 +72,17 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         lib.attn_sparse_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, i, vp, vp, vp, vp, vp]
         lib.attn_sparse_route_fwd_noalloc.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, f, i, i, vp]
         lib.attn_sparse_fused_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, f, i, i, vp, sz, vp, vp, vp, vp, vp]
+        lib.attn_na3d_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, i, f, i, i, vp]
+        ip, llp = ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_longlong)
+        lib.attn_na3d_plan.argtypes = [i, i, i, i, i, i, ip, ip, llp]
         lib.attn_last_device_status.argtypes = [vp]
         lib.attn_status_string.argtypes = [i]
         lib.attn_status_string.restype = ctypes.c_char_p
         lib.attn_selftest_wait_timeout.argtypes = [i, vp]
         for name in ("attn_dense_fwd", "attn_cross_splitkv_fwd", "attn_lse_merge", "attn_block_pool",
                      "attn_sparse_route_fwd", "attn_sparse_route", "attn_sparse_fwd", "attn_last_device_status",
-                     "attn_selftest_wait_timeout", "attn_sparse_route_fwd_noalloc", "attn_sparse_fused_fwd"):
+                     "attn_selftest_wait_timeout", "attn_sparse_route_fwd_noalloc", "attn_sparse_fused_fwd",
+                     "attn_na3d_fwd", "attn_na3d_plan"):
             getattr(lib, name).restype = ctypes.c_int
         if path is None:
             _lib = lib
@@ -118,6 +124,37 @@ def attn_dense_fwd(q, k, v, scale=None, out=None, lse=None, stream=None):
     lse = torch.empty((B, H, Sq), dtype=torch.float32, device=q.device) if lse is None else lse
     _check("attn_dense_fwd", lib.attn_dense_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, Sq, Skv, d,
                                                 scale, _stream(stream)))
+    return out, lse
+
+
+def attn_na3d_plan(grid, kernel, brick=0, pair_axis=-1):
+    """Tile plan of attn_na3d_fwd: (brick, pair_axis, key boxes multiplied per head).  Host only."""
+    lib = load_library()
+    b, pa, nb = ctypes.c_int(int(brick)), ctypes.c_int(int(pair_axis)), ctypes.c_longlong(0)
+    T, Y, X = (int(g) for g in grid)
+    Kt, Ky, Kx = (int(g) for g in kernel)
+    _check("attn_na3d_plan", lib.attn_na3d_plan(T, Y, X, Kt, Ky, Kx, ctypes.byref(b), ctypes.byref(pa),
+                                                ctypes.byref(nb)))
+    return b.value, pa.value, nb.value
+
+
+def attn_na3d_fwd(q, k, v, grid, kernel, scale=None, brick=0, pair_axis=-1, out=None, lse=None, stream=None):
+    """3D neighbourhood attention over a (T, Y, X) volume of raster-ordered tokens;
+    returns (out bf16 [B,H,S,d], lse fp32 [B,H,S]).  brick / pair_axis: 0 / -1 let
+    the library choose the tile plan (attn_na3d_plan)."""
+    lib = load_library()
+    B, H, S, d = _bhsd(q, "q")
+    if _bhsd(k, "k") != q.shape or _bhsd(v, "v") != q.shape:
+        raise ValueError("q, k and v must have the same shape")
+    T, Y, X = (int(g) for g in grid)
+    Kt, Ky, Kx = (int(g) for g in kernel)
+    if T * Y * X != S:
+        raise ValueError("grid does not match the sequence length")
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    out = torch.empty_like(q) if out is None else out
+    lse = torch.empty((B, H, S), dtype=torch.float32, device=q.device) if lse is None else lse
+    _check("attn_na3d_fwd", lib.attn_na3d_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, T, Y, X, d,
+                                              Kt, Ky, Kx, scale, int(brick), int(pair_axis), _stream(stream)))
     return out, lse
 
 

@@ -66,6 +66,88 @@ attn_status_t make_map(CUtensorMap* m, const void* ptr, int D, int S, int BH, in
   return r == CUDA_SUCCESS ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
+// 5-D map over a [BH][T][Y][X][D] bf16 tensor (raster token order): dims
+// (D, X, Y, T, BH), box (64, bx, by, bt, 1), 128-byte swizzle; positions
+// outside the volume read as zero.
+attn_status_t make_map_5d(CUtensorMap* m, const void* ptr, int D, int T, int Y, int X, int BH, int bt, int by,
+                          int bx) {
+  if (get_encoder() != ATTN_OK) return ATTN_ERR_CUDA;
+  memset(m, 0, sizeof(*m));
+  cuuint64_t dims[5] = {(cuuint64_t)D, (cuuint64_t)X, (cuuint64_t)Y, (cuuint64_t)T, (cuuint64_t)BH};
+  cuuint64_t strides[4] = {(cuuint64_t)D * 2, (cuuint64_t)X * D * 2, (cuuint64_t)Y * X * D * 2,
+                           (cuuint64_t)T * Y * X * D * 2};
+  cuuint32_t box[5] = {64, (cuuint32_t)bx, (cuuint32_t)by, (cuuint32_t)bt, 1};
+  cuuint32_t es[5] = {1, 1, 1, 1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(ptr), dims, strides, box, es,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+// ---- 3D neighbourhood-attention planning (host mirror of NAWalk's geometry)
+int na_start(int p, int K, int L) {
+  int s = p - K / 2;
+  s = s < 0 ? 0 : s;
+  return s > L - K ? L - K : s;
+}
+int na_mode_of(int brick) { return brick == 1 ? kModeNA1x8x16 : brick == 2 ? kModeNA2x8x8 : kModeNA4x4x8; }
+
+// Key boxes a (brick, pair axis) plan makes the CTAs multiply, summed over
+// every query tile of one head, and the number of CTAs per head.  The count
+// separates over the axes: along a non-pair axis a tile's boxes depend only on
+// its own coordinate, along the pair axis on the pair it belongs to.
+void na_plan_cost(const int L[3], const int K[3], int brick, int pair, long long* boxes, long long* ctas) {
+  const int mode = na_mode_of(brick);
+  const int B[3] = {na_brick_t(mode), na_brick_y(mode), na_brick_x(mode)};
+  long long prod = 1, n = 1;
+  for (int a = 0; a < 3; ++a) {
+    const int nq = (L[a] + B[a] - 1) / B[a];
+    auto lo_of = [&](int i) { return na_start(i * B[a], K[a], L[a]); };
+    auto hi_of = [&](int i) { return na_start((i + 1) * B[a] < L[a] ? (i + 1) * B[a] - 1 : L[a] - 1, K[a], L[a]) + K[a]; };
+    long long sum = 0;
+    if (a != pair) {
+      for (int i = 0; i < nq; ++i) sum += (hi_of(i) - lo_of(i) + B[a] - 1) / B[a];
+      n *= nq;
+    } else {
+      for (int j = 0; 2 * j < nq; ++j) {
+        const int cu = lo_of(2 * j);   // lo is non-decreasing in the brick index
+        for (int i = 2 * j; i < 2 * j + 2 && i < nq; ++i)
+          sum += (hi_of(i) - 1 - cu) / B[a] - (lo_of(i) - cu) / B[a] + 1;
+      }
+      n *= (nq + 1) / 2;
+    }
+    prod *= sum;
+  }
+  *boxes = prod;
+  *ctas = n;
+}
+
+// Picks the brick (1..3) and pair axis (0..2) with the least work when either is
+// left open (brick 0, pair -1); a CTA's fixed cost counts as a few boxes.
+void na_choose(const int L[3], const int K[3], int* brick, int* pair, long long* boxes) {
+  long long best = -1;
+  int bb = 1, bp = 0;
+  long long bboxes = 0;
+  for (int b = 1; b <= 3; ++b) {
+    if (*brick != 0 && b != *brick) continue;
+    for (int a = 0; a < 3; ++a) {
+      if (*pair >= 0 && a != *pair) continue;
+      long long nbox, ncta;
+      na_plan_cost(L, K, b, a, &nbox, &ncta);
+      const long long cost = nbox + 3 * ncta;
+      if (best < 0 || cost < best) {
+        best = cost;
+        bb = b;
+        bp = a;
+        bboxes = nbox;
+      }
+    }
+  }
+  *brick = bb;
+  *pair = bp;
+  *boxes = bboxes;
+}
+
 attn_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA; }
 
 bool valid_d(int d) { return d == 64 || d == 128; }
@@ -92,6 +174,13 @@ FwdParams base_params(int B, int H, int Sq, int Skv, float scale, int mode, int*
 // Sizes checked once: products that index memory must fit the kernels' ranges.
 bool sizes_ok(long long B, long long H, long long S) {
   return B >= 1 && H >= 1 && S >= 1 && B * H <= 0x7fffffffLL && S <= 0x3fffffffLL;
+}
+
+bool na_args_ok(int B, int H, int T, int Y, int X, int Kt, int Ky, int Kx) {
+  if (T < 1 || Y < 1 || X < 1) return false;
+  const long long S = (long long)T * Y * X;
+  if (!sizes_ok(B, H, S)) return false;
+  return Kt >= 1 && Kt <= T && Ky >= 1 && Ky <= Y && Kx >= 1 && Kx <= X;
 }
 
 struct SparseLayout {
@@ -161,6 +250,56 @@ attn_status_t attn_dense_fwd(const attn_bf16* q, const attn_bf16* k, const attn_
   p.out = out;
   p.lse = lse;
   return cuda_status(launch_fwd(d, 128, kModeDense, tq, tk, tv, p, stream));
+}
+
+attn_status_t attn_na3d_plan(int T, int Y, int X, int Kt, int Ky, int Kx, int* brick, int* pair_axis,
+                             long long* key_boxes) {
+  if (!brick || !pair_axis || !na_args_ok(1, 1, T, Y, X, Kt, Ky, Kx)) return ATTN_ERR_INVALID_ARG;
+  if (*brick < 0 || *brick > 3 || *pair_axis < -1 || *pair_axis > 2) return ATTN_ERR_INVALID_ARG;
+  const int L[3] = {T, Y, X}, K[3] = {Kt, Ky, Kx};
+  long long boxes = 0;
+  na_choose(L, K, brick, pair_axis, &boxes);
+  if (key_boxes) *key_boxes = boxes;
+  return ATTN_OK;
+}
+
+attn_status_t attn_na3d_fwd(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v, attn_bf16* out, float* lse,
+                            int B, int H, int T, int Y, int X, int d, int Kt, int Ky, int Kx, float scale, int brick,
+                            int pair_axis, cudaStream_t stream) {
+  if (!q || !k || !v || !out) return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || (lse && ((uintptr_t)lse & 3u)))
+    return ATTN_ERR_INVALID_ARG;
+  if (!na_args_ok(B, H, T, Y, X, Kt, Ky, Kx) || !(isfinite(scale) && scale > 0.f)) return ATTN_ERR_INVALID_ARG;
+  if (brick < 0 || brick > 3 || pair_axis < -1 || pair_axis > 2) return ATTN_ERR_INVALID_ARG;
+  if (!valid_d(d)) return ATTN_ERR_UNSUPPORTED;
+  const int L[3] = {T, Y, X}, K[3] = {Kt, Ky, Kx};
+  long long boxes = 0;
+  na_choose(L, K, &brick, &pair_axis, &boxes);
+  const int mode = na_mode_of(brick);
+  const int Bv[3] = {na_brick_t(mode), na_brick_y(mode), na_brick_x(mode)};
+  int* status = nullptr;
+  attn_status_t st = status_ptr(&status);
+  if (st != ATTN_OK) return st;
+  const int S = T * Y * X;
+  CUtensorMap tq, tk, tv;
+  if ((st = make_map_5d(&tq, q, d, T, Y, X, B * H, Bv[0], Bv[1], Bv[2])) != ATTN_OK) return st;
+  if ((st = make_map_5d(&tk, k, d, T, Y, X, B * H, Bv[0], Bv[1], Bv[2])) != ATTN_OK) return st;
+  if ((st = make_map_5d(&tv, v, d, T, Y, X, B * H, Bv[0], Bv[1], Bv[2])) != ATTN_OK) return st;
+  FwdParams p = base_params(B, H, S, S, scale, mode, status);
+  long long n_qg = 1;
+  for (int a = 0; a < 3; ++a) {
+    p.na_L[a] = L[a];
+    p.na_K[a] = K[a];
+    p.na_nq[a] = (L[a] + Bv[a] - 1) / Bv[a];
+    p.na_np[a] = a == pair_axis ? (p.na_nq[a] + 1) / 2 : p.na_nq[a];
+    n_qg *= p.na_np[a];
+  }
+  if (n_qg * B * H > 0x7fffffffLL) return ATTN_ERR_INVALID_ARG;
+  p.n_qg = (int)n_qg;
+  p.na_pair_axis = pair_axis;
+  p.out = out;
+  p.lse = lse;
+  return cuda_status(launch_fwd(d, 128, mode, tq, tk, tv, p, stream));
 }
 
 attn_status_t attn_cross_splitkv_fwd(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v, float* out_part,

@@ -17,6 +17,14 @@
 // moved (and O_t rescaled in TMEM) when a tile's max exceeds it by more than
 // kRescaleLog2, so P stays <= 2^kRescaleLog2 and the final normalisation by
 // the same stale max is exact.
+//
+// 3D neighbourhood attention (modes kModeNA*) runs on the same loop: a query
+// tile is a brick of 128 tokens (bt x by x bx) of the (T, Y, X) volume, loaded
+// by a 5-D TMA box straight from the raster layout; the CTA's two bricks are
+// neighbours along one axis.  The key tiles are boxes of the same shape laid on
+// a grid that starts at the corner of the union of the two bricks' windows;
+// every role walks that grid in the same order, and each query row masks the
+// keys outside its own window.
 #pragma once
 #include <float.h>
 #include <limits.h>
@@ -24,7 +32,21 @@
 
 namespace vdtb {
 
-enum FwdMode { kModeDense = 0, kModeSparse = 1, kModeSplit = 2, kModeSparseFused = 3 };
+enum FwdMode {
+  kModeDense = 0,
+  kModeSparse = 1,
+  kModeSplit = 2,
+  kModeSparseFused = 3,
+  // 3D neighbourhood attention; the suffix is the brick (frames x rows x columns)
+  kModeNA1x8x16 = 4,
+  kModeNA2x8x8 = 5,
+  kModeNA4x4x8 = 6,
+};
+
+__host__ __device__ constexpr bool is_na_mode(int m) { return m >= kModeNA1x8x16 && m <= kModeNA4x4x8; }
+__host__ __device__ constexpr int na_brick_t(int m) { return m == kModeNA4x4x8 ? 4 : (m == kModeNA2x8x8 ? 2 : 1); }
+__host__ __device__ constexpr int na_brick_y(int m) { return m == kModeNA4x4x8 ? 4 : 8; }
+__host__ __device__ constexpr int na_brick_x(int m) { return m == kModeNA1x8x16 ? 16 : 8; }
 
 constexpr float kRescaleLog2 = 8.0f;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -58,6 +80,94 @@ struct FwdParams {
   int32_t* out_sel_cnt;    // nullable, [BH][NQB]
   float* out_stats;        // nullable, [BH][NQB][4]
   float* out_taylor;       // nullable, [BH][NQB][D]
+  // 3D neighbourhood attention: volume (T, Y, X), window (Kt, Ky, Kx), query
+  // bricks per axis, CTA grid per axis (the pair axis holds ceil(nq / 2))
+  int na_L[3];
+  int na_K[3];
+  int na_nq[3];
+  int na_np[3];
+  int na_pair_axis;        // 0 = frames, 1 = rows, 2 = columns
+};
+
+// Window start along one axis: centred on p, moved inward at the borders
+// (1 <= K <= L).
+__device__ __forceinline__ int na_window_start(int p, int K, int L) {
+  int s = p - K / 2;
+  s = s < 0 ? 0 : s;
+  return s > L - K ? L - K : s;
+}
+
+// The key boxes of one neighbourhood-attention CTA, in the order every role
+// visits them.  Box u has origin cu + (ut, uy, ux) * brick (x fastest); bit t
+// of its flags is set when it overlaps query tile t's window union.
+template <int BT, int BY, int BX>
+struct NAWalk {
+  int org[2][3];   // query brick origins
+  int lo[2][3];    // per tile: union of its rows' windows, [lo, hi) per axis
+  int hi[2][3];
+  int cu[3];       // origin of the box grid
+  int nk[3];       // boxes per axis
+  int ntiles;
+  int u, nb;
+
+  __device__ __forceinline__ void init(const FwdParams& p, int qg) {
+    const int B[3] = {BT, BY, BX};
+    int idx[3];
+    idx[2] = qg % p.na_np[2];
+    const int r = qg / p.na_np[2];
+    idx[1] = r % p.na_np[1];
+    idx[0] = r / p.na_np[1];
+    ntiles = 0;
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+      int ib[3];
+#pragma unroll
+      for (int a = 0; a < 3; ++a) ib[a] = (a == p.na_pair_axis) ? 2 * idx[a] + t : idx[a];
+      const int pa = p.na_pair_axis;
+      const bool valid = (pa == 0 ? ib[0] : pa == 1 ? ib[1] : ib[2]) < (pa == 0 ? p.na_nq[0] : pa == 1 ? p.na_nq[1] : p.na_nq[2]);
+      if (valid) ntiles = t + 1;
+#pragma unroll
+      for (int a = 0; a < 3; ++a) {
+        org[t][a] = ib[a] * B[a];
+        const int last = min(org[t][a] + B[a], p.na_L[a]) - 1;
+        lo[t][a] = na_window_start(min(org[t][a], p.na_L[a] - 1), p.na_K[a], p.na_L[a]);
+        hi[t][a] = na_window_start(last, p.na_K[a], p.na_L[a]) + p.na_K[a];
+        if (!valid) {   // an absent second tile adds nothing to the union
+          lo[t][a] = lo[0][a];
+          hi[t][a] = hi[0][a];
+        }
+      }
+    }
+#pragma unroll
+    for (int a = 0; a < 3; ++a) {
+      cu[a] = min(lo[0][a], lo[1][a]);
+      nk[a] = (max(hi[0][a], hi[1][a]) - cu[a] + B[a] - 1) / B[a];
+    }
+    nb = nk[0] * nk[1] * nk[2];
+    u = 0;
+  }
+  // Next box overlapping at least one tile: its index, origin and flags; -1 at the end.
+  __device__ __forceinline__ int next(uint32_t& flags, int (&box)[3]) {
+    const int B[3] = {BT, BY, BX};
+    while (u < nb) {
+      const int uu = u++;
+      const int ux = uu % nk[2];
+      const int r = uu / nk[2];
+      box[2] = cu[2] + ux * BX;
+      box[1] = cu[1] + (r % nk[1]) * BY;
+      box[0] = cu[0] + (r / nk[1]) * BT;
+      flags = 0;
+#pragma unroll
+      for (int t = 0; t < 2; ++t) {
+        bool ov = t < ntiles;
+#pragma unroll
+        for (int a = 0; a < 3; ++a) ov = ov && box[a] < hi[t][a] && box[a] + B[a] > lo[t][a];
+        if (ov) flags |= 1u << t;
+      }
+      if (flags) return uu;
+    }
+    return -1;
+  }
 };
 
 // Walks the ascending union of up to 4 tile lists (one per query block the
@@ -110,6 +220,8 @@ template <int D, int BK, int MODE, int NQT, int NSTAGE>
 struct FwdCfg {
   static constexpr bool kSparseLike = MODE == kModeSparse || MODE == kModeSparseFused;
   static constexpr bool kFused = MODE == kModeSparseFused;
+  static constexpr bool kNA = is_na_mode(MODE);
+  static constexpr int kNaT = na_brick_t(MODE), kNaY = na_brick_y(MODE), kNaX = na_brick_x(MODE);
   static constexpr int QB = kSparseLike ? 128 / BK : 1;   // query blocks per 128-row tile
   // fused routing: query blocks per CTA, key-block capacity, staging chunk
   static constexpr int kFusedR = NQT * QB;
@@ -149,7 +261,18 @@ struct FwdCfg {
   static_assert(!kFused || kFusedCH * D * 4 + kFusedR * kFusedMaxNKB * 4 + kFusedR * D * 4 <= NSTAGE * kSlotBytes,
                 "fused routing scratch must fit in the K/V ring");
   static_assert(!kFused || NQT == 2, "fused routing runs on the two-tile CTA");
+  static_assert(!kNA || (NQT == 2 && BK == 128 && kNaT * kNaY * kNaX == 128), "neighbourhood bricks");
 };
+
+// Next key tile of a CTA's walk: neighbourhood boxes or the merged lists.
+template <bool NA, class Walk>
+__device__ __forceinline__ int next_tile(Walk& naw, TileMerge& merge, uint32_t& flags, int (&box)[3]) {
+  if constexpr (NA) {
+    return naw.next(flags, box);
+  } else {
+    return merge.next(flags);
+  }
+}
 
 __device__ __forceinline__ void named_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
@@ -357,6 +480,13 @@ __global__ void __launch_bounds__(NQT * 128 + 128, (NQT == 1) ? 2 : 1)
 #pragma unroll
   for (int t = 0; t < NQT; ++t)
     if (q_row0 + t * 128 < p.Sq) n_valid_tiles = t + 1;
+  constexpr bool kNA = Cfg::kNA;
+  NAWalk<Cfg::kNaT, Cfg::kNaY, Cfg::kNaX> naw;
+  int na_box[3] = {0, 0, 0};
+  if constexpr (kNA) {
+    naw.init(p, blockIdx.x % p.n_qg);
+    n_valid_tiles = naw.ntiles;
+  }
 
   TileMerge merge;
   merge.status = p.status;
@@ -446,9 +576,18 @@ __global__ void __launch_bounds__(NQT * 128 + 128, (NQT == 1) ? 2 : 1)
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
       mbar_expect_tx(&bar_q, n_valid_tiles * Cfg::kQTileBytes);
-      for (int t = 0; t < n_valid_tiles; ++t)
-        for (int h = 0; h < D / 64; ++h)
-          tma_load_3d(sQ + t * Cfg::kQTileBytes + h * 16384, &tm_q, &bar_q, h * 64, q_row0 + t * 128, bh);
+#pragma unroll
+      for (int t = 0; t < NQT; ++t) {
+        if (t >= n_valid_tiles) break;
+#pragma unroll
+        for (int h = 0; h < D / 64; ++h) {
+          if constexpr (kNA)
+            tma_load_5d(sQ + t * Cfg::kQTileBytes + h * 16384, &tm_q, &bar_q, h * 64, naw.org[t][2], naw.org[t][1],
+                        naw.org[t][0], bh);
+          else
+            tma_load_3d(sQ + t * Cfg::kQTileBytes + h * 16384, &tm_q, &bar_q, h * 64, q_row0 + t * 128, bh);
+        }
+      }
       int ld = 0;
       uint32_t flags;
       int u;
@@ -457,7 +596,7 @@ __global__ void __launch_bounds__(NQT * 128 + 128, (NQT == 1) ? 2 : 1)
         ok = bounded_wait(&bar_route, 0, &abort_flag, p.status);   // the ring holds routing scratch until then
         take_fused_lists();
       }
-      while (ok && (u = merge.next(flags)) >= 0) {
+      while (ok && (u = next_tile<kNA>(naw, merge, flags, na_box)) >= 0) {
         const int row = kv_lo + u * BK;
 #pragma unroll
         for (int kv = 0; kv < 2; ++kv) {
@@ -468,8 +607,13 @@ __global__ void __launch_bounds__(NQT * 128 + 128, (NQT == 1) ? 2 : 1)
           }
           uint8_t* dst = sKV + slot * Cfg::kSlotBytes;
           mbar_expect_tx(&bar_full[slot], Cfg::kSlotBytes);
-          for (int h = 0; h < D / 64; ++h)
-            tma_load_3d(dst + h * (BK * 128), kv == 0 ? &tm_k : &tm_v, &bar_full[slot], h * 64, row, bh);
+          for (int h = 0; h < D / 64; ++h) {
+            if constexpr (kNA)
+              tma_load_5d(dst + h * (BK * 128), kv == 0 ? &tm_k : &tm_v, &bar_full[slot], h * 64, na_box[2], na_box[1],
+                          na_box[0], bh);
+            else
+              tma_load_3d(dst + h * (BK * 128), kv == 0 ? &tm_k : &tm_v, &bar_full[slot], h * 64, row, bh);
+          }
           ++ld;
         }
       }
@@ -512,7 +656,7 @@ __global__ void __launch_bounds__(NQT * 128 + 128, (NQT == 1) ? 2 : 1)
         ++pv_count[t];
         pending[t] = false;
       };
-      while (ok && (u = merge.next(flags)) >= 0) {
+      while (ok && (u = next_tile<kNA>(naw, merge, flags, na_box)) >= 0) {
         const int kslot = ld % NSTAGE;
         if (!bounded_wait(&bar_full[kslot], (ld / NSTAGE) & 1, &abort_flag, p.status)) break;
         ++ld;
@@ -579,8 +723,19 @@ __global__ void __launch_bounds__(NQT * 128 + 128, (NQT == 1) ? 2 : 1)
     const int t = warp >> 2;
     const int w4 = warp & 3;
     const int r = w4 * 32 + lane;                  // row within the tile = TMEM lane
-    const int grow = q_row0 + t * 128 + r;         // row within the head
-    const bool row_valid = grow < p.Sq;
+    int grow = q_row0 + t * 128 + r;               // row within the head
+    bool row_valid = grow < p.Sq;
+    int na_ws[3] = {0, 0, 0};                      // this row's window start per axis
+    if constexpr (kNA) {
+      const bool second = t == 1 && n_valid_tiles == 2;   // warp-uniform
+      const int c[3] = {(second ? naw.org[1][0] : naw.org[0][0]) + r / (Cfg::kNaY * Cfg::kNaX),
+                        (second ? naw.org[1][1] : naw.org[0][1]) + (r / Cfg::kNaX) % Cfg::kNaY,
+                        (second ? naw.org[1][2] : naw.org[0][2]) + r % Cfg::kNaX};
+      row_valid = c[0] < p.na_L[0] && c[1] < p.na_L[1] && c[2] < p.na_L[2];
+      grow = (c[0] * p.na_L[1] + c[1]) * p.na_L[2] + c[2];
+#pragma unroll
+      for (int a = 0; a < 3; ++a) na_ws[a] = na_window_start(min(c[a], p.na_L[a] - 1), p.na_K[a], p.na_L[a]);
+    }
     const int qb = (QB == 2) ? (w4 >> 1) : 0;      // warp-uniform
     const uint32_t my_bit = 1u << (t * QB + qb);
     const uint32_t tile_mask = ((1u << QB) - 1u) << (t * QB);
@@ -602,7 +757,7 @@ __global__ void __launch_bounds__(NQT * 128 + 128, (NQT == 1) ? 2 : 1)
     uint32_t flags;
     int u;
     bool ok = t < n_valid_tiles;
-    while (ok && (u = merge.next(flags)) >= 0) {
+    while (ok && (u = next_tile<kNA>(naw, merge, flags, na_box)) >= 0) {
       if (!(flags & tile_mask)) continue;
       if (!__all_sync(0xffffffffu, bounded_wait(&bar_s[t], it & 1, &abort_flag, p.status))) break;
       tc_fence_after();
@@ -623,7 +778,38 @@ __global__ void __launch_bounds__(NQT * 128 + 128, (NQT == 1) ? 2 : 1)
       const bool mine = (flags & my_bit) != 0;
       // raw scores stay unscaled: the softmax scale is positive, so the max
       // commutes with it and the scaling folds into the exponent's FFMA
-      if (!(mine && n_valid == BK)) {
+      if constexpr (kNA) {
+        // keys of the box inside this row's window: a [lo, hi) range per axis
+        constexpr int BT = Cfg::kNaT, BY = Cfg::kNaY, BX = Cfg::kNaX;
+        int lo[3], hi[3];
+        const int Bd[3] = {BT, BY, BX};
+#pragma unroll
+        for (int a = 0; a < 3; ++a) {
+          lo[a] = min(max(na_ws[a] - na_box[a], 0), Bd[a]);
+          hi[a] = min(max(na_ws[a] + p.na_K[a] - na_box[a], 0), Bd[a]);
+        }
+        const bool full = lo[0] == 0 && hi[0] == BT && lo[1] == 0 && hi[1] == BY && lo[2] == 0 && hi[2] == BX;
+        if (!full) {
+          const bool any = lo[0] < hi[0] && lo[1] < hi[1] && lo[2] < hi[2];
+          const uint32_t xm = any ? (((1u << hi[2]) - 1u) & ~((1u << lo[2]) - 1u)) : 0u;
+          const uint32_t ym = ((1u << hi[1]) - 1u) & ~((1u << lo[1]) - 1u);
+          uint32_t lm = 0;   // bit (frame * BY + row) of the box: that line is in the window
+#pragma unroll
+          for (int ct = 0; ct < BT; ++ct)
+            if (ct >= lo[0] && ct < hi[0]) lm |= ym << (ct * BY);
+          constexpr int LPW = 32 / BX;   // lines per 32-column word
+#pragma unroll
+          for (int w = 0; w < BK / 32; ++w) {
+            uint32_t wd = 0;
+#pragma unroll
+            for (int j = 0; j < LPW; ++j)
+              if ((lm >> (w * LPW + j)) & 1u) wd |= xm << (j * BX);
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              if (!((wd >> j) & 1u)) x[w * 32 + j] = -INFINITY;
+          }
+        }
+      } else if (!(mine && n_valid == BK)) {
 #pragma unroll
         for (int c = 0; c < BK; ++c)
           if (!mine || c >= n_valid) x[c] = -INFINITY;
