@@ -222,7 +222,11 @@ attn_status_t attn_sparse_fused_fwd(const attn_bf16* q, const attn_bf16* k, cons
  *   brick         query/key tile shape, frames x rows x columns of 128 tokens:
  *                 1 = 1x8x16, 2 = 2x8x8, 3 = 4x4x8, 0 = chosen by the library.
  *   pair_axis     axis along which a CTA's two query bricks are neighbours:
- *                 0 = frames, 1 = rows, 2 = columns, -1 = chosen by the library.
+ *                 0 = frames, 1 = rows, 2 = columns; 3 = one brick per CTA
+ *                 (two CTAs share an SM); -1 = chosen by the library (one
+ *                 brick per CTA, the fastest on GB300 for every window
+ *                 measured; an open brick takes the shape with the least
+ *                 key boxes plus two per CTA).
  *   The choice only changes speed, never results beyond fp32 rounding order.
  *   Errors: ATTN_ERR_INVALID_ARG (null or misaligned pointer, a window outside
  *   [1, L], S > 2^30, non-positive scale, bad brick/pair code),

@@ -119,8 +119,9 @@ def na_start(p, K, L):
 
 
 def na_walk(grid, kernel, brick, pair):
-    """Python restatement of the kernel's box walk: yields, per CTA, the two query
-    bricks (origin or None) and the boxes with their tile flags."""
+    """Python restatement of the kernel's box walk: yields, per CTA, its query
+    bricks (two neighbours along ``pair``, or one when pair == 3) and the boxes
+    with their tile flags."""
     B = BRICKS[brick]
     nq = [-(-grid[a] // B[a]) for a in range(3)]
     np_ = [(-(-nq[a] // 2) if a == pair else nq[a]) for a in range(3)]
@@ -129,9 +130,9 @@ def na_walk(grid, kernel, brick, pair):
             for ix in range(np_[2]):
                 idx = [it, iy, ix]
                 tiles = []
-                for t in range(2):
+                for t in range(2 if pair < 3 else 1):
                     ib = [2 * idx[a] + t if a == pair else idx[a] for a in range(3)]
-                    if ib[pair] >= nq[pair]:
+                    if pair < 3 and ib[pair] >= nq[pair]:
                         continue
                     org = [ib[a] * B[a] for a in range(3)]
                     lo = [na_start(org[a], kernel[a], grid[a]) for a in range(3)]
@@ -154,7 +155,7 @@ def na_walk(grid, kernel, brick, pair):
 @pytest.mark.parametrize("grid,kernel", [((3, 13, 21), (3, 5, 7)), ((5, 11, 19), (3, 5, 4)), ((1, 20, 24), (1, 9, 9)),
                                          ((4, 16, 32), (2, 16, 1)), ((2, 5, 6), (2, 5, 6))])
 @pytest.mark.parametrize("brick", [1, 2, 3])
-@pytest.mark.parametrize("pair", [0, 1, 2])
+@pytest.mark.parametrize("pair", [0, 1, 2, 3])
 def test_na3d_walk_covers_every_window_and_plan_counts_it(lib, grid, kernel, brick, pair):
     B = BRICKS[brick]
     work = 0
@@ -186,24 +187,26 @@ def test_na3d_walk_covers_every_window_and_plan_counts_it(lib, grid, kernel, bri
 
 
 def test_na3d_plan_picks_the_least_work(lib):
-    # cost of a plan = key boxes multiplied + 3 per CTA; the open plan is the minimum over all nine
-    for grid, kernel in [((4, 128, 128), (3, 7, 7)), ((4, 64, 64), (3, 31, 31)), ((1, 96, 160), (1, 13, 13))]:
+    # an open pair axis means one brick per CTA; an open brick minimises key boxes + 2 per CTA
+    for grid, kernel in [((4, 128, 128), (3, 7, 7)), ((4, 64, 64), (3, 31, 31)), ((1, 96, 160), (1, 13, 13)),
+                         ((5, 11, 19), (3, 5, 4))]:
         costs = {}
         for brick in (1, 2, 3):
-            for pair in (0, 1, 2):
-                _, _, nbox = vd.attn_na3d_plan(grid, kernel, brick, pair)
-                nq = [-(-grid[a] // BRICKS[brick][a]) for a in range(3)]
-                ctas = np.prod([(-(-nq[a] // 2) if a == pair else nq[a]) for a in range(3)])
-                costs[(brick, pair)] = nbox + 3 * ctas
-                assert nbox * 128 * 128 >= np.prod(grid) * np.prod(kernel)   # the boxes hold every window
+            b, pa, nbox = vd.attn_na3d_plan(grid, kernel, brick, 3)
+            assert (b, pa) == (brick, 3)
+            ctas = np.prod([-(-grid[a] // BRICKS[brick][a]) for a in range(3)])
+            costs[brick] = nbox + 2 * ctas
+            assert nbox * 128 * 128 >= np.prod(grid) * np.prod(kernel)   # the boxes hold every window
         b, pa, nb = vd.attn_na3d_plan(grid, kernel)
-        assert costs[(b, pa)] == min(costs.values())
+        assert pa == 3 and costs[b] == min(costs.values())
+        # a fixed brick with an open pair axis keeps the brick
+        assert vd.attn_na3d_plan(grid, kernel, 2)[:2] == (2, 3)
 
 
 def test_na3d_rejections(lib):
     base = [P, P, P, P, P, 1, 2, 4, 16, 16, 128, 3, 5, 5, 0.088, 0, -1, None]
     for i, bad in [(11, 0), (11, 5), (12, 17), (13, 0), (7, 0), (14, 0.0), (14, math.nan), (15, 4), (15, -1),
-                   (16, 3), (16, -2)]:
+                   (16, 4), (16, -2)]:
         args = list(base)
         args[i] = bad
         assert lib.attn_na3d_fwd(*args) == 1, (i, bad)

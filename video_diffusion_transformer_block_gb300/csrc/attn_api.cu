@@ -105,7 +105,7 @@ void na_plan_cost(const int L[3], const int K[3], int brick, int pair, long long
     auto lo_of = [&](int i) { return na_start(i * B[a], K[a], L[a]); };
     auto hi_of = [&](int i) { return na_start((i + 1) * B[a] < L[a] ? (i + 1) * B[a] - 1 : L[a] - 1, K[a], L[a]) + K[a]; };
     long long sum = 0;
-    if (a != pair) {
+    if (a != pair) {   // (pair 3: no axis is paired)
       for (int i = 0; i < nq; ++i) sum += (hi_of(i) - lo_of(i) + B[a] - 1) / B[a];
       n *= nq;
     } else {
@@ -122,29 +122,28 @@ void na_plan_cost(const int L[3], const int K[3], int brick, int pair, long long
   *ctas = n;
 }
 
-// Picks the brick (1..3) and pair axis (0..2) with the least work when either is
-// left open (brick 0, pair -1); a CTA's fixed cost counts as a few boxes.
+// Picks the plan left open by the caller (brick 0, pair -1).  An open pair
+// axis means one brick per CTA (pair 3): two such CTAs share an SM, so one
+// CTA's prologue and epilogue overlap the other's main loop, which measured
+// faster than every paired plan on GB300.  An open brick takes the least
+// work, counting a CTA's fixed cost as two key boxes.
 void na_choose(const int L[3], const int K[3], int* brick, int* pair, long long* boxes) {
+  if (*pair < 0) *pair = 3;
   long long best = -1;
-  int bb = 1, bp = 0;
+  int bb = 1;
   long long bboxes = 0;
   for (int b = 1; b <= 3; ++b) {
     if (*brick != 0 && b != *brick) continue;
-    for (int a = 0; a < 3; ++a) {
-      if (*pair >= 0 && a != *pair) continue;
-      long long nbox, ncta;
-      na_plan_cost(L, K, b, a, &nbox, &ncta);
-      const long long cost = nbox + 3 * ncta;
-      if (best < 0 || cost < best) {
-        best = cost;
-        bb = b;
-        bp = a;
-        bboxes = nbox;
-      }
+    long long nbox, ncta;
+    na_plan_cost(L, K, b, *pair, &nbox, &ncta);
+    const long long cost = nbox + 2 * ncta;
+    if (best < 0 || cost < best) {
+      best = cost;
+      bb = b;
+      bboxes = nbox;
     }
   }
   *brick = bb;
-  *pair = bp;
   *boxes = bboxes;
 }
 
@@ -255,7 +254,7 @@ attn_status_t attn_dense_fwd(const attn_bf16* q, const attn_bf16* k, const attn_
 attn_status_t attn_na3d_plan(int T, int Y, int X, int Kt, int Ky, int Kx, int* brick, int* pair_axis,
                              long long* key_boxes) {
   if (!brick || !pair_axis || !na_args_ok(1, 1, T, Y, X, Kt, Ky, Kx)) return ATTN_ERR_INVALID_ARG;
-  if (*brick < 0 || *brick > 3 || *pair_axis < -1 || *pair_axis > 2) return ATTN_ERR_INVALID_ARG;
+  if (*brick < 0 || *brick > 3 || *pair_axis < -1 || *pair_axis > 3) return ATTN_ERR_INVALID_ARG;
   const int L[3] = {T, Y, X}, K[3] = {Kt, Ky, Kx};
   long long boxes = 0;
   na_choose(L, K, brick, pair_axis, &boxes);
@@ -270,7 +269,7 @@ attn_status_t attn_na3d_fwd(const attn_bf16* q, const attn_bf16* k, const attn_b
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || (lse && ((uintptr_t)lse & 3u)))
     return ATTN_ERR_INVALID_ARG;
   if (!na_args_ok(B, H, T, Y, X, Kt, Ky, Kx) || !(isfinite(scale) && scale > 0.f)) return ATTN_ERR_INVALID_ARG;
-  if (brick < 0 || brick > 3 || pair_axis < -1 || pair_axis > 2) return ATTN_ERR_INVALID_ARG;
+  if (brick < 0 || brick > 3 || pair_axis < -1 || pair_axis > 3) return ATTN_ERR_INVALID_ARG;
   if (!valid_d(d)) return ATTN_ERR_UNSUPPORTED;
   const int L[3] = {T, Y, X}, K[3] = {Kt, Ky, Kx};
   long long boxes = 0;

@@ -86,7 +86,7 @@ struct FwdParams {
   int na_K[3];
   int na_nq[3];
   int na_np[3];
-  int na_pair_axis;        // 0 = frames, 1 = rows, 2 = columns
+  int na_pair_axis;        // 0 = frames, 1 = rows, 2 = columns, 3 = one brick per CTA
 };
 
 // Window start along one axis: centred on p, moved inward at the borders
@@ -110,7 +110,9 @@ struct NAWalk {
   int ntiles;
   int u, nb;
 
-  __device__ __forceinline__ void init(const FwdParams& p, int qg) {
+  // paired: the CTA owns two bricks that are neighbours along p.na_pair_axis
+  // (the CTA grid holds pairs on that axis); otherwise one brick per CTA.
+  __device__ __forceinline__ void init(const FwdParams& p, int qg, bool paired) {
     const int B[3] = {BT, BY, BX};
     int idx[3];
     idx[2] = qg % p.na_np[2];
@@ -122,9 +124,11 @@ struct NAWalk {
     for (int t = 0; t < 2; ++t) {
       int ib[3];
 #pragma unroll
-      for (int a = 0; a < 3; ++a) ib[a] = (a == p.na_pair_axis) ? 2 * idx[a] + t : idx[a];
+      for (int a = 0; a < 3; ++a) ib[a] = (paired && a == p.na_pair_axis) ? 2 * idx[a] + t : idx[a];
       const int pa = p.na_pair_axis;
-      const bool valid = (pa == 0 ? ib[0] : pa == 1 ? ib[1] : ib[2]) < (pa == 0 ? p.na_nq[0] : pa == 1 ? p.na_nq[1] : p.na_nq[2]);
+      const bool valid = paired ? (pa == 0 ? ib[0] : pa == 1 ? ib[1] : ib[2]) <
+                                      (pa == 0 ? p.na_nq[0] : pa == 1 ? p.na_nq[1] : p.na_nq[2])
+                                : t == 0;
       if (valid) ntiles = t + 1;
 #pragma unroll
       for (int a = 0; a < 3; ++a) {
@@ -261,7 +265,7 @@ struct FwdCfg {
   static_assert(!kFused || kFusedCH * D * 4 + kFusedR * kFusedMaxNKB * 4 + kFusedR * D * 4 <= NSTAGE * kSlotBytes,
                 "fused routing scratch must fit in the K/V ring");
   static_assert(!kFused || NQT == 2, "fused routing runs on the two-tile CTA");
-  static_assert(!kNA || (NQT == 2 && BK == 128 && kNaT * kNaY * kNaX == 128), "neighbourhood bricks");
+  static_assert(!kNA || (BK == 128 && kNaT * kNaY * kNaX == 128), "neighbourhood bricks");
 };
 
 // Next key tile of a CTA's walk: neighbourhood boxes or the merged lists.
@@ -484,7 +488,7 @@ __global__ void __launch_bounds__(NQT * 128 + 128, (NQT == 1) ? 2 : 1)
   NAWalk<Cfg::kNaT, Cfg::kNaY, Cfg::kNaX> naw;
   int na_box[3] = {0, 0, 0};
   if constexpr (kNA) {
-    naw.init(p, blockIdx.x % p.n_qg);
+    naw.init(p, blockIdx.x % p.n_qg, NQT == 2);
     n_valid_tiles = naw.ntiles;
   }
 

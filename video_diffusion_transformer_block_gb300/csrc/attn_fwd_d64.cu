@@ -11,6 +11,9 @@ cudaError_t launch_attn_fwd_d64(int BK, int mode, const CUtensorMap& tq, const C
   if (mode == kModeSplit && BK == 128) return launch_fwd_cfg<64, 128, kModeSplit, 1, 4>(tq, tk, tv, p, stream);
   if (mode == kModeSparseFused && BK == 128) return launch_fwd_cfg<64, 128, kModeSparseFused, 2, 6>(tq, tk, tv, p, stream);
   if (mode == kModeSparseFused && BK == 64) return launch_fwd_cfg<64, 64, kModeSparseFused, 2, 8>(tq, tk, tv, p, stream);
+  if (mode == kModeNA1x8x16 && BK == 128 && p.na_pair_axis == 3) return launch_fwd_cfg<64, 128, kModeNA1x8x16, 1, 4>(tq, tk, tv, p, stream);
+  if (mode == kModeNA2x8x8 && BK == 128 && p.na_pair_axis == 3) return launch_fwd_cfg<64, 128, kModeNA2x8x8, 1, 4>(tq, tk, tv, p, stream);
+  if (mode == kModeNA4x4x8 && BK == 128 && p.na_pair_axis == 3) return launch_fwd_cfg<64, 128, kModeNA4x4x8, 1, 4>(tq, tk, tv, p, stream);
   if (mode == kModeNA1x8x16 && BK == 128) return launch_fwd_cfg<64, 128, kModeNA1x8x16, 2, 6>(tq, tk, tv, p, stream);
   if (mode == kModeNA2x8x8 && BK == 128) return launch_fwd_cfg<64, 128, kModeNA2x8x8, 2, 6>(tq, tk, tv, p, stream);
   if (mode == kModeNA4x4x8 && BK == 128) return launch_fwd_cfg<64, 128, kModeNA4x4x8, 2, 6>(tq, tk, tv, p, stream);
