@@ -285,7 +285,9 @@ def run_native(args, world, rank, local):
 def run_native_kernel(args, world, rank, local):
     """Secondary workloads (not the benchmark line): one kernel path per step.
       dense16k: attn_dense_fwd on B1 H32 S16384 d128 (tensor-bound)
-      cross:    attn_cross_splitkv_fwd + attn_lse_merge, 128 x 32768, 8 chunks (HBM-bound)"""
+      cross:    attn_cross_splitkv_fwd + attn_lse_merge, 128 x 32768, 8 chunks (HBM-bound)
+      na3d:     attn_na3d_fwd, 3D neighbourhood attention, 4x128x128 volume, window 3x7x7 (tensor-bound on
+                the executed key boxes; the value counts only the window's FLOPs)"""
     import video_diffusion_transformer_block_gb300 as vd
     from video_diffusion_transformer_block_gb300 import build as vbuild
 
@@ -307,6 +309,15 @@ def run_native_kernel(args, world, rank, local):
 
         def step():
             vd.attn_dense_fwd(q, k, v, out=out, lse=lse)
+    elif args.workload == "na3d":
+        launches = 1
+        kern = w0.extra["kernel"]
+        brick, pair, boxes = vd.attn_na3d_plan(w.grid, kern)
+        flops = 4.0 * B * H * Sq * math.prod(kern) * d                 # the windows' own work
+        exec_flops = 4.0 * B * H * boxes * 128 * 128 * d               # what the tensor cores run
+
+        def step():
+            vd.attn_na3d_fwd(q, k, v, w.grid, kern, out=out, lse=lse)
     else:
         n = w.n_split
         op = torch.empty((n, B, H, Sq, d), dtype=torch.float32, device=q.device)
@@ -338,7 +349,16 @@ def run_native_kernel(args, world, rank, local):
         raise RuntimeError(f"device status after timed region: {vd.attn_status_string(status)}")
     ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in evs) / args.steps, world)
     value = world * flops / (ms * 1e-3) / 1e12
-    if args.workload == "dense16k":
+    extra = {}
+    if args.workload == "na3d":
+        peak = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
+        ach = exec_flops / (ms * 1e-3) / 1e12
+        roof = {"bound": "tensor", "kernel": f"attn_fwd_kernel (3D neighbourhood, brick {brick}, pair {pair}, d={d})",
+                "achieved": round(ach, 2), "peak": peak, "unit": "TFLOP/s", "frac": round(ach / peak, 4),
+                "peak_source": f"{peaks_src} bf16_tflops (burst: one kernel per timed step, L2 flushed between)",
+                "traffic": None}
+        extra = {"executed_tflops": round(world * ach, 2), "window_fraction_of_executed": round(flops / exec_flops, 4)}
+    elif args.workload == "dense16k":
         peak = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
         roof = {"bound": "tensor", "kernel": "attn_fwd_kernel (dense, d=128)", "achieved": round(value / world, 2),
                 "peak": peak, "unit": "TFLOP/s", "frac": round(value / world / peak, 4),
@@ -353,9 +373,10 @@ def run_native_kernel(args, world, rank, local):
     return {"metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": f"{args.workload}: B={B} H={H} Sq={Sq} Skv={Skv} d={d}", "seq_len": Skv,
-                       "l2": "256 MB buffer written between timed steps (L2 flush)"},
-            "roofline": roof, "gpu_launches": launches * args.steps, "clocks": clocks.summary()}
+            "config": {"workload": f"{args.workload}: B={B} H={H} Sq={Sq} Skv={Skv} d={d}"
+                       + (f" volume {w.grid} window {w0.extra['kernel']}" if args.workload == "na3d" else ""),
+                       "seq_len": Skv, "l2": "256 MB buffer written between timed steps (L2 flush)"},
+            **extra, "roofline": roof, "gpu_launches": launches * args.steps, "clocks": clocks.summary()}
 
 
 def run_e2e(args, vd, w, qkv, cross, rt, ws, step_flops, world):
@@ -520,7 +541,7 @@ def main():
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
     ap.add_argument("--beta", type=float, default=1.0)
     ap.add_argument("--heads", type=int, default=32, help="heads (32 = the benchmark; fewer only for profiling)")
-    ap.add_argument("--workload", choices=["sparse64k", "dense16k", "cross"], default="sparse64k",
+    ap.add_argument("--workload", choices=["sparse64k", "dense16k", "cross", "na3d"], default="sparse64k",
                     help="sparse64k = the benchmark step; dense16k / cross time one kernel path each")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
