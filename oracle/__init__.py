@@ -17,6 +17,9 @@ hand-derived closed form of that reading: parity unpinned with respect to the
 pages.  3D neighbourhood attention follows the published definition of
 neighbourhood attention (the pages name the kernel but do not define it) and
 is pinned by closed forms, an independent brute force and a mirror symmetry.
+The FP8 (E4M3) codec, the per-row activation quantiser and the scaled FP8
+product are pinned by torch's float8_e4m3fn conversion, a nearest-value search
+and numpy's matmul.
 """
 from __future__ import annotations
 
@@ -63,8 +66,16 @@ def _configure(lib):
                                        ctypes.c_double, _I64, _i64, _D, _D]
     lib.oracle_na3d_rows.argtypes = [_D, _D, _D, _i64, _i64, _i64, _i64, _i64, _i64, _i64, _i64, ctypes.c_double,
                                      _I64, _i64, _D, _D]
+    lib.oracle_e4m3_decode.argtypes = [ctypes.c_uint8]
+    lib.oracle_e4m3_decode.restype = ctypes.c_double
+    lib.oracle_e4m3_encode.argtypes = [ctypes.c_float]
+    lib.oracle_e4m3_encode.restype = ctypes.c_uint8
+    _F = ctypes.POINTER(ctypes.c_float)
+    lib.oracle_fp8_quantize_rows.argtypes = [_F, _i64, _i64, _U8, _F]
+    lib.oracle_fp8_gemm.argtypes = [_U8, _F, _U8, _F, _i64, _i64, _i64, _D, _D]
     for f in (lib.oracle_attend_rows, lib.oracle_split_partials, lib.oracle_lse_merge, lib.oracle_block_pool,
-              lib.oracle_route, lib.oracle_sparse_rows, lib.oracle_na3d_rows):
+              lib.oracle_route, lib.oracle_sparse_rows, lib.oracle_na3d_rows, lib.oracle_fp8_quantize_rows,
+              lib.oracle_fp8_gemm):
         f.restype = None
     return lib
 
@@ -244,3 +255,50 @@ def na3d_attention(q, k, v, grid, kernel, scale: float, rows=None):
     if full:
         return out.reshape(B, H, S, d), lse.reshape(B, H, S)
     return out, lse
+
+
+def e4m3_decode(codes):
+    """float64 values of E4M3 codes (any integer array of 0..255)."""
+    lib = _load()
+    c = np.asarray(codes, dtype=np.uint8)
+    return np.vectorize(lambda x: lib.oracle_e4m3_decode(int(x)), otypes=[np.float64])(c) if c.size else \
+        np.zeros(c.shape)
+
+
+def e4m3_encode(values):
+    """E4M3 codes (uint8) of float32 values: nearest, ties to even, saturating at 448."""
+    lib = _load()
+    v = np.asarray(values, dtype=np.float32)
+    return np.vectorize(lambda x: lib.oracle_e4m3_encode(float(x)), otypes=[np.uint8])(v) if v.size else \
+        np.zeros(v.shape, dtype=np.uint8)
+
+
+def fp8_quantize_rows(x):
+    """Per-row E4M3 quantisation of x [M, K] (float32 values): (codes uint8 [M, K], scale float32 [M])."""
+    x = np.ascontiguousarray(np.asarray(x, dtype=np.float32))
+    if x.ndim != 2:
+        raise ValueError("expected [M, K]")
+    M, K = x.shape
+    q = np.empty((M, K), dtype=np.uint8)
+    s = np.empty(M, dtype=np.float32)
+    _load().oracle_fp8_quantize_rows(_p(x, ctypes.POINTER(ctypes.c_float)), M, K, _p(q, _U8),
+                                     _p(s, ctypes.POINTER(ctypes.c_float)))
+    return q, s
+
+
+def fp8_gemm(aq, sa, wq, sw):
+    """y[m, n] = sa[m] sw[n] sum_k dec(aq[m, k]) dec(wq[n, k]) in float64, and the matching
+    sum of absolute products (for error bounds).  aq [M, K], wq [N, K] uint8 codes."""
+    aq = np.ascontiguousarray(aq, dtype=np.uint8)
+    wq = np.ascontiguousarray(wq, dtype=np.uint8)
+    sa = np.ascontiguousarray(sa, dtype=np.float32)
+    sw = np.ascontiguousarray(sw, dtype=np.float32)
+    M, K = aq.shape
+    N = wq.shape[0]
+    if wq.shape[1] != K or sa.shape != (M,) or sw.shape != (N,):
+        raise ValueError("shape mismatch")
+    y = np.empty((M, N))
+    ya = np.empty((M, N))
+    F = ctypes.POINTER(ctypes.c_float)
+    _load().oracle_fp8_gemm(_p(aq, _U8), _p(sa, F), _p(wq, _U8), _p(sw, F), M, N, K, _p(y, _D), _p(ya, _D))
+    return y, ya

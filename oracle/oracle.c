@@ -30,6 +30,12 @@
  *    pages do not define the window; oracle_na3d_rows uses the published
  *    neighbourhood-attention definition (each query attends to the K keys per
  *    axis nearest to it, the window shifted inward at the borders).
+ *  - "LTX-2.5 at 4K, in half the time", section "Thinner seams": the weights
+ *    stay in FP8, the activations are converted to FP8 with one scale per row,
+ *    and the products accumulate in FP32; "Optimization Tips", section "FP8
+ *    Quantization": FP8 scaled matrix multiplication.  The FP8 format is
+ *    E4M3 (the OCP 8-bit floating-point definition: bias 7, three mantissa
+ *    bits, subnormals, no infinities, largest finite value 448).
  *
  * Parity status per function (what pins it is listed in the test suite):
  *  - oracle_attend_rows, oracle_split_partials, oracle_lse_merge,
@@ -38,12 +44,17 @@
  *  - oracle_na3d_rows: pinned by closed forms (a window of one token, a
  *    window covering the whole grid), a brute-force masked softmax with the
  *    window found by a different construction, and a mirror symmetry.
+ *  - oracle_e4m3_encode / oracle_e4m3_decode / oracle_fp8_quantize_rows /
+ *    oracle_fp8_gemm: pinned by torch's float8_e4m3fn conversion, a
+ *    nearest-value search over the code table, the quantiser's error bound
+ *    and numpy's matmul of the decoded operands.
  *  - oracle_route (Taylor aggregates W, T) and oracle_sparse_rows: the pages
  *    give no formula for the Taylor term.  The first-order block-level form
  *    used here is this build's reading; it is pinned by a hand-derived closed
  *    form and by invariants of that reading, so its agreement with the
  *    pages' (unprinted) formula is "parity unpinned".
  */
+#include <fenv.h>
 #include <math.h>
 #include <stdint.h>
 #include <stdlib.h>
@@ -382,5 +393,96 @@ void oracle_na3d_rows(const double* q, const double* k, const double* v, int64_t
     }
     free(kbuf);
     free(xbuf);
+  }
+}
+
+/* ---------------------------------------------------------------- FP8 (E4M3)
+ * Code layout S.EEEE.MMM.  E = 0: subnormal, value M * 2^-9.  E = 1..15:
+ * (1 + M/8) * 2^(E-7), except S.1111.111, which is NaN.  Largest finite value
+ * 1.75 * 2^8 = 448. */
+double oracle_e4m3_decode(uint8_t c) {
+  const int sgn = c >> 7, e = (c >> 3) & 15, m = c & 7;
+  if (e == 15 && m == 7) return NAN;
+  const double mag = e == 0 ? m * ldexp(1.0, -9) : (1.0 + m / 8.0) * ldexp(1.0, e - 7);
+  return sgn ? -mag : mag;
+}
+
+/* Round a finite value to the nearest E4M3 value, ties to the even code
+ * (mantissa LSB 0), and saturate magnitudes beyond 448 to 448.  NaN maps to
+ * the NaN code 0x7f.  The arithmetic below is exact in double for any float
+ * input: scaling by powers of two and taking the fractional mantissa. */
+uint8_t oracle_e4m3_encode(float v) {
+  if (isnan(v)) return 0x7f;
+  const uint8_t sgn = signbit(v) ? 0x80 : 0x00;
+  const double a = fabs((double)v);
+  if (a >= 448.0) return sgn | 0x7e;
+  if (a < ldexp(1.0, -6)) {
+    /* subnormal grid: multiples of 2^-9; 8 * 2^-9 is the smallest normal, code 0x08 */
+    const double r = nearbyint(a * 512.0);
+    return sgn | (uint8_t)r;
+  }
+  int E;
+  frexp(a, &E);              /* a = f * 2^E, f in [0.5, 1) */
+  int e = E - 1;             /* a = m * 2^e, m in [1, 2) */
+  const double m = ldexp(a, -e);
+  double r = nearbyint((m - 1.0) * 8.0);
+  if (r == 8.0) {            /* rounded up to the next binade */
+    r = 0.0;
+    ++e;
+  }
+  return sgn | (uint8_t)(((e + 7) << 3) | (int)r);
+}
+
+/* Per-row activation quantisation.  x: [M][K] (bf16 values widened to float).
+ * For each row: amax = max |x| (float), scale = amax / 448 (float division),
+ * code = e4m3(x / scale) (float division, then round-to-nearest-even with
+ * saturation).  A row of zeros gets scale 0 and zero codes.  The divisions are
+ * done in single precision because they decide the integer codes, exactly as
+ * the GPU decides them. */
+void oracle_fp8_quantize_rows(const float* x, int64_t M, int64_t K, uint8_t* q, float* scale) {
+#pragma omp parallel for schedule(static)
+  for (int64_t m = 0; m < M; ++m) {
+    const float* row = x + m * K;
+    float amax = 0.0f;
+    for (int64_t k = 0; k < K; ++k) {
+      const float a = fabsf(row[k]);
+      if (a > amax) amax = a;
+    }
+    if (amax == 0.0f) {
+      scale[m] = 0.0f;
+      for (int64_t k = 0; k < K; ++k) q[m * K + k] = 0;
+      continue;
+    }
+    volatile float s = amax / 448.0f;
+    scale[m] = s;
+    for (int64_t k = 0; k < K; ++k) {
+      volatile float v = row[k] / s;
+      q[m * K + k] = oracle_e4m3_encode(v);
+    }
+  }
+}
+
+/* Scaled FP8 matrix product.  aq: [M][K] codes with row scales sa[M]; wq: [N][K]
+ * codes (one output channel per row) with scales sw[N].
+ *   y[m][n]    = sa[m] * sw[n] * sum_k dec(aq[m][k]) * dec(wq[n][k])
+ *   yabs[m][n] = |sa[m] * sw[n]| * sum_k |dec(aq[m][k]) * dec(wq[n][k])|  (nullable)
+ * in double, k ascending. */
+void oracle_fp8_gemm(const uint8_t* aq, const float* sa, const uint8_t* wq, const float* sw, int64_t M, int64_t N,
+                     int64_t K, double* y, double* yabs) {
+  double lut[256];
+  for (int c = 0; c < 256; ++c) lut[c] = oracle_e4m3_decode((uint8_t)c);
+#pragma omp parallel for schedule(dynamic, 4)
+  for (int64_t m = 0; m < M; ++m) {
+    for (int64_t n = 0; n < N; ++n) {
+      double acc = 0.0, aacc = 0.0;
+      for (int64_t k = 0; k < K; ++k) {
+        const double t = lut[aq[m * K + k]] * lut[wq[n * K + k]];
+        acc += t;
+        aacc += fabs(t);
+      }
+      const double f = (double)sa[m] * (double)sw[n];
+      y[m * N + n] = f * acc;
+      if (yabs) yabs[m * N + n] = fabs(f) * aacc;
+    }
   }
 }

@@ -39,6 +39,14 @@ MUTANTS = [
     ("na: y-fastest raster order", "kbuf[n++] = (tt * Y + yy) * X + xx;", "kbuf[n++] = (tt * X + xx) * Y + yy;"),
     ("na: q.v instead of q.k", "dot += qrow[c] * kh[kbuf[j] * d + c];", "dot += qrow[c] * vh[kbuf[j] * d + c];"),
     ("na: lse without max", "lse[r] = M + log(l);", "lse[r] = log(l);"),
+    ("e4m3: exponent bias 8", "(1.0 + m / 8.0) * ldexp(1.0, e - 7)", "(1.0 + m / 8.0) * ldexp(1.0, e - 8)"),
+    ("e4m3: subnormal step 2^-10", "const double r = nearbyint(a * 512.0);", "const double r = nearbyint(a * 1024.0);"),
+    ("e4m3: ties away from zero", "double r = nearbyint((m - 1.0) * 8.0);", "double r = round((m - 1.0) * 8.0);"),
+    ("e4m3: truncation", "double r = nearbyint((m - 1.0) * 8.0);", "double r = floor((m - 1.0) * 8.0);"),
+    ("e4m3: no saturation", "if (a >= 448.0) return sgn | 0x7e;", "if (a >= 480.0) return sgn | 0x7e;"),
+    ("quant: scale over 240", "volatile float s = amax / 448.0f;", "volatile float s = amax / 240.0f;"),
+    ("gemm: weight scale dropped", "const double f = (double)sa[m] * (double)sw[n];", "const double f = (double)sa[m];"),
+    ("gemm: weight transposed", "lut[wq[n * K + k]]", "lut[wq[(k % N) * K + (n % K)]]"),
     ("na: no normalisation", "o[c] /= l;\n      lse[r] = M + log(l);", "\n      lse[r] = M + log(l);"),
 ]
 
@@ -63,6 +71,13 @@ PINS = [
     lambda: pins.test_na3d_window_indicator(*pins.NA_CASES[0]),
     pins.test_na3d_single_token_window_returns_own_value,
     lambda: pins.test_na3d_mirror_symmetry_odd_window(0),
+    pins.test_e4m3_decode_matches_library_for_every_code,
+    pins.test_e4m3_encode_round_trips_every_finite_code,
+    pins.test_e4m3_encode_matches_library_conversion,
+    pins.test_e4m3_encode_saturates,
+    pins.test_e4m3_encode_is_the_nearest_value_ties_to_even,
+    pins.test_quantize_rows_error_bound_and_row_max,
+    pins.test_fp8_gemm_matches_library_matmul_of_decoded_operands,
 ]
 
 

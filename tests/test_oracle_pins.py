@@ -473,3 +473,112 @@ def test_na3d_row_subset_matches_full():
     ro, rl = oracle.na3d_attention(q, k, v, grid, kernel, 0.4, rows=rows)
     np.testing.assert_array_equal(ro, out.reshape(-1, d)[rows])
     np.testing.assert_array_equal(rl, lse.reshape(-1)[rows])
+
+
+# ---------------------------------------------------------------- FP8 (E4M3) codec, quantiser and scaled product
+
+def torch_e4m3_values(codes):
+    """torch's own decoding of E4M3 codes (a library routine the oracle does not use)."""
+    return torch.from_numpy(np.asarray(codes, dtype=np.uint8)).view(torch.float8_e4m3fn).float().double().numpy()
+
+
+def test_e4m3_decode_matches_library_for_every_code():
+    codes = np.arange(256, dtype=np.uint8)
+    ours, lib = oracle.e4m3_decode(codes), torch_e4m3_values(codes)
+    np.testing.assert_array_equal(np.isnan(ours), np.isnan(lib))
+    np.testing.assert_array_equal(ours[~np.isnan(ours)], lib[~np.isnan(lib)])
+    assert np.isnan(ours[[0x7f, 0xff]]).all() and np.isnan(ours).sum() == 2
+    assert ours[0x7e] == 448.0 and ours[0x01] == 2.0 ** -9 and ours[0x08] == 2.0 ** -6 and ours[0x38] == 1.0
+
+
+def test_e4m3_encode_round_trips_every_finite_code():
+    codes = np.array([c for c in range(256) if c not in (0x7f, 0xff)], dtype=np.uint8)
+    vals = oracle.e4m3_decode(codes).astype(np.float32)
+    np.testing.assert_array_equal(oracle.e4m3_encode(vals), codes)
+
+
+def test_e4m3_encode_matches_library_conversion():
+    rng = np.random.default_rng(5)
+    v = np.concatenate([rng.uniform(-448, 448, 20000), rng.uniform(-0.02, 0.02, 20000),
+                        np.exp(rng.uniform(-12, 6, 20000)) * rng.choice([-1, 1], 20000)]).astype(np.float32)
+    lib = torch.from_numpy(v).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    np.testing.assert_array_equal(oracle.e4m3_encode(v), lib)
+
+
+def test_e4m3_encode_is_the_nearest_value_ties_to_even():
+    # brute force: search the whole finite code table for the nearest value
+    table_codes = np.array([c for c in range(128) if c != 0x7f], dtype=np.uint8)
+    table = oracle.e4m3_decode(table_codes)
+    rng = np.random.default_rng(6)
+    mids = (table[:-1] + table[1:]) / 2                     # exact ties between neighbours
+    v = np.concatenate([rng.uniform(0, 448, 3000), np.exp(rng.uniform(-14, 6, 3000)), mids]).astype(np.float32)
+    v = v[v.astype(np.float64) <= 448]
+    got = oracle.e4m3_encode(v)
+    for x, g in zip(v.astype(np.float64), got):
+        dist = np.abs(table - x)
+        best = np.flatnonzero(dist == dist.min())
+        if len(best) == 1:
+            assert g == table_codes[best[0]], (x, g)
+        else:                                               # a tie: the even code wins
+            assert g == [table_codes[b] for b in best if table_codes[b] % 2 == 0][0], (x, g)
+    # negative values mirror the positive ones with the sign bit
+    np.testing.assert_array_equal(oracle.e4m3_encode(-v), got | 0x80)
+
+
+def test_e4m3_encode_saturates():
+    big = np.array([448.0, 449.0, 463.9, 464.0, 470.0, 479.9, 500.0, 1e6, 3.4e38], dtype=np.float32)
+    np.testing.assert_array_equal(oracle.e4m3_encode(big), 0x7e)
+    np.testing.assert_array_equal(oracle.e4m3_encode(-big), 0xfe)
+
+
+def test_quantize_rows_error_bound_and_row_max():
+    rng = np.random.default_rng(7)
+    x = rng.standard_normal((37, 300)).astype(np.float32) * np.exp(rng.uniform(-8, 8, (37, 1))).astype(np.float32)
+    x[3] = 0.0                                             # a row of zeros
+    x[4, :] = 0.0
+    x[4, 17] = -2.5                                        # a single non-zero
+    q, s = oracle.fp8_quantize_rows(x)
+    dq = oracle.e4m3_decode(q) * s[:, None].astype(np.float64)
+    amax = np.abs(x).max(axis=1)
+    for m in range(x.shape[0]):
+        if amax[m] == 0:
+            assert s[m] == 0 and (q[m] == 0).all()
+            continue
+        # scale = amax / 448 in single precision, and the row max lands on +-448 (code 0x7e / 0xfe)
+        assert s[m] == np.float32(amax[m]) / np.float32(448.0)
+        j = int(np.argmax(np.abs(x[m])))
+        assert q[m, j] & 0x7f == 0x7e
+        # relative error <= 2^-4 for normal codes, absolute <= scale * 2^-10 on the subnormal grid (+ the
+        # single-precision division before rounding)
+        err = np.abs(dq[m] - x[m].astype(np.float64))
+        bound = np.maximum(np.abs(x[m]) * 2.0 ** -4, s[m] * 2.0 ** -10) * (1 + 1e-6)
+        assert (err <= bound).all()
+    # the lone non-zero is the row max: code -448, dequantised to -448 * fl32(2.5 / 448)
+    assert q[4, 17] == 0xfe and dq[4, 17] == -448.0 * float(s[4]) and abs(dq[4, 17] + 2.5) < 2.5 * 2.0 ** -23
+    assert (q[4, np.arange(300) != 17] == 0).all()
+
+
+def test_fp8_gemm_matches_library_matmul_of_decoded_operands():
+    rng = np.random.default_rng(8)
+    M, N, K = 23, 41, 96
+    aq = rng.integers(0, 256, (M, K), dtype=np.uint8)
+    wq = rng.integers(0, 256, (N, K), dtype=np.uint8)
+    aq[(aq & 0x7f) == 0x7f] = 0x10                          # no NaN codes
+    wq[(wq & 0x7f) == 0x7f] = 0x22
+    sa = rng.uniform(0.01, 2.0, M).astype(np.float32)
+    sw = rng.uniform(0.01, 2.0, N).astype(np.float32)
+    y, ya = oracle.fp8_gemm(aq, sa, wq, sw)
+    A, W = torch_e4m3_values(aq), torch_e4m3_values(wq)
+    ref = (sa[:, None].astype(np.float64) * (A @ W.T)) * sw[None, :].astype(np.float64)
+    np.testing.assert_allclose(y, ref, rtol=1e-12, atol=1e-12 * np.abs(ref).max())
+    np.testing.assert_allclose(ya, np.abs(sa)[:, None] * (np.abs(A) @ np.abs(W).T) * np.abs(sw)[None, :],
+                               rtol=1e-12)
+
+
+def test_fp8_gemm_identity_weight_returns_dequantised_rows():
+    rng = np.random.default_rng(9)
+    x = rng.standard_normal((9, 32)).astype(np.float32)
+    q, s = oracle.fp8_quantize_rows(x)
+    eye = np.where(np.eye(32, dtype=bool), np.uint8(0x38), np.uint8(0))   # 0x38 = 1.0
+    y, _ = oracle.fp8_gemm(q, s, eye, np.ones(32, dtype=np.float32))
+    np.testing.assert_array_equal(y, oracle.e4m3_decode(q) * s[:, None].astype(np.float64))

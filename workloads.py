@@ -116,6 +116,37 @@ WORKLOADS = {
 }
 
 
+@dataclass
+class LinearWorkload:
+    """A projection y = x W^T of the transformer block: x [M, K] tokens, W [N, K]."""
+    name: str
+    M: int
+    K: int
+    N: int
+    seed: int
+
+
+LINEAR_WORKLOADS = {
+    # the attention output projection of the Stage-2 block: 65664 tokens, hidden 32 x 128 = 4096
+    "fp8_proj": LinearWorkload("fp8_proj", M=65664, K=4096, N=4096, seed=8),
+}
+
+
+def make_linear(w: LinearWorkload, device="cpu", M: int | None = None):
+    """Draw (x bf16 [M, K], W bf16 [N, K]) for a projection.
+
+    x ~ N(0, 1) with a per-token gain exp(0.5 N(0, 1)) (activations of
+    different tokens differ in magnitude, which is what per-row scales are
+    for); W ~ N(0, 1/K).  ``M`` overrides the token count."""
+    M = w.M if M is None else M
+    g = torch.Generator(device=device)
+    g.manual_seed(w.seed)
+    gain = torch.exp(0.5 * torch.randn((M, 1), generator=g, device=device, dtype=torch.float32))
+    x = torch.randn((M, w.K), generator=g, device=device, dtype=torch.float32) * gain
+    W = torch.randn((w.N, w.K), generator=g, device=device, dtype=torch.float32) / math.sqrt(w.K)
+    return x.to(torch.bfloat16), W.to(torch.bfloat16)
+
+
 def make_qkv(w: Workload, device="cpu", Sq: int | None = None, Skv: int | None = None, H: int | None = None):
     """Draw (q, k, v) bf16 [B, H, S, d] for workload ``w``.
 
