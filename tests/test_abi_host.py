@@ -1,6 +1,6 @@
 """Host-side checks of the C ABI (no GPU): the library loads, exports every
-entry point include/attn_api.h declares, and rejects invalid arguments before
-touching the device."""
+entry point the headers in include/ declare, and rejects invalid arguments
+before touching the device."""
 import ctypes
 import math
 import os
@@ -13,7 +13,8 @@ import video_diffusion_transformer_block_gb300 as vd
 from video_diffusion_transformer_block_gb300 import build as vbuild
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-HEADER = os.path.join(ROOT, "include", "attn_api.h")
+HEADERS = [os.path.join(ROOT, "include", h) for h in sorted(os.listdir(os.path.join(ROOT, "include")))
+           if h.endswith(".h")]
 
 
 @pytest.fixture(scope="module")
@@ -23,9 +24,11 @@ def lib():
 
 
 def declared_functions():
-    text = open(HEADER).read()
-    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(attn_[a-z0-9_]+)\s*\(", text)))
+    names = set()
+    for h in HEADERS:
+        text = re.sub(r"/\*.*?\*/", "", open(h).read(), flags=re.S)
+        names.update(re.findall(r"\b((?:attn|fp8)_[a-z0-9_]+)\s*\(", text))
+    return sorted(names)
 
 
 def test_header_declares_the_binding_names():
@@ -221,3 +224,13 @@ def test_na3d_rejections(lib):
     assert lib.attn_na3d_fwd(*args) == 1
     b, pa = ctypes.c_int(0), ctypes.c_int(-1)
     assert lib.attn_na3d_plan(4, 16, 16, 5, 3, 3, ctypes.byref(b), ctypes.byref(pa), None) == 1   # Kt > T
+
+
+def test_fp8_rejections(lib):
+    for args in [(NULL, P, P, 4, 64), (P, MIS, P, 4, 64), (P, P, P, 0, 64), (P, P, P, 4, 8), (P, P, P, 4, 72)]:
+        assert lib.fp8_quantize_rows(*args, None) == 1, args
+    good = [P, P, P, P, P, 256, 512, 1024]
+    for i, bad in [(0, NULL), (2, MIS), (4, MIS), (5, 0), (6, 4), (6, 12), (7, 8), (7, 40)]:
+        args = list(good)
+        args[i] = bad
+        assert lib.fp8_scaled_gemm(*args, None) == 1, (i, bad)

@@ -21,7 +21,7 @@ __all__ = [
     "attn_sparse_workspace_bytes", "attn_sparse_route_fwd", "attn_sparse_route", "attn_sparse_fwd",
     "attn_last_device_status", "attn_status_string", "attn_selftest_wait_timeout",
     "attn_sparse_route_fwd_noalloc", "attn_sparse_fused_fwd", "attn_na3d_fwd", "attn_na3d_plan",
-    "NOALLOC_WORKSPACE_BYTES", "EXPORTED_SYMBOLS",
+    "fp8_quantize_rows", "fp8_scaled_gemm", "fp8_linear", "NOALLOC_WORKSPACE_BYTES", "EXPORTED_SYMBOLS",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -33,7 +33,7 @@ EXPORTED_SYMBOLS = (
     "attn_dense_fwd", "attn_cross_splitkv_fwd", "attn_lse_merge", "attn_block_pool", "attn_sparse_workspace_bytes",
     "attn_sparse_route_fwd", "attn_sparse_route", "attn_sparse_fwd", "attn_last_device_status", "attn_status_string",
     "attn_selftest_wait_timeout", "attn_sparse_route_fwd_noalloc", "attn_sparse_fused_fwd", "attn_na3d_fwd",
-    "attn_na3d_plan",
+    "attn_na3d_plan", "fp8_quantize_rows", "fp8_scaled_gemm",
 )
 
 # Size of the library-owned scratch of attn_sparse_route_fwd_noalloc (ATTN_NOALLOC_WORKSPACE_BYTES).
@@ -75,6 +75,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         lib.attn_na3d_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, i, f, i, i, vp]
         ip, llp = ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_longlong)
         lib.attn_na3d_plan.argtypes = [i, i, i, i, i, i, ip, ip, llp]
+        lib.fp8_quantize_rows.argtypes = [vp, vp, vp, i, i, vp]
+        lib.fp8_scaled_gemm.argtypes = [vp, vp, vp, vp, vp, i, i, i, vp]
         lib.attn_last_device_status.argtypes = [vp]
         lib.attn_status_string.argtypes = [i]
         lib.attn_status_string.restype = ctypes.c_char_p
@@ -82,7 +84,7 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         for name in ("attn_dense_fwd", "attn_cross_splitkv_fwd", "attn_lse_merge", "attn_block_pool",
                      "attn_sparse_route_fwd", "attn_sparse_route", "attn_sparse_fwd", "attn_last_device_status",
                      "attn_selftest_wait_timeout", "attn_sparse_route_fwd_noalloc", "attn_sparse_fused_fwd",
-                     "attn_na3d_fwd", "attn_na3d_plan"):
+                     "attn_na3d_fwd", "attn_na3d_plan", "fp8_quantize_rows", "fp8_scaled_gemm"):
             getattr(lib, name).restype = ctypes.c_int
         if path is None:
             _lib = lib
@@ -156,6 +158,43 @@ def attn_na3d_fwd(q, k, v, grid, kernel, scale=None, brick=0, pair_axis=-1, out=
     _check("attn_na3d_fwd", lib.attn_na3d_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, T, Y, X, d,
                                               Kt, Ky, Kx, scale, int(brick), int(pair_axis), _stream(stream)))
     return out, lse
+
+
+def _matrix(x, name, dtype):
+    if x.dtype != dtype or not x.is_cuda or x.dim() != 2 or not x.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous CUDA {dtype} matrix")
+    return x.shape
+
+
+def fp8_quantize_rows(x, q=None, scale=None, stream=None):
+    """Per-row E4M3 quantisation of a bf16 matrix [M, K]: (codes uint8 [M, K], scale fp32 [M])."""
+    lib = load_library()
+    M, K = _matrix(x, "x", torch.bfloat16)
+    q = torch.empty((M, K), dtype=torch.uint8, device=x.device) if q is None else q
+    scale = torch.empty(M, dtype=torch.float32, device=x.device) if scale is None else scale
+    _check("fp8_quantize_rows", lib.fp8_quantize_rows(_ptr(x), _ptr(q), _ptr(scale), M, K, _stream(stream)))
+    return q, scale
+
+
+def fp8_scaled_gemm(aq, a_scale, wq, w_scale, y=None, stream=None):
+    """y [M, N] bf16 = diag(a_scale) (aq wq^T) diag(w_scale); aq [M, K], wq [N, K] E4M3 codes (uint8)."""
+    lib = load_library()
+    M, K = _matrix(aq, "aq", torch.uint8)
+    N, K2 = _matrix(wq, "wq", torch.uint8)
+    if K2 != K or a_scale.shape != (M,) or w_scale.shape != (N,):
+        raise ValueError("shape mismatch")
+    if a_scale.dtype != torch.float32 or w_scale.dtype != torch.float32:
+        raise ValueError("scales must be float32")
+    y = torch.empty((M, N), dtype=torch.bfloat16, device=aq.device) if y is None else y
+    _check("fp8_scaled_gemm", lib.fp8_scaled_gemm(_ptr(aq), _ptr(a_scale), _ptr(wq), _ptr(w_scale), _ptr(y), M, N, K,
+                                                  _stream(stream)))
+    return y
+
+
+def fp8_linear(x, wq, w_scale, stream=None):
+    """y = x W^T with W held in FP8 (wq, w_scale) and x quantised per row on the fly."""
+    aq, sa = fp8_quantize_rows(x, stream=stream)
+    return fp8_scaled_gemm(aq, sa, wq, w_scale, stream=stream)
 
 
 def attn_cross_splitkv_fwd(q, k, v, n_split, scale=None, out_part=None, lse_part=None, stream=None):

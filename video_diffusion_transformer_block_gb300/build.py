@@ -20,7 +20,7 @@ INCLUDE = os.path.join(ROOT, "include")
 LIB_NAME = "libvdtb_attn.so"
 LIB_PATH = os.path.join(PKG, LIB_NAME)
 BUILD_DIR = os.path.join(PKG, "_build")
-SOURCES = ["attn_api.cu", "aux_kernels.cu", "attn_fwd_d128.cu", "attn_fwd_d64.cu"]
+SOURCES = ["attn_api.cu", "aux_kernels.cu", "attn_fwd_d128.cu", "attn_fwd_d64.cu", "fp8_gemm.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xptxas", "-warn-spills"]
 
@@ -37,8 +37,9 @@ def _fingerprint() -> str:
     for name in sorted(os.listdir(CSRC)):
         with open(os.path.join(CSRC, name), "rb") as f:
             h.update(name.encode() + f.read())
-    with open(os.path.join(INCLUDE, "attn_api.h"), "rb") as f:
-        h.update(f.read())
+    for name in sorted(os.listdir(INCLUDE)):
+        with open(os.path.join(INCLUDE, name), "rb") as f:
+            h.update(name.encode() + f.read())
     h.update(" ".join(ARCH + NVCC_FLAGS).encode())
     return h.hexdigest()
 

@@ -10,6 +10,7 @@
 #include <string.h>
 
 #include "attn_api.h"
+#include "fp8_api.h"
 #include "launch.h"
 
 namespace vdtb {
@@ -79,6 +80,21 @@ attn_status_t make_map_5d(CUtensorMap* m, const void* ptr, int D, int T, int Y, 
   cuuint32_t box[5] = {64, (cuuint32_t)bx, (cuuint32_t)by, (cuuint32_t)bt, 1};
   cuuint32_t es[5] = {1, 1, 1, 1, 1};
   CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(ptr), dims, strides, box, es,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+// 2-D map over a [rows][inner] uint8 matrix (row stride = inner bytes), box
+// (box_inner, box_rows), 128-byte swizzle; elements outside read as zero.
+attn_status_t make_map_2d_u8(CUtensorMap* m, const void* ptr, int inner, int rows, int box_inner, int box_rows) {
+  if (get_encoder() != ATTN_OK) return ATTN_ERR_CUDA;
+  memset(m, 0, sizeof(*m));
+  cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)inner};
+  cuuint32_t box[2] = {(cuuint32_t)box_inner, (cuuint32_t)box_rows};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(ptr), dims, strides, box, es,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? ATTN_OK : ATTN_ERR_CUDA;
@@ -299,6 +315,27 @@ attn_status_t attn_na3d_fwd(const attn_bf16* q, const attn_bf16* k, const attn_b
   p.out = out;
   p.lse = lse;
   return cuda_status(launch_fwd(d, 128, mode, tq, tk, tv, p, stream));
+}
+
+attn_status_t fp8_quantize_rows(const attn_bf16* x, uint8_t* q, float* scale, int M, int K, cudaStream_t stream) {
+  if (!x || !q || !scale || !aligned16(x) || !aligned16(q) || ((uintptr_t)scale & 3u)) return ATTN_ERR_INVALID_ARG;
+  if (M < 1 || K < 16 || K % 16 != 0 || K > (1 << 30)) return ATTN_ERR_INVALID_ARG;
+  return cuda_status(launch_fp8_quantize_rows(x, q, scale, M, K, stream));
+}
+
+attn_status_t fp8_scaled_gemm(const uint8_t* aq, const float* a_scale, const uint8_t* wq, const float* w_scale,
+                              attn_bf16* y, int M, int N, int K, cudaStream_t stream) {
+  if (!aq || !a_scale || !wq || !w_scale || !y) return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(aq) || !aligned16(wq) || !aligned16(y) || ((uintptr_t)a_scale & 3u) || ((uintptr_t)w_scale & 3u))
+    return ATTN_ERR_INVALID_ARG;
+  if (M < 1 || N < 8 || N % 8 != 0 || K < 16 || K % 16 != 0 || K > (1 << 30)) return ATTN_ERR_INVALID_ARG;
+  int* status = nullptr;
+  attn_status_t st = status_ptr(&status);
+  if (st != ATTN_OK) return st;
+  CUtensorMap ta, tb;
+  if ((st = make_map_2d_u8(&ta, aq, K, M, 128, 128)) != ATTN_OK) return st;
+  if ((st = make_map_2d_u8(&tb, wq, K, N, 128, 256)) != ATTN_OK) return st;
+  return cuda_status(launch_fp8_gemm(ta, tb, a_scale, w_scale, y, M, N, K, status, stream));
 }
 
 attn_status_t attn_cross_splitkv_fwd(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v, float* out_part,

@@ -1,0 +1,269 @@
+// FP8 (E4M3) projection path for sm_103a: per-row activation quantisation and
+// the scaled FP8 matrix product y = diag(sa) (Aq Wq^T) diag(sw), accumulated
+// in fp32 on the tensor cores (tcgen05 kind::f8f6f4) and written as bf16.
+//
+// GEMM CTA (persistent, one per SM): warp 0 = TMA producer, warp 1 = MMA
+// issuer (one thread), warps 2..5 = epilogue (thread r of the four warps owns
+// accumulator row r = TMEM lane r).  Output tiles are 128 x 256; K advances in
+// blocks of 128 bytes (one 128-byte swizzle atom, four MMAs of K = 32) through a
+// ring of kStages shared-memory slots.  The two halves of TMEM (2 x 256
+// columns) hold the accumulators of consecutive tiles, so the epilogue of tile
+// i overlaps the MMAs of tile i + 1.
+#include <cuda_fp8.h>
+
+#include "launch.h"
+#include "ptx.cuh"
+
+namespace vdtb {
+namespace {
+
+// ---------------------------------------------------------------- quantiser
+
+constexpr int kQuantThreads = 256;
+
+__device__ __forceinline__ float bf16_bits_to_float(uint32_t b) { return __uint_as_float(b << 16); }
+
+__device__ __forceinline__ void unpack8(const uint4& v, float (&f)[8]) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[2 * i] = bf16_bits_to_float(w[i] & 0xffffu);
+    f[2 * i + 1] = bf16_bits_to_float(w[i] >> 16);
+  }
+}
+
+// One CTA per row: amax over the row, scale = amax / 448, codes = e4m3(x /
+// scale) with round-to-nearest-even and saturation.  The second pass re-reads
+// the row, which the first pass has just brought into L1.
+__global__ void __launch_bounds__(kQuantThreads) fp8_quantize_rows_kernel(const uint16_t* __restrict__ x,
+                                                                          uint8_t* __restrict__ q,
+                                                                          float* __restrict__ scale, int K) {
+  const long long row = blockIdx.x;
+  const uint16_t* xr = x + row * K;
+  uint8_t* qr = q + row * K;
+  float amax = 0.f;
+  for (int i = threadIdx.x * 8; i < K; i += kQuantThreads * 8) {
+    float f[8];
+    unpack8(*reinterpret_cast<const uint4*>(xr + i), f);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(f[e]));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  __shared__ float red[kQuantThreads / 32];
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = amax;
+  __syncthreads();
+  amax = red[0];
+#pragma unroll
+  for (int w = 1; w < kQuantThreads / 32; ++w) amax = fmaxf(amax, red[w]);
+  const float s = amax > 0.f ? __fdiv_rn(amax, 448.0f) : 0.f;
+  if (threadIdx.x == 0) scale[row] = s;
+  for (int i = threadIdx.x * 8; i < K; i += kQuantThreads * 8) {
+    float f[8];
+    unpack8(*reinterpret_cast<const uint4*>(xr + i), f);
+    uint32_t lo = 0, hi = 0;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const uint32_t c = s > 0.f ? (uint32_t)__nv_cvt_float_to_fp8(__fdiv_rn(f[e], s), __NV_SATFINITE, __NV_E4M3) : 0u;
+      if (e < 4)
+        lo |= c << (8 * e);
+      else
+        hi |= c << (8 * (e - 4));
+    }
+    *reinterpret_cast<uint2*>(qr + i) = make_uint2(lo, hi);
+  }
+}
+
+// ---------------------------------------------------------------- GEMM
+
+constexpr int kBM = 128, kBN = 256, kBK = 128, kStages = 4;
+constexpr int kGemmThreads = 192;
+constexpr int kStageA = kBM * kBK, kStageB = kBN * kBK, kStageBytes = kStageA + kStageB;
+constexpr int kGemmSmem = 1024 + kStages * kStageBytes;
+constexpr uint32_t kTmemCols = 512;
+// instruction descriptor, kind::f8f6f4: fp32 accumulator (bit 4), A and B
+// E4M3 (type code 0 in bits 7-9 and 10-12), both K-major, N >> 3 at bit 17,
+// M >> 4 at bit 24
+constexpr uint32_t kIdescF8 = (1u << 4) | ((uint32_t)(kBN >> 3) << 17) | ((uint32_t)(kBM >> 4) << 24);
+
+__device__ __forceinline__ void mma_f8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                       uint32_t accum) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accum));
+}
+
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* m, uint64_t* bar, int x, int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];" ::"r"(
+          smem_u32(dst)),
+      "l"((uint64_t)m), "r"(smem_u32(bar)), "r"(x), "r"(y)
+      : "memory");
+}
+
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    fp8_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
+                    const float* __restrict__ sa, const float* __restrict__ sw, uint16_t* __restrict__ y, int M, int N,
+                    int K, int* status) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  __shared__ uint64_t bar_full[kStages], bar_empty[kStages], bar_acc_full[2], bar_acc_empty[2], bar_mma_done;
+  __shared__ uint32_t tmem_base_sh;
+  __shared__ volatile int abort_flag;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int n_nb = (N + kBN - 1) / kBN;
+  const int tiles = ((M + kBM - 1) / kBM) * n_nb;
+  const int nk = (K + kBK - 1) / kBK;
+
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&bar_full[s], 1);
+      mbar_init(&bar_empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&bar_acc_full[b], 1);
+      mbar_init(&bar_acc_empty[b], 128);
+    }
+    mbar_init(&bar_mma_done, 1);
+    abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) tmem_alloc(&tmem_base_sh, kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base_sh;
+
+  if (warp == 0) {
+    // ======================= TMA producer =======================
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_a);
+      tma_prefetch_desc(&tm_b);
+      int it = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < tiles; tile += gridDim.x) {
+        const int mb = tile / n_nb, nb = tile % n_nb;
+        for (int kb = 0; kb < nk; ++kb, ++it) {
+          const int slot = it % kStages;
+          if (it >= kStages && !bounded_wait(&bar_empty[slot], ((it / kStages) - 1) & 1, &abort_flag, status)) {
+            ok = false;
+            break;
+          }
+          uint8_t* sA = smem + slot * kStageBytes;
+          mbar_expect_tx(&bar_full[slot], kStageBytes);
+          tma_load_2d(sA, &tm_a, &bar_full[slot], kb * kBK, mb * kBM);
+          tma_load_2d(sA + kStageA, &tm_b, &bar_full[slot], kb * kBK, nb * kBN);
+        }
+      }
+      // drain: no copy may still be landing when the CTA exits
+      for (int j = (it > kStages ? it - kStages : 0); j < it; ++j)
+        bounded_wait(&bar_full[j % kStages], (j / kStages) & 1, nullptr, status);
+    }
+  } else if (warp == 1) {
+    // ======================= MMA issuer =======================
+    if (lane == 0) {
+      const uint32_t base = smem_u32(smem);
+      int it = 0, tcount = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < tiles; tile += gridDim.x, ++tcount) {
+        const int buf = tcount & 1, use = tcount >> 1;
+        if (use > 0 && !bounded_wait(&bar_acc_empty[buf], (use - 1) & 1, &abort_flag, status)) break;
+        tc_fence_after();
+        const uint32_t d = tmem + buf * kBN;
+        for (int kb = 0; kb < nk; ++kb, ++it) {
+          const int slot = it % kStages;
+          if (!bounded_wait(&bar_full[slot], (it / kStages) & 1, &abort_flag, status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_addr = base + slot * kStageBytes;
+          const uint32_t b_addr = a_addr + kStageA;
+#pragma unroll
+          for (int kk = 0; kk < kBK / 32; ++kk)
+            mma_f8(d, smem_desc_sw128(a_addr + kk * 32, 16, 1024), smem_desc_sw128(b_addr + kk * 32, 16, 1024),
+                   kIdescF8, (kb > 0 || kk > 0) ? 1u : 0u);
+          mma_commit(&bar_empty[slot]);
+        }
+        if (ok) mma_commit(&bar_acc_full[buf]);
+      }
+      // every MMA issued by this thread has completed before TMEM is released
+      mma_commit(&bar_mma_done);
+      bounded_wait(&bar_mma_done, 0, nullptr, status);
+    }
+  } else {
+    // ======================= epilogue =======================
+    const int quarter = warp & 3;                 // TMEM lanes [32 quarter, 32 quarter + 32)
+    const int r = quarter * 32 + lane;
+    int tcount = 0;
+    for (int tile = blockIdx.x; tile < tiles; tile += gridDim.x, ++tcount) {
+      const int buf = tcount & 1, use = tcount >> 1;
+      if (!__all_sync(0xffffffffu, bounded_wait(&bar_acc_full[buf], use & 1, &abort_flag, status))) break;
+      tc_fence_after();
+      const int mb = tile / n_nb, nb = tile % n_nb;
+      const long long grow = (long long)mb * kBM + r;
+      const bool row_ok = grow < M;
+      const float s_row = row_ok ? __ldg(sa + grow) : 0.f;
+      uint16_t* dst = y + grow * N;
+      const uint32_t t_addr = tmem + ((uint32_t)(quarter * 32) << 16) + buf * kBN;
+#pragma unroll 1
+      for (int c0 = 0; c0 < kBN; c0 += 32) {
+        uint32_t acc[32];
+        tmem_ld32(t_addr + c0, acc);
+        tmem_ld_wait();
+        tmem_reg_fence(acc);
+        const int col0 = nb * kBN + c0;
+        if (row_ok) {
+#pragma unroll
+          for (int j = 0; j < 32; j += 8) {
+            const int col = col0 + j;
+            if (col + 8 <= N) {
+              float o[8];
+#pragma unroll
+              for (int e = 0; e < 8; ++e) o[e] = __uint_as_float(acc[j + e]) * s_row * __ldg(sw + col + e);
+              uint4 pk;
+              pk.x = pack_bf16x2(o[0], o[1]);
+              pk.y = pack_bf16x2(o[2], o[3]);
+              pk.z = pack_bf16x2(o[4], o[5]);
+              pk.w = pack_bf16x2(o[6], o[7]);
+              *reinterpret_cast<uint4*>(dst + col) = pk;
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&bar_acc_empty[buf]);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_fp8_quantize_rows(const uint16_t* x, uint8_t* q, float* scale, int M, int K, cudaStream_t stream) {
+  fp8_quantize_rows_kernel<<<M, kQuantThreads, 0, stream>>>(x, q, scale, K);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fp8_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const float* sa, const float* sw,
+                            uint16_t* y, int M, int N, int K, int* status, cudaStream_t stream) {
+  cudaError_t e = cudaFuncSetAttribute(fp8_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmem);
+  if (e != cudaSuccess) return e;
+  int dev = 0, sms = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+  const long long tiles = (long long)((M + kBM - 1) / kBM) * ((N + kBN - 1) / kBN);
+  const int grid = (int)(tiles < sms ? tiles : sms);
+  fp8_gemm_kernel<<<grid, kGemmThreads, kGemmSmem, stream>>>(ta, tb, sa, sw, y, M, N, K, status);
+  return cudaGetLastError();
+}
+
+}  // namespace vdtb

@@ -33,6 +33,14 @@ inline int fwd_query_tiles(int mode) { return mode == kModeSplit ? 1 : 2; }
 // Largest key-block count the fused (on-chip routing) forward accepts.
 constexpr int kFusedMaxNKB = 1024;
 
+// Per-row E4M3 quantisation of x [M][K] bf16 (K % 8 == 0): codes q [M][K], scale [M].
+cudaError_t launch_fp8_quantize_rows(const uint16_t* x, uint8_t* q, float* scale, int M, int K, cudaStream_t stream);
+
+// y [M][N] bf16 = diag(sa) (Aq Wq^T) diag(sw); ta / tb: 2-D uint8 maps of Aq [M][K]
+// (box 128 x 128) and Wq [N][K] (box 128 x 256), 128-byte swizzle.
+cudaError_t launch_fp8_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const float* sa, const float* sw,
+                            uint16_t* y, int M, int N, int K, int* status, cudaStream_t stream);
+
 // Bounded-wait self-test kernel.
 cudaError_t launch_wait_selftest(int limit_us, int* status, cudaStream_t stream);
 
