@@ -434,11 +434,13 @@ uint8_t oracle_e4m3_encode(float v) {
 }
 
 /* Per-row activation quantisation.  x: [M][K] (bf16 values widened to float).
- * For each row: amax = max |x| (float), scale = amax / 448 (float division),
- * code = e4m3(x / scale) (float division, then round-to-nearest-even with
- * saturation).  A row of zeros gets scale 0 and zero codes.  The divisions are
- * done in single precision because they decide the integer codes, exactly as
- * the GPU decides them. */
+ * For each row: amax = max |x| (float), inv = 448 / amax and scale = amax / 448
+ * (float divisions, once per row), code = e4m3(x * inv) (float product, then
+ * round-to-nearest-even with saturation).  The row max lands on +-448 and
+ * x ~ scale * dec(code).  A row of zeros, or a row so small that 448 / amax
+ * overflows the float range, gets scale 0 and zero codes.  The arithmetic is
+ * single precision because it decides the integer codes, exactly as the GPU
+ * decides them. */
 void oracle_fp8_quantize_rows(const float* x, int64_t M, int64_t K, uint8_t* q, float* scale) {
 #pragma omp parallel for schedule(static)
   for (int64_t m = 0; m < M; ++m) {
@@ -448,7 +450,8 @@ void oracle_fp8_quantize_rows(const float* x, int64_t M, int64_t K, uint8_t* q, 
       const float a = fabsf(row[k]);
       if (a > amax) amax = a;
     }
-    if (amax == 0.0f) {
+    volatile float inv = amax > 0.0f ? 448.0f / amax : 0.0f;
+    if (!(amax > 0.0f) || isinf(inv)) {
       scale[m] = 0.0f;
       for (int64_t k = 0; k < K; ++k) q[m * K + k] = 0;
       continue;
@@ -456,7 +459,7 @@ void oracle_fp8_quantize_rows(const float* x, int64_t M, int64_t K, uint8_t* q, 
     volatile float s = amax / 448.0f;
     scale[m] = s;
     for (int64_t k = 0; k < K; ++k) {
-      volatile float v = row[k] / s;
+      volatile float v = row[k] * inv;
       q[m * K + k] = oracle_e4m3_encode(v);
     }
   }

@@ -45,6 +45,8 @@ MUTANTS = [
     ("e4m3: truncation", "double r = nearbyint((m - 1.0) * 8.0);", "double r = floor((m - 1.0) * 8.0);"),
     ("e4m3: no saturation", "if (a >= 448.0) return sgn | 0x7e;", "if (a >= 480.0) return sgn | 0x7e;"),
     ("quant: scale over 240", "volatile float s = amax / 448.0f;", "volatile float s = amax / 240.0f;"),
+    ("quant: inverse scale over 240", "volatile float inv = amax > 0.0f ? 448.0f / amax : 0.0f;",
+     "volatile float inv = amax > 0.0f ? 240.0f / amax : 0.0f;"),
     ("gemm: weight scale dropped", "const double f = (double)sa[m] * (double)sw[n];", "const double f = (double)sa[m];"),
     ("gemm: weight transposed", "lut[wq[n * K + k]]", "lut[wq[(k % N) * K + (n % K)]]"),
     ("na: no normalisation", "o[c] /= l;\n      lse[r] = M + log(l);", "\n      lse[r] = M + log(l);"),

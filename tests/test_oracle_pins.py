@@ -546,6 +546,10 @@ def test_quantize_rows_error_bound_and_row_max():
             continue
         # scale = amax / 448 in single precision, and the row max lands on +-448 (code 0x7e / 0xfe)
         assert s[m] == np.float32(amax[m]) / np.float32(448.0)
+        # codes are e4m3(x * (448 / amax)) with both operations in single precision: torch's conversion
+        inv = np.float32(448.0) / np.float32(amax[m])
+        lib = torch.from_numpy((x[m] * inv).astype(np.float32)).clamp(-448, 448).to(torch.float8_e4m3fn)
+        np.testing.assert_array_equal(q[m], lib.view(torch.uint8).numpy())
         j = int(np.argmax(np.abs(x[m])))
         assert q[m, j] & 0x7f == 0x7e
         # relative error <= 2^-4 for normal codes, absolute <= scale * 2^-10 on the subnormal grid (+ the
@@ -553,6 +557,11 @@ def test_quantize_rows_error_bound_and_row_max():
         err = np.abs(dq[m] - x[m].astype(np.float64))
         bound = np.maximum(np.abs(x[m]) * 2.0 ** -4, s[m] * 2.0 ** -10) * (1 + 1e-6)
         assert (err <= bound).all()
+    # a row too small for 448 / amax to stay finite is treated as zero
+    tiny = np.zeros((1, 32), dtype=np.float32)
+    tiny[0, 5] = np.float32(1e-39)
+    tq, ts = oracle.fp8_quantize_rows(tiny)
+    assert ts[0] == 0 and (tq == 0).all()
     # the lone non-zero is the row max: code -448, dequantised to -448 * fl32(2.5 / 448)
     assert q[4, 17] == 0xfe and dq[4, 17] == -448.0 * float(s[4]) and abs(dq[4, 17] + 2.5) < 2.5 * 2.0 ** -23
     assert (q[4, np.arange(300) != 17] == 0).all()
