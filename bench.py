@@ -32,7 +32,7 @@ if ROOT not in sys.path:
 import numpy as np  # noqa: E402
 import torch  # noqa: E402
 
-from workloads import WORKLOADS, Workload, make_qkv, to_f64  # noqa: E402
+from workloads import LINEAR_WORKLOADS, WORKLOADS, Workload, make_linear, make_qkv, to_f64  # noqa: E402
 
 METRIC = "attention TFLOP/s (executed & dense-equiv) and % bf16 tensor peak, S=64K, d=128"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
@@ -280,6 +280,77 @@ def run_native(args, world, rank, local):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(q, k, v, w, budget_s=args.cpu_seconds)
     return result
+
+
+def run_fp8_projection(args, world, rank, local):
+    """The block's attention output projection in FP8: per-row quantisation of the
+    activations (fp8_quantize_rows) + the scaled FP8 GEMM (fp8_scaled_gemm), x [65664, 4096]
+    against W [4096, 4096].  The weights ship in FP8, so W is quantised once before timing."""
+    import video_diffusion_transformer_block_gb300 as vd
+    from video_diffusion_transformer_block_gb300 import build as vbuild
+
+    vbuild.build()
+    vd.load_library()
+    peaks, peaks_src = load_peaks()
+    lw = LINEAR_WORKLOADS["fp8_proj"]
+    M = lw.M if args.tokens is None else args.tokens
+    x, W = make_linear(lw, device="cuda", M=M)
+    wq, sw = vd.fp8_quantize_rows(W)
+    K, N = lw.K, lw.N
+    aq = torch.empty((M, K), dtype=torch.uint8, device=x.device)
+    sa = torch.empty(M, dtype=torch.float32, device=x.device)
+    y = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
+    stream = torch.cuda.current_stream()
+    flops = 2.0 * M * N * K
+    q_bytes = M * K * 2 + M * K + M * 4                    # read x, write codes and scales
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+
+    def step(e=None):
+        if e is not None:
+            e[0].record(stream)
+        vd.fp8_quantize_rows(x, q=aq, scale=sa)
+        if e is not None:
+            e[1].record(stream)
+        vd.fp8_scaled_gemm(aq, sa, wq, sw, y=y)
+        if e is not None:
+            e[2].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        for e in ev:
+            step(e)
+        torch.cuda.synchronize()
+    barrier(world)
+    status = vd.attn_last_device_status()
+    if status != 0:
+        raise RuntimeError(f"device status after timed region: {vd.attn_status_string(status)}")
+    ms = max_over_ranks(sum(e[0].elapsed_time(e[2]) for e in ev) / args.steps, world)
+    ms_q = sum(e[0].elapsed_time(e[1]) for e in ev) / args.steps
+    ms_g = sum(e[1].elapsed_time(e[2]) for e in ev) / args.steps
+    value = world * flops / (ms * 1e-3) / 1e12
+    peak_bf16 = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
+    peak = 2.0 * peak_bf16                                  # fp8 = 2 x bf16 (nominal 4.5 / 2.25 PFLOP/s)
+    ach = flops / (ms_g * 1e-3) / 1e12
+    hbm = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
+    q_gbs = q_bytes / (ms_q * 1e-3) / 1e9
+    return {"metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "fp8 (e4m3) x fp8, fp32 accumulate, bf16 out", "data": "synthetic",
+            "config": {"workload": f"fp8_proj: y = x W^T, x [{M}, {K}] quantised per row, W [{N}, {K}] in FP8",
+                       "seq_len": M, "l2": "inputs (538 MB of activations per step) larger than L2; no flush"},
+            "breakdown_ms": {"quantize": round(ms_q, 4), "gemm": round(ms_g, 4)},
+            "roofline": {"bound": "tensor", "kernel": "fp8_gemm_kernel (tcgen05 kind::f8f6f4, 128x256 tiles)",
+                         "achieved": round(ach, 2), "peak": round(peak, 1), "unit": "TFLOP/s",
+                         "frac": round(ach / peak, 4),
+                         "peak_source": f"{peaks_src} bf16_tflops x 2 (the nominal fp8 / bf16 ratio), burst",
+                         "traffic": None},
+            "quantize_roofline": {"bound": "hbm", "kernel": "fp8_quantize_rows_reg_kernel", "achieved": round(q_gbs, 1),
+                                  "peak": hbm, "unit": "GB/s", "frac": round(q_gbs / hbm, 4), "traffic": None},
+            "gpu_launches": 2 * args.steps, "clocks": clocks.summary()}
 
 
 def run_native_kernel(args, world, rank, local):
@@ -541,8 +612,10 @@ def main():
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
     ap.add_argument("--beta", type=float, default=1.0)
     ap.add_argument("--heads", type=int, default=32, help="heads (32 = the benchmark; fewer only for profiling)")
-    ap.add_argument("--workload", choices=["sparse64k", "dense16k", "cross", "na3d"], default="sparse64k",
-                    help="sparse64k = the benchmark step; dense16k / cross time one kernel path each")
+    ap.add_argument("--workload", choices=["sparse64k", "dense16k", "cross", "na3d", "fp8_proj"], default="sparse64k",
+                    help="sparse64k = the benchmark step; dense16k / cross / na3d / fp8_proj time one path each")
+    ap.add_argument("--tokens", type=int, default=None,
+                    help="fp8_proj only: activation rows (default 65664; fewer only for profiling)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
@@ -552,6 +625,8 @@ def main():
     world, rank, local = dist_setup()
     if args.impl == "reference":
         res = run_reference(args, world, rank)
+    elif args.workload == "fp8_proj":
+        res = run_fp8_projection(args, world, rank, local)
     elif args.workload != "sparse64k":
         res = run_native_kernel(args, world, rank, local)
     else:

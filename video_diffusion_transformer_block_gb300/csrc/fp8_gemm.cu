@@ -3,8 +3,9 @@
 // in fp32 on the tensor cores (tcgen05 kind::f8f6f4) and written as bf16.
 //
 // GEMM CTA (persistent, one per SM): warp 0 = TMA producer, warp 1 = MMA
-// issuer (one thread), warps 2..5 = epilogue (thread r of the four warps owns
-// accumulator row r = TMEM lane r).  Output tiles are 128 x 256; K advances in
+// issuer (one thread), warps 2..9 = epilogue: two warps per TMEM lane quarter
+// (a warp may only read its own quarter of the lanes), each taking 128 of the
+// tile's 256 columns for its 32 rows.  Output tiles are 128 x 256; K advances in
 // blocks of 128 bytes (one 128-byte swizzle atom, four MMAs of K = 32) through a
 // ring of kStages shared-memory slots.  The two halves of TMEM (2 x 256
 // columns) hold the accumulators of consecutive tiles, so the epilogue of tile
@@ -32,9 +33,38 @@ __device__ __forceinline__ void unpack8(const uint4& v, float (&f)[8]) {
   }
 }
 
-// One CTA per row: amax over the row, scale = amax / 448, codes = e4m3(x /
-// scale) with round-to-nearest-even and saturation.  The second pass re-reads
-// the row, which the first pass has just brought into L1.
+// Row scales from the row's amax: the dequantisation scale amax / 448 and the
+// inverse 448 / amax (fp32 divisions, once per row).  A zero row, or one whose
+// inverse overflows, quantises to zeros with scale 0.
+__device__ __forceinline__ void row_scales(float amax, float& s, float& inv) {
+  inv = amax > 0.f ? __fdiv_rn(448.0f, amax) : 0.f;
+  if (!(amax > 0.f) || isinf(inv)) {
+    s = 0.f;
+    inv = 0.f;
+  } else {
+    s = __fdiv_rn(amax, 448.0f);
+  }
+}
+
+// Codes of 8 values: e4m3(x * inv), nearest even, saturating at +-448.
+__device__ __forceinline__ uint2 quantize8(const uint4& v, float inv) {
+  float f[8];
+  unpack8(v, f);
+  uint32_t lo = 0, hi = 0;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    const uint32_t c = (uint32_t)__nv_cvt_float_to_fp8(__fmul_rn(f[e], inv), __NV_SATFINITE, __NV_E4M3);
+    if (e < 4)
+      lo |= c << (8 * e);
+    else
+      hi |= c << (8 * (e - 4));
+  }
+  return make_uint2(lo, hi);
+}
+
+// One CTA per row (rows longer than the register-resident kernel takes): amax
+// over the row, then the codes.  The second pass re-reads the row, which the
+// first pass has just brought into L1.
 __global__ void __launch_bounds__(kQuantThreads) fp8_quantize_rows_kernel(const uint16_t* __restrict__ x,
                                                                           uint8_t* __restrict__ q,
                                                                           float* __restrict__ scale, int K) {
@@ -56,28 +86,58 @@ __global__ void __launch_bounds__(kQuantThreads) fp8_quantize_rows_kernel(const 
   amax = red[0];
 #pragma unroll
   for (int w = 1; w < kQuantThreads / 32; ++w) amax = fmaxf(amax, red[w]);
-  const float s = amax > 0.f ? __fdiv_rn(amax, 448.0f) : 0.f;
+  float s, inv;
+  row_scales(amax, s, inv);
   if (threadIdx.x == 0) scale[row] = s;
-  for (int i = threadIdx.x * 8; i < K; i += kQuantThreads * 8) {
-    float f[8];
-    unpack8(*reinterpret_cast<const uint4*>(xr + i), f);
-    uint32_t lo = 0, hi = 0;
+  for (int i = threadIdx.x * 8; i < K; i += kQuantThreads * 8)
+    *reinterpret_cast<uint2*>(qr + i) = quantize8(*reinterpret_cast<const uint4*>(xr + i), inv);
+}
+
+// One CTA of 128 threads per row for rows of up to NV * 1024 elements: each
+// thread keeps its NV 16-byte vectors in registers between the amax and the
+// quantisation, so HBM is read once and every load is issued up front.
+template <int NV>
+__global__ void __launch_bounds__(128) fp8_quantize_rows_reg_kernel(const uint16_t* __restrict__ x,
+                                                                    uint8_t* __restrict__ q,
+                                                                    float* __restrict__ scale, int K) {
+  const long long row = blockIdx.x;
+  const uint16_t* xr = x + row * K;
+  uint8_t* qr = q + row * K;
+  uint4 v[NV];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      const uint32_t c = s > 0.f ? (uint32_t)__nv_cvt_float_to_fp8(__fdiv_rn(f[e], s), __NV_SATFINITE, __NV_E4M3) : 0u;
-      if (e < 4)
-        lo |= c << (8 * e);
-      else
-        hi |= c << (8 * (e - 4));
-    }
-    *reinterpret_cast<uint2*>(qr + i) = make_uint2(lo, hi);
+  for (int c = 0; c < NV; ++c) {
+    const int i = (c * 128 + threadIdx.x) * 8;
+    v[c] = i < K ? __ldcs(reinterpret_cast<const uint4*>(xr + i)) : make_uint4(0, 0, 0, 0);
+  }
+  float amax = 0.f;
+#pragma unroll
+  for (int c = 0; c < NV; ++c) {
+    float f[8];
+    unpack8(v[c], f);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(f[e]));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  __shared__ float red[4];
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = amax;
+  __syncthreads();
+  amax = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
+  float s, inv;
+  row_scales(amax, s, inv);
+  if (threadIdx.x == 0) scale[row] = s;
+#pragma unroll
+  for (int c = 0; c < NV; ++c) {
+    const int i = (c * 128 + threadIdx.x) * 8;
+    if (i < K) __stcs(reinterpret_cast<uint2*>(qr + i), quantize8(v[c], inv));
   }
 }
 
 // ---------------------------------------------------------------- GEMM
 
 constexpr int kBM = 128, kBN = 256, kBK = 128, kStages = 4;
-constexpr int kGemmThreads = 192;
+constexpr int kGemmThreads = 320;
+constexpr int kEpilogueThreads = 256;
 constexpr int kStageA = kBM * kBK, kStageB = kBN * kBK, kStageBytes = kStageA + kStageB;
 constexpr int kGemmSmem = 1024 + kStages * kStageBytes;
 constexpr uint32_t kTmemCols = 512;
@@ -124,7 +184,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&bar_acc_full[b], 1);
-      mbar_init(&bar_acc_empty[b], 128);
+      mbar_init(&bar_acc_empty[b], kEpilogueThreads);
     }
     mbar_init(&bar_mma_done, 1);
     abort_flag = 0;
@@ -196,6 +256,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   } else {
     // ======================= epilogue =======================
     const int quarter = warp & 3;                 // TMEM lanes [32 quarter, 32 quarter + 32)
+    const int half = (warp - 2) >> 2;             // columns [128 half, 128 half + 128)
     const int r = quarter * 32 + lane;
     int tcount = 0;
     for (int tile = blockIdx.x; tile < tiles; tile += gridDim.x, ++tcount) {
@@ -209,7 +270,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       uint16_t* dst = y + grow * N;
       const uint32_t t_addr = tmem + ((uint32_t)(quarter * 32) << 16) + buf * kBN;
 #pragma unroll 1
-      for (int c0 = 0; c0 < kBN; c0 += 32) {
+      for (int c0 = half * (kBN / 2); c0 < (half + 1) * (kBN / 2); c0 += 32) {
         uint32_t acc[32];
         tmem_ld32(t_addr + c0, acc);
         tmem_ld_wait();
@@ -220,9 +281,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           for (int j = 0; j < 32; j += 8) {
             const int col = col0 + j;
             if (col + 8 <= N) {
+              // column scales: the same 8 floats for every lane (broadcast loads)
+              const float4 w0 = __ldg(reinterpret_cast<const float4*>(sw + col));
+              const float4 w1 = __ldg(reinterpret_cast<const float4*>(sw + col + 4));
+              const float ws[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
               float o[8];
 #pragma unroll
-              for (int e = 0; e < 8; ++e) o[e] = __uint_as_float(acc[j + e]) * s_row * __ldg(sw + col + e);
+              for (int e = 0; e < 8; ++e) o[e] = __uint_as_float(acc[j + e]) * s_row * ws[e];
               uint4 pk;
               pk.x = pack_bf16x2(o[0], o[1]);
               pk.y = pack_bf16x2(o[2], o[3]);
@@ -249,7 +314,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 }  // namespace
 
 cudaError_t launch_fp8_quantize_rows(const uint16_t* x, uint8_t* q, float* scale, int M, int K, cudaStream_t stream) {
-  fp8_quantize_rows_kernel<<<M, kQuantThreads, 0, stream>>>(x, q, scale, K);
+  if (K <= 1024)
+    fp8_quantize_rows_reg_kernel<1><<<M, 128, 0, stream>>>(x, q, scale, K);
+  else if (K <= 2048)
+    fp8_quantize_rows_reg_kernel<2><<<M, 128, 0, stream>>>(x, q, scale, K);
+  else if (K <= 4096)
+    fp8_quantize_rows_reg_kernel<4><<<M, 128, 0, stream>>>(x, q, scale, K);
+  else
+    fp8_quantize_rows_kernel<<<M, kQuantThreads, 0, stream>>>(x, q, scale, K);
   return cudaGetLastError();
 }
 
