@@ -326,7 +326,7 @@ attn_status_t fp8_quantize_rows(const attn_bf16* x, uint8_t* q, float* scale, in
 attn_status_t fp8_scaled_gemm(const uint8_t* aq, const float* a_scale, const uint8_t* wq, const float* w_scale,
                               attn_bf16* y, int M, int N, int K, cudaStream_t stream) {
   if (!aq || !a_scale || !wq || !w_scale || !y) return ATTN_ERR_INVALID_ARG;
-  if (!aligned16(aq) || !aligned16(wq) || !aligned16(y) || ((uintptr_t)a_scale & 3u) || ((uintptr_t)w_scale & 3u))
+  if (!aligned16(aq) || !aligned16(wq) || !aligned16(y) || ((uintptr_t)a_scale & 3u) || !aligned16(w_scale))
     return ATTN_ERR_INVALID_ARG;
   if (M < 1 || N < 8 || N % 8 != 0 || K < 16 || K % 16 != 0 || K > (1 << 30)) return ATTN_ERR_INVALID_ARG;
   int* status = nullptr;

@@ -1,7 +1,10 @@
 // tcgen05 attention forward for sm_103a: dense, block-sparse (selected-block
 // lists + Taylor term) and split-KV (chunk partials) share one main loop.
 //
-// CTA = NQT query tiles of 128 rows that share every K/V tile load.
+// CTA = NQT query tiles of 128 rows that share every K/V tile load.  Dense,
+// sparse, split and (by default) neighbourhood launches use NQT = 1 with two
+// CTAs per SM; the two-tile CTA serves the fused routing and the paired
+// neighbourhood plans.
 //   warps 0..4*NQT-1 : softmax/epilogue, one warpgroup per query tile; thread
 //                      r of the warpgroup owns query row r = TMEM lane r
 //   warp  4*NQT      : TMA producer (Q once, then K_s, V_s for every step s
