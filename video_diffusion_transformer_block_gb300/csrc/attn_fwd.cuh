@@ -177,15 +177,17 @@ struct NAWalk {
   }
 };
 
-// Walks the ascending union of up to 4 tile lists (one per query block the
-// CTA owns).  Each step yields the kv tile index and a bit per list that
+// Walks the ascending union of up to NL tile lists (one per query block the
+// CTA owns; NL is fixed at compile time so that a one-list CTA carries one
+// list's state).  Each step yields the kv tile index and a bit per list that
 // contains it.  Dense/split lists are implicit ranges [0, n).
+template <int NL>
 struct TileMerge {
-  const int32_t* ptr[4];
-  const uint16_t* sptr[4];   // lists in shared memory (fused routing)
+  const int32_t* ptr[NL];
+  const uint16_t* sptr[NL];   // lists in shared memory (fused routing)
   bool smem_lists;
-  int n[4];
-  int pos[4];
+  int n[NL];
+  int pos[NL];
   int nlists;
   int limit;      // valid tile indices are [0, limit)
   bool implicit;
@@ -204,9 +206,9 @@ struct TileMerge {
   // Returns the next tile index, or -1 when every list is exhausted.
   __device__ __forceinline__ int next(uint32_t& flags) {
     int u = INT_MAX;
-    int h[4];
+    int h[NL];
 #pragma unroll
-    for (int l = 0; l < 4; ++l) {
+    for (int l = 0; l < NL; ++l) {
       h[l] = INT_MAX;
       if (l < nlists && pos[l] < n[l]) h[l] = head(l);
       u = min(u, h[l]);
@@ -214,7 +216,7 @@ struct TileMerge {
     if (u == INT_MAX) return -1;
     flags = 0;
 #pragma unroll
-    for (int l = 0; l < 4; ++l)
+    for (int l = 0; l < NL; ++l)
       if (h[l] == u) {
         flags |= 1u << l;
         ++pos[l];
@@ -247,8 +249,10 @@ struct FwdCfg {
   // softmax warpgroups after setmaxnreg.inc.  The split must add up to the
   // launch allocation: NQT*128*kRegsSoftmax + 128*kRegsControl <= kThreads*kRegsLaunch.
   static constexpr int kRegsLaunch = NQT == 2 ? 168 : 128;
-  static constexpr int kRegsControl = NQT == 2 ? 64 : 56;
-  static constexpr int kRegsSoftmax = NQT == 2 ? 216 : 200;
+  // (one-tile CTA: 208 / 48 leaves the dense, split and neighbourhood softmax
+  // without spills; the sparse walk measured faster with 200 / 56)
+  static constexpr int kRegsControl = NQT == 2 ? 64 : (kSparseLike ? 56 : 48);
+  static constexpr int kRegsSoftmax = NQT == 2 ? 216 : (kSparseLike ? 200 : 208);
   static_assert(NQT * 128 * kRegsSoftmax + 128 * kRegsControl <= kThreads * kRegsLaunch, "register split");
   static constexpr int kQTileBytes = 128 * D * 2;
   static constexpr int kSlotBytes = BK * D * 2;
@@ -272,8 +276,8 @@ struct FwdCfg {
 };
 
 // Next key tile of a CTA's walk: neighbourhood boxes or the merged lists.
-template <bool NA, class Walk>
-__device__ __forceinline__ int next_tile(Walk& naw, TileMerge& merge, uint32_t& flags, int (&box)[3]) {
+template <bool NA, class Walk, class Merge>
+__device__ __forceinline__ int next_tile(Walk& naw, Merge& merge, uint32_t& flags, int (&box)[3]) {
   if constexpr (NA) {
     return naw.next(flags, box);
   } else {
@@ -495,11 +499,12 @@ __global__ void __launch_bounds__(NQT * 128 + 128, (NQT == 1) ? 2 : 1)
     n_valid_tiles = naw.ntiles;
   }
 
-  TileMerge merge;
+  constexpr int kNL = Cfg::kSparseLike ? NQT * QB : NQT;   // lists this CTA walks at most
+  TileMerge<kNL> merge;
   merge.status = p.status;
   merge.smem_lists = false;
 #pragma unroll
-  for (int l = 0; l < 4; ++l) merge.sptr[l] = f_lists;
+  for (int l = 0; l < kNL; ++l) merge.sptr[l] = f_lists;
   if (MODE == kModeSparseFused) {
     // counts are filled in once the on-chip routing is done (route_ready)
     merge.implicit = false;
@@ -507,7 +512,7 @@ __global__ void __launch_bounds__(NQT * 128 + 128, (NQT == 1) ? 2 : 1)
     merge.nlists = FR;
     merge.limit = p.NKB;
 #pragma unroll
-    for (int l = 0; l < 4; ++l) {
+    for (int l = 0; l < kNL; ++l) {
       merge.pos[l] = 0;
       merge.n[l] = 0;
       merge.ptr[l] = nullptr;
@@ -518,7 +523,7 @@ __global__ void __launch_bounds__(NQT * 128 + 128, (NQT == 1) ? 2 : 1)
     merge.nlists = NQT * QB;
     merge.limit = p.NKB;
 #pragma unroll
-    for (int l = 0; l < 4; ++l) {
+    for (int l = 0; l < kNL; ++l) {
       merge.pos[l] = 0;
       merge.n[l] = 0;
       merge.ptr[l] = p.sel_idx;
@@ -538,7 +543,7 @@ __global__ void __launch_bounds__(NQT * 128 + 128, (NQT == 1) ? 2 : 1)
     int nt = (kv_hi - kv_lo + BK - 1) / BK;
     merge.limit = nt;
 #pragma unroll
-    for (int l = 0; l < 4; ++l) {
+    for (int l = 0; l < kNL; ++l) {
       merge.pos[l] = 0;
       merge.n[l] = nt;
       merge.ptr[l] = nullptr;
@@ -571,7 +576,7 @@ __global__ void __launch_bounds__(NQT * 128 + 128, (NQT == 1) ? 2 : 1)
   // fused routing: lists are ready once the softmax threads arrive on bar_route
   auto take_fused_lists = [&]() {
 #pragma unroll
-    for (int l = 0; l < 4; ++l) merge.n[l] = (l < FR) ? f_cnt[l] : 0;
+    for (int l = 0; l < kNL; ++l) merge.n[l] = (l < FR) ? f_cnt[l] : 0;
   };
 
   if (warp >= Cfg::kProducerWarp) {
