@@ -456,8 +456,9 @@ def run_e2e(args, vd, w, qkv, cross, rt, ws, step_flops, world):
     Every step copies its inputs host->device (q, k, v and the cross-attention
     inputs) and reads its outputs (out, lse and the cross-attention out, lse)
     back to pinned host memory, inside the timed region.  Like a serving loop,
-    the copies are double-buffered on a second stream: step i+1's inputs are
-    uploaded and step i-1's outputs downloaded while step i computes."""
+    the copies are double-buffered: step i+1's inputs are uploaded (one copy
+    stream) and step i-1's outputs downloaded (another copy stream, so the two
+    directions of the host link run concurrently) while step i computes."""
     q, k, v = qkv
     qa, kx, vx = cross
     B, H, S, d, block = w.B, w.H, w.Sq, w.d, w.block
@@ -475,16 +476,16 @@ def run_e2e(args, vd, w, qkv, cross, rt, ws, step_flops, world):
     h2d = sum(t.numel() * t.element_size() for t in hin)
     d2h = sum(t.numel() * t.element_size() for t in hout)
     comp = torch.cuda.current_stream()
-    copy = torch.cuda.Stream()
+    upload, download = torch.cuda.Stream(), torch.cuda.Stream()
 
     def run(steps):
         up = [torch.cuda.Event() for _ in range(steps + 1)]
         done = [torch.cuda.Event() for _ in range(steps)]
         down = [torch.cuda.Event() for _ in range(steps)]
-        with torch.cuda.stream(copy):
+        with torch.cuda.stream(upload):
             for dst, src in zip(din[0], hin):
                 dst.copy_(src, non_blocking=True)
-            up[0].record(copy)
+            up[0].record(upload)
         for i in range(steps):
             buf, ob = din[i % 2], dout[i % 2]
             comp.wait_event(up[i])
@@ -495,18 +496,20 @@ def run_e2e(args, vd, w, qkv, cross, rt, ws, step_flops, world):
             vd.attn_cross_splitkv_fwd(buf[3], buf[4], buf[5], CROSS_N_SPLIT, out_part=op, lse_part=lp, stream=comp)
             vd.attn_lse_merge(op, lp, out=ob[2], lse=ob[3], stream=comp)
             done[i].record(comp)
-            with torch.cuda.stream(copy):
-                if i + 1 < steps:
+            if i + 1 < steps:
+                with torch.cuda.stream(upload):
                     if i >= 1:
-                        copy.wait_event(done[i - 1])      # the other input buffer is free again
+                        upload.wait_event(done[i - 1])    # the other input buffer is free again
                     for dst, src in zip(din[(i + 1) % 2], hin):
                         dst.copy_(src, non_blocking=True)
-                    up[i + 1].record(copy)
-                copy.wait_event(done[i])
+                    up[i + 1].record(upload)
+            with torch.cuda.stream(download):
+                download.wait_event(done[i])
                 for dst, src in zip(hout, ob):
                     dst.copy_(src, non_blocking=True)
-                down[i].record(copy)
-        comp.wait_stream(copy)
+                down[i].record(download)
+        comp.wait_stream(upload)
+        comp.wait_stream(download)
 
     run(2)
     torch.cuda.synchronize()
@@ -522,7 +525,8 @@ def run_e2e(args, vd, w, qkv, cross, rt, ws, step_flops, world):
     ms = max_over_ranks(e0.elapsed_time(e1), world) / steps
     return {"value": round(world * step_flops / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s", "ms_per_step": round(ms, 4),
             "steps": steps, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-            "pipelining": "double-buffered: uploads/downloads on a second stream overlap the previous/next step's compute"}
+            "pipelining": "double-buffered: uploads and downloads on two copy streams overlap each other and the "
+                          "previous/next step's compute"}
 
 
 # ============================================================ oracle (CPU baseline / reference arm)
