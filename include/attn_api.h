@@ -200,6 +200,34 @@ attn_status_t attn_sparse_fused_fwd(const attn_bf16* q, const attn_bf16* k, cons
                                     int32_t* sel_cnt, float* stats, float* taylor_t, cudaStream_t stream);
 
 /*
+ * Split-KV cross attention with the merge fused into the split kernel's tail.
+ * ("LTX-2.5 at 4K, in half the time", section "Attention across two GPUs":
+ * partial answers over slices of the keys, merged exactly.)
+ *
+ *   Computes what attn_cross_splitkv_fwd followed by attn_lse_merge computes,
+ *   in one launch: the CTA of the last key chunk to finish for a (head, 128-row
+ *   query tile) merges that tile's partials (same arithmetic as
+ *   attn_lse_merge, so the results are identical to the two-call path).
+ *   q, k, v, out, lse   as attn_dense_fwd (lse nullable); Sq >= 1, Skv >= 1.
+ *   n_split             1 <= n_split <= Skv, balanced unpadded chunks; at most
+ *                       32 (ATTN_ERR_UNSUPPORTED beyond: use the two calls).
+ *   workspace           device, 16-byte aligned, >= attn_cross_workspace_bytes
+ *                       bytes: the partials and one arrival counter per
+ *                       (head, query tile).  The counters must be zero before
+ *                       the first call on a workspace (e.g. a zero-filled
+ *                       allocation); every call leaves them at zero.  After a
+ *                       call that ended in ATTN_ERR_TIMEOUT, zero the
+ *                       workspace again before reusing it.
+ *   Errors: ATTN_ERR_INVALID_ARG, ATTN_ERR_UNSUPPORTED (d), ATTN_ERR_WORKSPACE
+ *   (too small), ATTN_ERR_CUDA.  Asynchronous on stream; calls sharing a
+ *   workspace must be ordered (same stream).
+ */
+size_t attn_cross_workspace_bytes(int B, int H, int Sq, int d, int n_split);
+attn_status_t attn_cross_fwd(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v, attn_bf16* out, float* lse,
+                             int B, int H, int Sq, int Skv, int d, int n_split, float scale, void* workspace,
+                             size_t workspace_bytes, cudaStream_t stream);
+
+/*
  * 3D neighbourhood attention over a (T, Y, X) token volume.
  * ("LTX-2.5 at 4K, in half the time", section "Inside the decoder": the video
  * decoder's time goes mostly to a neighbourhood-attention kernel; "Optimization

@@ -28,11 +28,12 @@ extern "C" {
 /*
  * Per-row quantisation.  For row m of x [M][K] (bf16, row-major):
  *   amax_m   = max_k |x[m][k]|
- *   scale[m] = amax_m / 448                      (fp32 division)
- *   q[m][k]  = e4m3(x[m][k] / scale[m])          (fp32 division, then round to
+ *   scale[m] = amax_m / 448,  inv_m = 448 / amax_m   (fp32 divisions)
+ *   q[m][k]  = e4m3(x[m][k] * inv_m)             (fp32 product, then round to
  *              nearest, ties to even, saturating at +-448)
  * so the row's largest magnitude maps to +-448 and x ~ scale[m] * q.  A row of
- * zeros gets scale 0 and zero codes.  NaN inputs are not supported.
+ * zeros, or one with amax < 448 / FLT_MAX (inv_m overflows), gets scale 0 and
+ * zero codes.  NaN inputs are not supported.
  *   x      device, 16-byte aligned, [M][K] bf16.
  *   q      device, 16-byte aligned, [M][K] E4M3 codes (uint8).
  *   scale  device, [M] fp32.
@@ -51,8 +52,8 @@ attn_status_t fp8_quantize_rows(const attn_bf16* x, uint8_t* q, float* scale, in
  *   a_scale  device, [M] fp32 (per-row activation scales).
  *   wq       device, 16-byte aligned, [N][K] E4M3 codes (one output channel
  *            per row, i.e. W of y = x W^T).
- *   w_scale  device, [N] fp32 (per-output-channel weight scales; a per-tensor
- *            scale is the case of equal entries).
+ *   w_scale  device, 16-byte aligned, [N] fp32 (per-output-channel weight
+ *            scales; a per-tensor scale is the case of equal entries).
  *   y        device, 16-byte aligned, [M][N] bf16 (row-major).
  *   Errors: ATTN_ERR_INVALID_ARG (null or misaligned pointer, M < 1, N < 8 or
  *   not a multiple of 8, K < 16 or not a multiple of 16), ATTN_ERR_CUDA

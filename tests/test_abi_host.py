@@ -230,7 +230,26 @@ def test_fp8_rejections(lib):
     for args in [(NULL, P, P, 4, 64), (P, MIS, P, 4, 64), (P, P, P, 0, 64), (P, P, P, 4, 8), (P, P, P, 4, 72)]:
         assert lib.fp8_quantize_rows(*args, None) == 1, args
     good = [P, P, P, P, P, 256, 512, 1024]
-    for i, bad in [(0, NULL), (2, MIS), (4, MIS), (5, 0), (6, 4), (6, 12), (7, 8), (7, 40)]:
+    for i, bad in [(0, NULL), (2, MIS), (3, MIS), (4, MIS), (5, 0), (6, 4), (6, 12), (7, 8), (7, 40)]:
         args = list(good)
         args[i] = bad
         assert lib.fp8_scaled_gemm(*args, None) == 1, (i, bad)
+
+
+def test_cross_fused_rejections(lib):
+    need = lib.attn_cross_workspace_bytes(1, 32, 128, 128, 8)
+    rows = 32 * 128
+    assert need >= 8 * rows * 129 * 4 + 32 * 4
+    assert lib.attn_cross_workspace_bytes(1, 32, 128, 96, 8) == 0
+    ws = ctypes.c_void_p(0x100000)
+    base = [P, P, P, P, P, 1, 32, 128, 4096, 128, 8, 0.088, ws, need, None]
+    args = list(base); args[13] = need - 1
+    assert lib.attn_cross_fwd(*args) == 3                 # workspace too small
+    args = list(base); args[12] = None
+    assert lib.attn_cross_fwd(*args) == 1                 # no workspace
+    args = list(base); args[12] = MIS
+    assert lib.attn_cross_fwd(*args) == 1                 # misaligned workspace
+    args = list(base); args[10] = 4097
+    assert lib.attn_cross_fwd(*args) == 1                 # more chunks than keys
+    args = list(base); args[10] = 33; args[13] = 1 << 40
+    assert lib.attn_cross_fwd(*args) == 2                 # more chunks than the tail merges

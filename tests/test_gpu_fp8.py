@@ -36,7 +36,7 @@ def check_gemm(y_gpu, y_ref, y_abs, K, what):
                           f"{float(np.max((np.abs(g - y_ref) - bound)[bad])):.3e}"
 
 
-@pytest.mark.parametrize("M,K", [(1, 16), (7, 144), (300, 4096), (129, 4112), (64, 1024)])
+@pytest.mark.parametrize("M,K", [(1, 16), (7, 144), (300, 4096), (129, 4112), (64, 1024), (33, 2048), (9, 8192), (17, 272)])
 def test_quantize_rows_bit_exact(M, K):
     x, _ = make_linear(LinearWorkload("q", M=M, K=K, N=8, seed=M + K), device="cuda")
     x[min(3, M - 1)] = 0                                      # a zero row

@@ -253,3 +253,26 @@ def test_bounded_wait_reports_timeout_and_context_survives():
     torch.cuda.synchronize()
     ro, _ = oracle.attention(host(q), host(k), host(v), 1 / 8)
     assert_close(host(out), ro, "dense after timeout self-test")
+
+
+# ---------------------------------------------------------------- split-KV with the merge in the tail
+
+@pytest.mark.parametrize("H,Sq,Skv,d,n", [(2, 128, 4096, 128, 8), (2, 300, 4097, 128, 3), (1, 100, 1000, 64, 7),
+                                          (3, 129, 517, 128, 1), (2, 1, 2, 64, 2)])
+def test_cross_fused_merge_matches_two_launch_path_and_oracle(H, Sq, Skv, d, n):
+    q, k, v = rnd_qkv(1, H, Sq, Skv, d, seed=77 + Sq + n)
+    ws = torch.zeros(vd.attn_cross_workspace_bytes(1, H, Sq, d, n), dtype=torch.uint8, device=DEV)
+    out, lse = vd.attn_cross_fwd(q, k, v, n, workspace=ws)
+    op, lp = vd.attn_cross_splitkv_fwd(q, k, v, n)
+    out2, lse2 = vd.attn_lse_merge(op, lp)
+    # the workspace is ready for the next call: a second call gives the same bits
+    out3, lse3 = vd.attn_cross_fwd(q, k, v, n, workspace=ws)
+    torch.cuda.synchronize()
+    assert torch.equal(out, out2) and torch.equal(lse, lse2)
+    assert torch.equal(out, out3) and torch.equal(lse, lse3)
+    tiles = H * ((Sq + 127) // 128)                       # counters: the workspace's last 256-aligned region
+    off = ws.numel() - ((4 * tiles + 255) // 256) * 256
+    assert int(ws[off:off + 4 * tiles].view(torch.int32).abs().sum()) == 0      # counters back at zero
+    ro, rl = oracle.attention(host(q), host(k), host(v), 1 / math.sqrt(d))
+    assert_close(host(out), ro, "fused cross out")
+    assert_close(host(lse), rl, "fused cross lse")

@@ -21,7 +21,8 @@ __all__ = [
     "attn_sparse_workspace_bytes", "attn_sparse_route_fwd", "attn_sparse_route", "attn_sparse_fwd",
     "attn_last_device_status", "attn_status_string", "attn_selftest_wait_timeout",
     "attn_sparse_route_fwd_noalloc", "attn_sparse_fused_fwd", "attn_na3d_fwd", "attn_na3d_plan",
-    "fp8_quantize_rows", "fp8_scaled_gemm", "fp8_linear", "NOALLOC_WORKSPACE_BYTES", "EXPORTED_SYMBOLS",
+    "fp8_quantize_rows", "fp8_scaled_gemm", "fp8_linear", "attn_cross_fwd", "attn_cross_workspace_bytes",
+    "NOALLOC_WORKSPACE_BYTES", "EXPORTED_SYMBOLS",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -33,7 +34,7 @@ EXPORTED_SYMBOLS = (
     "attn_dense_fwd", "attn_cross_splitkv_fwd", "attn_lse_merge", "attn_block_pool", "attn_sparse_workspace_bytes",
     "attn_sparse_route_fwd", "attn_sparse_route", "attn_sparse_fwd", "attn_last_device_status", "attn_status_string",
     "attn_selftest_wait_timeout", "attn_sparse_route_fwd_noalloc", "attn_sparse_fused_fwd", "attn_na3d_fwd",
-    "attn_na3d_plan", "fp8_quantize_rows", "fp8_scaled_gemm",
+    "attn_na3d_plan", "fp8_quantize_rows", "fp8_scaled_gemm", "attn_cross_fwd", "attn_cross_workspace_bytes",
 )
 
 # Size of the library-owned scratch of attn_sparse_route_fwd_noalloc (ATTN_NOALLOC_WORKSPACE_BYTES).
@@ -75,6 +76,9 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         lib.attn_na3d_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, i, f, i, i, vp]
         ip, llp = ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_longlong)
         lib.attn_na3d_plan.argtypes = [i, i, i, i, i, i, ip, ip, llp]
+        lib.attn_cross_workspace_bytes.argtypes = [i, i, i, i, i]
+        lib.attn_cross_workspace_bytes.restype = sz
+        lib.attn_cross_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, vp, sz, vp]
         lib.fp8_quantize_rows.argtypes = [vp, vp, vp, i, i, vp]
         lib.fp8_scaled_gemm.argtypes = [vp, vp, vp, vp, vp, i, i, i, vp]
         lib.attn_last_device_status.argtypes = [vp]
@@ -84,7 +88,7 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         for name in ("attn_dense_fwd", "attn_cross_splitkv_fwd", "attn_lse_merge", "attn_block_pool",
                      "attn_sparse_route_fwd", "attn_sparse_route", "attn_sparse_fwd", "attn_last_device_status",
                      "attn_selftest_wait_timeout", "attn_sparse_route_fwd_noalloc", "attn_sparse_fused_fwd",
-                     "attn_na3d_fwd", "attn_na3d_plan", "fp8_quantize_rows", "fp8_scaled_gemm"):
+                     "attn_na3d_fwd", "attn_na3d_plan", "fp8_quantize_rows", "fp8_scaled_gemm", "attn_cross_fwd"):
             getattr(lib, name).restype = ctypes.c_int
         if path is None:
             _lib = lib
@@ -212,6 +216,30 @@ def attn_cross_splitkv_fwd(q, k, v, n_split, scale=None, out_part=None, lse_part
            lib.attn_cross_splitkv_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out_part), _ptr(lse_part), B, H, Sq, Skv, d,
                                       int(n_split), scale, _stream(stream)))
     return out_part, lse_part
+
+
+def attn_cross_workspace_bytes(B, H, Sq, d, n_split) -> int:
+    return int(load_library().attn_cross_workspace_bytes(B, H, Sq, d, n_split))
+
+
+def attn_cross_fwd(q, k, v, n_split, scale=None, out=None, lse=None, workspace=None, stream=None):
+    """Split-KV attention with the exact merge fused into the split kernel's tail (one launch);
+    returns (out bf16 [B,H,Sq,d], lse fp32 [B,H,Sq]).  ``workspace``: a uint8 device tensor of at
+    least attn_cross_workspace_bytes, zero-filled before its first use (a fresh zeroed one is made
+    when omitted); calls leave it ready for the next call."""
+    lib = load_library()
+    B, H, Sq, d = _bhsd(q, "q")
+    Skv = _bhsd(k, "k")[2]
+    _bhsd(v, "v")
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    need = attn_cross_workspace_bytes(B, H, Sq, d, n_split)
+    workspace = torch.zeros(max(need, 1), dtype=torch.uint8, device=q.device) if workspace is None else workspace
+    out = torch.empty_like(q) if out is None else out
+    lse = torch.empty((B, H, Sq), dtype=torch.float32, device=q.device) if lse is None else lse
+    _check("attn_cross_fwd", lib.attn_cross_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, Sq, Skv, d,
+                                                int(n_split), scale, _ptr(workspace),
+                                                workspace.numel() * workspace.element_size(), _stream(stream)))
+    return out, lse
 
 
 def attn_lse_merge(out_part, lse_part, out=None, lse=None, stream=None):

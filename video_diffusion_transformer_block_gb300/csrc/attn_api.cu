@@ -361,6 +361,46 @@ attn_status_t attn_cross_splitkv_fwd(const attn_bf16* q, const attn_bf16* k, con
   return cuda_status(launch_fwd(d, 128, kModeSplit, tq, tk, tv, p, stream));
 }
 
+size_t attn_cross_workspace_bytes(int B, int H, int Sq, int d, int n_split) {
+  if (!sizes_ok(B, H, Sq) || !valid_d(d) || n_split < 1) return 0;
+  const size_t rows = (size_t)B * H * Sq;
+  const size_t tiles = (size_t)B * H * ((Sq + 127) / 128);
+  return align256((size_t)n_split * rows * d * 4) + align256((size_t)n_split * rows * 4) + align256(tiles * 4);
+}
+
+attn_status_t attn_cross_fwd(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v, attn_bf16* out, float* lse,
+                             int B, int H, int Sq, int Skv, int d, int n_split, float scale, void* workspace,
+                             size_t workspace_bytes, cudaStream_t stream) {
+  if (!q || !k || !v || !out || !workspace) return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(workspace) ||
+      (lse && ((uintptr_t)lse & 3u)))
+    return ATTN_ERR_INVALID_ARG;
+  if (!sizes_ok(B, H, Sq) || !sizes_ok(B, H, Skv) || !(isfinite(scale) && scale > 0.f)) return ATTN_ERR_INVALID_ARG;
+  if (n_split < 1 || n_split > Skv) return ATTN_ERR_INVALID_ARG;
+  if (!valid_d(d)) return ATTN_ERR_UNSUPPORTED;
+  if (n_split > kMergeMaxSplit) return ATTN_ERR_UNSUPPORTED;
+  const size_t need = attn_cross_workspace_bytes(B, H, Sq, d, n_split);
+  if (workspace_bytes < need) return ATTN_ERR_WORKSPACE;
+  int* status = nullptr;
+  attn_status_t st = status_ptr(&status);
+  if (st != ATTN_OK) return st;
+  CUtensorMap tq, tk, tv;
+  if ((st = make_map(&tq, q, d, Sq, B * H, 128)) != ATTN_OK) return st;
+  if ((st = make_map(&tk, k, d, Skv, B * H, 128)) != ATTN_OK) return st;
+  if ((st = make_map(&tv, v, d, Skv, B * H, 128)) != ATTN_OK) return st;
+  const size_t rows = (size_t)B * H * Sq;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  FwdParams p = base_params(B, H, Sq, Skv, scale, kModeSplit, status);
+  p.out_part = reinterpret_cast<float*>(ws);
+  p.lse_part = reinterpret_cast<float*>(ws + align256((size_t)n_split * rows * d * 4));
+  p.merge_count = reinterpret_cast<int*>(ws + align256((size_t)n_split * rows * d * 4) +
+                                         align256((size_t)n_split * rows * 4));
+  p.n_split = n_split;
+  p.out = out;
+  p.lse = lse;
+  return cuda_status(launch_fwd(d, 128, kModeSplit, tq, tk, tv, p, stream));
+}
+
 attn_status_t attn_lse_merge(const float* out_part, const float* lse_part, attn_bf16* out, float* lse, int n_split,
                              int B, int H, int Sq, int d, cudaStream_t stream) {
   if (!out_part || !lse_part || !out) return ATTN_ERR_INVALID_ARG;

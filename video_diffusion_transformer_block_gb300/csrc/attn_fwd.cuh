@@ -54,6 +54,8 @@ __host__ __device__ constexpr int na_brick_x(int m) { return m == kModeNA1x8x16 
 constexpr float kRescaleLog2 = 8.0f;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
+// largest chunk count the split-KV kernel merges in its tail
+constexpr int kMergeMaxSplit = 32;
 
 struct FwdParams {
   int BH;             // B * H
@@ -90,6 +92,10 @@ struct FwdParams {
   int na_nq[3];
   int na_np[3];
   int na_pair_axis;        // 0 = frames, 1 = rows, 2 = columns, 3 = one brick per CTA
+  // split-KV with the merge in the tail (nullable): one arrival counter per
+  // (head, query tile), zero between calls; the last chunk's CTA merges the
+  // partials of its rows into out (bf16) and lse
+  int* merge_count;
 };
 
 // Window start along one axis: centred on p, moved inward at the borders
@@ -273,6 +279,9 @@ struct FwdCfg {
                 "fused routing scratch must fit in the K/V ring");
   static_assert(!kFused || NQT == 2, "fused routing runs on the two-tile CTA");
   static_assert(!kNA || (BK == 128 && kNaT * kNaY * kNaX == 128), "neighbourhood bricks");
+  static_assert(MODE != kModeSplit || NQT == 1, "split-KV CTAs take one query tile (the merge tail assumes it)");
+  static_assert(MODE != kModeSplit || 128 * (kMergeMaxSplit + 1) * 4 <= NSTAGE * kSlotBytes,
+                "the merge weights live in the idle K/V ring");
 };
 
 // Next key tile of a CTA's walk: neighbourhood boxes or the merged lists.
@@ -287,6 +296,139 @@ __device__ __forceinline__ int next_tile(Walk& naw, Merge& merge, uint32_t& flag
 
 __device__ __forceinline__ void named_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// Split-KV tail with the merge fused in (one-tile CTA, run by its 128 softmax
+// threads after they stored this chunk's partials): the partials are made
+// visible device-wide, the (head, query tile) counter counts this chunk, and
+// the CTA of the last chunk to arrive merges every chunk's partials of its
+// 128 rows exactly (L = log sum exp lse_c, o = sum exp(lse_c - L) o_c, the
+// arithmetic of lse_merge_kernel, so the result is bit-identical to the
+// two-launch path) and resets the counter for the next call.  Partials written
+// by other CTAs of this launch are read through L2.  To keep the merge off the
+// latency path, thread r first loads row r's n lse values at once and leaves
+// the weights exp(lse_c - L) in shared memory (`wbuf`, n <= kMergeMaxSplit);
+// then each warp merges four rows at a time with all their chunk loads in
+// flight.
+template <int D>
+__device__ __forceinline__ void split_merge_tail(const FwdParams& p, int bh, int qg, int q_row0, int r,
+                                                 int& merge_last, volatile int& abort_flag, float* wbuf) {
+  __threadfence();
+  named_sync(2, 128);
+  if (r == 0) {
+    int last = 0;
+    if (!abort_flag) {   // an aborted CTA (device timeout, reported in the status word) does not count
+      int* cnt = p.merge_count + ((long long)bh * p.n_qg + qg);
+      const int old = atomicAdd(cnt, 1);
+      last = old == p.n_split - 1;
+      if (last) atomicExch(cnt, 0);
+    }
+    merge_last = last;
+  }
+  named_sync(2, 128);
+  if (!merge_last) return;
+  __threadfence();
+  const int n = p.n_split;
+  const long long rows = (long long)p.BH * p.Sq;
+  constexpr int WS = kMergeMaxSplit + 1;   // wbuf row: n weights, then L
+  // ---- weights of row r
+  {
+    const int grow = q_row0 + r;
+    float ls[kMergeMaxSplit];
+    float M = -INFINITY;
+    if (grow < p.Sq) {
+      const long long row = (long long)bh * p.Sq + grow;
+#pragma unroll
+      for (int c = 0; c < kMergeMaxSplit; ++c) ls[c] = c < n ? __ldcg(p.lse_part + (long long)c * rows + row) : -INFINITY;
+#pragma unroll
+      for (int c = 0; c < kMergeMaxSplit; ++c)
+        if (c < n) M = fmaxf(M, ls[c]);
+    }
+    float L = -INFINITY;
+    if (M != -INFINITY) {
+      float ssum = 0.f;
+#pragma unroll
+      for (int c = 0; c < kMergeMaxSplit; ++c)
+        if (c < n) ssum += expf(ls[c] - M);
+      L = M + logf(ssum);
+#pragma unroll
+      for (int c = 0; c < kMergeMaxSplit; ++c)
+        if (c < n) wbuf[r * WS + c] = expf(ls[c] - L);
+    }
+    wbuf[r * WS + kMergeMaxSplit] = L;
+    if (grow < p.Sq && p.lse != nullptr) p.lse[(long long)bh * p.Sq + grow] = L;
+  }
+  named_sync(2, 128);
+  // ---- outputs: warp w merges rows w + 4 i, four at a time, lanes across d
+  constexpr int PER = D / 32;
+  constexpr int RB = 4;
+  const int lane = r & 31, w = r >> 5;
+  for (int i0 = w; i0 < 128; i0 += 4 * RB) {
+    float o[RB][PER];
+    bool live[RB];
+#pragma unroll
+    for (int b = 0; b < RB; ++b) {
+      const int i = i0 + 4 * b;
+      live[b] = i < 128 && q_row0 + i < p.Sq && wbuf[i * WS + kMergeMaxSplit] != -INFINITY;
+#pragma unroll
+      for (int e = 0; e < PER; ++e) o[b][e] = 0.f;
+    }
+    int c = 0;
+    for (; c + 1 < n; c += 2) {
+      float a0[RB][PER], a1[RB][PER];
+#pragma unroll
+      for (int b = 0; b < RB; ++b) {
+        if (!live[b]) continue;
+        const long long row = (long long)bh * p.Sq + q_row0 + i0 + 4 * b;
+        const float* s0 = p.out_part + ((long long)c * rows + row) * D + lane * PER;
+        const float* s1 = s0 + rows * D;
+        if constexpr (PER == 4) {
+          const float4 v0 = __ldcg(reinterpret_cast<const float4*>(s0));
+          const float4 v1 = __ldcg(reinterpret_cast<const float4*>(s1));
+          a0[b][0] = v0.x; a0[b][1] = v0.y; a0[b][2] = v0.z; a0[b][3] = v0.w;
+          a1[b][0] = v1.x; a1[b][1] = v1.y; a1[b][2] = v1.z; a1[b][3] = v1.w;
+        } else {
+          const float2 v0 = __ldcg(reinterpret_cast<const float2*>(s0));
+          const float2 v1 = __ldcg(reinterpret_cast<const float2*>(s1));
+          a0[b][0] = v0.x; a0[b][1] = v0.y;
+          a1[b][0] = v1.x; a1[b][1] = v1.y;
+        }
+      }
+#pragma unroll
+      for (int b = 0; b < RB; ++b) {
+        if (!live[b]) continue;
+        const float* wr = wbuf + (i0 + 4 * b) * WS;
+        const float w0 = wr[c], w1 = wr[c + 1];
+#pragma unroll
+        for (int e = 0; e < PER; ++e) o[b][e] = fmaf(w1, a1[b][e], fmaf(w0, a0[b][e], o[b][e]));
+      }
+    }
+    if (c < n) {
+#pragma unroll
+      for (int b = 0; b < RB; ++b) {
+        if (!live[b]) continue;
+        const long long row = (long long)bh * p.Sq + q_row0 + i0 + 4 * b;
+        const float* s0 = p.out_part + ((long long)c * rows + row) * D + lane * PER;
+        const float w0 = wbuf[(i0 + 4 * b) * WS + c];
+#pragma unroll
+        for (int e = 0; e < PER; ++e) o[b][e] = fmaf(w0, __ldcg(s0 + e), o[b][e]);
+      }
+    }
+#pragma unroll
+    for (int b = 0; b < RB; ++b) {
+      const int i = i0 + 4 * b;
+      if (i >= 128 || q_row0 + i >= p.Sq) continue;
+      uint16_t* dst = p.out + ((long long)bh * p.Sq + q_row0 + i) * D + lane * PER;
+      if constexpr (PER == 4) {
+        uint2 pk;
+        pk.x = pack_bf16x2(o[b][0], o[b][1]);
+        pk.y = pack_bf16x2(o[b][2], o[b][3]);
+        *reinterpret_cast<uint2*>(dst) = pk;
+      } else {
+        *reinterpret_cast<uint32_t*>(dst) = pack_bf16x2(o[b][0], o[b][1]);
+      }
+    }
+  }
 }
 
 // Sol-Attn routing of the CTA's R query blocks, computed on chip by the TH
@@ -471,6 +613,7 @@ __global__ void __launch_bounds__(NQT * 128 + 128, (NQT == 1) ? 2 : 1)
   __shared__ uint64_t bar_mma_done, bar_drain, bar_route;
   __shared__ uint32_t tmem_base_sh;
   __shared__ volatile int abort_flag;
+  __shared__ int merge_last;
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
@@ -969,6 +1112,11 @@ __global__ void __launch_bounds__(NQT * 128 + 128, (NQT == 1) ? 2 : 1)
         if (row_valid && p.lse != nullptr)
           p.lse[(long long)bh * p.Sq + grow] = empty ? -INFINITY : (m_run + __log2f(l_run)) * kLn2;
       }
+    }
+    // reached by all 128 softmax threads whatever happened above (its barriers have no time limit)
+    if constexpr (MODE == kModeSplit) {
+      if (p.merge_count != nullptr)
+        split_merge_tail<D>(p, bh, qg, q_row0, r, merge_last, abort_flag, reinterpret_cast<float*>(sKV));
     }
   }
 
