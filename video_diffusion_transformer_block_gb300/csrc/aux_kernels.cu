@@ -448,14 +448,107 @@ __global__ void __launch_bounds__(256) lse_merge_kernel(const float* __restrict_
   if (lse != nullptr && lane == 0) lse[row] = L;
 }
 
+// Same merge with every load of a row issued before any arithmetic (rows with
+// n <= NMAX partials): the n lse values (one broadcast load each) and the
+// n slices of the partial outputs go into registers at once, so a row costs one
+// memory round trip instead of three dependent ones.  The arithmetic and its
+// order are those of lse_merge_kernel, so the results are bit-identical.
+template <int D, int NMAX>
+__global__ void __launch_bounds__(256) lse_merge_reg_kernel(const float* __restrict__ o_part,
+                                                            const float* __restrict__ lse_part,
+                                                            uint16_t* __restrict__ out, float* __restrict__ lse, int n,
+                                                            long long rows) {
+  constexpr int PER = D / 32;
+  // programmatic dependent launch: let the next kernel in the stream start its
+  // launch now, and wait until the kernel before this one (which may have
+  // produced the partials) has completed and its writes are visible
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= rows) return;
+  float ls[NMAX];
+  float a[NMAX][PER];
+#pragma unroll
+  for (int c = 0; c < NMAX; ++c) {
+    if (c < n) {
+      ls[c] = __ldg(lse_part + (long long)c * rows + row);
+      const float* src = o_part + ((long long)c * rows + row) * D + lane * PER;
+      if constexpr (PER == 4) {
+        const float4 v = __ldcs(reinterpret_cast<const float4*>(src));
+        a[c][0] = v.x; a[c][1] = v.y; a[c][2] = v.z; a[c][3] = v.w;
+      } else {
+        const float2 v = __ldcs(reinterpret_cast<const float2*>(src));
+        a[c][0] = v.x; a[c][1] = v.y;
+      }
+    }
+  }
+  float M = -INFINITY;
+#pragma unroll
+  for (int c = 0; c < NMAX; ++c)
+    if (c < n) M = fmaxf(M, ls[c]);
+  float o[PER];
+#pragma unroll
+  for (int e = 0; e < PER; ++e) o[e] = 0.f;
+  float L = -INFINITY;
+  if (M != -INFINITY) {
+    float ssum = 0.f;
+#pragma unroll
+    for (int c = 0; c < NMAX; ++c)
+      if (c < n) ssum += expf(ls[c] - M);
+    L = M + logf(ssum);
+#pragma unroll
+    for (int c = 0; c + 1 < NMAX; c += 2) {
+      if (c + 1 < n) {
+        const float w0 = expf(ls[c] - L);
+        const float w1 = expf(ls[c + 1] - L);
+#pragma unroll
+        for (int e = 0; e < PER; ++e) o[e] = fmaf(w1, a[c + 1][e], fmaf(w0, a[c][e], o[e]));
+      } else if (c < n) {   // odd n: the last partial alone
+        const float w0 = expf(ls[c] - L);
+#pragma unroll
+        for (int e = 0; e < PER; ++e) o[e] = fmaf(w0, a[c][e], o[e]);
+      }
+    }
+  }
+  uint16_t* dst = out + row * D + lane * PER;
+  if constexpr (PER == 4) {
+    uint2 pk;
+    pk.x = pack_bf16x2(o[0], o[1]);
+    pk.y = pack_bf16x2(o[2], o[3]);
+    *reinterpret_cast<uint2*>(dst) = pk;
+  } else {
+    *reinterpret_cast<uint32_t*>(dst) = pack_bf16x2(o[0], o[1]);
+  }
+  if (lse != nullptr && lane == 0) lse[row] = L;
+}
+
 cudaError_t launch_merge(const float* o_part, const float* lse_part, uint16_t* out, float* lse, int n, long long rows,
                          int D, cudaStream_t stream) {
   long long grid = (rows + 7) / 8;
   if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  if (D == 128)
-    lse_merge_kernel<128><<<(unsigned)grid, 256, 0, stream>>>(o_part, lse_part, out, lse, n, rows);
-  else
-    lse_merge_kernel<64><<<(unsigned)grid, 256, 0, stream>>>(o_part, lse_part, out, lse, n, rows);
+  const unsigned g = (unsigned)grid;
+  // the register kernels are launched with programmatic stream serialisation
+  // (they wait for their predecessor themselves, see griddepcontrol above)
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(g);
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (D == 128) {
+    if (n <= 8) return cudaLaunchKernelEx(&cfg, lse_merge_reg_kernel<128, 8>, o_part, lse_part, out, lse, n, rows);
+    if (n <= 16) return cudaLaunchKernelEx(&cfg, lse_merge_reg_kernel<128, 16>, o_part, lse_part, out, lse, n, rows);
+    lse_merge_kernel<128><<<g, 256, 0, stream>>>(o_part, lse_part, out, lse, n, rows);
+  } else {
+    if (n <= 8) return cudaLaunchKernelEx(&cfg, lse_merge_reg_kernel<64, 8>, o_part, lse_part, out, lse, n, rows);
+    if (n <= 16) return cudaLaunchKernelEx(&cfg, lse_merge_reg_kernel<64, 16>, o_part, lse_part, out, lse, n, rows);
+    lse_merge_kernel<64><<<g, 256, 0, stream>>>(o_part, lse_part, out, lse, n, rows);
+  }
   return cudaGetLastError();
 }
 
