@@ -969,11 +969,12 @@ __global__ void __launch_bounds__(NQT * 128 + 128, (NQT == 1) ? 2 : 1)
         for (int c = 0; c < BK; ++c)
           if (!mine || c >= n_valid) x[c] = -INFINITY;
       }
-      float mx0 = x[0], mx1 = x[1];
+      // row max: two chains of three-input maxima (max is exact, so the order is free)
+      float mx0 = fmaxf(x[0], x[1]), mx1 = fmaxf(x[2], x[3]);
 #pragma unroll
-      for (int c = 2; c < BK; c += 2) {
-        mx0 = fmaxf(mx0, x[c]);
-        mx1 = fmaxf(mx1, x[c + 1]);
+      for (int c = 4; c < BK; c += 4) {
+        mx0 = fmax3(mx0, x[c], x[c + 1]);
+        mx1 = fmax3(mx1, x[c + 2], x[c + 3]);
       }
       const float mt = fmaxf(mx0, mx1) * p.scale_log2;
       // lazy rescale of the running max
@@ -996,26 +997,34 @@ __global__ void __launch_bounds__(NQT * 128 + 128, (NQT == 1) ? 2 : 1)
           tmem_ld_wait();
           tmem_reg_fence(rr);
 #pragma unroll
-          for (int j = 0; j < 32; ++j) rr[j] = __float_as_uint(__uint_as_float(rr[j]) * a);
+          for (int j = 0; j < 32; j += 2) {
+            const float2 v = __fmul2_rn(make_float2(__uint_as_float(rr[j]), __uint_as_float(rr[j + 1])),
+                                        make_float2(a, a));
+            rr[j] = __float_as_uint(v.x);
+            rr[j + 1] = __float_as_uint(v.y);
+          }
           tmem_st32(tO + c0, rr);
         }
       }
       const float nbase = (m_run == -INFINITY) ? 0.f : -m_run;
-      float ls0 = 0.f, ls1 = 0.f;
+      // pairs of columns through the packed fp32 pipe: the same fused multiply-add
+      // and the same two (even / odd) row-sum chains as scalar code, half the instructions
+      const float2 sc2 = make_float2(p.scale_log2, p.scale_log2), nb2 = make_float2(nbase, nbase);
+      float2 ls = make_float2(0.f, 0.f);
 #pragma unroll
       for (int c0 = 0; c0 < BK; c0 += 64) {
         uint32_t pk[32];
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
-          float p0 = ex2_approx(fmaf(x[c0 + 2 * j], p.scale_log2, nbase));
-          float p1 = ex2_approx(fmaf(x[c0 + 2 * j + 1], p.scale_log2, nbase));
-          ls0 += p0;
-          ls1 += p1;
+          const float2 arg = __ffma2_rn(make_float2(x[c0 + 2 * j], x[c0 + 2 * j + 1]), sc2, nb2);
+          const float p0 = ex2_approx(arg.x);
+          const float p1 = ex2_approx(arg.y);
+          ls = __fadd2_rn(ls, make_float2(p0, p1));
           pk[j] = pack_bf16x2(p0, p1);
         }
         tmem_st32(tS + c0 / 2, pk);
       }
-      l_run += ls0 + ls1;
+      l_run += ls.x + ls.y;
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(&bar_p[t]);

@@ -183,6 +183,13 @@ __device__ __forceinline__ void setmaxnreg_dec() {
 }
 
 // ---------------------------------------------------------------- math helpers
+// max of three floats in one instruction (sm_100 family)
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
 __device__ __forceinline__ float ex2_approx(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
