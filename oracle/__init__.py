@@ -10,8 +10,8 @@ and the sources they follow.
 Parity status: dense attention, split-KV partials, the LSE merge, pooling,
 proxy scores, mu/sigma/tau and the selection are pinned by closed forms,
 library routines and invariants in ``tests/test_oracle_pins.py``.  The Taylor
-aggregates (W, T) and the Taylor-corrected sparse output follow this build's
-reading of the Sol-Attn page (first order about the row-mean proxy score,
+aggregates (W, T) and the Taylor-corrected sparse output follow a reading
+of the Sol-Attn page (first order about the row-mean proxy score,
 applied per block with pooled V); they are pinned only against a
 hand-derived closed form of that reading: parity unpinned with respect to the
 pages.  3D neighbourhood attention follows the published definition of

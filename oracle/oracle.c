@@ -50,7 +50,7 @@
  *    and numpy's matmul of the decoded operands.
  *  - oracle_route (Taylor aggregates W, T) and oracle_sparse_rows: the pages
  *    give no formula for the Taylor term.  The first-order block-level form
- *    used here is this build's reading; it is pinned by a hand-derived closed
+ *    used here is a reading of the page; it is pinned by a hand-derived closed
  *    form and by invariants of that reading, so its agreement with the
  *    pages' (unprinted) formula is "parity unpinned".
  */
