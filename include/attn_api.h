@@ -66,7 +66,7 @@ typedef enum {
  * Requires B, H, Sq, Skv >= 1, d in {64, 128}, scale finite and > 0.
  * Source: "Accelerating LTX-2.5 with Sol Engine", section "Stage 2
  * Optimization" (attention over long video sequences dominates Stage 2);
- * "LTX-2.5 Optimization" (openltx.com), attention-backend paragraph.
+ * "Optimization" (openltx.com, hardware benchmarks), attention-backend paragraph.
  */
 attn_status_t attn_dense_fwd(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v, attn_bf16* out, float* lse,
                              int B, int H, int Sq, int Skv, int d, float scale, cudaStream_t stream);
