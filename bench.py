@@ -201,19 +201,30 @@ def run_native(args, world, rank, local):
     oa = torch.empty((B, H, CROSS_SQ, d), dtype=torch.bfloat16, device=dev)
     la = torch.empty((B, H, CROSS_SQ), dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream()
+    # the audio->video cross attention needs none of the self-attention's results: it runs on a
+    # second stream, beside pool/route (HBM- and shared-memory-bound) and the sparse forward
+    xstream = stream if args.serial_cross else torch.cuda.Stream()
     kernels_per_step = 5  # pool, route, sparse forward, split-KV forward, merge
 
-    def step(ev=None):
-        if ev is not None:
-            ev[0].record(stream)
+    def step(ev=None, xev=None):
+        start = ev[0] if ev is not None else torch.cuda.Event()
+        start.record(stream)
+        if xstream is not stream:
+            xstream.wait_event(start)
+        with torch.cuda.stream(xstream):
+            if xev is not None:
+                xev[0].record(xstream)
+            vd.attn_cross_splitkv_fwd(qa, kx, vx, CROSS_N_SPLIT, out_part=op, lse_part=lp, stream=xstream)
+            vd.attn_lse_merge(op, lp, out=oa, lse=la, stream=xstream)
+            xdone = xev[1] if xev is not None else torch.cuda.Event()
+            xdone.record(xstream)
         vd.attn_sparse_route(q, k, v, args.beta, block=block, route=rt, workspace=ws)
         if ev is not None:
             ev[1].record(stream)
         vd.attn_sparse_fwd(q, k, v, rt, block=block, out=out, lse=lse)
         if ev is not None:
             ev[2].record(stream)
-        vd.attn_cross_splitkv_fwd(qa, kx, vx, CROSS_N_SPLIT, out_part=op, lse_part=lp)
-        vd.attn_lse_merge(op, lp, out=oa, lse=la)
+        stream.wait_event(xdone)
         if ev is not None:
             ev[3].record(stream)
 
@@ -229,11 +240,12 @@ def run_native(args, world, rank, local):
     density = sparse_flops / dense_eq
 
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    xevs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
     barrier(world)
     torch.cuda.synchronize()
     with ClockSampler(local) as clocks:
         for i in range(args.steps):
-            step(evs[i])
+            step(evs[i], xevs[i])
         torch.cuda.synchronize()
     barrier(world)
     status = vd.attn_last_device_status()
@@ -242,7 +254,7 @@ def run_native(args, world, rank, local):
     total_ms = evs[0][0].elapsed_time(evs[-1][3])
     route_ms = sum(e[0].elapsed_time(e[1]) for e in evs) / args.steps
     fwd_ms = sum(e[1].elapsed_time(e[2]) for e in evs) / args.steps
-    cross_ms = sum(e[2].elapsed_time(e[3]) for e in evs) / args.steps
+    cross_ms = sum(e[0].elapsed_time(e[1]) for e in xevs) / args.steps
     total_ms = max_over_ranks(total_ms, world)
     ms_per_step = total_ms / args.steps
     step_flops = sparse_flops + cross_flops
@@ -267,6 +279,9 @@ def run_native(args, world, rank, local):
         "pct_bf16_peak_executed": round(100 * value / world / peak_sus, 2),
         "breakdown_ms": {"pool_route": round(route_ms, 4), "sparse_fwd": round(fwd_ms, 4),
                          "cross_splitkv_merge": round(cross_ms, 4)},
+        "schedule": ("one stream" if args.serial_cross else
+                     "cross attention on a second stream, concurrent with pool/route and the sparse forward "
+                     "(breakdown times overlap)"),
         "roofline": {"bound": "tensor", "kernel": "attn_fwd_kernel (sparse, d=128, block 128)",
                      "achieved": round(fwd_tflops, 2), "peak": peak_sus, "unit": "TFLOP/s",
                      "frac": round(fwd_tflops / peak_sus, 4), "frac_of_burst_peak": round(fwd_tflops / peak_burst, 4),
@@ -540,6 +555,7 @@ def run_e2e(args, vd, w, qkv, cross, rt, ws, step_flops, world):
     h2d = sum(t.numel() * t.element_size() for t in hin)
     d2h = sum(t.numel() * t.element_size() for t in hout)
     comp = torch.cuda.current_stream()
+    xcomp = comp if args.serial_cross else torch.cuda.Stream()   # the cross attention, as in the device-timed step
     upload, download = torch.cuda.Stream(), torch.cuda.Stream()
 
     def run(steps):
@@ -552,13 +568,17 @@ def run_e2e(args, vd, w, qkv, cross, rt, ws, step_flops, world):
             up[0].record(upload)
         for i in range(steps):
             buf, ob = din[i % 2], dout[i % 2]
-            comp.wait_event(up[i])
-            if i >= 2:
-                comp.wait_event(down[i - 2])              # this output buffer has been read back
+            for st in {comp, xcomp}:
+                st.wait_event(up[i])
+                if i >= 2:
+                    st.wait_event(down[i - 2])            # this output buffer has been read back
+            vd.attn_cross_splitkv_fwd(buf[3], buf[4], buf[5], CROSS_N_SPLIT, out_part=op, lse_part=lp, stream=xcomp)
+            vd.attn_lse_merge(op, lp, out=ob[2], lse=ob[3], stream=xcomp)
+            xdone = torch.cuda.Event()
+            xdone.record(xcomp)
             vd.attn_sparse_route(buf[0], buf[1], buf[2], args.beta, block=block, route=rt, workspace=ws, stream=comp)
             vd.attn_sparse_fwd(buf[0], buf[1], buf[2], rt, block=block, out=ob[0], lse=ob[1], stream=comp)
-            vd.attn_cross_splitkv_fwd(buf[3], buf[4], buf[5], CROSS_N_SPLIT, out_part=op, lse_part=lp, stream=comp)
-            vd.attn_lse_merge(op, lp, out=ob[2], lse=ob[3], stream=comp)
+            comp.wait_event(xdone)
             done[i].record(comp)
             if i + 1 < steps:
                 with torch.cuda.stream(upload):
@@ -590,7 +610,7 @@ def run_e2e(args, vd, w, qkv, cross, rt, ws, step_flops, world):
     return {"value": round(world * step_flops / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s", "ms_per_step": round(ms, 4),
             "steps": steps, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
             "pipelining": "double-buffered: uploads and downloads on two copy streams overlap each other and the "
-                          "previous/next step's compute"}
+                          "previous/next step's compute; the cross attention on its own compute stream"}
 
 
 # ============================================================ oracle (CPU baseline / reference arm)
@@ -686,6 +706,8 @@ def main():
     ap.add_argument("--tokens", type=int, default=None,
                     help="fp8_proj only: activation rows (default 65664; fewer only for profiling)")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--serial-cross", action="store_true",
+                    help="run the cross attention after the self-attention on one stream (no overlap)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     args = ap.parse_args()
