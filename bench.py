@@ -633,24 +633,34 @@ def oracle_sample(qh, kh, vh, w, n_rows, rng):
     return dt, flops
 
 
-def host_head0(q, k, v):
-    return [to_f64(x[:, :1].contiguous()) for x in (q, k, v)]
+def host_head(q, k, v, h=0):
+    return [to_f64(x[:, h:h + 1].contiguous()) for x in (q, k, v)]
 
 
 def cpu_baseline(q, k, v, w, budget_s=15.0):
+    """The oracle on the host cores over heads 0, 1, ... of the same inputs until about budget_s
+    seconds of work: each head's pool + route, then its block-sparse attention on sampled rows
+    (all rows while the budget lasts)."""
     import oracle
     oracle.build()
-    qh, kh, vh = host_head0(q, k, v)
     rng = np.random.default_rng(0)
+    qh, kh, vh = host_head(q, k, v, 0)
     dt0, _ = oracle_sample(qh, kh, vh, w, 64, rng)                     # calibration
     per_row = max(dt0 / 64, 1e-6)
-    n_rows = int(min(w.Sq, max(256, budget_s / per_row)))
-    dt, flops = oracle_sample(qh, kh, vh, w, n_rows, rng)
+    dt = flops = 0.0
+    heads, rows_done = 0, 0
+    while heads < w.H and (heads == 0 or dt < budget_s * 0.8):
+        if heads > 0:
+            qh, kh, vh = host_head(q, k, v, heads)
+        n_rows = int(min(w.Sq, max(256, (budget_s - dt) / per_row)))
+        t, f = oracle_sample(qh, kh, vh, w, n_rows, rng)
+        dt, flops, heads, rows_done = dt + t, flops + f, heads + 1, rows_done + n_rows
     cores = len(os.sched_getaffinity(0))
     return {"value": round(flops / dt / 1e12, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
             "seconds": round(dt, 3),
-            "sample": f"head 0 of the sparse64k workload: block pool + route of the head and block-sparse attention "
-                      f"of {n_rows} seeded sampled query rows (fp64 C oracle, OpenMP on {cores} threads)"}
+            "sample": f"heads 0-{heads - 1} of the sparse64k workload: per head, block pool + route and block-sparse "
+                      f"attention of seeded sampled query rows ({rows_done} rows in all; fp64 C oracle, OpenMP on "
+                      f"{cores} threads)"}
 
 
 def run_reference(args, world, rank):
