@@ -276,3 +276,34 @@ def test_cross_fused_merge_matches_two_launch_path_and_oracle(H, Sq, Skv, d, n):
     ro, rl = oracle.attention(host(q), host(k), host(v), 1 / math.sqrt(d))
     assert_close(host(out), ro, "fused cross out")
     assert_close(host(lse), rl, "fused cross lse")
+
+
+# ---------------------------------------------------------------- degenerate routing cases
+
+@pytest.mark.parametrize("fn", [None, "fused"])
+def test_sparse_identical_pooled_keys_select_everything(fn):
+    # every key block holds the same rows, so all pooled keys are equal: sigma = 0, tau = mu, and
+    # every proxy ties with tau and is selected; the result is dense attention
+    B, H, S, d, block = 1, 2, 1024, 128, 128
+    q, k, v = rnd_qkv(B, H, S, S, d, seed=61)
+    k = k[:, :, :block].repeat(1, 1, S // block, 1).contiguous()
+    f = vd.attn_sparse_fused_fwd if fn == "fused" else None
+    # an exact tie: the GPU's fp32 Welford mean of identical proxies is exact (sigma = 0, all selected),
+    # while the fp64 oracle's two-pass mean may round by an ulp and put tau a hair above them; such
+    # flips lie inside the 1e-4 band that sparse_check accepts
+    flips, density, _ = sparse_check(q, k, v, block, 1.5, fn=f)
+    if fn == "fused":
+        return   # the prologue's two-pass fp32 mean can round the tie too (checked against the band above)
+    assert density == 1.0
+    out, lse, _ = vd.attn_sparse_route_fwd(q, k, v, 1.5, block=block, route=True)
+    dense, dlse = vd.attn_dense_fwd(q, k, v)
+    torch.cuda.synchronize()
+    assert_close(host(out), host(dense), "identical keys vs dense (GPU)")
+
+
+@pytest.mark.parametrize("S,block", [(100, 128), (64, 64), (1, 64)])
+def test_sparse_shorter_than_one_block(S, block):
+    # one query block and one key block: the argmax keeps it, there is nothing to reject
+    q, k, v = rnd_qkv(1, 2, S, S, 64, seed=62 + S)
+    flips, density, _ = sparse_check(q, k, v, block, 2.0)
+    assert flips == 0 and density == 1.0
