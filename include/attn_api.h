@@ -72,8 +72,8 @@ attn_status_t attn_dense_fwd(const attn_bf16* q, const attn_bf16* k, const attn_
                              int B, int H, int Sq, int Skv, int d, float scale, cudaStream_t stream);
 
 /*
- * Split-KV partial answers for few-query cross attention (about a hundred
- * audio queries against tens of thousands of video keys).  Chunk c of
+ * Split-KV partial answers for few-query cross attention (on the order of a
+ * hundred audio queries over 10^4 - 10^5 video keys).  Chunk c of
  * n_split covers keys [floor(c*Skv/n_split), floor((c+1)*Skv/n_split)):
  * balanced bounds, nothing padded.  For each chunk and query row the kernel
  * writes the chunk-normalised output and the chunk's log-sum-exp:
@@ -81,8 +81,9 @@ attn_status_t attn_dense_fwd(const attn_bf16* q, const attn_bf16* k, const attn_
  * An empty chunk (possible only when n_split > Skv, which is rejected) would
  * be o = 0, lse = -inf.  Requires 1 <= n_split <= Skv.
  * Source: "LTX-2.5 at 4K, in half the time", section "Attention across two
- * GPUs" (each partial answer carries its running maximum and sum of
- * exponentials; the kernel splits the work along the keys).
+ * GPUs" (answers computed over separate slices of the keys keep, per row, the
+ * maximum and the exponential sum that make combining them exact; this kernel
+ * cuts the keys into such slices on one GPU).
  */
 attn_status_t attn_cross_splitkv_fwd(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v, float* out_part,
                                      float* lse_part, int B, int H, int Sq, int Skv, int d, int n_split, float scale,

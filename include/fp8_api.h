@@ -3,9 +3,9 @@
  * FP8 matrix product of the transformer block's linear layers.
  *
  * Source: "LTX-2.5 at 4K, in half the time" (doubleai.com), section "Thinner
- * seams": the weights stay in FP8, the activations are converted to FP8 with a
- * separate scale for each row, and the products accumulate in FP32 so the
- * tensor cores run at their FP8 rate.  "Optimization Tips" (LTX-2 pipelines
+ * seams": weights are kept in FP8 instead of being widened to BF16 before
+ * each product, activations are quantised to FP8 at run time with one scale
+ * per row, and the tensor cores accumulate in FP32 at FP8 throughput.  "Optimization Tips" (LTX-2 pipelines
  * documentation), section "FP8 Quantization": FP8 scaled matrix
  * multiplication.
  *

@@ -15,14 +15,15 @@
  *
  * Sources (page title, section):
  *  - "LTX-2.5 at 4K, in half the time" (doubleai.com), section "Attention
- *    across two GPUs": each partial answer over a slice of the keys carries
- *    its running maximum and sum of exponentials, and partial answers are
- *    merged exactly; the padded key is dropped rather than masked.
+ *    across two GPUs": answers computed over separate slices of the keys
+ *    keep their row maximum and exponential sum, which makes combining them
+ *    exact; an odd key count is handled by leaving the padding key out rather
+ *    than masking it.
  *  - "Accelerating LTX-2.5 with Sol Engine" (nvlabs.github.io), section
  *    "Stage 2 Optimization - Core Technology: Sol-Attn": per-row threshold
  *    tau_i = mu_i + beta*sigma_i over block proxy-score statistics, pooled
- *    keys, and a Taylor expansion around the row-wise mean score for rejected
- *    blocks.
+ *    keys, and rejected blocks approximated to first order about the mean
+ *    proxy score of their query block.
  *  - "LTX-2.5 at 4K, in half the time", section "Inside the decoder", and
  *    "Optimization Tips" (LTX-2 pipelines documentation), section "Diffusion
  *    VAE Decoder": the video decoder spends most of its time in a
