@@ -1,15 +1,24 @@
 // tcgen05 attention forward for sm_103a: dense, block-sparse (selected-block
 // lists + Taylor term) and split-KV (chunk partials) share one main loop.
 //
-// CTA = NQT query tiles of 128 rows that share every K/V tile load.  Dense,
-// sparse, split and (by default) neighbourhood launches use NQT = 1 with two
-// CTAs per SM; the two-tile CTA serves the fused routing and the paired
-// neighbourhood plans.
+// CTA = NQT query tiles of 128 rows.  Three layouts:
+//  - two-issuer CTA (dense and sparse, NQT = 2, one CTA per SM): the two tiles
+//    run like two one-tile CTAs, each with its own list walk, its own half of
+//    the K/V ring, its own TMA producer warp and MMA-issuing warp; the issuers
+//    take a shared-memory lock around each step's MMA batch.  Two one-tile
+//    CTAs on an SM were measured to fall into step with each other (both
+//    issuing MMAs, then both in softmax, with the tensor pipe idle); the lock
+//    makes one tile's batch run while the other tile's softmax does.
+//  - one-tile CTA (split-KV and one-brick neighbourhood plans, two per SM).
+//  - shared-walk two-tile CTA (fused routing, paired neighbourhood plans):
+//    one producer and one issuer walk the union of the tiles' lists and every
+//    K/V load serves both tiles.
 //   warps 0..4*NQT-1 : softmax/epilogue, one warpgroup per query tile; thread
 //                      r of the warpgroup owns query row r = TMEM lane r
 //   warp  4*NQT      : TMA producer (Q once, then K_s, V_s for every step s
 //                      into a ring of NSTAGE slots)
 //   warp  4*NQT+1    : tcgen05 MMA issuer (one thread); allocates TMEM
+//   (two-issuer CTA: warps 8, 9 are tile 0's producer and issuer, 10, 11 tile 1's)
 // TMEM, per query tile t: S_t at columns [256t, 256t+BK) in fp32; P_t (bf16
 // pairs) overwrites the first BK/2 columns of S_t; O_t at [256t+128, +D).
 // Per step s: S_t = Q_t K_s^T (SS MMA, both K-major, 128B swizzle), softmax
@@ -236,6 +245,13 @@ struct FwdCfg {
   static constexpr bool kSparseLike = MODE == kModeSparse || MODE == kModeSparseFused;
   static constexpr bool kFused = MODE == kModeSparseFused;
   static constexpr bool kNA = is_na_mode(MODE);
+  // two independent query tiles per CTA (dense / sparse with NQT = 2): each
+  // tile has its own list walk, its own half of the K/V ring, its own TMA
+  // producer warp and its own MMA-issuing warp, like two one-tile CTAs; the
+  // two issuers take a shared-memory lock around each step's MMA batch
+  // (PV of the previous key tile, S of the current one)
+  static constexpr bool kDual = NQT == 2 && (MODE == kModeDense || MODE == kModeSparse);
+  static constexpr int kSPT = kDual ? NSTAGE / 2 : NSTAGE;   // ring slots per tile walk
   static constexpr int kNaT = na_brick_t(MODE), kNaY = na_brick_y(MODE), kNaX = na_brick_x(MODE);
   static constexpr int QB = kSparseLike ? 128 / BK : 1;   // query blocks per 128-row tile
   // fused routing: query blocks per CTA, key-block capacity, staging chunk
@@ -250,6 +266,7 @@ struct FwdCfg {
   static constexpr int kThreads = NQT * 128 + 128;
   static constexpr int kProducerWarp = NQT * 4;
   static constexpr int kMmaWarp = NQT * 4 + 1;
+  // (two independent tiles: tile t's producer is warp kProducerWarp + 2t, its MMA issuer the next warp)
   // Registers per thread: at launch (65536 / (threads * CTAs per SM), rounded
   // down to 8), for the control warpgroup after setmaxnreg.dec, and for the
   // softmax warpgroups after setmaxnreg.inc.  The split must add up to the
@@ -275,6 +292,7 @@ struct FwdCfg {
   static_assert(NQT == 1 || NQT == 2, "query tiles per CTA");
   static_assert(NQT * QB <= 4, "lists per CTA");
   static_assert(NSTAGE >= 2, "ring depth");
+  static_assert(!kDual || (NSTAGE % 2 == 0 && NSTAGE >= 4), "two rings of two or more slots");
   static_assert(!kFused || kFusedCH * D * 4 + kFusedR * kFusedMaxNKB * 4 + kFusedR * D * 4 <= NSTAGE * kSlotBytes,
                 "fused routing scratch must fit in the K/V ring");
   static_assert(!kFused || NQT == 2, "fused routing runs on the two-tile CTA");
@@ -293,6 +311,67 @@ __device__ __forceinline__ int next_tile(Walk& naw, Merge& merge, uint32_t& flag
     return merge.next(flags);
   }
 }
+
+// The lists of query tile `qtile` (independent tiles): the selected lists of
+// its QB query blocks (sparse), or the implicit range of all key tiles (dense;
+// empty for a tile past the end of the sequence).
+template <int QB, bool SPARSE>
+__device__ __forceinline__ void tile_walk_init(TileMerge<QB>& w, const FwdParams& p, int bh, int qtile, bool valid,
+                                               int n_kv_tiles) {
+  w.status = p.status;
+  w.smem_lists = false;
+#pragma unroll
+  for (int l = 0; l < QB; ++l) {
+    w.sptr[l] = nullptr;
+    w.pos[l] = 0;
+    w.n[l] = 0;
+    w.ptr[l] = p.sel_idx;
+  }
+  if constexpr (SPARSE) {
+    w.implicit = false;
+    w.nlists = QB;
+    w.limit = p.NKB;
+#pragma unroll
+    for (int l = 0; l < QB; ++l) {
+      const long long i = (long long)qtile * QB + l;
+      if (valid && i < p.NQB) {
+        const long long row = (long long)bh * p.NQB + i;
+        const int c = __ldg(p.sel_cnt + row);
+        w.n[l] = c < 0 ? 0 : (c > p.NKB ? p.NKB : c);
+        w.ptr[l] = p.sel_idx + row * p.NKB;
+      }
+    }
+  } else {
+    w.implicit = true;
+    w.nlists = 1;
+    w.limit = n_kv_tiles;
+    w.n[0] = valid ? n_kv_tiles : 0;
+  }
+}
+
+// Next key tile of a softmax warpgroup: its own tile's walk (independent tiles) or the CTA's walk.
+template <bool DUAL, bool NA, class Own, class Walk, class Merge>
+__device__ __forceinline__ int next_step(Own& own, Walk& naw, Merge& merge, uint32_t& flags, int (&box)[3]) {
+  if constexpr (DUAL) {
+    return own.next(flags);
+  } else {
+    return next_tile<NA>(naw, merge, flags, box);
+  }
+}
+
+// Spin lock in shared memory with a time limit: on timeout the caller goes on
+// without it (the lock only orders MMA issue between the CTA's two tiles; no
+// result depends on it).
+__device__ __forceinline__ bool issue_lock(int* lock, volatile int* abort_flag) {
+  if (atomicCAS(lock, 0, 1) == 0) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (true) {
+    for (int i = 0; i < 32; ++i)
+      if (atomicCAS(lock, 0, 1) == 0) return true;
+    if (*abort_flag || global_timer_ns() - t0 > 1000000ull) return false;
+  }
+}
+__device__ __forceinline__ void issue_unlock(int* lock) { atomicExch(lock, 0); }
 
 __device__ __forceinline__ void named_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
@@ -611,6 +690,8 @@ __global__ void __launch_bounds__(NQT * 128 + 128, (NQT == 1) ? 2 : 1)
   __shared__ uint64_t bar_full[NSTAGE], bar_empty[NSTAGE];
   __shared__ uint64_t bar_s[NQT], bar_p[NQT], bar_o[NQT];
   __shared__ uint64_t bar_mma_done, bar_drain, bar_route;
+  __shared__ uint64_t bar_qt[NQT], bar_done_t[NQT];   // independent tiles: Q landed, tile's MMAs done
+  __shared__ int mma_lock;
   __shared__ uint32_t tmem_base_sh;
   __shared__ volatile int abort_flag;
   __shared__ int merge_last;
@@ -706,6 +787,11 @@ __global__ void __launch_bounds__(NQT * 128 + 128, (NQT == 1) ? 2 : 1)
       mbar_init(&bar_o[t], 1);
     }
     mbar_init(&bar_mma_done, 1);
+    for (int t = 0; t < NQT; ++t) {
+      mbar_init(&bar_qt[t], 1);
+      mbar_init(&bar_done_t[t], 1);
+    }
+    mma_lock = 0;
     mbar_init(&bar_drain, 1);
     mbar_init(&bar_route, 1);
     abort_flag = 0;
@@ -724,6 +810,116 @@ __global__ void __launch_bounds__(NQT * 128 + 128, (NQT == 1) ? 2 : 1)
 
   if (warp >= Cfg::kProducerWarp) {
     setmaxnreg_dec<Cfg::kRegsControl>();
+  if constexpr (Cfg::kDual) {
+    // warps kProducerWarp + {0, 1, 2, 3}: producer of tile 0, MMA of tile 0, producer of tile 1, MMA of tile 1
+    const int role = warp - Cfg::kProducerWarp;
+    const int t = role >> 1;
+    constexpr int SPT = Cfg::kSPT;
+    if (lane == 0) {
+      TileMerge<QB> w;
+      tile_walk_init<QB, Cfg::kSparseLike>(w, p, bh, qg * 2 + t, t < n_valid_tiles, (kv_hi - kv_lo + BK - 1) / BK);
+      uint32_t fl;
+      int u;
+      if ((role & 1) == 0) {
+        // ---- TMA producer of tile t: Q_t, then K, V of each of its key tiles into slots [t*SPT, t*SPT+SPT)
+        tma_prefetch_desc(&tm_q);
+        tma_prefetch_desc(&tm_k);
+        tma_prefetch_desc(&tm_v);
+        const bool valid = t < n_valid_tiles;
+        if (valid) {
+          mbar_expect_tx(&bar_qt[t], Cfg::kQTileBytes);
+          for (int h = 0; h < D / 64; ++h)
+            tma_load_3d(sQ + t * Cfg::kQTileBytes + h * 16384, &tm_q, &bar_qt[t], h * 64, q_row0 + t * 128, bh);
+        }
+        int ld = 0;
+        bool ok = true;
+        while (ok && (u = w.next(fl)) >= 0) {
+          for (int kv = 0; kv < 2; ++kv) {
+            const int slot = t * SPT + ld % SPT;
+            if (ld >= SPT && !bounded_wait(&bar_empty[slot], ((ld / SPT) - 1) & 1, &abort_flag, p.status)) {
+              ok = false;
+              break;
+            }
+            uint8_t* dst = sKV + slot * Cfg::kSlotBytes;
+            mbar_expect_tx(&bar_full[slot], Cfg::kSlotBytes);
+            for (int h = 0; h < D / 64; ++h)
+              tma_load_3d(dst + h * (BK * 128), kv == 0 ? &tm_k : &tm_v, &bar_full[slot], h * 64, kv_lo + u * BK, bh);
+            ++ld;
+          }
+        }
+        // drain: no copy may still be landing when the CTA exits
+        if (valid) bounded_wait(&bar_qt[t], 0, nullptr, p.status);
+        for (int j = (ld > SPT ? ld - SPT : 0); j < ld; ++j)
+          bounded_wait(&bar_full[t * SPT + j % SPT], (j / SPT) & 1, nullptr, p.status);
+      } else {
+        // ---- MMA issuer of tile t: per step PV_t(s-1) then S_t(s), under the issue lock
+        bool ok = t < n_valid_tiles && bounded_wait(&bar_qt[t], 0, &abort_flag, p.status);
+        tc_fence_after();
+        const uint32_t q_addr = smem_u32(sQ) + t * Cfg::kQTileBytes;
+        const uint32_t kv_base = smem_u32(sKV);
+        const uint32_t s_tmem = tmem + t * 256, o_tmem = tmem + t * 256 + 128;
+        int ld = 0, pvc = 0;
+        bool pending = false;
+        int prev_vslot = 0, prev_vpar = 0;
+        while (ok && (u = w.next(fl)) >= 0) {
+          const int kslot = t * SPT + ld % SPT;
+          if (!bounded_wait(&bar_full[kslot], (ld / SPT) & 1, &abort_flag, p.status)) break;
+          ++ld;
+          const int vslot = t * SPT + ld % SPT;
+          const int vpar = (ld / SPT) & 1;
+          ++ld;
+          if (pending && (!bounded_wait(&bar_full[prev_vslot], prev_vpar, &abort_flag, p.status) ||
+                          !bounded_wait(&bar_p[t], pvc & 1, &abort_flag, p.status))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const bool locked = issue_lock(&mma_lock, &abort_flag);
+          if (pending) {
+            const uint32_t v_addr = kv_base + prev_vslot * Cfg::kSlotBytes;
+#pragma unroll
+            for (int kk = 0; kk < BK / 16; ++kk) {
+              uint64_t bdesc = smem_desc_sw128(v_addr + kk * 16 * 128, BK * 128, 1024);
+              mma_ts(o_tmem, s_tmem + kk * 8, bdesc, Cfg::kIdescPV, (pvc > 0 || kk > 0) ? 1u : 0u);
+            }
+            mma_commit(&bar_o[t]);
+            ++pvc;
+          }
+          const uint32_t k_addr = kv_base + kslot * Cfg::kSlotBytes;
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            uint64_t adesc = smem_desc_sw128(q_addr + (kk / 4) * 16384 + (kk % 4) * 32, 16, 1024);
+            uint64_t bdesc = smem_desc_sw128(k_addr + (kk / 4) * (BK * 128) + (kk % 4) * 32, 16, 1024);
+            mma_ss(s_tmem, adesc, bdesc, Cfg::kIdescS, kk > 0 ? 1u : 0u);
+          }
+          mma_commit(&bar_s[t]);
+          if (locked) issue_unlock(&mma_lock);
+          mma_commit(&bar_empty[kslot]);
+          if (pending) mma_commit(&bar_empty[prev_vslot]);
+          pending = true;
+          prev_vslot = vslot;
+          prev_vpar = vpar;
+        }
+        if (ok && pending && bounded_wait(&bar_full[prev_vslot], prev_vpar, &abort_flag, p.status) &&
+            bounded_wait(&bar_p[t], pvc & 1, &abort_flag, p.status)) {
+          tc_fence_after();
+          const bool locked = issue_lock(&mma_lock, &abort_flag);
+          const uint32_t v_addr = kv_base + prev_vslot * Cfg::kSlotBytes;
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            uint64_t bdesc = smem_desc_sw128(v_addr + kk * 16 * 128, BK * 128, 1024);
+            mma_ts(o_tmem, s_tmem + kk * 8, bdesc, Cfg::kIdescPV, (pvc > 0 || kk > 0) ? 1u : 0u);
+          }
+          mma_commit(&bar_o[t]);
+          if (locked) issue_unlock(&mma_lock);
+          mma_commit(&bar_empty[prev_vslot]);
+        }
+        // every MMA this thread issued has completed before TMEM is released
+        mma_commit(&bar_done_t[t]);
+        bounded_wait(&bar_done_t[t], 0, nullptr, p.status);
+      }
+    }
+  } else
   if (warp == Cfg::kProducerWarp) {
     // ======================= TMA producer =======================
     if (lane == 0) {
@@ -892,8 +1088,12 @@ __global__ void __launch_bounds__(NQT * 128 + 128, (NQT == 1) ? 2 : 1)
       for (int a = 0; a < 3; ++a) na_ws[a] = na_window_start(min(c[a], p.na_L[a] - 1), p.na_K[a], p.na_L[a]);
     }
     const int qb = (QB == 2) ? (w4 >> 1) : 0;      // warp-uniform
-    const uint32_t my_bit = 1u << (t * QB + qb);
-    const uint32_t tile_mask = ((1u << QB) - 1u) << (t * QB);
+    // list bits: of the CTA's merged walk, or (independent tiles) of this tile's own walk
+    const uint32_t my_bit = Cfg::kDual ? (1u << qb) : (1u << (t * QB + qb));
+    const uint32_t tile_mask = Cfg::kDual ? ((1u << QB) - 1u) : (((1u << QB) - 1u) << (t * QB));
+    TileMerge<QB> wk;
+    if constexpr (Cfg::kDual)
+      tile_walk_init<QB, Cfg::kSparseLike>(wk, p, bh, qg * 2 + t, t < n_valid_tiles, (kv_hi - kv_lo + BK - 1) / BK);
     const uint32_t lane_base = (uint32_t)(w4 * 32) << 16;
     const uint32_t tS = tmem + lane_base + t * 256;
     const uint32_t tO = tS + 128;
@@ -912,7 +1112,7 @@ __global__ void __launch_bounds__(NQT * 128 + 128, (NQT == 1) ? 2 : 1)
     uint32_t flags;
     int u;
     bool ok = t < n_valid_tiles;
-    while (ok && (u = next_tile<kNA>(naw, merge, flags, na_box)) >= 0) {
+    while (ok && (u = next_step<Cfg::kDual, kNA>(wk, naw, merge, flags, na_box)) >= 0) {
       if (!(flags & tile_mask)) continue;
       if (!__all_sync(0xffffffffu, bounded_wait(&bar_s[t], it & 1, &abort_flag, p.status))) break;
       tc_fence_after();

@@ -28,11 +28,14 @@ cudaError_t launch_attn_fwd_d128(int BK, int mode, const CUtensorMap& tq, const 
                                  const FwdParams& p, cudaStream_t stream);
 
 // Query tiles of 128 rows per CTA for a mode (the grid is BH * ceil(Sq / (128 * tiles)) [* n_split]).
-// Dense, sparse and split CTAs take one tile and run two per SM: the two CTAs'
-// softmax and MMA phases interleave on the SM, and one CTA's prologue and
-// epilogue overlap the other's main loop.  The fused-routing CTA routes two
-// tiles' query blocks together and keeps two tiles.
-inline int fwd_query_tiles(int mode) { return mode == kModeSparseFused ? 2 : 1; }
+// Dense and sparse CTAs take two tiles, each with its own list walk, K/V ring,
+// TMA producer and MMA issuer, and one CTA per SM; the issuers take turns on
+// the tensor pipe (see attn_fwd.cuh).  Split CTAs take one tile and run two per
+// SM.  The fused-routing CTA routes two tiles' query blocks together and keeps
+// two tiles.
+inline int fwd_query_tiles(int mode) {
+  return (mode == kModeSparseFused || mode == kModeDense || mode == kModeSparse) ? 2 : 1;
+}
 
 // Largest key-block count the fused (on-chip routing) forward accepts.
 constexpr int kFusedMaxNKB = 1024;
