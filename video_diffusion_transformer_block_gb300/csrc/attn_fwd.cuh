@@ -882,8 +882,8 @@ __global__ void __launch_bounds__(NQT * 128 + 128, (NQT == 1) ? 2 : 1)
               uint64_t bdesc = smem_desc_sw128(v_addr + kk * 16 * 128, BK * 128, 1024);
               mma_ts(o_tmem, s_tmem + kk * 8, bdesc, Cfg::kIdescPV, (pvc > 0 || kk > 0) ? 1u : 0u);
             }
-            mma_commit(&bar_o[t]);
-            ++pvc;
+            ++pvc;   // (bar_o is committed once, after the last PV: the softmax's
+                     // bar_s already implies the earlier PVs have completed)
           }
           const uint32_t k_addr = kv_base + kslot * Cfg::kSlotBytes;
 #pragma unroll
@@ -1186,9 +1186,10 @@ __global__ void __launch_bounds__(NQT * 128 + 128, (NQT == 1) ? 2 : 1)
         m_run = mt;
       }
       if (__any_sync(0xffffffffu, need && alpha != 0.f && it > 0)) {
-        // O_t holds the sum over earlier steps: wait for the last PV, rescale in TMEM
-        if (!__all_sync(0xffffffffu, bounded_wait(&bar_o[t], (it - 1) & 1, &abort_flag, p.status))) break;
-        tc_fence_after();
+        // O_t holds the sum over earlier steps; rescale it in TMEM.  No wait is
+        // needed: the issuer committed bar_s for this step's S after issuing the
+        // previous PV of this tile, and a commit tracks every earlier MMA of the
+        // issuing thread, so that PV has completed as well.
         const float a = (need && it > 0) ? alpha : 1.f;
 #pragma unroll
         for (int c0 = 0; c0 < D; c0 += 32) {
@@ -1233,7 +1234,9 @@ __global__ void __launch_bounds__(NQT * 128 + 128, (NQT == 1) ? 2 : 1)
     // ---- epilogue
     if (t < n_valid_tiles && !abort_flag) {
       bool have_o = it > 0;
-      if (have_o && !__all_sync(0xffffffffu, bounded_wait(&bar_o[t], (it - 1) & 1, &abort_flag, p.status))) have_o = false;
+      // (the two-issuer CTA commits bar_o once, after the tile's last PV)
+      const uint32_t o_par = Cfg::kDual ? 0u : (uint32_t)((it - 1) & 1);
+      if (have_o && !__all_sync(0xffffffffu, bounded_wait(&bar_o[t], o_par, &abort_flag, p.status))) have_o = false;
       tc_fence_after();
       if (MODE == kModeSplit) {
         const bool empty = !have_o || l_run == 0.f;
