@@ -246,12 +246,13 @@ struct FwdCfg {
   static constexpr bool kFused = MODE == kModeSparseFused;
   static constexpr bool kNA = is_na_mode(MODE);
   // two independent query tiles per CTA (dense / sparse with NQT = 2): each
-  // tile has its own list walk, its own half of the K/V ring, its own TMA
-  // producer warp and its own MMA-issuing warp, like two one-tile CTAs; the
-  // two issuers take a shared-memory lock around each step's MMA batch
-  // (PV of the previous key tile, S of the current one)
+  // tile has its own list walk, its own two K/V slots, its own TMA producer
+  // warp and its own MMA-issuing warp, like two one-tile CTAs; the two issuers
+  // take a shared-memory lock around each step's MMA batch (PV of the previous
+  // key tile, S of the current one).  Per tile and step one barrier pair:
+  // K of key tile g and V of key tile g-1 land together on the tile's full
+  // barrier, and one commit after the batch frees both slots.
   static constexpr bool kDual = NQT == 2 && (MODE == kModeDense || MODE == kModeSparse);
-  static constexpr int kSPT = kDual ? NSTAGE / 2 : NSTAGE;   // ring slots per tile walk
   static constexpr int kNaT = na_brick_t(MODE), kNaY = na_brick_y(MODE), kNaX = na_brick_x(MODE);
   static constexpr int QB = kSparseLike ? 128 / BK : 1;   // query blocks per 128-row tile
   // fused routing: query blocks per CTA, key-block capacity, staging chunk
@@ -292,7 +293,7 @@ struct FwdCfg {
   static_assert(NQT == 1 || NQT == 2, "query tiles per CTA");
   static_assert(NQT * QB <= 4, "lists per CTA");
   static_assert(NSTAGE >= 2, "ring depth");
-  static_assert(!kDual || (NSTAGE % 2 == 0 && NSTAGE >= 4), "two rings of two or more slots");
+  static_assert(!kDual || NSTAGE == 4, "two K/V slots per tile");
   static_assert(!kFused || kFusedCH * D * 4 + kFusedR * kFusedMaxNKB * 4 + kFusedR * D * 4 <= NSTAGE * kSlotBytes,
                 "fused routing scratch must fit in the K/V ring");
   static_assert(!kFused || NQT == 2, "fused routing runs on the two-tile CTA");
@@ -814,14 +815,13 @@ __global__ void __launch_bounds__(NQT * 128 + 128, (NQT == 1) ? 2 : 1)
     // warps kProducerWarp + {0, 1, 2, 3}: producer of tile 0, MMA of tile 0, producer of tile 1, MMA of tile 1
     const int role = warp - Cfg::kProducerWarp;
     const int t = role >> 1;
-    constexpr int SPT = Cfg::kSPT;
     if (lane == 0) {
       TileMerge<QB> w;
       tile_walk_init<QB, Cfg::kSparseLike>(w, p, bh, qg * 2 + t, t < n_valid_tiles, (kv_hi - kv_lo + BK - 1) / BK);
       uint32_t fl;
       int u;
       if ((role & 1) == 0) {
-        // ---- TMA producer of tile t: Q_t, then K, V of each of its key tiles into slots [t*SPT, t*SPT+SPT)
+        // ---- TMA producer of tile t: Q_t, then per step group the K and V tiles into slots 2t, 2t+1
         tma_prefetch_desc(&tm_q);
         tma_prefetch_desc(&tm_k);
         tma_prefetch_desc(&tm_v);
@@ -831,89 +831,80 @@ __global__ void __launch_bounds__(NQT * 128 + 128, (NQT == 1) ? 2 : 1)
           for (int h = 0; h < D / 64; ++h)
             tma_load_3d(sQ + t * Cfg::kQTileBytes + h * 16384, &tm_q, &bar_qt[t], h * 64, q_row0 + t * 128, bh);
         }
-        int ld = 0;
+        // group g: K of key tile g into slot 2t, V of key tile g-1 into slot 2t+1, both on
+        // bar_full[2t]; the group is loaded once batch g-1 (PV of g-2, S of g-1) has completed
+        const int kslot = 2 * t, vslot = 2 * t + 1;
+        int g = 0, prev = -1;
         bool ok = true;
-        while (ok && (u = w.next(fl)) >= 0) {
-          for (int kv = 0; kv < 2; ++kv) {
-            const int slot = t * SPT + ld % SPT;
-            if (ld >= SPT && !bounded_wait(&bar_empty[slot], ((ld / SPT) - 1) & 1, &abort_flag, p.status)) {
-              ok = false;
-              break;
-            }
-            uint8_t* dst = sKV + slot * Cfg::kSlotBytes;
-            mbar_expect_tx(&bar_full[slot], Cfg::kSlotBytes);
-            for (int h = 0; h < D / 64; ++h)
-              tma_load_3d(dst + h * (BK * 128), kv == 0 ? &tm_k : &tm_v, &bar_full[slot], h * 64, kv_lo + u * BK, bh);
-            ++ld;
+        while (ok) {
+          u = w.next(fl);
+          if (u < 0 && prev < 0) break;
+          if (g >= 1 && !bounded_wait(&bar_s[t], (g - 1) & 1, &abort_flag, p.status)) {
+            ok = false;
+            break;
           }
+          mbar_expect_tx(&bar_full[kslot], ((u >= 0) + (prev >= 0)) * Cfg::kSlotBytes);
+          if (u >= 0)
+            for (int h = 0; h < D / 64; ++h)
+              tma_load_3d(sKV + kslot * Cfg::kSlotBytes + h * (BK * 128), &tm_k, &bar_full[kslot], h * 64,
+                          kv_lo + u * BK, bh);
+          if (prev >= 0)
+            for (int h = 0; h < D / 64; ++h)
+              tma_load_3d(sKV + vslot * Cfg::kSlotBytes + h * (BK * 128), &tm_v, &bar_full[kslot], h * 64,
+                          kv_lo + prev * BK, bh);
+          prev = u;
+          ++g;
+          if (u < 0) break;
         }
         // drain: no copy may still be landing when the CTA exits
         if (valid) bounded_wait(&bar_qt[t], 0, nullptr, p.status);
-        for (int j = (ld > SPT ? ld - SPT : 0); j < ld; ++j)
-          bounded_wait(&bar_full[t * SPT + j % SPT], (j / SPT) & 1, nullptr, p.status);
+        if (g >= 1) bounded_wait(&bar_full[kslot], (g - 1) & 1, nullptr, p.status);
       } else {
-        // ---- MMA issuer of tile t: per step PV_t(s-1) then S_t(s), under the issue lock
+        // ---- MMA issuer of tile t: per group PV_t(g-1) then S_t(g), under the issue lock
         bool ok = t < n_valid_tiles && bounded_wait(&bar_qt[t], 0, &abort_flag, p.status);
         tc_fence_after();
         const uint32_t q_addr = smem_u32(sQ) + t * Cfg::kQTileBytes;
         const uint32_t kv_base = smem_u32(sKV);
         const uint32_t s_tmem = tmem + t * 256, o_tmem = tmem + t * 256 + 128;
-        int ld = 0, pvc = 0;
+        const int kslot = 2 * t, vslot = 2 * t + 1;
+        const uint32_t k_addr = kv_base + kslot * Cfg::kSlotBytes, v_addr = kv_base + vslot * Cfg::kSlotBytes;
+        int g = 0, pvc = 0;
         bool pending = false;
-        int prev_vslot = 0, prev_vpar = 0;
-        while (ok && (u = w.next(fl)) >= 0) {
-          const int kslot = t * SPT + ld % SPT;
-          if (!bounded_wait(&bar_full[kslot], (ld / SPT) & 1, &abort_flag, p.status)) break;
-          ++ld;
-          const int vslot = t * SPT + ld % SPT;
-          const int vpar = (ld / SPT) & 1;
-          ++ld;
-          if (pending && (!bounded_wait(&bar_full[prev_vslot], prev_vpar, &abort_flag, p.status) ||
-                          !bounded_wait(&bar_p[t], pvc & 1, &abort_flag, p.status))) {
+        while (ok) {
+          u = w.next(fl);
+          if (u < 0 && !pending) break;
+          if (!bounded_wait(&bar_full[kslot], g & 1, &abort_flag, p.status) ||
+              (pending && !bounded_wait(&bar_p[t], pvc & 1, &abort_flag, p.status))) {
             ok = false;
             break;
           }
           tc_fence_after();
           const bool locked = issue_lock(&mma_lock, &abort_flag);
           if (pending) {
-            const uint32_t v_addr = kv_base + prev_vslot * Cfg::kSlotBytes;
 #pragma unroll
             for (int kk = 0; kk < BK / 16; ++kk) {
               uint64_t bdesc = smem_desc_sw128(v_addr + kk * 16 * 128, BK * 128, 1024);
               mma_ts(o_tmem, s_tmem + kk * 8, bdesc, Cfg::kIdescPV, (pvc > 0 || kk > 0) ? 1u : 0u);
             }
-            ++pvc;   // (bar_o is committed once, after the last PV: the softmax's
-                     // bar_s already implies the earlier PVs have completed)
+            ++pvc;
           }
-          const uint32_t k_addr = kv_base + kslot * Cfg::kSlotBytes;
+          if (u >= 0) {
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            uint64_t adesc = smem_desc_sw128(q_addr + (kk / 4) * 16384 + (kk % 4) * 32, 16, 1024);
-            uint64_t bdesc = smem_desc_sw128(k_addr + (kk / 4) * (BK * 128) + (kk % 4) * 32, 16, 1024);
-            mma_ss(s_tmem, adesc, bdesc, Cfg::kIdescS, kk > 0 ? 1u : 0u);
+            for (int kk = 0; kk < D / 16; ++kk) {
+              uint64_t adesc = smem_desc_sw128(q_addr + (kk / 4) * 16384 + (kk % 4) * 32, 16, 1024);
+              uint64_t bdesc = smem_desc_sw128(k_addr + (kk / 4) * (BK * 128) + (kk % 4) * 32, 16, 1024);
+              mma_ss(s_tmem, adesc, bdesc, Cfg::kIdescS, kk > 0 ? 1u : 0u);
+            }
           }
+          if (locked) issue_unlock(&mma_lock);
+          // one commit serves the softmax (S ready) and the producer (both slots free)
           mma_commit(&bar_s[t]);
-          if (locked) issue_unlock(&mma_lock);
-          mma_commit(&bar_empty[kslot]);
-          if (pending) mma_commit(&bar_empty[prev_vslot]);
-          pending = true;
-          prev_vslot = vslot;
-          prev_vpar = vpar;
+          pending = u >= 0;
+          ++g;
+          if (u < 0) break;
         }
-        if (ok && pending && bounded_wait(&bar_full[prev_vslot], prev_vpar, &abort_flag, p.status) &&
-            bounded_wait(&bar_p[t], pvc & 1, &abort_flag, p.status)) {
-          tc_fence_after();
-          const bool locked = issue_lock(&mma_lock, &abort_flag);
-          const uint32_t v_addr = kv_base + prev_vslot * Cfg::kSlotBytes;
-#pragma unroll
-          for (int kk = 0; kk < BK / 16; ++kk) {
-            uint64_t bdesc = smem_desc_sw128(v_addr + kk * 16 * 128, BK * 128, 1024);
-            mma_ts(o_tmem, s_tmem + kk * 8, bdesc, Cfg::kIdescPV, (pvc > 0 || kk > 0) ? 1u : 0u);
-          }
-          mma_commit(&bar_o[t]);
-          if (locked) issue_unlock(&mma_lock);
-          mma_commit(&bar_empty[prev_vslot]);
-        }
+        // the epilogue waits for the last PV here; a commit tracks every earlier MMA of this thread
+        mma_commit(&bar_o[t]);
         // every MMA this thread issued has completed before TMEM is released
         mma_commit(&bar_done_t[t]);
         bounded_wait(&bar_done_t[t], 0, nullptr, p.status);

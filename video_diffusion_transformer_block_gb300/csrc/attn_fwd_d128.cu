@@ -7,7 +7,7 @@ cudaError_t launch_attn_fwd_d128(int BK, int mode, const CUtensorMap& tq, const 
                                  const FwdParams& p, cudaStream_t stream) {
   if (mode == kModeDense && BK == 128) return launch_fwd_cfg<128, 128, kModeDense, 2, 4>(tq, tk, tv, p, stream);
   if (mode == kModeSparse && BK == 128) return launch_fwd_cfg<128, 128, kModeSparse, 2, 4>(tq, tk, tv, p, stream);
-  if (mode == kModeSparse && BK == 64) return launch_fwd_cfg<128, 64, kModeSparse, 2, 8>(tq, tk, tv, p, stream);
+  if (mode == kModeSparse && BK == 64) return launch_fwd_cfg<128, 64, kModeSparse, 2, 4>(tq, tk, tv, p, stream);
   if (mode == kModeSplit && BK == 128) return launch_fwd_cfg<128, 128, kModeSplit, 1, 2>(tq, tk, tv, p, stream);
   if (mode == kModeSparseFused && BK == 128) return launch_fwd_cfg<128, 128, kModeSparseFused, 2, 4>(tq, tk, tv, p, stream);
   if (mode == kModeSparseFused && BK == 64) return launch_fwd_cfg<128, 64, kModeSparseFused, 2, 6>(tq, tk, tv, p, stream);

@@ -5,9 +5,9 @@ namespace vdtb {
 
 cudaError_t launch_attn_fwd_d64(int BK, int mode, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                                 const FwdParams& p, cudaStream_t stream) {
-  if (mode == kModeDense && BK == 128) return launch_fwd_cfg<64, 128, kModeDense, 2, 8>(tq, tk, tv, p, stream);
-  if (mode == kModeSparse && BK == 128) return launch_fwd_cfg<64, 128, kModeSparse, 2, 8>(tq, tk, tv, p, stream);
-  if (mode == kModeSparse && BK == 64) return launch_fwd_cfg<64, 64, kModeSparse, 2, 16>(tq, tk, tv, p, stream);
+  if (mode == kModeDense && BK == 128) return launch_fwd_cfg<64, 128, kModeDense, 2, 4>(tq, tk, tv, p, stream);
+  if (mode == kModeSparse && BK == 128) return launch_fwd_cfg<64, 128, kModeSparse, 2, 4>(tq, tk, tv, p, stream);
+  if (mode == kModeSparse && BK == 64) return launch_fwd_cfg<64, 64, kModeSparse, 2, 4>(tq, tk, tv, p, stream);
   if (mode == kModeSplit && BK == 128) return launch_fwd_cfg<64, 128, kModeSplit, 1, 4>(tq, tk, tv, p, stream);
   if (mode == kModeSparseFused && BK == 128) return launch_fwd_cfg<64, 128, kModeSparseFused, 2, 6>(tq, tk, tv, p, stream);
   if (mode == kModeSparseFused && BK == 64) return launch_fwd_cfg<64, 64, kModeSparseFused, 2, 8>(tq, tk, tv, p, stream);
