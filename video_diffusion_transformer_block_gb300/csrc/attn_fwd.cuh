@@ -253,6 +253,12 @@ struct FwdCfg {
   // K of key tile g and V of key tile g-1 land together on the tile's full
   // barrier, and one commit after the batch frees both slots.
   static constexpr bool kDual = NQT == 2 && (MODE == kModeDense || MODE == kModeSparse);
+  // per-tile roles (the two-issuer CTA and the one-tile split-KV / dense / sparse CTAs): tile t
+  // has its own producer and issuer warps and K/V slots 2t, 2t+1 with one full barrier per step.
+  // The neighbourhood CTAs and the shared-walk two-tile CTA (fused routing) keep one producer
+  // and one issuer with a barrier per slot (for the one-brick neighbourhood CTA the per-tile
+  // roles measured no faster: its control warps spill the walk's box state).
+  static constexpr bool kPerTile = kDual || (NQT == 1 && !kNA);
   static constexpr int kNaT = na_brick_t(MODE), kNaY = na_brick_y(MODE), kNaX = na_brick_x(MODE);
   static constexpr int QB = kSparseLike ? 128 / BK : 1;   // query blocks per 128-row tile
   // fused routing: query blocks per CTA, key-block capacity, staging chunk
@@ -294,6 +300,7 @@ struct FwdCfg {
   static_assert(NQT * QB <= 4, "lists per CTA");
   static_assert(NSTAGE >= 2, "ring depth");
   static_assert(!kDual || NSTAGE == 4, "two K/V slots per tile");
+  static_assert(!kPerTile || NSTAGE >= 2 * NQT, "two K/V slots per tile");
   static_assert(!kFused || kFusedCH * D * 4 + kFusedR * kFusedMaxNKB * 4 + kFusedR * D * 4 <= NSTAGE * kSlotBytes,
                 "fused routing scratch must fit in the K/V ring");
   static_assert(!kFused || NQT == 2, "fused routing runs on the two-tile CTA");
@@ -350,7 +357,7 @@ __device__ __forceinline__ void tile_walk_init(TileMerge<QB>& w, const FwdParams
   }
 }
 
-// Next key tile of a softmax warpgroup: its own tile's walk (independent tiles) or the CTA's walk.
+// Next key tile of a per-tile role: its own tile's walk (two-issuer CTA) or the CTA's walk.
 template <bool DUAL, bool NA, class Own, class Walk, class Merge>
 __device__ __forceinline__ int next_step(Own& own, Walk& naw, Merge& merge, uint32_t& flags, int (&box)[3]) {
   if constexpr (DUAL) {
@@ -811,13 +818,15 @@ __global__ void __launch_bounds__(NQT * 128 + 128, (NQT == 1) ? 2 : 1)
 
   if (warp >= Cfg::kProducerWarp) {
     setmaxnreg_dec<Cfg::kRegsControl>();
-  if constexpr (Cfg::kDual) {
-    // warps kProducerWarp + {0, 1, 2, 3}: producer of tile 0, MMA of tile 0, producer of tile 1, MMA of tile 1
+  if constexpr (Cfg::kPerTile) {
+    // warps kProducerWarp + {0, 1, 2, 3}: producer of tile 0, issuer of tile 0, producer of tile 1,
+    // issuer of tile 1 (a one-tile CTA uses the first two)
     const int role = warp - Cfg::kProducerWarp;
     const int t = role >> 1;
-    if (lane == 0) {
+    if (lane == 0 && t < NQT) {
       TileMerge<QB> w;
-      tile_walk_init<QB, Cfg::kSparseLike>(w, p, bh, qg * 2 + t, t < n_valid_tiles, (kv_hi - kv_lo + BK - 1) / BK);
+      if constexpr (Cfg::kDual)
+        tile_walk_init<QB, Cfg::kSparseLike>(w, p, bh, qg * 2 + t, t < n_valid_tiles, (kv_hi - kv_lo + BK - 1) / BK);
       uint32_t fl;
       int u;
       if ((role & 1) == 0) {
@@ -828,31 +837,41 @@ __global__ void __launch_bounds__(NQT * 128 + 128, (NQT == 1) ? 2 : 1)
         const bool valid = t < n_valid_tiles;
         if (valid) {
           mbar_expect_tx(&bar_qt[t], Cfg::kQTileBytes);
-          for (int h = 0; h < D / 64; ++h)
-            tma_load_3d(sQ + t * Cfg::kQTileBytes + h * 16384, &tm_q, &bar_qt[t], h * 64, q_row0 + t * 128, bh);
+          for (int h = 0; h < D / 64; ++h) {
+            if constexpr (kNA)
+              tma_load_5d(sQ + h * 16384, &tm_q, &bar_qt[t], h * 64, naw.org[0][2], naw.org[0][1], naw.org[0][0], bh);
+            else
+              tma_load_3d(sQ + t * Cfg::kQTileBytes + h * 16384, &tm_q, &bar_qt[t], h * 64, q_row0 + t * 128, bh);
+          }
         }
         // group g: K of key tile g into slot 2t, V of key tile g-1 into slot 2t+1, both on
         // bar_full[2t]; the group is loaded once batch g-1 (PV of g-2, S of g-1) has completed
         const int kslot = 2 * t, vslot = 2 * t + 1;
         int g = 0, prev = -1;
+        int pbox[3] = {0, 0, 0};
         bool ok = true;
         while (ok) {
-          u = w.next(fl);
+          u = next_step<Cfg::kDual, kNA>(w, naw, merge, fl, na_box);
           if (u < 0 && prev < 0) break;
           if (g >= 1 && !bounded_wait(&bar_s[t], (g - 1) & 1, &abort_flag, p.status)) {
             ok = false;
             break;
           }
           mbar_expect_tx(&bar_full[kslot], ((u >= 0) + (prev >= 0)) * Cfg::kSlotBytes);
-          if (u >= 0)
-            for (int h = 0; h < D / 64; ++h)
-              tma_load_3d(sKV + kslot * Cfg::kSlotBytes + h * (BK * 128), &tm_k, &bar_full[kslot], h * 64,
-                          kv_lo + u * BK, bh);
-          if (prev >= 0)
-            for (int h = 0; h < D / 64; ++h)
-              tma_load_3d(sKV + vslot * Cfg::kSlotBytes + h * (BK * 128), &tm_v, &bar_full[kslot], h * 64,
-                          kv_lo + prev * BK, bh);
+          for (int h = 0; h < D / 64; ++h) {
+            uint8_t* kd = sKV + kslot * Cfg::kSlotBytes + h * (BK * 128);
+            uint8_t* vd = sKV + vslot * Cfg::kSlotBytes + h * (BK * 128);
+            if constexpr (kNA) {
+              if (u >= 0) tma_load_5d(kd, &tm_k, &bar_full[kslot], h * 64, na_box[2], na_box[1], na_box[0], bh);
+              if (prev >= 0) tma_load_5d(vd, &tm_v, &bar_full[kslot], h * 64, pbox[2], pbox[1], pbox[0], bh);
+            } else {
+              if (u >= 0) tma_load_3d(kd, &tm_k, &bar_full[kslot], h * 64, kv_lo + u * BK, bh);
+              if (prev >= 0) tma_load_3d(vd, &tm_v, &bar_full[kslot], h * 64, kv_lo + prev * BK, bh);
+            }
+          }
           prev = u;
+#pragma unroll
+          for (int a = 0; a < 3; ++a) pbox[a] = na_box[a];
           ++g;
           if (u < 0) break;
         }
@@ -860,7 +879,7 @@ __global__ void __launch_bounds__(NQT * 128 + 128, (NQT == 1) ? 2 : 1)
         if (valid) bounded_wait(&bar_qt[t], 0, nullptr, p.status);
         if (g >= 1) bounded_wait(&bar_full[kslot], (g - 1) & 1, nullptr, p.status);
       } else {
-        // ---- MMA issuer of tile t: per group PV_t(g-1) then S_t(g), under the issue lock
+        // ---- MMA issuer of tile t: per group PV_t(g-1) then S_t(g) (two-issuer CTA: under the issue lock)
         bool ok = t < n_valid_tiles && bounded_wait(&bar_qt[t], 0, &abort_flag, p.status);
         tc_fence_after();
         const uint32_t q_addr = smem_u32(sQ) + t * Cfg::kQTileBytes;
@@ -871,7 +890,7 @@ __global__ void __launch_bounds__(NQT * 128 + 128, (NQT == 1) ? 2 : 1)
         int g = 0, pvc = 0;
         bool pending = false;
         while (ok) {
-          u = w.next(fl);
+          u = next_step<Cfg::kDual, kNA>(w, naw, merge, fl, na_box);
           if (u < 0 && !pending) break;
           if (!bounded_wait(&bar_full[kslot], g & 1, &abort_flag, p.status) ||
               (pending && !bounded_wait(&bar_p[t], pvc & 1, &abort_flag, p.status))) {
@@ -879,7 +898,7 @@ __global__ void __launch_bounds__(NQT * 128 + 128, (NQT == 1) ? 2 : 1)
             break;
           }
           tc_fence_after();
-          const bool locked = issue_lock(&mma_lock, &abort_flag);
+          const bool locked = Cfg::kDual && issue_lock(&mma_lock, &abort_flag);
           if (pending) {
 #pragma unroll
             for (int kk = 0; kk < BK / 16; ++kk) {
@@ -1225,8 +1244,8 @@ __global__ void __launch_bounds__(NQT * 128 + 128, (NQT == 1) ? 2 : 1)
     // ---- epilogue
     if (t < n_valid_tiles && !abort_flag) {
       bool have_o = it > 0;
-      // (the two-issuer CTA commits bar_o once, after the tile's last PV)
-      const uint32_t o_par = Cfg::kDual ? 0u : (uint32_t)((it - 1) & 1);
+      // (per-tile issuers commit bar_o once, after the tile's last PV)
+      const uint32_t o_par = Cfg::kPerTile ? 0u : (uint32_t)((it - 1) & 1);
       if (have_o && !__all_sync(0xffffffffu, bounded_wait(&bar_o[t], o_par, &abort_flag, p.status))) have_o = false;
       tc_fence_after();
       if (MODE == kModeSplit) {
