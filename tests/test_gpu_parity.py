@@ -203,6 +203,52 @@ def test_sparse_batch_gt_one():
         assert_close(host(lse[b:b + 1]), rl, f"batch {b} lse")
 
 
+@pytest.mark.parametrize("d,block", [(128, 128), (128, 64), (64, 128)])
+def test_sparse_given_lists_uneven_between_paired_tiles(d, block):
+    # Hand-made selections through attn_sparse_fwd: neighbouring query tiles (the two
+    # tiles a dense/sparse CTA holds) get lists of very different lengths (all key
+    # blocks against one, one against none-but-the-last, ...), so one tile's walk ends
+    # long before the other's.  The Taylor aggregates for the forced selection come
+    # from the oracle's routing, and the oracle computes the same attention.
+    B, H, S = 1, 2, 1000
+    q, k, v = rnd_qkv(B, H, S, S, d, seed=61 + d + block)
+    nqb = (S + block - 1) // block
+    rng = np.random.default_rng(5)
+    sel = np.zeros((B, H, nqb, nqb), dtype=bool)
+    for h in range(H):
+        for i in range(nqb):
+            kind = (i + h) % 4
+            if kind == 0:
+                sel[0, h, i, :] = True                       # every key block
+            elif kind == 1:
+                sel[0, h, i, nqb - 1] = True                 # only the ragged last block
+            elif kind == 2:
+                sel[0, h, i, i] = True                       # only the diagonal
+            else:
+                sel[0, h, i, rng.choice(nqb, size=max(1, nqb // 3), replace=False)] = True
+    qh, kh, vh = host(q), host(k), host(v)
+    qp, kp, vp = (oracle.block_pool(x, block) for x in (qh, kh, vh))
+    scale = 1 / math.sqrt(d)
+    forced = oracle.route(qp, kp, vp, S, block, scale, 0.0, force_sel=sel)
+    rt = vd.sparse_route_buffers(B, H, S, d, block, DEV)
+    idx = np.zeros((B, H, nqb, nqb), dtype=np.int32)
+    cnt = sel.sum(-1).astype(np.int32)
+    for h in range(H):
+        for i in range(nqb):
+            lst = np.flatnonzero(sel[0, h, i])
+            idx[0, h, i, :lst.size] = lst
+    stats = np.stack([forced["mu"], forced["sigma"], forced["tau"], forced["W"]], axis=-1)
+    rt["sel_idx"].copy_(torch.from_numpy(idx))
+    rt["sel_cnt"].copy_(torch.from_numpy(cnt))
+    rt["stats"].copy_(torch.from_numpy(stats.astype(np.float32)))
+    rt["taylor_t"].copy_(torch.from_numpy(np.ascontiguousarray(forced["T"], dtype=np.float32)))
+    out, lse = vd.attn_sparse_fwd(q, k, v, rt, block=block)
+    torch.cuda.synchronize()
+    ro, rl = oracle.sparse_attention(qh, kh, vh, block, block, sel, forced["mu"], forced["W"], forced["T"], scale)
+    assert_close(host(out), ro, "sparse given-lists out")
+    assert_close(host(lse), rl, "sparse given-lists lse")
+
+
 # ---------------------------------------------------------------- routing folded into the forward
 
 @pytest.mark.parametrize("beta", [0.5, -math.inf, 3.0])
