@@ -697,7 +697,7 @@ __global__ void __launch_bounds__(NQT * 128 + 128, (NQT == 1) ? 2 : 1)
   __shared__ uint64_t bar_q;
   __shared__ uint64_t bar_full[NSTAGE], bar_empty[NSTAGE];
   __shared__ uint64_t bar_s[NQT], bar_p[NQT], bar_o[NQT];
-  __shared__ uint64_t bar_mma_done, bar_drain, bar_route;
+  __shared__ uint64_t bar_mma_done, bar_route;
   __shared__ uint64_t bar_qt[NQT], bar_done_t[NQT];   // independent tiles: Q landed, tile's MMAs done
   __shared__ int mma_lock;
   __shared__ uint32_t tmem_base_sh;
@@ -800,7 +800,6 @@ __global__ void __launch_bounds__(NQT * 128 + 128, (NQT == 1) ? 2 : 1)
       mbar_init(&bar_done_t[t], 1);
     }
     mma_lock = 0;
-    mbar_init(&bar_drain, 1);
     mbar_init(&bar_route, 1);
     abort_flag = 0;
     fence_barrier_init();
