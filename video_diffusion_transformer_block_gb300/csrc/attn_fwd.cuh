@@ -1012,7 +1012,6 @@ __global__ void __launch_bounds__(NQT * 128 + 128, (NQT == 1) ? 2 : 1)
           uint64_t bdesc = smem_desc_sw128(v_addr + kk * 16 * 128, BK * 128, 1024);
           mma_ts(d_tmem, p_tmem + kk * 8, bdesc, Cfg::kIdescPV, (pv_count[t] > 0 || kk > 0) ? 1u : 0u);
         }
-        mma_commit(&bar_o[t]);
         ++pv_count[t];
         pending[t] = false;
       };
@@ -1072,6 +1071,9 @@ __global__ void __launch_bounds__(NQT * 128 + 128, (NQT == 1) ? 2 : 1)
         }
         if (any_pv) mma_commit(&bar_empty[prev_vslot]);
       }
+      // the epilogues wait for the last PVs here (a commit tracks every earlier MMA of this thread)
+#pragma unroll
+      for (int t = 0; t < NQT; ++t) mma_commit(&bar_o[t]);
       // every MMA issued by this thread has completed before TMEM is released
       mma_commit(&bar_mma_done);
       bounded_wait(&bar_mma_done, 0, nullptr, p.status);
@@ -1243,9 +1245,8 @@ __global__ void __launch_bounds__(NQT * 128 + 128, (NQT == 1) ? 2 : 1)
     // ---- epilogue
     if (t < n_valid_tiles && !abort_flag) {
       bool have_o = it > 0;
-      // (per-tile issuers commit bar_o once, after the tile's last PV)
-      const uint32_t o_par = Cfg::kPerTile ? 0u : (uint32_t)((it - 1) & 1);
-      if (have_o && !__all_sync(0xffffffffu, bounded_wait(&bar_o[t], o_par, &abort_flag, p.status))) have_o = false;
+      // (every issuer commits bar_o once, after its last PV)
+      if (have_o && !__all_sync(0xffffffffu, bounded_wait(&bar_o[t], 0, &abort_flag, p.status))) have_o = false;
       tc_fence_after();
       if (MODE == kModeSplit) {
         const bool empty = !have_o || l_run == 0.f;
