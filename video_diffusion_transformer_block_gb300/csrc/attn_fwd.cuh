@@ -3,28 +3,33 @@
 //
 // CTA = NQT query tiles of 128 rows.  Three layouts:
 //  - two-issuer CTA (dense and sparse, NQT = 2, one CTA per SM): the two tiles
-//    run like two one-tile CTAs, each with its own list walk, its own half of
-//    the K/V ring, its own TMA producer warp and MMA-issuing warp; the issuers
-//    take a shared-memory lock around each step's MMA batch.  Two one-tile
-//    CTAs on an SM were measured to fall into step with each other (both
-//    issuing MMAs, then both in softmax, with the tensor pipe idle); the lock
-//    makes one tile's batch run while the other tile's softmax does.
-//  - one-tile CTA (split-KV and one-brick neighbourhood plans, two per SM).
+//    run like two one-tile CTAs, each with its own list walk, its own two K/V
+//    slots, its own TMA producer warp and MMA-issuing warp; the issuers take a
+//    shared-memory lock around each step's MMA batch.  Two one-tile CTAs on an
+//    SM were measured to fall into step with each other (both issuing MMAs,
+//    then both in softmax, with the tensor pipe idle); the lock makes one
+//    tile's batch run while the other tile's softmax does.  Per tile and step
+//    one full barrier (K of key tile s with V of key tile s-1) and one commit
+//    (S ready, both slots free): each barrier operation of an issuer costs
+//    100-200 clocks while the score MMAs keep shared memory busy.
+//  - one-tile CTA, two per SM: split-KV (the same per-tile roles) and the
+//    one-brick neighbourhood plans (one producer, one issuer, a full/empty
+//    barrier pair per slot).
 //  - shared-walk two-tile CTA (fused routing, paired neighbourhood plans):
 //    one producer and one issuer walk the union of the tiles' lists and every
 //    K/V load serves both tiles.
 //   warps 0..4*NQT-1 : softmax/epilogue, one warpgroup per query tile; thread
 //                      r of the warpgroup owns query row r = TMEM lane r
 //   warp  4*NQT      : TMA producer (Q once, then K_s, V_s for every step s
-//                      into a ring of NSTAGE slots)
+//                      into the K/V slots)
 //   warp  4*NQT+1    : tcgen05 MMA issuer (one thread); allocates TMEM
 //   (two-issuer CTA: warps 8, 9 are tile 0's producer and issuer, 10, 11 tile 1's)
 // TMEM, per query tile t: S_t at columns [256t, 256t+BK) in fp32; P_t (bf16
 // pairs) overwrites the first BK/2 columns of S_t; O_t at [256t+128, +D).
 // Per step s: S_t = Q_t K_s^T (SS MMA, both K-major, 128B swizzle), softmax
-// writes P_t, O_t += P_t V_s (TS MMA, P from TMEM, V MN-major).  The MMA
-// thread issues PV_t(s-1) immediately before S_t(s), so the tensor pipe
-// works on one tile while the other tile's softmax runs.
+// writes P_t, O_t += P_t V_s (TS MMA, P from TMEM, V MN-major).  An issuer
+// issues PV_t(s-1) immediately before S_t(s) (which overwrites P_t), so the
+// tensor pipe works on one tile while the other tile's softmax runs.
 // Online softmax in base 2 with a lazy rescale: the running max is only
 // moved (and O_t rescaled in TMEM) when a tile's max exceeds it by more than
 // kRescaleLog2, so P stays <= 2^kRescaleLog2 and the final normalisation by
@@ -32,9 +37,9 @@
 //
 // 3D neighbourhood attention (modes kModeNA*) runs on the same loop: a query
 // tile is a brick of 128 tokens (bt x by x bx) of the (T, Y, X) volume, loaded
-// by a 5-D TMA box straight from the raster layout; the CTA's two bricks are
-// neighbours along one axis.  The key tiles are boxes of the same shape laid on
-// a grid that starts at the corner of the union of the two bricks' windows;
+// by a 5-D TMA box straight from the raster layout; a paired CTA's two bricks
+// are neighbours along one axis.  The key tiles are boxes of the same shape
+// laid on a grid that starts at the corner of the union of the bricks' windows;
 // every role walks that grid in the same order, and each query row masks the
 // keys outside its own window.
 #pragma once
