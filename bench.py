@@ -597,6 +597,18 @@ def run_e2e(args, vd, w, qkv, cross, rt, ws, step_flops, world):
 
     run(2)
     torch.cuda.synchronize()
+    # the host link's own rate in this run (the step is bound by it): one upload of q from pinned
+    # memory and one download into pinned memory, timed with CUDA events on the copy streams
+    def link_gbs(dst, src, st):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(st):
+            e0.record(st)
+            dst.copy_(src, non_blocking=True)
+            e1.record(st)
+        e1.synchronize()
+        return src.numel() * src.element_size() / (e0.elapsed_time(e1) * 1e-3) / 1e9
+    link = {"h2d_gbs": round(link_gbs(din[0][0], hin[0], upload), 1),
+            "d2h_gbs": round(link_gbs(hin[0], din[0][0], download), 1)}
     steps = max(3, args.steps // 2)
     barrier(world)
     torch.cuda.synchronize()
@@ -609,6 +621,7 @@ def run_e2e(args, vd, w, qkv, cross, rt, ws, step_flops, world):
     ms = max_over_ranks(e0.elapsed_time(e1), world) / steps
     return {"value": round(world * step_flops / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s", "ms_per_step": round(ms, 4),
             "steps": steps, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+            "host_link_measured": link,
             "pipelining": "double-buffered: uploads and downloads on two copy streams overlap each other and the "
                           "previous/next step's compute; the cross attention on its own compute stream"}
 
