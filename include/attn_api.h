@@ -28,9 +28,9 @@
  *               which attn_last_device_status reports as ATTN_ERR_TIMEOUT.
  *               No exception or process exit crosses this ABI.
  *   Lengths     There are no masks: ragged and odd lengths (S not a multiple
- *               of any tile, odd key counts) are handled by in-kernel bounds,
- *               the way the LTX-2.5 page drops the padded key instead of
- *               masking it ("LTX-2.5 at 4K, in half the time", section
+ *               of any tile, odd key counts) are handled by in-kernel bounds;
+ *               an odd key count is split unevenly rather than padded, as on
+ *               the LTX-2.5 page ("LTX-2.5 at 4K, in half the time", section
  *               "Attention across two GPUs").
  *   Numerics    bf16 inputs, fp32 accumulation and softmax, bf16 outputs
  *               rounded to nearest even, lse in natural log (fp32).  The
