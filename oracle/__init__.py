@@ -12,9 +12,11 @@ proxy scores, mu/sigma/tau and the selection are pinned by closed forms,
 library routines and invariants in ``tests/test_oracle_pins.py``.  The Taylor
 aggregates (W, T) and the Taylor-corrected sparse output follow a reading
 of the Sol-Attn page (first order about the row-mean proxy score,
-applied per block with pooled V); they are pinned only against a
-hand-derived closed form of that reading: parity unpinned with respect to the
-pages.  3D neighbourhood attention follows the published definition of
+applied per block with pooled V); they are pinned against exact softmax
+attention in the small-deviation limit (the error must shrink as the square of
+the score spread) and against a hand-derived closed form of that reading; the
+pages' own block-level form is not printed, so parity is unpinned with respect
+to the pages.  3D neighbourhood attention follows the published definition of
 neighbourhood attention (the pages name the kernel but do not define it) and
 is pinned by closed forms, an independent brute force and a mirror symmetry.
 The FP8 (E4M3) codec, the per-row activation quantiser and the scaled FP8

@@ -51,9 +51,12 @@
  *    and numpy's matmul of the decoded operands.
  *  - oracle_route (Taylor aggregates W, T) and oracle_sparse_rows: the pages
  *    give no formula for the Taylor term.  The first-order block-level form
- *    used here is a reading of the page; it is pinned by a hand-derived closed
- *    form and by invariants of that reading, so its agreement with the
- *    pages' (unprinted) formula is "parity unpinned".
+ *    used here is a reading of the page; it is pinned against exact softmax
+ *    attention in the small-deviation limit (with block-constant keys its
+ *    error must shrink as the square of the score spread), by a hand-derived
+ *    closed form and by invariants of that reading.  What no pin can fix is
+ *    the pages' own (unprinted) block-level form, so agreement with it is
+ *    "parity unpinned".
  */
 #include <fenv.h>
 #include <math.h>

@@ -28,6 +28,8 @@ MUTANTS = [
     ("route: beta sign", "m + beta * sd;", "m - beta * sd;"),
     ("taylor: weight sign", "double w = (double)nk[j] * (1.0 + s[j] - m);", "double w = (double)nk[j] * (1.0 - s[j] + m);"),
     ("taylor: block size dropped", "double w = (double)nk[j] * (1.0 + s[j] - m);", "double w = (1.0 + s[j] - m);"),
+    ("taylor: expansion point shifted", "double w = (double)nk[j] * (1.0 + s[j] - m);",
+     "double w = (double)nk[j] * (1.0 + s[j] - m - 0.05);"),
     ("taylor: pooled K instead of V", "const double* vb = vp + (bh * NKB + j) * d;", "const double* vb = kp + (bh * NKB + j) * d;"),
     ("sparse: factor sign", "double f = exp(mu[t] - M);", "double f = exp(M - mu[t]);"),
     ("sparse: Taylor mass missing in den", "den += f * W[t];", ""),
@@ -68,6 +70,7 @@ PINS = [
     pins.test_sparse_without_taylor_equals_masked_library_attention,
     pins.test_taylor_hand_derived_closed_form,
     pins.test_taylor_constant_v_and_unit_mass,
+    pins.test_taylor_term_converges_quadratically_to_exact_attention,
     lambda: pins.test_na3d_matches_masked_library_attention(*pins.NA_CASES[0]),
     lambda: pins.test_na3d_matches_masked_library_attention(*pins.NA_CASES[1]),
     lambda: pins.test_na3d_window_indicator(*pins.NA_CASES[0]),

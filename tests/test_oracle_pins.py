@@ -336,6 +336,50 @@ def test_taylor_hand_derived_closed_form():
     np.testing.assert_allclose(lse[0, 0, 3], 0.4 + math.log(2 + 2 * r1), atol=1e-14)
 
 
+def test_taylor_term_converges_quadratically_to_exact_attention():
+    """The Taylor term is a first-order expansion of exp about the row-mean proxy
+    score, so it must agree with exact softmax attention up to second-order terms.
+
+    Self-attention over S = 90 tokens in blocks of 16 (the last block ragged, 10
+    tokens).  Every query row is the same unit vector and the keys are identical
+    inside each key block, so every token score equals its block's proxy score,
+    mu + delta * t_j (t_j fixed, |t_j| <= 1), for every row.  Query block i keeps
+    only key block i; the others go through the Taylor term.  Exact attention over
+    all keys and the Taylor-corrected output then differ by O(delta^2): shrinking
+    delta tenfold must shrink the error about a hundredfold.  A dropped term, a
+    wrong sign or a missing block-size factor n_j would leave an error of order
+    delta or 1."""
+    b, d, S = 16, 8, 90
+    nkb = (S + b - 1) // b
+    t = np.array([0.9, -0.5, 0.3, -0.8, 0.6, -0.2])
+    rng = np.random.default_rng(11)
+    vblk = rng.standard_normal((nkb, d))
+    rest = rng.standard_normal((nkb, d - 1))
+    sel = np.eye(nkb, dtype=bool)[None, None]
+    errs, lerrs = [], []
+    for delta in (1e-1, 1e-2, 1e-3):
+        q = np.zeros((1, 1, S, d))
+        q[..., 0] = 1.0                                   # score = the key's first coordinate
+        kblk = np.concatenate([(0.7 + delta * t)[:, None], rest], axis=1)
+        k = np.repeat(kblk, b, axis=0)[:S][None, None]
+        v = np.repeat(vblk, b, axis=0)[:S][None, None]
+        qp, kp, vp = (oracle.block_pool(x, b) for x in (q, k, v))
+        forced = oracle.route(qp, kp, vp, S, b, 1.0, 0.0, force_sel=sel)
+        np.testing.assert_allclose(forced["proxy"][0, 0], np.tile(0.7 + delta * t, (nkb, 1)), atol=1e-14)
+        out, lse = oracle.sparse_attention(q, k, v, b, b, sel, forced["mu"], forced["W"], forced["T"], 1.0)
+        s_tok = np.repeat(0.7 + delta * t, b)[:S]
+        p = np.exp(s_tok - s_tok.max())
+        exact = (p[:, None] * v[0, 0]).sum(0) / p.sum()
+        exact_lse = s_tok.max() + math.log(p.sum())
+        errs.append(np.abs(out[0, 0] - exact).max())
+        lerrs.append(np.abs(lse[0, 0] - exact_lse).max())
+    for e in (errs, lerrs):
+        assert e[2] < 1e-6, e
+        for m in (0, 1):
+            ratio = e[m] / e[m + 1]
+            assert 60 < ratio < 160, (e, ratio)
+
+
 def test_taylor_constant_v_and_unit_mass():
     # with V constant, num = c * den exactly in exact arithmetic: the output is that constant,
     # i.e. the selected probabilities plus the Taylor mass sum to one
