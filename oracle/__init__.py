@@ -20,8 +20,9 @@ to the pages.  3D neighbourhood attention follows the published definition of
 neighbourhood attention (the pages name the kernel but do not define it) and
 is pinned by closed forms, an independent brute force and a mirror symmetry.
 The FP8 (E4M3) codec, the per-row activation quantiser and the scaled FP8
-product are pinned by torch's float8_e4m3fn conversion, a nearest-value search
-and numpy's matmul.
+product are pinned by torch's float8_e4m3fn conversion, a nearest-value search,
+exact rational arithmetic (Python fractions) for the quantiser's codes, and
+numpy's matmul.
 """
 from __future__ import annotations
 
@@ -70,7 +71,7 @@ def _configure(lib):
                                      _I64, _i64, _D, _D]
     lib.oracle_e4m3_decode.argtypes = [ctypes.c_uint8]
     lib.oracle_e4m3_decode.restype = ctypes.c_double
-    lib.oracle_e4m3_encode.argtypes = [ctypes.c_float]
+    lib.oracle_e4m3_encode.argtypes = [ctypes.c_double]
     lib.oracle_e4m3_encode.restype = ctypes.c_uint8
     _F = ctypes.POINTER(ctypes.c_float)
     lib.oracle_fp8_quantize_rows.argtypes = [_F, _i64, _i64, _U8, _F]
@@ -268,15 +269,18 @@ def e4m3_decode(codes):
 
 
 def e4m3_encode(values):
-    """E4M3 codes (uint8) of float32 values: nearest, ties to even, saturating at 448."""
+    """E4M3 codes (uint8) of values (taken as float64): nearest, ties to even, saturating at 448."""
     lib = _load()
-    v = np.asarray(values, dtype=np.float32)
+    v = np.asarray(values, dtype=np.float64)
     return np.vectorize(lambda x: lib.oracle_e4m3_encode(float(x)), otypes=[np.uint8])(v) if v.size else \
         np.zeros(v.shape, dtype=np.uint8)
 
 
 def fp8_quantize_rows(x):
-    """Per-row E4M3 quantisation of x [M, K] (float32 values): (codes uint8 [M, K], scale float32 [M])."""
+    """Per-row E4M3 quantisation of x [M, K] (float32 values): (codes uint8 [M, K], scale float32 [M]).
+
+    scale[m] = amax_m / 448 (nearest float); codes are the E4M3 values nearest to the exact quotient
+    x * 448 / amax_m, ties to even; rows whose scale is zero or not a normal float quantise to zeros."""
     x = np.ascontiguousarray(np.asarray(x, dtype=np.float32))
     if x.ndim != 2:
         raise ValueError("expected [M, K]")

@@ -47,8 +47,10 @@
  *    window found by a different construction, and a mirror symmetry.
  *  - oracle_e4m3_encode / oracle_e4m3_decode / oracle_fp8_quantize_rows /
  *    oracle_fp8_gemm: pinned by torch's float8_e4m3fn conversion, a
- *    nearest-value search over the code table, the quantiser's error bound
- *    and numpy's matmul of the decoded operands.
+ *    nearest-value search over the code table, codes computed in exact
+ *    rational arithmetic (including inputs placed next to rounding
+ *    midpoints), the quantiser's error bound and numpy's matmul of the
+ *    decoded operands.
  *  - oracle_route (Taylor aggregates W, T) and oracle_sparse_rows: the pages
  *    give no formula for the Taylor term.  The first-order block-level form
  *    used here is a reading of the page; it is pinned against exact softmax
@@ -411,14 +413,14 @@ double oracle_e4m3_decode(uint8_t c) {
   return sgn ? -mag : mag;
 }
 
-/* Round a finite value to the nearest E4M3 value, ties to the even code
- * (mantissa LSB 0), and saturate magnitudes beyond 448 to 448.  NaN maps to
- * the NaN code 0x7f.  The arithmetic below is exact in double for any float
- * input: scaling by powers of two and taking the fractional mantissa. */
-uint8_t oracle_e4m3_encode(float v) {
+/* Round a value to the nearest E4M3 value, ties to the even code (mantissa
+ * LSB 0), and saturate magnitudes beyond 448 to 448.  NaN maps to the NaN code
+ * 0x7f.  The arithmetic below is exact in double: scaling by powers of two and
+ * taking the fractional mantissa. */
+uint8_t oracle_e4m3_encode(double v) {
   if (isnan(v)) return 0x7f;
   const uint8_t sgn = signbit(v) ? 0x80 : 0x00;
-  const double a = fabs((double)v);
+  const double a = fabs(v);
   if (a >= 448.0) return sgn | 0x7e;
   if (a < ldexp(1.0, -6)) {
     /* subnormal grid: multiples of 2^-9; 8 * 2^-9 is the smallest normal, code 0x08 */
@@ -437,35 +439,38 @@ uint8_t oracle_e4m3_encode(float v) {
   return sgn | (uint8_t)(((e + 7) << 3) | (int)r);
 }
 
-/* Per-row activation quantisation.  x: [M][K] (bf16 values widened to float).
- * For each row: amax = max |x| (float), inv = 448 / amax and scale = amax / 448
- * (float divisions, once per row), code = e4m3(x * inv) (float product, then
- * round-to-nearest-even with saturation).  The row max lands on +-448 and
- * x ~ scale * dec(code).  A row of zeros, or a row so small that 448 / amax
- * overflows the float range, gets scale 0 and zero codes.  The arithmetic is
- * single precision because it decides the integer codes, exactly as the GPU
- * decides them. */
+/* Per-row activation quantisation ("a separate scale for each row").  x:
+ * [M][K] (bf16 values widened to float).  For row m:
+ *   amax = max_k |x_mk|
+ *   s_m  = amax / 448           (the dequantisation scale, stored as float)
+ *   code = E4M3 value nearest to the exact quotient x_mk / (amax / 448)
+ *        = x_mk * 448 / amax    (ties to the even code)
+ * so the row max maps to +-448 and x ~ s_m * dec(code).  The code is decided
+ * on the exact quotient, not on a rounded scale: the quotient is formed in
+ * double, where x * 448 is exact and the one rounding of the division cannot
+ * carry a value across an E4M3 rounding midpoint (a midpoint has at most five
+ * significant bits, so a quotient of float-significand numbers that is not a
+ * midpoint lies farther from it than one double ulp; one that is a midpoint is
+ * computed exactly).  s_m is the float nearest to amax / 448.  A row of zeros,
+ * or a row whose scale is not a normal float (amax / 448 < 2^-126), gets
+ * s_m = 0 and zero codes. */
 void oracle_fp8_quantize_rows(const float* x, int64_t M, int64_t K, uint8_t* q, float* scale) {
 #pragma omp parallel for schedule(static)
   for (int64_t m = 0; m < M; ++m) {
     const float* row = x + m * K;
-    float amax = 0.0f;
+    double amax = 0.0;
     for (int64_t k = 0; k < K; ++k) {
-      const float a = fabsf(row[k]);
+      const double a = fabs((double)row[k]);
       if (a > amax) amax = a;
     }
-    volatile float inv = amax > 0.0f ? 448.0f / amax : 0.0f;
-    if (!(amax > 0.0f) || isinf(inv)) {
+    const float s = (float)(amax / 448.0);
+    if (!(s >= ldexp(1.0, -126))) {
       scale[m] = 0.0f;
       for (int64_t k = 0; k < K; ++k) q[m * K + k] = 0;
       continue;
     }
-    volatile float s = amax / 448.0f;
     scale[m] = s;
-    for (int64_t k = 0; k < K; ++k) {
-      volatile float v = row[k] * inv;
-      q[m * K + k] = oracle_e4m3_encode(v);
-    }
+    for (int64_t k = 0; k < K; ++k) q[m * K + k] = oracle_e4m3_encode((double)row[k] * 448.0 / amax);
   }
 }
 

@@ -46,9 +46,13 @@ MUTANTS = [
     ("e4m3: ties away from zero", "double r = nearbyint((m - 1.0) * 8.0);", "double r = round((m - 1.0) * 8.0);"),
     ("e4m3: truncation", "double r = nearbyint((m - 1.0) * 8.0);", "double r = floor((m - 1.0) * 8.0);"),
     ("e4m3: no saturation", "if (a >= 448.0) return sgn | 0x7e;", "if (a >= 480.0) return sgn | 0x7e;"),
-    ("quant: scale over 240", "volatile float s = amax / 448.0f;", "volatile float s = amax / 240.0f;"),
-    ("quant: inverse scale over 240", "volatile float inv = amax > 0.0f ? 448.0f / amax : 0.0f;",
-     "volatile float inv = amax > 0.0f ? 240.0f / amax : 0.0f;"),
+    ("quant: scale over 240", "const float s = (float)(amax / 448.0);", "const float s = (float)(amax / 240.0);"),
+    ("quant: quotient over 240", "(double)row[k] * 448.0 / amax", "(double)row[k] * 240.0 / amax"),
+    ("quant: code from the float product with the rounded inverse scale", "(double)row[k] * 448.0 / amax",
+     "(double)(row[k] * (448.0f / (float)amax))"),
+    ("quant: code from the float quotient by the rounded scale", "(double)row[k] * 448.0 / amax",
+     "(double)(row[k] / s)"),
+    ("quant: subnormal scales kept", "if (!(s >= ldexp(1.0, -126))) {", "if (!(s > 0.0f)) {"),
     ("gemm: weight scale dropped", "const double f = (double)sa[m] * (double)sw[n];", "const double f = (double)sa[m];"),
     ("gemm: weight transposed", "lut[wq[n * K + k]]", "lut[wq[(k % N) * K + (n % K)]]"),
     ("na: no normalisation", "o[c] /= l;\n      lse[r] = M + log(l);", "\n      lse[r] = M + log(l);"),
@@ -82,6 +86,7 @@ PINS = [
     pins.test_e4m3_encode_saturates,
     pins.test_e4m3_encode_is_the_nearest_value_ties_to_even,
     pins.test_quantize_rows_error_bound_and_row_max,
+    pins.test_quantize_rows_codes_are_the_exact_quotients_nearest_value,
     pins.test_fp8_gemm_matches_library_matmul_of_decoded_operands,
 ]
 

@@ -4,8 +4,10 @@ Each test checks the oracle against something other than itself, chosen so
 that a plausible slip (a dropped term, a wrong sign or index, a transposed
 operand, an off-by-one chunk bound) fails at least one of them.  CPU only.
 """
+import bisect
 import math
 import os
+from fractions import Fraction
 
 import numpy as np
 import pytest
@@ -575,12 +577,82 @@ def test_e4m3_encode_saturates():
     np.testing.assert_array_equal(oracle.e4m3_encode(-big), 0xfe)
 
 
+# Positive finite E4M3 values in code order (codes 0x00..0x7e are increasing), decoded by torch.
+_E4M3_POS = [Fraction(float(v)) for v in torch_e4m3_values(np.arange(0x7f))]
+
+
+def exact_e4m3_code(value: Fraction, negative: bool) -> int:
+    """E4M3 code of an exact rational: the nearest value, ties to the even code, saturating at 448
+    (a search over torch's decoding of the code table, in exact arithmetic)."""
+    a = abs(value)
+    sgn = 0x80 if negative else 0
+    if a >= _E4M3_POS[-1]:
+        return sgn | 0x7e
+    hi = bisect.bisect_left(_E4M3_POS, a)
+    if _E4M3_POS[hi] == a:
+        return sgn | hi
+    lo = hi - 1
+    dlo, dhi = a - _E4M3_POS[lo], _E4M3_POS[hi] - a
+    if dlo != dhi:
+        return sgn | (lo if dlo < dhi else hi)
+    return sgn | (lo if lo % 2 == 0 else hi)
+
+
+def exact_quantize_row(row):
+    """The per-row quantiser's definition in exact rational arithmetic: s = amax / 448 (nearest
+    float), codes nearest to x * 448 / amax.  Returns (codes, s, amax) for a row with a normal scale."""
+    amax = max(abs(Fraction(float(x))) for x in row)
+    codes = np.array([exact_e4m3_code(Fraction(float(x)) * 448 / amax, math.copysign(1.0, float(x)) < 0)
+                      for x in row], dtype=np.uint8)
+    return codes, np.float32(float(amax / 448)), amax
+
+
+def near_midpoint_rows():
+    """Rows whose values sit exactly on, or one float step either side of, the inputs whose exact
+    quotient x * 448 / amax is an E4M3 rounding midpoint; each row holds its amax as the row max."""
+    mids = [(a + b) / 2 for a, b in zip(_E4M3_POS[:-1], _E4M3_POS[1:])]
+    rows = []
+    for amax in (3.0, 5.0, 7.0, 11.0, 0.3, 1.7, 2.9, 6.1, 123.456, 0.0123, 1.1e-3, 37.5):
+        a32 = np.float32(amax)
+        row = [a32]
+        for m in mids[::3]:
+            t = np.float32(float(m * Fraction(float(a32)) / 448))
+            for c in (np.nextafter(t, np.float32(-np.inf)), t, np.nextafter(t, np.float32(np.inf))):
+                if 0 < c < a32:
+                    row += [c, -c]
+        rows.append(np.array(row, dtype=np.float32))
+    return rows
+
+
+def test_quantize_rows_codes_are_the_exact_quotients_nearest_value():
+    """Codes against the definition in exact rational arithmetic, on inputs placed next to rounding
+    midpoints: there a float-rounded scale or inverse scale would move the quotient across the
+    midpoint, so this separates the exact quotient from single-precision shortcuts."""
+    rows = near_midpoint_rows()
+    n_product_differs = n_quotient_differs = 0
+    for row in rows:
+        q, s = oracle.fp8_quantize_rows(row[None, :])
+        codes, s_exact, amax = exact_quantize_row(row)
+        assert s[0] == s_exact
+        np.testing.assert_array_equal(q[0], codes)
+        # how often the two single-precision shortcuts would decide otherwise (the pin must see some)
+        a32 = np.float32(float(amax))
+        inv32 = np.float32(448.0) / a32
+        for x, c in zip(row, codes):
+            by_product = exact_e4m3_code(Fraction(float(np.float32(x * inv32))), x < 0)
+            by_quotient = exact_e4m3_code(Fraction(float(np.float32(x / s_exact))), x < 0)
+            n_product_differs += by_product != c
+            n_quotient_differs += by_quotient != c
+    assert n_product_differs >= 5 and n_quotient_differs >= 5, (n_product_differs, n_quotient_differs)
+
+
 def test_quantize_rows_error_bound_and_row_max():
     rng = np.random.default_rng(7)
     x = rng.standard_normal((37, 300)).astype(np.float32) * np.exp(rng.uniform(-8, 8, (37, 1))).astype(np.float32)
     x[3] = 0.0                                             # a row of zeros
     x[4, :] = 0.0
     x[4, 17] = -2.5                                        # a single non-zero
+    x[6] = torch.from_numpy(x[6]).bfloat16().float().numpy()     # bf16 values, as the GPU's inputs are
     q, s = oracle.fp8_quantize_rows(x)
     dq = oracle.e4m3_decode(q) * s[:, None].astype(np.float64)
     amax = np.abs(x).max(axis=1)
@@ -588,24 +660,30 @@ def test_quantize_rows_error_bound_and_row_max():
         if amax[m] == 0:
             assert s[m] == 0 and (q[m] == 0).all()
             continue
-        # scale = amax / 448 in single precision, and the row max lands on +-448 (code 0x7e / 0xfe)
-        assert s[m] == np.float32(amax[m]) / np.float32(448.0)
-        # codes are e4m3(x * (448 / amax)) with both operations in single precision: torch's conversion
-        inv = np.float32(448.0) / np.float32(amax[m])
-        lib = torch.from_numpy((x[m] * inv).astype(np.float32)).clamp(-448, 448).to(torch.float8_e4m3fn)
-        np.testing.assert_array_equal(q[m], lib.view(torch.uint8).numpy())
+        # the definition in exact arithmetic: scale = amax / 448 (nearest float), codes nearest to x * 448 / amax
+        codes, s_exact, _ = exact_quantize_row(x[m])
+        assert s[m] == s_exact
+        np.testing.assert_array_equal(q[m], codes)
+        # and against torch's float -> E4M3 conversion of the quotient (in double, then to float: no value
+        # of this row lies next to a midpoint)
+        lib = torch.from_numpy(x[m].astype(np.float64) * 448.0 / float(amax[m])).float().clamp(-448, 448)
+        np.testing.assert_array_equal(q[m], lib.to(torch.float8_e4m3fn).view(torch.uint8).numpy())
         j = int(np.argmax(np.abs(x[m])))
         assert q[m, j] & 0x7f == 0x7e
         # relative error <= 2^-4 for normal codes, absolute <= scale * 2^-10 on the subnormal grid (+ the
-        # single-precision division before rounding)
+        # rounding of the scale to float)
         err = np.abs(dq[m] - x[m].astype(np.float64))
         bound = np.maximum(np.abs(x[m]) * 2.0 ** -4, s[m] * 2.0 ** -10) * (1 + 1e-6)
         assert (err <= bound).all()
-    # a row too small for 448 / amax to stay finite is treated as zero
-    tiny = np.zeros((1, 32), dtype=np.float32)
+    # a row whose scale amax / 448 is below the smallest normal float (2^-126) is treated as zero;
+    # one just above it is quantised
+    tiny = np.zeros((3, 32), dtype=np.float32)
     tiny[0, 5] = np.float32(1e-39)
+    tiny[1, 5] = np.float32(448 * 2.0 ** -126 * 0.999)
+    tiny[2, 5], tiny[2, 6] = np.float32(448 * 2.0 ** -126 * 1.001), np.float32(448 * 2.0 ** -126 * 0.3)
     tq, ts = oracle.fp8_quantize_rows(tiny)
-    assert ts[0] == 0 and (tq == 0).all()
+    assert ts[0] == 0 and ts[1] == 0 and (tq[:2] == 0).all()
+    assert ts[2] >= np.float32(2.0 ** -126) and tq[2, 5] == 0x7e and tq[2, 6] == exact_quantize_row(tiny[2])[0][6]
     # the lone non-zero is the row max: code -448, dequantised to -448 * fl32(2.5 / 448)
     assert q[4, 17] == 0xfe and dq[4, 17] == -448.0 * float(s[4]) and abs(dq[4, 17] + 2.5) < 2.5 * 2.0 ** -23
     assert (q[4, np.arange(300) != 17] == 0).all()
