@@ -319,9 +319,12 @@ attn_status_t attn_sparse_route_fwd_noalloc(const attn_bf16* q, const attn_bf16*
 
 /*
  * Synchronises `stream`, reads and clears the current device's status word.
- * Returns ATTN_OK, ATTN_ERR_TIMEOUT if a kernel gave up on a barrier wait,
- * ATTN_ERR_INVALID_ARG if a kernel met a corrupt selected-block list, or
- * ATTN_ERR_CUDA if the synchronisation itself failed.
+ * Returns ATTN_OK, ATTN_ERR_TIMEOUT if a kernel gave up on a barrier wait
+ * (every wait has a 2 s limit; once one wait of a launch gives up, the rest
+ * of that launch's CTAs stop waiting and return, so the launch ends soon
+ * after), ATTN_ERR_INVALID_ARG if a kernel met a corrupt selected-block list
+ * or (bounds-checked build only) skipped a store outside its output buffer,
+ * or ATTN_ERR_CUDA if the synchronisation itself failed.
  */
 attn_status_t attn_last_device_status(cudaStream_t stream);
 
@@ -336,6 +339,19 @@ const char* attn_status_string(attn_status_t status);
  * ATTN_ERR_TIMEOUT.  Leaves the context usable.
  */
 attn_status_t attn_selftest_wait_timeout(int limit_us, cudaStream_t stream);
+
+/*
+ * Self-test of the launch-wide abort: launches `n_ctas` CTAs (1..65536), each
+ * holding 160 KB of shared memory so that one runs per SM and the grid runs in
+ * waves, and each waiting on a barrier nothing arrives on with a limit of
+ * `limit_us` microseconds (1..1000000).  The first wait to give up records the
+ * timeout and marks the launch aborted; the CTAs still waiting give up within
+ * tens of microseconds and the CTAs that start afterwards return at once, so
+ * the launch ends about one limit after it starts instead of one limit per
+ * wave.  A following attn_last_device_status returns ATTN_ERR_TIMEOUT; the
+ * context stays usable, and later launches are not affected.
+ */
+attn_status_t attn_selftest_wait_timeout_grid(int limit_us, int n_ctas, cudaStream_t stream);
 
 #ifdef __cplusplus
 }

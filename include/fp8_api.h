@@ -28,12 +28,14 @@ extern "C" {
 /*
  * Per-row quantisation.  For row m of x [M][K] (bf16, row-major):
  *   amax_m   = max_k |x[m][k]|
- *   scale[m] = amax_m / 448,  inv_m = 448 / amax_m   (fp32 divisions)
- *   q[m][k]  = e4m3(x[m][k] * inv_m)             (fp32 product, then round to
- *              nearest, ties to even, saturating at +-448)
+ *   scale[m] = amax_m / 448                     (the nearest fp32 value)
+ *   q[m][k]  = the E4M3 value nearest to the exact quotient x[m][k] * 448 / amax_m,
+ *              ties to even (bit-exact: the kernel multiplies by the rounded
+ *              inverse scale and re-forms the quotient with a correctly rounded
+ *              division wherever that product lies next to a rounding midpoint)
  * so the row's largest magnitude maps to +-448 and x ~ scale[m] * q.  A row of
- * zeros, or one with amax < 448 / FLT_MAX (inv_m overflows), gets scale 0 and
- * zero codes.  NaN inputs are not supported.
+ * zeros, or one whose scale is not a normal float (amax_m / 448 < 2^-126), gets
+ * scale 0 and zero codes.  NaN inputs are not supported.
  *   x      device, 16-byte aligned, [M][K] bf16.
  *   q      device, 16-byte aligned, [M][K] E4M3 codes (uint8).
  *   scale  device, [M] fp32.

@@ -1,9 +1,14 @@
 """GPU parity of the FP8 projection path against the oracle, through the C ABI.
 
-The quantiser's codes and scales must be bit-identical to the oracle's (both
-take the decisions in fp32).  The scaled product is compared element by
-element with the bound |y_gpu - y| <= 2^-8 |y| + K 2^-24 sum|terms|: the bf16
-rounding of the output plus the worst case of fp32 accumulation over K terms.
+The quantiser's codes and scales must be bit-identical to the oracle's, which
+takes each code as the E4M3 value nearest to the exact quotient x * 448 / amax.
+The kernel decides most codes from the product with a rounded inverse scale and
+re-forms the quotient exactly where that product lies next to a rounding
+midpoint; rows built to hit exact midpoints (amax with significand 3, 5, 7, ...
+and small-integer multiples) exercise that path.  The scaled product is
+compared element by element with the bound |y_gpu - y| <= 2^-8 |y| + K 2^-24
+sum|terms|: the bf16 rounding of the output plus the worst case of fp32
+accumulation over K terms.
 """
 import numpy as np
 import pytest
@@ -42,11 +47,41 @@ def test_quantize_rows_bit_exact(M, K):
     x[min(3, M - 1)] = 0                                      # a zero row
     if M > 5:
         x[5] *= 1e-4                                          # tiny values: subnormal codes
+    if M > 8:
+        x[8:] = midpoint_rows(M - 8, K, seed=M).to(x.device)  # exact E4M3 rounding midpoints
     q, s = vd.fp8_quantize_rows(x)
     torch.cuda.synchronize()
-    rq, rs = oracle.fp8_quantize_rows(f32(x))
+    xh = f32(x)
+    rq, rs = oracle.fp8_quantize_rows(xh)
     np.testing.assert_array_equal(s.cpu().numpy(), rs)
     np.testing.assert_array_equal(q.cpu().numpy(), rq)
+    ties = exact_midpoint_count(xh)
+    print(f"quantize {M}x{K}: {ties} elements whose exact quotient is an E4M3 rounding midpoint")
+    if M > 8:
+        assert ties > 0
+
+
+def midpoint_rows(n, K, seed):
+    """bf16 rows whose row max has significand 3, 5, 7, ... and whose other values are small-integer
+    multiples of a power of two: many quotients x * 448 / amax land exactly on E4M3 rounding midpoints,
+    where a product with the rounded inverse scale 448 / amax would round the wrong way."""
+    g = torch.Generator(device="cpu").manual_seed(seed)
+    amax = torch.tensor([3.0, 5.0, 7.0, 11.0, 13.0, 0.375, 1.25, 6.5, 3e-3, 5e4])
+    rows = torch.randint(-64, 65, (n, K), generator=g).float()
+    rows *= 2.0 ** torch.randint(-9, -1, (n, 1), generator=g).float()
+    a = amax[torch.randint(0, amax.numel(), (n,), generator=g)] * 2.0 ** torch.randint(-4, 4, (n,), generator=g)
+    rows = torch.maximum(torch.minimum(rows * a[:, None] / 3.0, a[:, None]), -a[:, None])
+    rows[:, 0] = a
+    return rows.bfloat16()
+
+
+def exact_midpoint_count(x):
+    """Elements of x [M, K] (float32) whose exact quotient x * 448 / amax is an E4M3 rounding midpoint."""
+    amax = np.abs(x).max(axis=1, keepdims=True).astype(np.float64)
+    v = np.abs(x.astype(np.float64)) * 448.0 / np.where(amax > 0, amax, 1.0)
+    pos = np.sort(np.unique(oracle.e4m3_decode(np.arange(0x7f, dtype=np.uint8))))
+    mids = (pos[:-1] + pos[1:]) / 2
+    return int(np.isin(v, mids).sum())
 
 
 @pytest.mark.parametrize("M,N,K", [

@@ -7,6 +7,7 @@ output element.  Tolerances: max-abs 2e-2 and relative L2 5e-3 on outputs
 band around tau.
 """
 import math
+import time
 
 import numpy as np
 import pytest
@@ -271,9 +272,11 @@ def test_fused_local_workload_ragged(d, block, beta):
 
 
 def test_fused_agrees_with_two_kernel_path_and_dense():
-    q, k, v = rnd_qkv(2, 2, 1000, 1000, 128, seed=47, std=1.0)
-    o1, l1, r1 = vd.attn_sparse_route_fwd(q, k, v, 0.6, block=128, route=True)
-    o2, l2, r2 = vd.attn_sparse_fused_fwd(q, k, v, 0.6, block=128, route=True)
+    B, H, S, d, block, beta = 2, 2, 1000, 128, 128, 0.6
+    scale = 1 / math.sqrt(d)
+    q, k, v = rnd_qkv(B, H, S, S, d, seed=47, std=1.0)
+    o1, l1, r1 = vd.attn_sparse_route_fwd(q, k, v, beta, block=block, route=True)
+    o2, l2, r2 = vd.attn_sparse_fused_fwd(q, k, v, beta, block=block, route=True)
     torch.cuda.synchronize()
     s1 = gpu_selection(r1["sel_idx"], r1["sel_cnt"])
     s2 = gpu_selection(r2["sel_idx"], r2["sel_cnt"])
@@ -281,9 +284,21 @@ def test_fused_agrees_with_two_kernel_path_and_dense():
     if np.array_equal(s1, s2):
         assert_close(host(o2), host(o1), "fused vs two-kernel")
         np.testing.assert_allclose(host(r2["taylor_t"]), host(r1["taylor_t"]), atol=1e-2, rtol=1e-4)
+    # whether or not the two selections agree: each may differ from the oracle's only inside the
+    # near-tau band, and each path's output must match the oracle evaluated on its own selection
+    for b in range(B):
+        qh, kh, vh = (host(x[b:b + 1]) for x in (q, k, v))
+        _, _, ort, (qp, kp, vp) = oracle.sparse_route_attention(qh, kh, vh, block, block, scale, beta, rows=[0])
+        for name, o, l, sel in (("two-kernel", o1, l1, s1), ("fused", o2, l2, s2)):
+            compare_selection(sel[b:b + 1], ort)
+            forced = oracle.route(qp, kp, vp, S, block, scale, beta, force_sel=sel[b:b + 1])
+            ro, rl = oracle.sparse_attention(qh, kh, vh, block, block, sel[b:b + 1], forced["mu"], forced["W"],
+                                             forced["T"], scale)
+            assert_close(host(o[b:b + 1]), ro, f"{name} out, batch {b}")
+            assert_close(host(l[b:b + 1]), rl, f"{name} lse, batch {b}")
     # with every block kept, the fused path runs exactly the dense arithmetic
     od, ld = vd.attn_dense_fwd(q, k, v)
-    of, lf = vd.attn_sparse_fused_fwd(q, k, v, -math.inf, block=128)
+    of, lf = vd.attn_sparse_fused_fwd(q, k, v, -math.inf, block=block)
     torch.cuda.synchronize()
     assert torch.equal(of, od) and torch.equal(lf, ld)
 
@@ -299,6 +314,32 @@ def test_bounded_wait_reports_timeout_and_context_survives():
     torch.cuda.synchronize()
     ro, _ = oracle.attention(host(q), host(k), host(v), 1 / 8)
     assert_close(host(out), ro, "dense after timeout self-test")
+
+
+def test_launch_wide_abort_ends_a_broken_launch_quickly():
+    # 16 waves of one CTA per SM, every CTA waiting on a barrier nothing arrives on with a 20 ms limit:
+    # waited out wave by wave that would take >= 320 ms; with the launch-wide abort the first timeout
+    # stops the CTAs still waiting and the later waves return at once, so the launch takes ~20 ms
+    vd.attn_selftest_wait_timeout(10)                    # loads the module; its timeout is read and cleared
+    assert vd.attn_last_device_status() == 5
+    n_sm = torch.cuda.get_device_properties(0).multi_processor_count
+    limit_us, waves = 20000, 16
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    vd.attn_selftest_wait_timeout_grid(limit_us, waves * n_sm)
+    status = vd.attn_last_device_status()
+    elapsed = time.perf_counter() - t0
+    assert status == 5
+    assert elapsed < 0.1, f"aborted launch took {elapsed * 1e3:.1f} ms"
+    print(f"aborted launch of {waves * n_sm} CTAs ended after {elapsed * 1e3:.1f} ms (wait limit {limit_us / 1e3} ms)")
+    assert vd.attn_last_device_status() == 0
+    # later launches carry their own ids and are not affected
+    q, k, v = rnd_qkv(1, 2, 300, 517, 128, seed=2)
+    out, lse = vd.attn_dense_fwd(q, k, v)
+    torch.cuda.synchronize()
+    ro, rl = oracle.attention(host(q), host(k), host(v), 1 / math.sqrt(128))
+    assert_close(host(out), ro, "dense after an aborted launch")
+    assert_close(host(lse), rl, "dense lse after an aborted launch")
 
 
 # ---------------------------------------------------------------- split-KV with the merge in the tail

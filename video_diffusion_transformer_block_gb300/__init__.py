@@ -19,7 +19,7 @@ import torch
 __all__ = [
     "AttnError", "load_library", "attn_dense_fwd", "attn_cross_splitkv_fwd", "attn_lse_merge", "attn_block_pool",
     "attn_sparse_workspace_bytes", "attn_sparse_route_fwd", "attn_sparse_route", "attn_sparse_fwd",
-    "attn_last_device_status", "attn_status_string", "attn_selftest_wait_timeout",
+    "attn_last_device_status", "attn_status_string", "attn_selftest_wait_timeout", "attn_selftest_wait_timeout_grid",
     "attn_sparse_route_fwd_noalloc", "attn_sparse_fused_fwd", "attn_na3d_fwd", "attn_na3d_plan",
     "fp8_quantize_rows", "fp8_scaled_gemm", "fp8_linear", "attn_cross_fwd", "attn_cross_workspace_bytes",
     "NOALLOC_WORKSPACE_BYTES", "EXPORTED_SYMBOLS",
@@ -33,8 +33,9 @@ _lib = None
 EXPORTED_SYMBOLS = (
     "attn_dense_fwd", "attn_cross_splitkv_fwd", "attn_lse_merge", "attn_block_pool", "attn_sparse_workspace_bytes",
     "attn_sparse_route_fwd", "attn_sparse_route", "attn_sparse_fwd", "attn_last_device_status", "attn_status_string",
-    "attn_selftest_wait_timeout", "attn_sparse_route_fwd_noalloc", "attn_sparse_fused_fwd", "attn_na3d_fwd",
-    "attn_na3d_plan", "fp8_quantize_rows", "fp8_scaled_gemm", "attn_cross_fwd", "attn_cross_workspace_bytes",
+    "attn_selftest_wait_timeout", "attn_selftest_wait_timeout_grid", "attn_sparse_route_fwd_noalloc",
+    "attn_sparse_fused_fwd", "attn_na3d_fwd", "attn_na3d_plan", "fp8_quantize_rows", "fp8_scaled_gemm",
+    "attn_cross_fwd", "attn_cross_workspace_bytes",
 )
 
 # Size of the library-owned scratch of attn_sparse_route_fwd_noalloc (ATTN_NOALLOC_WORKSPACE_BYTES).
@@ -85,9 +86,11 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         lib.attn_status_string.argtypes = [i]
         lib.attn_status_string.restype = ctypes.c_char_p
         lib.attn_selftest_wait_timeout.argtypes = [i, vp]
+        lib.attn_selftest_wait_timeout_grid.argtypes = [i, i, vp]
         for name in ("attn_dense_fwd", "attn_cross_splitkv_fwd", "attn_lse_merge", "attn_block_pool",
                      "attn_sparse_route_fwd", "attn_sparse_route", "attn_sparse_fwd", "attn_last_device_status",
-                     "attn_selftest_wait_timeout", "attn_sparse_route_fwd_noalloc", "attn_sparse_fused_fwd",
+                     "attn_selftest_wait_timeout", "attn_selftest_wait_timeout_grid", "attn_sparse_route_fwd_noalloc",
+                     "attn_sparse_fused_fwd",
                      "attn_na3d_fwd", "attn_na3d_plan", "fp8_quantize_rows", "fp8_scaled_gemm", "attn_cross_fwd"):
             getattr(lib, name).restype = ctypes.c_int
         if path is None:
@@ -396,3 +399,8 @@ def attn_last_device_status(stream=None) -> int:
 
 def attn_selftest_wait_timeout(limit_us: int, stream=None):
     _check("attn_selftest_wait_timeout", load_library().attn_selftest_wait_timeout(int(limit_us), _stream(stream)))
+
+
+def attn_selftest_wait_timeout_grid(limit_us: int, n_ctas: int, stream=None):
+    _check("attn_selftest_wait_timeout_grid",
+           load_library().attn_selftest_wait_timeout_grid(int(limit_us), int(n_ctas), _stream(stream)))

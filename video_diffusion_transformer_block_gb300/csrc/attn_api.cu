@@ -4,7 +4,9 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
+#include <nvtx3/nvToolsExt.h>
 #include <math.h>
+#include <atomic>
 #include <mutex>
 #include <stdint.h>
 #include <string.h>
@@ -15,8 +17,9 @@
 
 namespace vdtb {
 
-// One status word per device; kernels receive its address.
-__device__ int g_status_word;
+// Two status words per device; kernels receive their address: [0] the status
+// bits, [1] the id of the last launch in which a wait timed out (see ptx.cuh).
+__device__ int g_status_word[2];
 
 namespace {
 
@@ -27,6 +30,28 @@ std::mutex g_status_mutex;
 int* g_status_ptr[kMaxDevices] = {nullptr};
 
 bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+// An NVTX range around each C-ABI call, named after the entry point, so that a
+// profiler can select one call's kernels (e.g. ncu --nvtx --nvtx-include).
+// Without a profiler attached the push/pop are no-ops.
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
+
+// Every launch of a kernel with barrier waits gets its own id (never 0, the
+// abort word's initial value), so a timeout aborts only the launch it
+// happened in.
+std::atomic<unsigned> g_launch_counter{0};
+unsigned next_launch_id() {
+  unsigned id;
+  do {
+    id = g_launch_counter.fetch_add(1u) + 1u;
+  } while (id == 0u);
+  return id;
+}
 
 attn_status_t status_ptr(int** out) {
   int dev = 0;
@@ -183,6 +208,7 @@ FwdParams base_params(int B, int H, int Sq, int Skv, float scale, int mode, int*
   p.n_qg = (Sq + rows_per_cta - 1) / rows_per_cta;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.status = status;
+  p.launch_id = next_launch_id();
   return p;
 }
 
@@ -249,6 +275,7 @@ const char* attn_status_string(attn_status_t status) {
 
 attn_status_t attn_dense_fwd(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v, attn_bf16* out, float* lse,
                              int B, int H, int Sq, int Skv, int d, float scale, cudaStream_t stream) {
+  const NvtxRange nvtx_range("attn_dense_fwd");
   if (!q || !k || !v || !out) return ATTN_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || (lse && ((uintptr_t)lse & 3u)))
     return ATTN_ERR_INVALID_ARG;
@@ -281,6 +308,7 @@ attn_status_t attn_na3d_plan(int T, int Y, int X, int Kt, int Ky, int Kx, int* b
 attn_status_t attn_na3d_fwd(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v, attn_bf16* out, float* lse,
                             int B, int H, int T, int Y, int X, int d, int Kt, int Ky, int Kx, float scale, int brick,
                             int pair_axis, cudaStream_t stream) {
+  const NvtxRange nvtx_range("attn_na3d_fwd");
   if (!q || !k || !v || !out) return ATTN_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || (lse && ((uintptr_t)lse & 3u)))
     return ATTN_ERR_INVALID_ARG;
@@ -318,6 +346,7 @@ attn_status_t attn_na3d_fwd(const attn_bf16* q, const attn_bf16* k, const attn_b
 }
 
 attn_status_t fp8_quantize_rows(const attn_bf16* x, uint8_t* q, float* scale, int M, int K, cudaStream_t stream) {
+  const NvtxRange nvtx_range("fp8_quantize_rows");
   if (!x || !q || !scale || !aligned16(x) || !aligned16(q) || ((uintptr_t)scale & 3u)) return ATTN_ERR_INVALID_ARG;
   if (M < 1 || K < 16 || K % 16 != 0 || K > (1 << 30)) return ATTN_ERR_INVALID_ARG;
   return cuda_status(launch_fp8_quantize_rows(x, q, scale, M, K, stream));
@@ -325,6 +354,7 @@ attn_status_t fp8_quantize_rows(const attn_bf16* x, uint8_t* q, float* scale, in
 
 attn_status_t fp8_scaled_gemm(const uint8_t* aq, const float* a_scale, const uint8_t* wq, const float* w_scale,
                               attn_bf16* y, int M, int N, int K, cudaStream_t stream) {
+  const NvtxRange nvtx_range("fp8_scaled_gemm");
   if (!aq || !a_scale || !wq || !w_scale || !y) return ATTN_ERR_INVALID_ARG;
   if (!aligned16(aq) || !aligned16(wq) || !aligned16(y) || ((uintptr_t)a_scale & 3u) || !aligned16(w_scale))
     return ATTN_ERR_INVALID_ARG;
@@ -335,12 +365,13 @@ attn_status_t fp8_scaled_gemm(const uint8_t* aq, const float* a_scale, const uin
   CUtensorMap ta, tb;
   if ((st = make_map_2d_u8(&ta, aq, K, M, 128, 128)) != ATTN_OK) return st;
   if ((st = make_map_2d_u8(&tb, wq, K, N, 128, 256)) != ATTN_OK) return st;
-  return cuda_status(launch_fp8_gemm(ta, tb, a_scale, w_scale, y, M, N, K, status, stream));
+  return cuda_status(launch_fp8_gemm(ta, tb, a_scale, w_scale, y, M, N, K, status, next_launch_id(), stream));
 }
 
 attn_status_t attn_cross_splitkv_fwd(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v, float* out_part,
                                      float* lse_part, int B, int H, int Sq, int Skv, int d, int n_split, float scale,
                                      cudaStream_t stream) {
+  const NvtxRange nvtx_range("attn_cross_splitkv_fwd");
   if (!q || !k || !v || !out_part || !lse_part) return ATTN_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out_part) || ((uintptr_t)lse_part & 3u))
     return ATTN_ERR_INVALID_ARG;
@@ -371,6 +402,7 @@ size_t attn_cross_workspace_bytes(int B, int H, int Sq, int d, int n_split) {
 attn_status_t attn_cross_fwd(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v, attn_bf16* out, float* lse,
                              int B, int H, int Sq, int Skv, int d, int n_split, float scale, void* workspace,
                              size_t workspace_bytes, cudaStream_t stream) {
+  const NvtxRange nvtx_range("attn_cross_fwd");
   if (!q || !k || !v || !out || !workspace) return ATTN_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(workspace) ||
       (lse && ((uintptr_t)lse & 3u)))
@@ -403,6 +435,7 @@ attn_status_t attn_cross_fwd(const attn_bf16* q, const attn_bf16* k, const attn_
 
 attn_status_t attn_lse_merge(const float* out_part, const float* lse_part, attn_bf16* out, float* lse, int n_split,
                              int B, int H, int Sq, int d, cudaStream_t stream) {
+  const NvtxRange nvtx_range("attn_lse_merge");
   if (!out_part || !lse_part || !out) return ATTN_ERR_INVALID_ARG;
   if (!aligned16(out_part) || ((uintptr_t)lse_part & 3u) || !aligned16(out) || (lse && ((uintptr_t)lse & 3u)))
     return ATTN_ERR_INVALID_ARG;
@@ -414,6 +447,7 @@ attn_status_t attn_lse_merge(const float* out_part, const float* lse_part, attn_
 
 attn_status_t attn_block_pool(const attn_bf16* x, float* x_pool, int B, int H, int S, int d, int block,
                               cudaStream_t stream) {
+  const NvtxRange nvtx_range("attn_block_pool");
   if (!x || !x_pool || !aligned16(x) || !aligned16(x_pool)) return ATTN_ERR_INVALID_ARG;
   if (!sizes_ok(B, H, S)) return ATTN_ERR_INVALID_ARG;
   if (!valid_d(d) || (block != 64 && block != 128)) return ATTN_ERR_UNSUPPORTED;
@@ -495,6 +529,7 @@ attn_status_t attn_sparse_route(const attn_bf16* q, const attn_bf16* k, const at
                                 int d, float scale, float beta, int block_q, int block_k, void* workspace,
                                 size_t workspace_bytes, int32_t* sel_idx, int32_t* sel_cnt, float* stats,
                                 float* taylor_t, cudaStream_t stream) {
+  const NvtxRange nvtx_range("attn_sparse_route");
   SparseArgs a{q, k, v, B, H, S, d, block_q, block_k, scale};
   attn_status_t st = sparse_common_checks(a);
   if (st != ATTN_OK) return st;
@@ -508,6 +543,7 @@ attn_status_t attn_sparse_fwd(const attn_bf16* q, const attn_bf16* k, const attn
                               int B, int H, int S, int d, float scale, int block_q, int block_k,
                               const int32_t* sel_idx, const int32_t* sel_cnt, const float* stats,
                               const float* taylor_t, cudaStream_t stream) {
+  const NvtxRange nvtx_range("attn_sparse_fwd");
   SparseArgs a{q, k, v, B, H, S, d, block_q, block_k, scale};
   attn_status_t st = sparse_common_checks(a);
   if (st != ATTN_OK) return st;
@@ -521,6 +557,7 @@ attn_status_t attn_sparse_route_fwd(const attn_bf16* q, const attn_bf16* k, cons
                                     float* lse, int B, int H, int S, int d, float scale, float beta, int block_q,
                                     int block_k, void* workspace, size_t workspace_bytes, int32_t* sel_idx,
                                     int32_t* sel_cnt, float* stats, float* taylor_t, cudaStream_t stream) {
+  const NvtxRange nvtx_range("attn_sparse_route_fwd");
   SparseArgs a{q, k, v, B, H, S, d, block_q, block_k, scale};
   attn_status_t st = sparse_common_checks(a);
   if (st != ATTN_OK) return st;
@@ -543,6 +580,7 @@ attn_status_t attn_sparse_fused_fwd(const attn_bf16* q, const attn_bf16* k, cons
                                     float* lse, int B, int H, int S, int d, float scale, float beta, int block_q,
                                     int block_k, void* workspace, size_t workspace_bytes, int32_t* sel_idx,
                                     int32_t* sel_cnt, float* stats, float* taylor_t, cudaStream_t stream) {
+  const NvtxRange nvtx_range("attn_sparse_fused_fwd");
   SparseArgs a{q, k, v, B, H, S, d, block_q, block_k, scale};
   attn_status_t st = sparse_common_checks(a);
   if (st != ATTN_OK) return st;
@@ -613,6 +651,7 @@ attn_status_t noalloc_workspace(void** out) {
 attn_status_t attn_sparse_route_fwd_noalloc(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v,
                                             attn_bf16* out, float* lse, int B, int H, int S, int d, float scale,
                                             float beta, int block_q, int block_k, cudaStream_t stream) {
+  const NvtxRange nvtx_range("attn_sparse_route_fwd_noalloc");
   const size_t need = attn_sparse_workspace_bytes(B, H, S, d, block_q, block_k);
   if (need > ATTN_NOALLOC_WORKSPACE_BYTES) return ATTN_ERR_WORKSPACE;
   void* ws = nullptr;
@@ -626,6 +665,7 @@ attn_status_t attn_sparse_route_fwd_noalloc(const attn_bf16* q, const attn_bf16*
 }
 
 attn_status_t attn_last_device_status(cudaStream_t stream) {
+  const NvtxRange nvtx_range("attn_last_device_status");
   int* status = nullptr;
   attn_status_t st = status_ptr(&status);
   if (st != ATTN_OK) return st;
@@ -637,16 +677,27 @@ attn_status_t attn_last_device_status(cudaStream_t stream) {
     if (cudaMemcpy(status, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) return ATTN_ERR_CUDA;
   }
   if (word & ATTN_DEVICE_TIMEOUT) return ATTN_ERR_TIMEOUT;
-  if (word & ATTN_DEVICE_BAD_LIST) return ATTN_ERR_INVALID_ARG;
+  if (word & (ATTN_DEVICE_BAD_LIST | ATTN_DEVICE_OOB)) return ATTN_ERR_INVALID_ARG;
   return ATTN_OK;
 }
 
 attn_status_t attn_selftest_wait_timeout(int limit_us, cudaStream_t stream) {
+  const NvtxRange nvtx_range("attn_selftest_wait_timeout");
   if (limit_us < 1 || limit_us > 1000000) return ATTN_ERR_INVALID_ARG;
   int* status = nullptr;
   attn_status_t st = status_ptr(&status);
   if (st != ATTN_OK) return st;
-  return cuda_status(launch_wait_selftest(limit_us, status, stream));
+  return cuda_status(launch_wait_selftest(limit_us, 1, 0, status, next_launch_id(), stream));
+}
+
+attn_status_t attn_selftest_wait_timeout_grid(int limit_us, int n_ctas, cudaStream_t stream) {
+  const NvtxRange nvtx_range("attn_selftest_wait_timeout_grid");
+  if (limit_us < 1 || limit_us > 1000000 || n_ctas < 1 || n_ctas > 65536) return ATTN_ERR_INVALID_ARG;
+  int* status = nullptr;
+  attn_status_t st = status_ptr(&status);
+  if (st != ATTN_OK) return st;
+  // 160 KB of shared memory per CTA: one CTA per SM, so the grid runs in waves
+  return cuda_status(launch_wait_selftest(limit_us, n_ctas, 160 * 1024, status, next_launch_id(), stream));
 }
 
 }  // extern "C"

@@ -86,7 +86,8 @@ struct FwdParams {
   const float* stats;      // sparse: [BH][NQB][4] = mu, sigma, tau, W
   const float* taylor_t;   // sparse: [BH][NQB][D]
   int NQB, NKB;
-  int* status;             // device status word
+  int* status;             // device status words (status bits, id of the last launch that timed out)
+  unsigned launch_id;      // this launch (never 0)
   // fused routing (kModeSparseFused): pooled inputs, routing constants and
   // optional copies of the routing the kernel computed on chip
   const float* qbar;       // [BH][NQB][D]
@@ -706,8 +707,11 @@ __global__ void __launch_bounds__(NQT * 128 + 128, (NQT == 1) ? 2 : 1)
   __shared__ uint64_t bar_qt[NQT], bar_done_t[NQT];   // independent tiles: Q landed, tile's MMAs done
   __shared__ int mma_lock;
   __shared__ uint32_t tmem_base_sh;
-  __shared__ volatile int abort_flag;
+  __shared__ WaitState wstate;
   __shared__ int merge_last;
+  __shared__ int skip_cta;   // the launch had already aborted when this CTA started
+  WaitState* const wc = &wstate;
+  volatile int& abort_flag = wstate.abort;
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
@@ -806,7 +810,7 @@ __global__ void __launch_bounds__(NQT * 128 + 128, (NQT == 1) ? 2 : 1)
     }
     mma_lock = 0;
     mbar_init(&bar_route, 1);
-    abort_flag = 0;
+    skip_cta = wait_state_init(wstate, p.status, p.launch_id);
     fence_barrier_init();
   }
   if (warp == Cfg::kMmaWarp) tmem_alloc(&tmem_base_sh, Cfg::kTmemCols);
@@ -814,6 +818,7 @@ __global__ void __launch_bounds__(NQT * 128 + 128, (NQT == 1) ? 2 : 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_base_sh;
+  if (!skip_cta) {
   // fused routing: lists are ready once the softmax threads arrive on bar_route
   auto take_fused_lists = [&]() {
 #pragma unroll
@@ -857,7 +862,7 @@ __global__ void __launch_bounds__(NQT * 128 + 128, (NQT == 1) ? 2 : 1)
         while (ok) {
           u = next_step<Cfg::kDual, kNA>(w, naw, merge, fl, na_box);
           if (u < 0 && prev < 0) break;
-          if (g >= 1 && !bounded_wait(&bar_s[t], (g - 1) & 1, &abort_flag, p.status)) {
+          if (g >= 1 && !bounded_wait(&bar_s[t], (g - 1) & 1, wc)) {
             ok = false;
             break;
           }
@@ -880,11 +885,11 @@ __global__ void __launch_bounds__(NQT * 128 + 128, (NQT == 1) ? 2 : 1)
           if (u < 0) break;
         }
         // drain: no copy may still be landing when the CTA exits
-        if (valid) bounded_wait(&bar_qt[t], 0, nullptr, p.status);
-        if (g >= 1) bounded_wait(&bar_full[kslot], (g - 1) & 1, nullptr, p.status);
+        if (valid) drain_wait(&bar_qt[t], 0, wc);
+        if (g >= 1) drain_wait(&bar_full[kslot], (g - 1) & 1, wc);
       } else {
         // ---- MMA issuer of tile t: per group PV_t(g-1) then S_t(g) (two-issuer CTA: under the issue lock)
-        bool ok = t < n_valid_tiles && bounded_wait(&bar_qt[t], 0, &abort_flag, p.status);
+        bool ok = t < n_valid_tiles && bounded_wait(&bar_qt[t], 0, wc);
         tc_fence_after();
         const uint32_t q_addr = smem_u32(sQ) + t * Cfg::kQTileBytes;
         const uint32_t kv_base = smem_u32(sKV);
@@ -896,8 +901,8 @@ __global__ void __launch_bounds__(NQT * 128 + 128, (NQT == 1) ? 2 : 1)
         while (ok) {
           u = next_step<Cfg::kDual, kNA>(w, naw, merge, fl, na_box);
           if (u < 0 && !pending) break;
-          if (!bounded_wait(&bar_full[kslot], g & 1, &abort_flag, p.status) ||
-              (pending && !bounded_wait(&bar_p[t], pvc & 1, &abort_flag, p.status))) {
+          if (!bounded_wait(&bar_full[kslot], g & 1, wc) ||
+              (pending && !bounded_wait(&bar_p[t], pvc & 1, wc))) {
             ok = false;
             break;
           }
@@ -930,7 +935,7 @@ __global__ void __launch_bounds__(NQT * 128 + 128, (NQT == 1) ? 2 : 1)
         mma_commit(&bar_o[t]);
         // every MMA this thread issued has completed before TMEM is released
         mma_commit(&bar_done_t[t]);
-        bounded_wait(&bar_done_t[t], 0, nullptr, p.status);
+        drain_wait(&bar_done_t[t], 0, wc);
       }
     }
   } else
@@ -958,7 +963,7 @@ __global__ void __launch_bounds__(NQT * 128 + 128, (NQT == 1) ? 2 : 1)
       int u;
       bool ok = true;
       if (MODE == kModeSparseFused) {
-        ok = bounded_wait(&bar_route, 0, &abort_flag, p.status);   // the ring holds routing scratch until then
+        ok = bounded_wait(&bar_route, 0, wc);   // the ring holds routing scratch until then
         take_fused_lists();
       }
       while (ok && (u = next_tile<kNA>(naw, merge, flags, na_box)) >= 0) {
@@ -966,7 +971,7 @@ __global__ void __launch_bounds__(NQT * 128 + 128, (NQT == 1) ? 2 : 1)
 #pragma unroll
         for (int kv = 0; kv < 2; ++kv) {
           const int slot = ld % NSTAGE;
-          if (ld >= NSTAGE && !bounded_wait(&bar_empty[slot], ((ld / NSTAGE) - 1) & 1, &abort_flag, p.status)) {
+          if (ld >= NSTAGE && !bounded_wait(&bar_empty[slot], ((ld / NSTAGE) - 1) & 1, wc)) {
             ok = false;
             break;
           }
@@ -983,15 +988,15 @@ __global__ void __launch_bounds__(NQT * 128 + 128, (NQT == 1) ? 2 : 1)
         }
       }
       // drain: make sure no copy is still landing when the CTA exits
-      bounded_wait(&bar_q, 0, nullptr, p.status);
-      for (int j = (ld > NSTAGE ? ld - NSTAGE : 0); j < ld; ++j) bounded_wait(&bar_full[j % NSTAGE], (j / NSTAGE) & 1, nullptr, p.status);
+      drain_wait(&bar_q, 0, wc);
+      for (int j = (ld > NSTAGE ? ld - NSTAGE : 0); j < ld; ++j) drain_wait(&bar_full[j % NSTAGE], (j / NSTAGE) & 1, wc);
     }
   } else if (warp == Cfg::kMmaWarp) {
     // ======================= MMA issuer =======================
     if (lane == 0) {
-      bool ok = bounded_wait(&bar_q, 0, &abort_flag, p.status);
+      bool ok = bounded_wait(&bar_q, 0, wc);
       if (MODE == kModeSparseFused) {
-        ok = ok && bounded_wait(&bar_route, 0, &abort_flag, p.status);
+        ok = ok && bounded_wait(&bar_route, 0, wc);
         take_fused_lists();
       }
       tc_fence_after();
@@ -1022,7 +1027,7 @@ __global__ void __launch_bounds__(NQT * 128 + 128, (NQT == 1) ? 2 : 1)
       };
       while (ok && (u = next_tile<kNA>(naw, merge, flags, na_box)) >= 0) {
         const int kslot = ld % NSTAGE;
-        if (!bounded_wait(&bar_full[kslot], (ld / NSTAGE) & 1, &abort_flag, p.status)) break;
+        if (!bounded_wait(&bar_full[kslot], (ld / NSTAGE) & 1, wc)) break;
         ++ld;
         const int vslot = ld % NSTAGE;
         const int vpar = (ld / NSTAGE) & 1;
@@ -1033,10 +1038,10 @@ __global__ void __launch_bounds__(NQT * 128 + 128, (NQT == 1) ? 2 : 1)
         for (int t = 0; t < NQT; ++t) {
           if (pending[t]) {
             if (!prev_v_ready) {
-              if (!bounded_wait(&bar_full[prev_vslot], prev_vpar, &abort_flag, p.status)) { ok = false; break; }
+              if (!bounded_wait(&bar_full[prev_vslot], prev_vpar, wc)) { ok = false; break; }
               prev_v_ready = true;
             }
-            if (!bounded_wait(&bar_p[t], pv_count[t] & 1, &abort_flag, p.status)) { ok = false; break; }
+            if (!bounded_wait(&bar_p[t], pv_count[t] & 1, wc)) { ok = false; break; }
             tc_fence_after();
             issue_pv(t, prev_vslot);
             any_pv = true;
@@ -1066,10 +1071,10 @@ __global__ void __launch_bounds__(NQT * 128 + 128, (NQT == 1) ? 2 : 1)
         for (int t = 0; t < NQT; ++t) {
           if (!pending[t]) continue;
           if (!v_ready) {
-            if (!bounded_wait(&bar_full[prev_vslot], prev_vpar, &abort_flag, p.status)) break;
+            if (!bounded_wait(&bar_full[prev_vslot], prev_vpar, wc)) break;
             v_ready = true;
           }
-          if (!bounded_wait(&bar_p[t], pv_count[t] & 1, &abort_flag, p.status)) break;
+          if (!bounded_wait(&bar_p[t], pv_count[t] & 1, wc)) break;
           tc_fence_after();
           issue_pv(t, prev_vslot);
           any_pv = true;
@@ -1081,7 +1086,7 @@ __global__ void __launch_bounds__(NQT * 128 + 128, (NQT == 1) ? 2 : 1)
       for (int t = 0; t < NQT; ++t) mma_commit(&bar_o[t]);
       // every MMA issued by this thread has completed before TMEM is released
       mma_commit(&bar_mma_done);
-      bounded_wait(&bar_mma_done, 0, nullptr, p.status);
+      drain_wait(&bar_mma_done, 0, wc);
     }
   }
   } else {
@@ -1130,7 +1135,7 @@ __global__ void __launch_bounds__(NQT * 128 + 128, (NQT == 1) ? 2 : 1)
     bool ok = t < n_valid_tiles;
     while (ok && (u = next_step<Cfg::kDual, kNA>(wk, naw, merge, flags, na_box)) >= 0) {
       if (!(flags & tile_mask)) continue;
-      if (!__all_sync(0xffffffffu, bounded_wait(&bar_s[t], it & 1, &abort_flag, p.status))) break;
+      if (!__all_sync(0xffffffffu, bounded_wait(&bar_s[t], it & 1, wc))) break;
       tc_fence_after();
       float x[BK];
       {
@@ -1251,7 +1256,7 @@ __global__ void __launch_bounds__(NQT * 128 + 128, (NQT == 1) ? 2 : 1)
     if (t < n_valid_tiles && !abort_flag) {
       bool have_o = it > 0;
       // (every issuer commits bar_o once, after its last PV)
-      if (have_o && !__all_sync(0xffffffffu, bounded_wait(&bar_o[t], 0, &abort_flag, p.status))) have_o = false;
+      if (have_o && !__all_sync(0xffffffffu, bounded_wait(&bar_o[t], 0, wc))) have_o = false;
       tc_fence_after();
       if (MODE == kModeSplit) {
         const bool empty = !have_o || l_run == 0.f;
@@ -1346,6 +1351,8 @@ __global__ void __launch_bounds__(NQT * 128 + 128, (NQT == 1) ? 2 : 1)
         split_merge_tail<D>(p, bh, qg, q_row0, r, merge_last, abort_flag, reinterpret_cast<float*>(sKV));
     }
   }
+
+  }   // !skip_cta
 
   tc_fence_before();
   __syncthreads();

@@ -553,22 +553,29 @@ cudaError_t launch_merge(const float* o_part, const float* lse_part, uint16_t* o
 }
 
 // ============================================================ bounded-wait self-test
-// One thread waits on a barrier that nothing arrives on; the wait gives up
-// after limit_us and records the timeout in the status word.
-__global__ void wait_selftest_kernel(int* status, unsigned long long limit_ns) {
+// Every CTA's thread 0 waits on a barrier that nothing arrives on; the first
+// wait to give up after limit_us records the timeout and aborts the launch,
+// so the CTAs still waiting give up too and the CTAs that start afterwards
+// return at once (the launch-wide abort of bounded_wait).
+__global__ void wait_selftest_kernel(int* status, unsigned launch_id, unsigned long long limit_ns) {
   __shared__ uint64_t bar;
-  __shared__ volatile int abort_flag;
+  __shared__ WaitState wstate;
+  __shared__ int skip_cta;
   if (threadIdx.x == 0) {
     mbar_init(&bar, 1);
-    abort_flag = 0;
+    skip_cta = wait_state_init(wstate, status, launch_id);
     fence_barrier_init();
   }
   __syncthreads();
-  if (threadIdx.x == 0) bounded_wait(&bar, 0, &abort_flag, status, limit_ns);
+  if (skip_cta) return;
+  if (threadIdx.x == 0) bounded_wait(&bar, 0, &wstate, limit_ns);
 }
 
-cudaError_t launch_wait_selftest(int limit_us, int* status, cudaStream_t stream) {
-  wait_selftest_kernel<<<1, 32, 0, stream>>>(status, (unsigned long long)limit_us * 1000ull);
+cudaError_t launch_wait_selftest(int limit_us, int n_ctas, int smem_bytes, int* status, unsigned launch_id,
+                                 cudaStream_t stream) {
+  cudaError_t e = cudaFuncSetAttribute(wait_selftest_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+  if (e != cudaSuccess) return e;
+  wait_selftest_kernel<<<n_ctas, 32, smem_bytes, stream>>>(status, launch_id, (unsigned long long)limit_us * 1000ull);
   return cudaGetLastError();
 }
 

@@ -33,27 +33,57 @@ __device__ __forceinline__ void unpack8(const uint4& v, float (&f)[8]) {
   }
 }
 
-// Row scales from the row's amax: the dequantisation scale amax / 448 and the
-// inverse 448 / amax (fp32 divisions, once per row).  A zero row, or one whose
-// inverse overflows, quantises to zeros with scale 0.
+// Row scales from the row's amax: the dequantisation scale s = amax / 448 and
+// the inverse 448 / amax (fp32 divisions, once per row).  A row whose scale is
+// zero or not a normal float (amax / 448 < 2^-126) quantises to zeros with
+// scale 0; otherwise the inverse is at most 2^126 and finite.
 __device__ __forceinline__ void row_scales(float amax, float& s, float& inv) {
-  inv = amax > 0.f ? __fdiv_rn(448.0f, amax) : 0.f;
-  if (!(amax > 0.f) || isinf(inv)) {
+  s = __fdiv_rn(amax, 448.0f);
+  if (!(s >= 0x1p-126f)) {
     s = 0.f;
     inv = 0.f;
   } else {
-    s = __fdiv_rn(amax, 448.0f);
+    inv = __fdiv_rn(448.0f, amax);
   }
 }
 
-// Codes of 8 values: e4m3(x * inv), nearest even, saturating at +-448.
-__device__ __forceinline__ uint2 quantize8(const uint4& v, float inv) {
+// The code of a bf16 value x is the E4M3 value nearest to the exact quotient
+// x * 448 / amax (ties to even).  The product x * inv, with inv the rounded
+// inverse scale, lies within two float roundings of that quotient, so it
+// decides the same code unless it sits within a few float steps of an E4M3
+// rounding midpoint; for those values, and for the E4M3 subnormal grid
+// (0 < |v| < 2^-6), the quotient is formed again with one correctly rounded
+// division.  For bf16 operands that decides exactly: x * 0.875 is exact, and a
+// quotient of bf16 values either is a midpoint (at most five significant bits,
+// so the division returns it exactly) or lies at least 2^-13 of its size away
+// from every midpoint.  Tiny rows are scaled by 2^64 first so that no operand
+// of the division is subnormal.
+__device__ __noinline__ float exact_quotient(float x, float amax) {
+  if (amax < 0x1p-60f) {
+    x *= 0x1p64f;
+    amax *= 0x1p64f;
+  }
+  return __fmul_rn(__fdiv_rn(__fmul_rn(x, 0.875f), amax), 512.0f);
+}
+
+__device__ __forceinline__ uint32_t e4m3_code(float x, float inv, float amax) {
+  float v = __fmul_rn(x, inv);
+  const uint32_t u = __float_as_uint(v) & 0x7fffffffu;
+  // |v| in (0, 2^-6), or within 8 float steps of the midpoint of the E4M3 step
+  // (the low 20 mantissa bits are the position inside a step of the normal range)
+  const bool near = (u - 1u < 0x3C7FFFFFu) || (((u & 0xFFFFFu) - 0x7FFF8u) <= 16u);
+  if (near) v = exact_quotient(x, amax);
+  return (uint32_t)__nv_cvt_float_to_fp8(v, __NV_SATFINITE, __NV_E4M3);
+}
+
+// Codes of 8 values.
+__device__ __forceinline__ uint2 quantize8(const uint4& v, float inv, float amax) {
   float f[8];
   unpack8(v, f);
   uint32_t lo = 0, hi = 0;
 #pragma unroll
   for (int e = 0; e < 8; ++e) {
-    const uint32_t c = (uint32_t)__nv_cvt_float_to_fp8(__fmul_rn(f[e], inv), __NV_SATFINITE, __NV_E4M3);
+    const uint32_t c = e4m3_code(f[e], inv, amax);
     if (e < 4)
       lo |= c << (8 * e);
     else
@@ -90,7 +120,7 @@ __global__ void __launch_bounds__(kQuantThreads) fp8_quantize_rows_kernel(const 
   row_scales(amax, s, inv);
   if (threadIdx.x == 0) scale[row] = s;
   for (int i = threadIdx.x * 8; i < K; i += kQuantThreads * 8)
-    *reinterpret_cast<uint2*>(qr + i) = quantize8(*reinterpret_cast<const uint4*>(xr + i), inv);
+    *reinterpret_cast<uint2*>(qr + i) = quantize8(*reinterpret_cast<const uint4*>(xr + i), inv, amax);
 }
 
 // One CTA of 128 threads per row for rows of up to NV * 1024 elements: each
@@ -129,7 +159,7 @@ __global__ void __launch_bounds__(128) fp8_quantize_rows_reg_kernel(const uint16
 #pragma unroll
   for (int c = 0; c < NV; ++c) {
     const int i = (c * 128 + threadIdx.x) * 8;
-    if (i < K) __stcs(reinterpret_cast<uint2*>(qr + i), quantize8(v[c], inv));
+    if (i < K) __stcs(reinterpret_cast<uint2*>(qr + i), quantize8(v[c], inv, amax));
   }
 }
 
@@ -165,12 +195,14 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* m, uin
 __global__ void __launch_bounds__(kGemmThreads, 1)
     fp8_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                     const float* __restrict__ sa, const float* __restrict__ sw, uint16_t* __restrict__ y, int M, int N,
-                    int K, int* status) {
+                    int K, int* status, unsigned launch_id) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   __shared__ uint64_t bar_full[kStages], bar_empty[kStages], bar_acc_full[2], bar_acc_empty[2], bar_mma_done;
   __shared__ uint32_t tmem_base_sh;
-  __shared__ volatile int abort_flag;
+  __shared__ WaitState wstate;
+  __shared__ int skip_cta;   // the launch had already aborted when this CTA started
+  WaitState* const wc = &wstate;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int n_nb = (N + kBN - 1) / kBN;
@@ -187,7 +219,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       mbar_init(&bar_acc_empty[b], kEpilogueThreads);
     }
     mbar_init(&bar_mma_done, 1);
-    abort_flag = 0;
+    skip_cta = wait_state_init(wstate, status, launch_id);
     fence_barrier_init();
   }
   if (warp == 1) tmem_alloc(&tmem_base_sh, kTmemCols);
@@ -195,6 +227,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_base_sh;
+  if (!skip_cta) {
 
   if (warp == 0) {
     // ======================= TMA producer =======================
@@ -207,7 +240,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const int mb = tile / n_nb, nb = tile % n_nb;
         for (int kb = 0; kb < nk; ++kb, ++it) {
           const int slot = it % kStages;
-          if (it >= kStages && !bounded_wait(&bar_empty[slot], ((it / kStages) - 1) & 1, &abort_flag, status)) {
+          if (it >= kStages && !bounded_wait(&bar_empty[slot], ((it / kStages) - 1) & 1, wc)) {
             ok = false;
             break;
           }
@@ -219,7 +252,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       }
       // drain: no copy may still be landing when the CTA exits
       for (int j = (it > kStages ? it - kStages : 0); j < it; ++j)
-        bounded_wait(&bar_full[j % kStages], (j / kStages) & 1, nullptr, status);
+        drain_wait(&bar_full[j % kStages], (j / kStages) & 1, wc);
     }
   } else if (warp == 1) {
     // ======================= MMA issuer =======================
@@ -229,12 +262,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       bool ok = true;
       for (int tile = blockIdx.x; ok && tile < tiles; tile += gridDim.x, ++tcount) {
         const int buf = tcount & 1, use = tcount >> 1;
-        if (use > 0 && !bounded_wait(&bar_acc_empty[buf], (use - 1) & 1, &abort_flag, status)) break;
+        if (use > 0 && !bounded_wait(&bar_acc_empty[buf], (use - 1) & 1, wc)) break;
         tc_fence_after();
         const uint32_t d = tmem + buf * kBN;
         for (int kb = 0; kb < nk; ++kb, ++it) {
           const int slot = it % kStages;
-          if (!bounded_wait(&bar_full[slot], (it / kStages) & 1, &abort_flag, status)) {
+          if (!bounded_wait(&bar_full[slot], (it / kStages) & 1, wc)) {
             ok = false;
             break;
           }
@@ -251,7 +284,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       }
       // every MMA issued by this thread has completed before TMEM is released
       mma_commit(&bar_mma_done);
-      bounded_wait(&bar_mma_done, 0, nullptr, status);
+      drain_wait(&bar_mma_done, 0, wc);
     }
   } else {
     // ======================= epilogue =======================
@@ -261,7 +294,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     int tcount = 0;
     for (int tile = blockIdx.x; tile < tiles; tile += gridDim.x, ++tcount) {
       const int buf = tcount & 1, use = tcount >> 1;
-      if (!__all_sync(0xffffffffu, bounded_wait(&bar_acc_full[buf], use & 1, &abort_flag, status))) break;
+      if (!__all_sync(0xffffffffu, bounded_wait(&bar_acc_full[buf], use & 1, wc))) break;
       tc_fence_after();
       const int mb = tile / n_nb, nb = tile % n_nb;
       const long long grow = (long long)mb * kBM + r;
@@ -302,6 +335,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       mbar_arrive(&bar_acc_empty[buf]);
     }
   }
+  }   // !skip_cta
 
   tc_fence_before();
   __syncthreads();
@@ -326,7 +360,8 @@ cudaError_t launch_fp8_quantize_rows(const uint16_t* x, uint8_t* q, float* scale
 }
 
 cudaError_t launch_fp8_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const float* sa, const float* sw,
-                            uint16_t* y, int M, int N, int K, int* status, cudaStream_t stream) {
+                            uint16_t* y, int M, int N, int K, int* status, unsigned launch_id,
+                            cudaStream_t stream) {
   cudaError_t e = cudaFuncSetAttribute(fp8_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmem);
   if (e != cudaSuccess) return e;
   int dev = 0, sms = 0;
@@ -334,7 +369,7 @@ cudaError_t launch_fp8_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const 
   if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
   const long long tiles = (long long)((M + kBM - 1) / kBM) * ((N + kBN - 1) / kBN);
   const int grid = (int)(tiles < sms ? tiles : sms);
-  fp8_gemm_kernel<<<grid, kGemmThreads, kGemmSmem, stream>>>(ta, tb, sa, sw, y, M, N, K, status);
+  fp8_gemm_kernel<<<grid, kGemmThreads, kGemmSmem, stream>>>(ta, tb, sa, sw, y, M, N, K, status, launch_id);
   return cudaGetLastError();
 }
 

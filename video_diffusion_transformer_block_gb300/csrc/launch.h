@@ -46,9 +46,12 @@ cudaError_t launch_fp8_quantize_rows(const uint16_t* x, uint8_t* q, float* scale
 // y [M][N] bf16 = diag(sa) (Aq Wq^T) diag(sw); ta / tb: 2-D uint8 maps of Aq [M][K]
 // (box 128 x 128) and Wq [N][K] (box 128 x 256), 128-byte swizzle.
 cudaError_t launch_fp8_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const float* sa, const float* sw,
-                            uint16_t* y, int M, int N, int K, int* status, cudaStream_t stream);
+                            uint16_t* y, int M, int N, int K, int* status, unsigned launch_id,
+                            cudaStream_t stream);
 
-// Bounded-wait self-test kernel.
-cudaError_t launch_wait_selftest(int limit_us, int* status, cudaStream_t stream);
+// Bounded-wait self-test: n_ctas CTAs (each with `smem_bytes` of dynamic shared
+// memory, which limits how many share an SM) wait on barriers nothing arrives on.
+cudaError_t launch_wait_selftest(int limit_us, int n_ctas, int smem_bytes, int* status, unsigned launch_id,
+                                 cudaStream_t stream);
 
 }  // namespace vdtb

@@ -2,10 +2,14 @@
 // tcgen05 MMA / TMEM, plus a time-bounded barrier wait.
 //
 // Every wait in the library goes through `bounded_wait`: it polls with
-// mbarrier.try_wait and gives up after a wall-clock limit (globaltimer),
-// records ATTN_DEVICE_TIMEOUT in the library's device status word (passed to
-// every kernel as a pointer) and raises
-// a CTA-local abort flag so that the other roles of the CTA stop waiting too.
+// mbarrier.try_wait and gives up after a wall-clock limit (globaltimer).  A
+// wait that gives up records ATTN_DEVICE_TIMEOUT in the library's device
+// status word, raises a CTA-local abort flag so that the other roles of the
+// CTA stop waiting, and publishes the launch's id in a second device word, so
+// that every other CTA of the same launch gives up too: a wait that has lasted
+// kAbortPollNs starts polling that word, and a CTA that starts later returns
+// at once.  A broken launch therefore ends about one wait limit after its
+// first timeout instead of one limit per CTA.
 #pragma once
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -16,16 +20,37 @@ namespace vdtb {
 // Device-side status bits (read back by attn_last_device_status).
 constexpr int ATTN_DEVICE_TIMEOUT = 1;
 constexpr int ATTN_DEVICE_BAD_LIST = 2;
+constexpr int ATTN_DEVICE_OOB = 4;   // bounds-checked build: a store outside its buffer was skipped
 
 // Wall-clock limit of a single barrier wait (nanoseconds).
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;
+// A wait that has lasted this long also polls the launch-wide abort word.
+constexpr unsigned long long kAbortPollNs = 20000ull;
+// Limit of the drain waits at a CTA's end: they wait for copies and MMAs that
+// were issued and complete in microseconds, and are not cut short by an abort.
+constexpr unsigned long long kDrainLimitNs = 20000000ull;
 
+// What a wait needs besides its barrier, kept in shared memory (one per CTA,
+// written once before the CTA's first barrier sync) so that no register holds
+// it.  `status` points at the library's two device words: status[0] holds the
+// status bits, status[1] the id of the last launch in which a wait timed out.
+// Launch ids come from a host counter and are never 0.
+struct WaitState {
+  volatile int abort;   // CTA-local abort flag
+  unsigned launch_id;   // this launch
+  int* status;
+};
 __device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
 __device__ __forceinline__ uint64_t global_timer_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
   return t;
+}
+
+// True once a wait of launch `launch_id` has timed out (in any CTA).
+__device__ __forceinline__ bool launch_aborted(const int* status, unsigned launch_id) {
+  return *reinterpret_cast<const volatile unsigned*>(status + 1) == launch_id;
 }
 
 // ---------------------------------------------------------------- mbarrier
@@ -50,28 +75,47 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Wait until the phase with parity `parity` of `bar` has completed, or until
-// `limit_ns` expires or (when `abort_flag` is non-null) another role of the
-// CTA has aborted.  Returns false on timeout/abort.  A null `abort_flag` is
-// used by the drain waits at the end of a kernel, which must not be cut
-// short by an abort.
-static __device__ __forceinline__ bool bounded_wait_slow(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int* status,
-                                               unsigned long long limit_ns) {
-  uint64_t t0 = global_timer_ns();
+// `limit_ns` expires, or (abortable waits) until another role of the CTA or
+// another CTA of the launch has aborted.  Returns false on timeout/abort.
+static __device__ __forceinline__ bool bounded_wait_slow(uint64_t* bar, uint32_t parity, WaitState* ws,
+                                                         bool abortable, unsigned long long limit_ns) {
+  const uint64_t t0 = global_timer_ns();
   while (true) {
     for (int i = 0; i < 64; ++i)
       if (mbar_try_wait(bar, parity)) return true;
-    if (abort_flag != nullptr && *abort_flag) return false;
-    if (global_timer_ns() - t0 > limit_ns) {
-      atomicOr(status, ATTN_DEVICE_TIMEOUT);
-      if (abort_flag != nullptr) *abort_flag = 1;
+    if (abortable && ws->abort) return false;
+    const uint64_t elapsed = global_timer_ns() - t0;
+    if (abortable && elapsed > kAbortPollNs && launch_aborted(ws->status, ws->launch_id)) {
+      ws->abort = 1;
+      return false;
+    }
+    if (elapsed > limit_ns) {
+      atomicOr(ws->status, ATTN_DEVICE_TIMEOUT);
+      atomicExch(reinterpret_cast<unsigned*>(ws->status + 1), ws->launch_id);
+      if (abortable) ws->abort = 1;
       return false;
     }
   }
 }
-__device__ __forceinline__ bool bounded_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int* status,
+__device__ __forceinline__ bool bounded_wait(uint64_t* bar, uint32_t parity, WaitState* ws,
                                              unsigned long long limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
-  return bounded_wait_slow(bar, parity, abort_flag, status, limit_ns);
+  return bounded_wait_slow(bar, parity, ws, true, limit_ns);
+}
+// Drain wait at a CTA's end: for copies or MMAs already in flight, which must
+// complete before the CTA exits; not cut short by an abort, short limit.
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, WaitState* ws) {
+  if (mbar_try_wait(bar, parity)) return;
+  bounded_wait_slow(bar, parity, ws, false, kDrainLimitNs);
+}
+// Thread 0 at CTA set-up: fills the CTA's wait state and returns whether the
+// launch had already aborted (then the CTA skips its work).
+__device__ __forceinline__ bool wait_state_init(WaitState& ws, int* status, unsigned launch_id) {
+  const bool aborted = launch_aborted(status, launch_id);
+  ws.abort = aborted;
+  ws.launch_id = launch_id;
+  ws.status = status;
+  return aborted;
 }
 
 // ---------------------------------------------------------------- TMA
