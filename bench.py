@@ -450,6 +450,73 @@ def run_merge64(args, world, rank, local):
             "gpu_launches": inst * args.steps, "clocks": clocks.summary()}
 
 
+def run_sweep(args, world, rank, local):
+    """The beta sweep workload at S = 131072 (32x64x64 grid, H32 d128, block 128) for one beta
+    (--beta): pool + route (attn_sparse_route) and the block-sparse forward (attn_sparse_fwd) per
+    step, timed separately with CUDA events; inputs (3.2 GB) are larger than L2."""
+    import video_diffusion_transformer_block_gb300 as vd
+    from video_diffusion_transformer_block_gb300 import build as vbuild
+
+    vbuild.build()
+    vd.load_library()
+    peaks, peaks_src = load_peaks()
+    w0 = WORKLOADS["sweep128k"]
+    w = Workload(w0.name, B=w0.B, H=args.heads, Sq=w0.Sq, Skv=w0.Skv, d=w0.d, seed=w0.seed + 1000 * rank,
+                 q_std=w0.q_std, k_std=w0.k_std, grid=w0.grid, pe=True, block=w0.block, beta=args.beta)
+    q, k, v = make_qkv(w, device="cuda")
+    B, H, S, d, block = w.B, w.H, w.Sq, w.d, w.block
+    ws = torch.empty(vd.attn_sparse_workspace_bytes(B, H, S, d, block, block), dtype=torch.uint8, device=q.device)
+    rt = vd.sparse_route_buffers(B, H, S, d, block, q.device)
+    out = torch.empty_like(q)
+    lse = torch.empty((B, H, S), dtype=torch.float32, device=q.device)
+    stream = torch.cuda.current_stream()
+
+    def step(e=None):
+        if e is not None:
+            e[0].record(stream)
+        vd.attn_sparse_route(q, k, v, args.beta, block=block, route=rt, workspace=ws)
+        if e is not None:
+            e[1].record(stream)
+        vd.attn_sparse_fwd(q, k, v, rt, block=block, out=out, lse=lse)
+        if e is not None:
+            e[2].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    flops = executed_sparse_flops(rt["sel_idx"], rt["sel_cnt"], S, block, d)
+    dense_eq = 4.0 * B * H * S * S * d
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        for e in evs:
+            step(e)
+        torch.cuda.synchronize()
+    barrier(world)
+    status = vd.attn_last_device_status()
+    if status != 0:
+        raise RuntimeError(f"device status after timed region: {vd.attn_status_string(status)}")
+    ms = max_over_ranks(sum(e[0].elapsed_time(e[2]) for e in evs) / args.steps, world)
+    ms_route = sum(e[0].elapsed_time(e[1]) for e in evs) / args.steps
+    ms_fwd = sum(e[1].elapsed_time(e[2]) for e in evs) / args.steps
+    value = world * flops / (ms * 1e-3) / 1e12
+    peak = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
+    fwd = flops / (ms_fwd * 1e-3) / 1e12
+    return {"metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": f"sweep128k: B1 H{H} S{S} (32x64x64) d128 block 128 beta {args.beta}",
+                       "seq_len": S, "l2": "inputs (3.2 GB) larger than L2; no flush"},
+            "density": round(flops / dense_eq, 5),
+            "dense_equiv_tflops": round(world * dense_eq / (ms * 1e-3) / 1e12, 2),
+            "breakdown_ms": {"pool_route": round(ms_route, 4), "sparse_fwd": round(ms_fwd, 4)},
+            "roofline": {"bound": "tensor", "kernel": "attn_fwd_kernel (sparse, d=128, block 128)",
+                         "achieved": round(fwd, 2), "peak": peak, "unit": "TFLOP/s", "frac": round(fwd / peak, 4),
+                         "peak_source": f"{peaks_src} bf16_tflops (burst)", "traffic": None},
+            "gpu_launches": 3 * args.steps, "clocks": clocks.summary()}
+
+
 def run_native_kernel(args, world, rank, local):
     """Secondary workloads (not the benchmark line): one kernel path per step.
       dense16k: attn_dense_fwd on B1 H32 S16384 d128 (tensor-bound)
@@ -823,7 +890,8 @@ def main():
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
     ap.add_argument("--beta", type=float, default=1.0)
     ap.add_argument("--heads", type=int, default=32, help="heads (32 = the benchmark; fewer only for profiling)")
-    ap.add_argument("--workload", choices=["sparse64k", "dense16k", "cross", "na3d", "fp8_proj", "merge64"],
+    ap.add_argument("--workload", choices=["sparse64k", "dense16k", "cross", "na3d", "fp8_proj", "merge64",
+                                           "sweep128k"],
                     default="sparse64k",
                     help="sparse64k = the benchmark step; dense16k / cross / na3d / fp8_proj time one path each")
     ap.add_argument("--tokens", type=int, default=None,
@@ -843,6 +911,8 @@ def main():
         res = run_fp8_projection(args, world, rank, local)
     elif args.workload == "merge64":
         res = run_merge64(args, world, rank, local)
+    elif args.workload == "sweep128k":
+        res = run_sweep(args, world, rank, local)
     elif args.workload != "sparse64k":
         res = run_native_kernel(args, world, rank, local)
     else:

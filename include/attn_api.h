@@ -115,7 +115,9 @@ attn_status_t attn_block_pool(const attn_bf16* x, float* x_pool, int B, int H, i
 /*
  * Bytes of device workspace attn_sparse_route_fwd needs for these sizes
  * (pooled Q/K/V, selected-block lists, per-block statistics, Taylor
- * aggregates).  Returns 0 for sizes the library does not support.
+ * aggregates, and the tf32 hi/lo halves of the pooled keys and of the
+ * transposed pooled values that the tensor-core routing multiplies).
+ * Returns 0 for sizes the library does not support.
  */
 size_t attn_sparse_workspace_bytes(int B, int H, int S, int d, int block_q, int block_k);
 
@@ -137,7 +139,10 @@ size_t attn_sparse_workspace_bytes(int B, int H, int S, int d, int block_q, int 
  *   M = max scale*q.k,  num = sum e^(x-M) v + e^(mu_i-M) T_i,
  *   den = sum e^(x-M) + e^(mu_i-M) W_i,  out = num/den,  lse = M + ln den.
  * (When Sel_i is every block the Taylor terms are skipped.)
- * The proxy scores are recomputed on chip and never written to memory.
+ * The proxy scores and T are computed on the tensor cores with fp32-grade
+ * accuracy (three tf32 products of hi/lo operand halves); the proxy scores
+ * live in tensor memory, are recomputed for the selection pass, and are never
+ * written to memory.
  *
  *   q, k, v, out [B][H][S][d] bf16,  lse [B][H][S] fp32 (nullable)
  *   block_q == block_k, in {64, 128}
@@ -302,7 +307,7 @@ attn_status_t attn_na3d_plan(int T, int Y, int X, int Kt, int Ky, int Kx, int* b
  *   Limit       sizes whose attn_sparse_workspace_bytes(...) exceeds
  *               ATTN_NOALLOC_WORKSPACE_BYTES are rejected with
  *               ATTN_ERR_WORKSPACE before anything is launched (for H = 32,
- *               d = 128, block 128 that is S up to about 32K tokens).
+ *               d = 128, block 128 that is S up to about 27K tokens).
  *   Set-up      the first call on a device looks up the device address of
  *               the array (once per device, with that device current); make
  *               that first call before any stream capture.

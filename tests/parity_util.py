@@ -71,3 +71,26 @@ def compare_selection(gpu_sel, oracle_rt, band=NEAR_TAU):
     bad = diff & ~near
     assert not bad.any(), f"{int(bad.sum())} selection mismatches outside the near-tau band"
     return int(diff.sum())
+
+
+GUARD_BYTES = 4096
+GUARD_PATTERN = 0x5A
+
+
+class Guarded:
+    """A device tensor placed between two guard bands of GUARD_BYTES.  The bands and the tensor
+    itself are filled with GUARD_PATTERN (as fp32 or bf16 that reads 1.5e16, so an element no
+    kernel wrote also shows up in a comparison); `check` asserts that both bands are unchanged,
+    i.e. that no store landed just before or just past the buffer."""
+
+    def __init__(self, shape, dtype, device="cuda"):
+        self.nbytes = int(np.prod(shape)) * torch.empty((), dtype=dtype).element_size()
+        self.raw = torch.full((self.nbytes + 2 * GUARD_BYTES,), GUARD_PATTERN, dtype=torch.uint8, device=device)
+        self.t = self.raw[GUARD_BYTES:GUARD_BYTES + self.nbytes].view(dtype).view(shape)
+
+    def check(self, what):
+        head = self.raw[:GUARD_BYTES]
+        tail = self.raw[GUARD_BYTES + self.nbytes:]
+        ok_head = bool((head == GUARD_PATTERN).all())
+        ok_tail = bool((tail == GUARD_PATTERN).all())
+        assert ok_head and ok_tail, f"{what}: store outside the buffer (leading band ok={ok_head}, trailing ok={ok_tail})"

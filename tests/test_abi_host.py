@@ -43,6 +43,14 @@ def test_library_exports_every_declared_symbol(lib):
         assert re.search(rf"\bT {name}\b", out), f"{name} not exported"
 
 
+def test_bounds_checked_library_exports_every_declared_symbol(lib):
+    # built beside the regular library by build(), from the same sources with -DATTN_DEBUG
+    assert os.path.exists(vbuild.DEBUG_LIB_PATH)
+    out = os.popen(f"nm -D --defined-only {vbuild.DEBUG_LIB_PATH}").read()
+    for name in declared_functions():
+        assert re.search(rf"\bT {name}\b", out), f"{name} not exported by the bounds-checked build"
+
+
 def test_status_strings(lib):
     for code, name in [(0, "ATTN_OK"), (1, "ATTN_ERR_INVALID_ARG"), (5, "ATTN_ERR_TIMEOUT"), (99, "ATTN_ERR_UNKNOWN")]:
         assert lib.attn_status_string(code).decode() == name
@@ -82,8 +90,12 @@ def test_merge_and_pool_reject(lib):
 def test_sparse_workspace_and_rejections(lib):
     n = lib.attn_sparse_workspace_bytes(1, 32, 65664, 128, 128, 128)
     nq = 513
-    expect_min = 32 * nq * 128 * 4 * 3 + 32 * nq * nq * 4 + 32 * nq * 4 * 5 + 32 * nq * 128 * 4
-    assert expect_min <= n <= expect_min + 7 * 256
+    nqp = (nq + 3) // 4 * 4
+    # pooled q, k, v; lists; counts + stats; Taylor T; tf32 hi / lo of the pooled keys and of the transposed
+    # pooled values (rows padded to a multiple of 4)
+    expect_min = (32 * nq * 128 * 4 * 3 + 32 * nq * nq * 4 + 32 * nq * 4 * 5 + 32 * nq * 128 * 4
+                  + 2 * 32 * nq * 128 * 4 + 2 * 32 * 128 * nqp * 4)
+    assert expect_min <= n <= expect_min + 11 * 256
     assert lib.attn_sparse_workspace_bytes(1, 1, 1000, 128, 64, 128) == 0      # block_q != block_k
     assert lib.attn_sparse_workspace_bytes(1, 1, 1000, 96, 64, 64) == 0        # bad d
     ws = ctypes.c_void_p(0x100000)

@@ -110,6 +110,23 @@ attn_status_t make_map_5d(CUtensorMap* m, const void* ptr, int D, int T, int Y, 
   return r == CUDA_SUCCESS ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
+// 3-D map over an fp32 tensor with dims (d0, d1, d2) (d0 innermost), row
+// strides s1, s2 in bytes, box (box0, box1, 1), 128-byte swizzle (box0 * 4 =
+// 128 bytes); elements outside read as zero.
+attn_status_t make_map_f32(CUtensorMap* m, const void* ptr, uint64_t d0, uint64_t d1, uint64_t d2, uint64_t s1,
+                           uint64_t s2, uint32_t box0, uint32_t box1) {
+  if (get_encoder() != ATTN_OK) return ATTN_ERR_CUDA;
+  memset(m, 0, sizeof(*m));
+  cuuint64_t dims[3] = {(cuuint64_t)d0, (cuuint64_t)d1, (cuuint64_t)d2};
+  cuuint64_t strides[2] = {(cuuint64_t)s1, (cuuint64_t)s2};
+  cuuint32_t box[3] = {box0, box1, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(ptr), dims, strides, box, es,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
 // 2-D map over a [rows][inner] uint8 matrix (row stride = inner bytes), box
 // (box_inner, box_rows), 128-byte swizzle; elements outside read as zero.
 attn_status_t make_map_2d_u8(CUtensorMap* m, const void* ptr, int inner, int rows, int box_inner, int box_rows) {
@@ -225,7 +242,8 @@ bool na_args_ok(int B, int H, int T, int Y, int X, int Kt, int Ky, int Kx) {
 }
 
 struct SparseLayout {
-  size_t qp, kp, vp, sel_idx, sel_cnt, stats, taylor, total;
+  size_t qp, kp, vp, sel_idx, sel_cnt, stats, taylor, kh, kl, vth, vtl, total;
+  int NKBp;   // row pitch (floats) of the transposed pooled values
 };
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
@@ -250,6 +268,16 @@ bool sparse_layout(int B, int H, int S, int d, int block_q, int block_k, SparseL
   off = align256(off + BH * NQB * 4 * 4);
   L->taylor = off;
   off = align256(off + BH * NQB * d * 4);
+  // tf32 hi / lo copies of the pooled keys and of the transposed pooled values (tensor-core routing)
+  L->NKBp = (int)((NKB + 3) & ~(size_t)3);
+  L->kh = off;
+  off = align256(off + BH * NKB * d * 4);
+  L->kl = off;
+  off = align256(off + BH * NKB * d * 4);
+  L->vth = off;
+  off = align256(off + BH * d * L->NKBp * 4);
+  L->vtl = off;
+  off = align256(off + BH * d * L->NKBp * 4);
   L->total = off;
   return true;
 }
@@ -349,7 +377,10 @@ attn_status_t fp8_quantize_rows(const attn_bf16* x, uint8_t* q, float* scale, in
   const NvtxRange nvtx_range("fp8_quantize_rows");
   if (!x || !q || !scale || !aligned16(x) || !aligned16(q) || ((uintptr_t)scale & 3u)) return ATTN_ERR_INVALID_ARG;
   if (M < 1 || K < 16 || K % 16 != 0 || K > (1 << 30)) return ATTN_ERR_INVALID_ARG;
-  return cuda_status(launch_fp8_quantize_rows(x, q, scale, M, K, stream));
+  int* status = nullptr;
+  attn_status_t st = status_ptr(&status);
+  if (st != ATTN_OK) return st;
+  return cuda_status(launch_fp8_quantize_rows(x, q, scale, M, K, status, stream));
 }
 
 attn_status_t fp8_scaled_gemm(const uint8_t* aq, const float* a_scale, const uint8_t* wq, const float* w_scale,
@@ -442,7 +473,10 @@ attn_status_t attn_lse_merge(const float* out_part, const float* lse_part, attn_
   if (!sizes_ok(B, H, Sq) || n_split < 1) return ATTN_ERR_INVALID_ARG;
   if (!valid_d(d)) return ATTN_ERR_UNSUPPORTED;
   const long long rows = (long long)B * H * Sq;
-  return cuda_status(launch_merge(out_part, lse_part, out, lse, n_split, rows, d, stream));
+  int* status = nullptr;
+  attn_status_t st = status_ptr(&status);
+  if (st != ATTN_OK) return st;
+  return cuda_status(launch_merge(out_part, lse_part, out, lse, n_split, rows, d, status, stream));
 }
 
 attn_status_t attn_block_pool(const attn_bf16* x, float* x_pool, int B, int H, int S, int d, int block,
@@ -451,7 +485,10 @@ attn_status_t attn_block_pool(const attn_bf16* x, float* x_pool, int B, int H, i
   if (!x || !x_pool || !aligned16(x) || !aligned16(x_pool)) return ATTN_ERR_INVALID_ARG;
   if (!sizes_ok(B, H, S)) return ATTN_ERR_INVALID_ARG;
   if (!valid_d(d) || (block != 64 && block != 128)) return ATTN_ERR_UNSUPPORTED;
-  return cuda_status(launch_pool(x, x, x, x_pool, x_pool, x_pool, 1, B * H, S, d, block, stream));
+  int* status = nullptr;
+  attn_status_t st = status_ptr(&status);
+  if (st != ATTN_OK) return st;
+  return cuda_status(launch_pool(x, x, x, x_pool, x_pool, x_pool, 1, B * H, S, d, block, PoolSplit{}, status, stream));
 }
 
 size_t attn_sparse_workspace_bytes(int B, int H, int S, int d, int block_q, int block_k) {
@@ -489,9 +526,25 @@ attn_status_t run_route(const SparseArgs& a, float beta, void* workspace, size_t
   float* vp = (float*)(ws + L.vp);
   const int BH = a.B * a.H;
   const int NQB = (a.S + a.block_q - 1) / a.block_q, NKB = (a.S + a.block_k - 1) / a.block_k;
-  if (launch_pool(a.q, a.k, a.v, qp, kp, vp, 3, BH, a.S, a.d, a.block_q, stream) != cudaSuccess) return ATTN_ERR_CUDA;
-  if (launch_route(qp, kp, vp, BH, NQB, NKB, a.S, a.d, a.block_k, a.scale, beta, si, sc, stt, tt, stream) !=
-      cudaSuccess)
+  int* status = nullptr;
+  attn_status_t st = status_ptr(&status);
+  if (st != ATTN_OK) return st;
+  PoolSplit split;
+  split.kh = (float*)(ws + L.kh);
+  split.kl = (float*)(ws + L.kl);
+  split.vth = (float*)(ws + L.vth);
+  split.vtl = (float*)(ws + L.vtl);
+  split.NBp = L.NKBp;
+  CUtensorMap tkh, tkl, tvh, tvl;
+  const uint64_t d = (uint64_t)a.d, nk = (uint64_t)NKB, nkp = (uint64_t)L.NKBp;
+  if ((st = make_map_f32(&tkh, split.kh, d, nk, BH, d * 4, nk * d * 4, 32, 128)) != ATTN_OK) return st;
+  if ((st = make_map_f32(&tkl, split.kl, d, nk, BH, d * 4, nk * d * 4, 32, 128)) != ATTN_OK) return st;
+  if ((st = make_map_f32(&tvh, split.vth, nk, d, BH, nkp * 4, d * nkp * 4, 32, (uint32_t)d)) != ATTN_OK) return st;
+  if ((st = make_map_f32(&tvl, split.vtl, nk, d, BH, nkp * 4, d * nkp * 4, 32, (uint32_t)d)) != ATTN_OK) return st;
+  if (launch_pool(a.q, a.k, a.v, qp, kp, vp, 3, BH, a.S, a.d, a.block_q, split, status, stream) != cudaSuccess)
+    return ATTN_ERR_CUDA;
+  if (launch_route_tc(tkh, tkl, tvh, tvl, qp, BH, NQB, NKB, a.S, a.d, a.block_k, a.scale, beta, si, sc, stt, tt,
+                      status, next_launch_id(), stream) != cudaSuccess)
     return ATTN_ERR_CUDA;
   return ATTN_OK;
 }
@@ -603,7 +656,8 @@ attn_status_t attn_sparse_fused_fwd(const attn_bf16* q, const attn_bf16* k, cons
   if ((st = make_map(&tq, q, d, S, BH, 128)) != ATTN_OK) return st;
   if ((st = make_map(&tk, k, d, S, BH, block_k)) != ATTN_OK) return st;
   if ((st = make_map(&tv, v, d, S, BH, block_k)) != ATTN_OK) return st;
-  if (launch_pool(q, k, v, qp, kp, vp, 3, BH, S, d, block_q, stream) != cudaSuccess) return ATTN_ERR_CUDA;
+  if (launch_pool(q, k, v, qp, kp, vp, 3, BH, S, d, block_q, PoolSplit{}, status, stream) != cudaSuccess)
+    return ATTN_ERR_CUDA;
   FwdParams p = base_params(B, H, S, S, scale, kModeSparseFused, status);
   p.out = out;
   p.lse = lse;

@@ -449,7 +449,8 @@ __device__ __forceinline__ void split_merge_tail(const FwdParams& p, int bh, int
         if (c < n) wbuf[r * WS + c] = expf(ls[c] - L);
     }
     wbuf[r * WS + kMergeMaxSplit] = L;
-    if (grow < p.Sq && p.lse != nullptr) p.lse[(long long)bh * p.Sq + grow] = L;
+    if (grow < p.Sq && p.lse != nullptr && ATTN_CHECKED((long long)bh * p.Sq + grow, 1, rows, p.status))
+      p.lse[(long long)bh * p.Sq + grow] = L;
   }
   named_sync(2, 128);
   // ---- outputs: warp w merges rows w + 4 i, four at a time, lanes across d
@@ -511,7 +512,9 @@ __device__ __forceinline__ void split_merge_tail(const FwdParams& p, int bh, int
     for (int b = 0; b < RB; ++b) {
       const int i = i0 + 4 * b;
       if (i >= 128 || q_row0 + i >= p.Sq) continue;
-      uint16_t* dst = p.out + ((long long)bh * p.Sq + q_row0 + i) * D + lane * PER;
+      const long long off = ((long long)bh * p.Sq + q_row0 + i) * D + lane * PER;
+      if (!ATTN_CHECKED(off, PER, rows * D, p.status)) continue;
+      uint16_t* dst = p.out + off;
       if constexpr (PER == 4) {
         uint2 pk;
         pk.x = pack_bf16x2(o[b][0], o[b][1]);
@@ -626,8 +629,9 @@ __device__ __forceinline__ void fused_route(const FwdParams& p, int bh, int qb0,
     }
     if (i < NQB) {
       const long long rrow = (long long)bh * NQB + i;
-      if (p.out_sel_cnt != nullptr && lane == 0) p.out_sel_cnt[rrow] = cnt;
-      if (p.out_stats != nullptr && lane == 0) {
+      [[maybe_unused]] const long long nrows = (long long)p.BH * NQB;
+      if (p.out_sel_cnt != nullptr && lane == 0 && ATTN_CHECKED(rrow, 1, nrows, p.status)) p.out_sel_cnt[rrow] = cnt;
+      if (p.out_stats != nullptr && lane == 0 && ATTN_CHECKED(rrow * 4, 4, nrows * 4, p.status)) {
         p.out_stats[rrow * 4 + 0] = mu;
         p.out_stats[rrow * 4 + 1] = sigma;
         p.out_stats[rrow * 4 + 2] = tau;
@@ -635,7 +639,8 @@ __device__ __forceinline__ void fused_route(const FwdParams& p, int bh, int qb0,
       }
       if (p.out_sel_idx != nullptr) {
         __syncwarp();
-        for (int k = lane; k < cnt; k += 32) p.out_sel_idx[rrow * NKB + k] = lists[w * KMAX + k];
+        for (int k = lane; k < cnt; k += 32)
+          if (ATTN_CHECKED(rrow * NKB + k, 1, nrows * NKB, p.status)) p.out_sel_idx[rrow * NKB + k] = lists[w * KMAX + k];
       }
     }
   }
@@ -672,7 +677,9 @@ __device__ __forceinline__ void fused_route(const FwdParams& p, int bh, int qb0,
     if (e < R * D) {
       Ts[e] = acc[k];
       const int r = e / D, i = qb0 + r;
-      if (p.out_taylor != nullptr && i < NQB) p.out_taylor[((long long)bh * NQB + i) * D + e % D] = acc[k];
+      if (p.out_taylor != nullptr && i < NQB &&
+          ATTN_CHECKED(((long long)bh * NQB + i) * D + e % D, 1, (long long)p.BH * NQB * D, p.status))
+        p.out_taylor[((long long)bh * NQB + i) * D + e % D] = acc[k];
     }
   }
   // the ring is handed over to TMA (async proxy) after these generic accesses
@@ -1279,11 +1286,13 @@ __global__ void __launch_bounds__(NQT * 128 + 128, (NQT == 1) ? 2 : 1)
               o4.y = have_o ? __uint_as_float(rr[j + 1]) * inv : 0.f;
               o4.z = have_o ? __uint_as_float(rr[j + 2]) * inv : 0.f;
               o4.w = have_o ? __uint_as_float(rr[j + 3]) * inv : 0.f;
-              *reinterpret_cast<float4*>(dst + c0 + j) = o4;
+              if (ATTN_CHECKED(orow * D + c0 + j, 4, (long long)p.n_split * p.BH * p.Sq * D, p.status))
+                *reinterpret_cast<float4*>(dst + c0 + j) = o4;
             }
           }
         }
-        if (row_valid) p.lse_part[orow] = empty ? -INFINITY : (m_run + __log2f(l_run)) * kLn2;
+        if (row_valid && ATTN_CHECKED(orow, 1, (long long)p.n_split * p.BH * p.Sq, p.status))
+          p.lse_part[orow] = empty ? -INFINITY : (m_run + __log2f(l_run)) * kLn2;
       } else {
         // Taylor term for the rejected blocks of this row's query block
         float f = 0.f;
@@ -1337,11 +1346,12 @@ __global__ void __launch_bounds__(NQT * 128 + 128, (NQT == 1) ? 2 : 1)
               pk.y = pack_bf16x2(o[2], o[3]);
               pk.z = pack_bf16x2(o[4], o[5]);
               pk.w = pack_bf16x2(o[6], o[7]);
-              *reinterpret_cast<uint4*>(dst + c0 + j) = pk;
+              if (ATTN_CHECKED(((long long)bh * p.Sq + grow) * D + c0 + j, 8, (long long)p.BH * p.Sq * D, p.status))
+                *reinterpret_cast<uint4*>(dst + c0 + j) = pk;
             }
           }
         }
-        if (row_valid && p.lse != nullptr)
+        if (row_valid && p.lse != nullptr && ATTN_CHECKED((long long)bh * p.Sq + grow, 1, (long long)p.BH * p.Sq, p.status))
           p.lse[(long long)bh * p.Sq + grow] = empty ? -INFINITY : (m_run + __log2f(l_run)) * kLn2;
       }
     }

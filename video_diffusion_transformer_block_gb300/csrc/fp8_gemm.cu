@@ -48,17 +48,15 @@ __device__ __forceinline__ void row_scales(float amax, float& s, float& inv) {
 }
 
 // The code of a bf16 value x is the E4M3 value nearest to the exact quotient
-// x * 448 / amax (ties to even).  The product x * inv, with inv the rounded
-// inverse scale, lies within two float roundings of that quotient, so it
-// decides the same code unless it sits within a few float steps of an E4M3
-// rounding midpoint; for those values, and for the E4M3 subnormal grid
-// (0 < |v| < 2^-6), the quotient is formed again with one correctly rounded
-// division.  For bf16 operands that decides exactly: x * 0.875 is exact, and a
-// quotient of bf16 values either is a midpoint (at most five significant bits,
-// so the division returns it exactly) or lies at least 2^-13 of its size away
-// from every midpoint.  Tiny rows are scaled by 2^64 first so that no operand
-// of the division is subnormal.
-__device__ __noinline__ float exact_quotient(float x, float amax) {
+// x * 448 / amax (ties to even).  The product v = x * inv with the rounded
+// inverse scale inv lies within two float steps of that quotient, so it decides
+// the same code unless it sits next to an E4M3 rounding midpoint.  Where it
+// might, the quotient is formed again with one correctly rounded division,
+// which for bf16 operands decides exactly: x * 0.875 is exact, and a quotient of bf16
+// values either is a midpoint (returned exactly by the division) or lies at
+// least 2^-13 of its size away from every midpoint.  Tiny rows are scaled by
+// 2^64 first so that no operand of the division is subnormal.
+__device__ __forceinline__ float exact_quotient(float x, float amax) {
   if (amax < 0x1p-60f) {
     x *= 0x1p64f;
     amax *= 0x1p64f;
@@ -66,29 +64,49 @@ __device__ __noinline__ float exact_quotient(float x, float amax) {
   return __fmul_rn(__fdiv_rn(__fmul_rn(x, 0.875f), amax), 512.0f);
 }
 
-__device__ __forceinline__ uint32_t e4m3_code(float x, float inv, float amax) {
-  float v = __fmul_rn(x, inv);
-  const uint32_t u = __float_as_uint(v) & 0x7fffffffu;
-  // |v| in (0, 2^-6), or within 8 float steps of the midpoint of the E4M3 step
-  // (the low 20 mantissa bits are the position inside a step of the normal range)
-  const bool near = (u - 1u < 0x3C7FFFFFu) || (((u & 0xFFFFFu) - 0x7FFF8u) <= 16u);
-  if (near) v = exact_quotient(x, amax);
-  return (uint32_t)__nv_cvt_float_to_fp8(v, __NV_SATFINITE, __NV_E4M3);
+// Whether the product with the rounded inverse scale may decide a code other
+// than the exact quotient for some value of the row in the normal E4M3 range
+// (|v| >= 2^-6).  There the decision depends only on the value's bf16
+// significand, so thread t (0..127) tries the significand 1 + t/128 at the
+// row's scale (x = (1 + t/128) * 2^(E-1) with amax in [2^E, 2^(E+1)), so that
+// x * 448 / amax lies in (112, 448)) both ways: the product and the exact
+// division.  The row is flagged when any significand's codes differ (about
+// 2% of random rows); flagged rows take every code from the division.
+__device__ __forceinline__ bool row_product_differs(float amax, float inv, int t) {
+  const uint32_t e = __float_as_uint(amax) >> 23;   // biased exponent of amax (> 8 for a non-flushed row)
+  const float x = __uint_as_float(((e - 1u) << 23) | ((uint32_t)(t & 127) << 16));
+  const uint32_t fast = (uint32_t)__nv_cvt_float_to_fp8(__fmul_rn(x, inv), __NV_SATFINITE, __NV_E4M3);
+  const uint32_t exact = (uint32_t)__nv_cvt_float_to_fp8(exact_quotient(x, amax), __NV_SATFINITE, __NV_E4M3);
+  return fast != exact;
 }
 
-// Codes of 8 values.
-__device__ __forceinline__ uint2 quantize8(const uint4& v, float inv, float amax) {
-  float f[8];
+// Two codes in one conversion (round to nearest even, saturating at +-448):
+// `lo` in the low byte, `hi` in the high byte.
+__device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Codes of 8 values: from the products, except values on the E4M3 subnormal
+// grid (0 < |v| < 2^-6, where the grid is not scale-free) and every value of a
+// flagged row, which take the exact division.
+__device__ __forceinline__ uint2 quantize8(const uint4& v, float inv, float amax, bool row_exact) {
+  float f[8], t[8];
   unpack8(v, f);
-  uint32_t lo = 0, hi = 0;
+  bool sub = false;
 #pragma unroll
   for (int e = 0; e < 8; ++e) {
-    const uint32_t c = e4m3_code(f[e], inv, amax);
-    if (e < 4)
-      lo |= c << (8 * e);
-    else
-      hi |= c << (8 * (e - 4));
+    t[e] = __fmul_rn(f[e], inv);
+    sub |= fabsf(t[e]) < 0x1p-6f && t[e] != 0.f;
   }
+  if (sub || row_exact) {
+#pragma unroll
+    for (int e = 0; e < 8; ++e)
+      if (row_exact || (fabsf(t[e]) < 0x1p-6f && t[e] != 0.f)) t[e] = exact_quotient(f[e], amax);
+  }
+  const uint32_t lo = e4m3x2(t[0], t[1]) | (e4m3x2(t[2], t[3]) << 16);
+  const uint32_t hi = e4m3x2(t[4], t[5]) | (e4m3x2(t[6], t[7]) << 16);
   return make_uint2(lo, hi);
 }
 
@@ -97,7 +115,8 @@ __device__ __forceinline__ uint2 quantize8(const uint4& v, float inv, float amax
 // first pass has just brought into L1.
 __global__ void __launch_bounds__(kQuantThreads) fp8_quantize_rows_kernel(const uint16_t* __restrict__ x,
                                                                           uint8_t* __restrict__ q,
-                                                                          float* __restrict__ scale, int K) {
+                                                                          float* __restrict__ scale, int K,
+                                                                          int* status) {
   const long long row = blockIdx.x;
   const uint16_t* xr = x + row * K;
   uint8_t* qr = q + row * K;
@@ -118,9 +137,12 @@ __global__ void __launch_bounds__(kQuantThreads) fp8_quantize_rows_kernel(const 
   for (int w = 1; w < kQuantThreads / 32; ++w) amax = fmaxf(amax, red[w]);
   float s, inv;
   row_scales(amax, s, inv);
-  if (threadIdx.x == 0) scale[row] = s;
+  const bool row_exact = __syncthreads_or(inv != 0.f && row_product_differs(amax, inv, threadIdx.x));
+  [[maybe_unused]] const long long M = gridDim.x;
+  if (threadIdx.x == 0 && ATTN_CHECKED(row, 1, M, status)) scale[row] = s;
   for (int i = threadIdx.x * 8; i < K; i += kQuantThreads * 8)
-    *reinterpret_cast<uint2*>(qr + i) = quantize8(*reinterpret_cast<const uint4*>(xr + i), inv, amax);
+    if (ATTN_CHECKED(row * K + i, 8, M * K, status))
+      *reinterpret_cast<uint2*>(qr + i) = quantize8(*reinterpret_cast<const uint4*>(xr + i), inv, amax, row_exact);
 }
 
 // One CTA of 128 threads per row for rows of up to NV * 1024 elements: each
@@ -129,7 +151,7 @@ __global__ void __launch_bounds__(kQuantThreads) fp8_quantize_rows_kernel(const 
 template <int NV>
 __global__ void __launch_bounds__(128) fp8_quantize_rows_reg_kernel(const uint16_t* __restrict__ x,
                                                                     uint8_t* __restrict__ q,
-                                                                    float* __restrict__ scale, int K) {
+                                                                    float* __restrict__ scale, int K, int* status) {
   const long long row = blockIdx.x;
   const uint16_t* xr = x + row * K;
   uint8_t* qr = q + row * K;
@@ -155,11 +177,14 @@ __global__ void __launch_bounds__(128) fp8_quantize_rows_reg_kernel(const uint16
   amax = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
   float s, inv;
   row_scales(amax, s, inv);
-  if (threadIdx.x == 0) scale[row] = s;
+  const bool row_exact = __syncthreads_or(inv != 0.f && row_product_differs(amax, inv, threadIdx.x));
+  [[maybe_unused]] const long long M = gridDim.x;
+  if (threadIdx.x == 0 && ATTN_CHECKED(row, 1, M, status)) scale[row] = s;
 #pragma unroll
   for (int c = 0; c < NV; ++c) {
     const int i = (c * 128 + threadIdx.x) * 8;
-    if (i < K) __stcs(reinterpret_cast<uint2*>(qr + i), quantize8(v[c], inv, amax));
+    if (i < K && ATTN_CHECKED(row * K + i, 8, M * K, status))
+      __stcs(reinterpret_cast<uint2*>(qr + i), quantize8(v[c], inv, amax, row_exact));
   }
 }
 
@@ -326,7 +351,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
               pk.y = pack_bf16x2(o[2], o[3]);
               pk.z = pack_bf16x2(o[4], o[5]);
               pk.w = pack_bf16x2(o[6], o[7]);
-              *reinterpret_cast<uint4*>(dst + col) = pk;
+              if (ATTN_CHECKED(grow * N + col, 8, (long long)M * N, status)) *reinterpret_cast<uint4*>(dst + col) = pk;
             }
           }
         }
@@ -347,15 +372,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
 }  // namespace
 
-cudaError_t launch_fp8_quantize_rows(const uint16_t* x, uint8_t* q, float* scale, int M, int K, cudaStream_t stream) {
+cudaError_t launch_fp8_quantize_rows(const uint16_t* x, uint8_t* q, float* scale, int M, int K, int* status,
+                                     cudaStream_t stream) {
   if (K <= 1024)
-    fp8_quantize_rows_reg_kernel<1><<<M, 128, 0, stream>>>(x, q, scale, K);
+    fp8_quantize_rows_reg_kernel<1><<<M, 128, 0, stream>>>(x, q, scale, K, status);
   else if (K <= 2048)
-    fp8_quantize_rows_reg_kernel<2><<<M, 128, 0, stream>>>(x, q, scale, K);
+    fp8_quantize_rows_reg_kernel<2><<<M, 128, 0, stream>>>(x, q, scale, K, status);
   else if (K <= 4096)
-    fp8_quantize_rows_reg_kernel<4><<<M, 128, 0, stream>>>(x, q, scale, K);
+    fp8_quantize_rows_reg_kernel<4><<<M, 128, 0, stream>>>(x, q, scale, K, status);
   else
-    fp8_quantize_rows_kernel<<<M, kQuantThreads, 0, stream>>>(x, q, scale, K);
+    fp8_quantize_rows_kernel<<<M, kQuantThreads, 0, stream>>>(x, q, scale, K, status);
   return cudaGetLastError();
 }
 

@@ -8,18 +8,35 @@
 
 namespace vdtb {
 
+// Optional tf32 hi / lo copies the pool kernel writes for the tensor-core
+// routing: pooled keys [BH][NB][D] (kh, kl) and transposed pooled values
+// [BH][D][NBp] (vth, vtl; NBp = NB rounded up to a multiple of 4).  Null
+// pointers: not written.
+struct PoolSplit {
+  float* kh = nullptr;
+  float* kl = nullptr;
+  float* vth = nullptr;
+  float* vtl = nullptr;
+  int NBp = 0;
+};
+
 // Block mean-pool of `ntensors` (1..3) bf16 tensors [BH][S][D] into fp32 [BH][NB][D].
 cudaError_t launch_pool(const uint16_t* x0, const uint16_t* x1, const uint16_t* x2, float* p0, float* p1, float* p2,
-                        int ntensors, int BH, int S, int D, int block, cudaStream_t stream);
+                        int ntensors, int BH, int S, int D, int block, const PoolSplit& split, int* status,
+                        cudaStream_t stream);
 
-// Sol-Attn routing from pooled tensors (one CTA per head and 32 query blocks).
-cudaError_t launch_route(const float* qp, const float* kp, const float* vp, int BH, int NQB, int NKB, int S, int D,
-                         int block_k, float scale, float beta, int32_t* sel_idx, int32_t* sel_cnt, float* stats,
-                         float* taylor_t, cudaStream_t stream);
+// Sol-Attn routing on the tensor cores (route_tc.cu): one CTA per head and 128
+// query blocks.  tkh / tkl: 3-D fp32 maps of the pooled keys' hi / lo (dims
+// D, NKB, BH; box 32 x 128); tvh / tvl: of the transposed pooled values' hi /
+// lo (dims NKB, D, BH; box 32 x D); qp: pooled queries [BH][NQB][D].
+cudaError_t launch_route_tc(const CUtensorMap& tkh, const CUtensorMap& tkl, const CUtensorMap& tvh,
+                            const CUtensorMap& tvl, const float* qp, int BH, int NQB, int NKB, int S, int D,
+                            int block_k, float scale, float beta, int32_t* sel_idx, int32_t* sel_cnt, float* stats,
+                            float* taylor_t, int* status, unsigned launch_id, cudaStream_t stream);
 
 // Exact log-sum-exp merge of n partials, rows = B*H*Sq.
 cudaError_t launch_merge(const float* o_part, const float* lse_part, uint16_t* out, float* lse, int n, long long rows,
-                         int D, cudaStream_t stream);
+                         int D, int* status, cudaStream_t stream);
 
 // tcgen05 attention forward.  mode: kModeDense / kModeSparse / kModeSplit.
 cudaError_t launch_attn_fwd_d64(int BK, int mode, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
@@ -41,7 +58,8 @@ inline int fwd_query_tiles(int mode) {
 constexpr int kFusedMaxNKB = 1024;
 
 // Per-row E4M3 quantisation of x [M][K] bf16 (K % 8 == 0): codes q [M][K], scale [M].
-cudaError_t launch_fp8_quantize_rows(const uint16_t* x, uint8_t* q, float* scale, int M, int K, cudaStream_t stream);
+cudaError_t launch_fp8_quantize_rows(const uint16_t* x, uint8_t* q, float* scale, int M, int K, int* status,
+                                     cudaStream_t stream);
 
 // y [M][N] bf16 = diag(sa) (Aq Wq^T) diag(sw); ta / tb: 2-D uint8 maps of Aq [M][K]
 // (box 128 x 128) and Wq [N][K] (box 128 x 256), 128-byte swizzle.

@@ -53,6 +53,23 @@ __device__ __forceinline__ bool launch_aborted(const int* status, unsigned launc
   return *reinterpret_cast<const volatile unsigned*>(status + 1) == launch_id;
 }
 
+// Bounds-checked build (-DATTN_DEBUG): every global store of the kernels is
+// guarded by ATTN_CHECKED(first, count, extent, status), which is true when
+// elements [first, first + count) lie inside [0, extent) of the buffer; a store
+// outside is skipped and reported in the status word (ATTN_DEVICE_OOB) instead
+// of writing past the buffer.  In the regular build the guard is `true`.
+#ifdef ATTN_DEBUG
+__device__ __forceinline__ bool checked_store(long long first, long long count, long long extent, int* status) {
+  if (first >= 0 && first + count <= extent) return true;
+  atomicOr(status, ATTN_DEVICE_OOB);
+  return false;
+}
+#define ATTN_CHECKED(first, count, extent, status) \
+  ::vdtb::checked_store((long long)(first), (long long)(count), (long long)(extent), (status))
+#else
+#define ATTN_CHECKED(first, count, extent, status) true
+#endif
+
 // ---------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
@@ -164,6 +181,24 @@ __device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_
 __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc, uint32_t accum) {
   asm volatile(
       "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accum));
+}
+// Instruction descriptor of kind::tf32 with tf32 A/B (both K-major) and f32 accumulator.
+__host__ __device__ constexpr uint32_t idesc_tf32_f32(int M, int N) {
+  return (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+// D[tmem] (+)= A[smem] * B[smem], tf32 operands (K = 8 per instruction)
+__device__ __forceinline__ void mma_ss_tf32(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                            uint32_t accum) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accum));
+}
+// D[tmem] (+)= A[tmem] * B[smem], tf32 operands; A holds one element per TMEM column
+__device__ __forceinline__ void mma_ts_tf32(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                            uint32_t accum) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
       "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accum));
 }
 // Arrive once on `bar` when every tcgen05 op issued so far by this thread has completed.
