@@ -541,10 +541,13 @@ attn_status_t run_route(const SparseArgs& a, float beta, void* workspace, size_t
   if ((st = make_map_f32(&tkl, split.kl, d, nk, BH, d * 4, nk * d * 4, 32, 128)) != ATTN_OK) return st;
   if ((st = make_map_f32(&tvh, split.vth, nk, d, BH, nkp * 4, d * nkp * 4, 32, (uint32_t)d)) != ATTN_OK) return st;
   if ((st = make_map_f32(&tvl, split.vtl, nk, d, BH, nkp * 4, d * nkp * 4, 32, (uint32_t)d)) != ATTN_OK) return st;
+  CUtensorMap tqp;
+  const uint64_t nq = (uint64_t)NQB;
+  if ((st = make_map_f32(&tqp, qp, d, nq, BH, d * 4, nq * d * 4, 32, 128)) != ATTN_OK) return st;
   if (launch_pool(a.q, a.k, a.v, qp, kp, vp, 3, BH, a.S, a.d, a.block_q, split, status, stream) != cudaSuccess)
     return ATTN_ERR_CUDA;
-  if (launch_route_tc(tkh, tkl, tvh, tvl, qp, BH, NQB, NKB, a.S, a.d, a.block_k, a.scale, beta, si, sc, stt, tt,
-                      status, next_launch_id(), stream) != cudaSuccess)
+  if (launch_route_tc(tkh, tkl, tvh, tvl, tqp, qp, kp, vp, BH, NQB, NKB, a.S, a.d, a.block_k, a.scale, beta, si, sc,
+                      stt, tt, status, next_launch_id(), stream) != cudaSuccess)
     return ATTN_ERR_CUDA;
   return ATTN_OK;
 }

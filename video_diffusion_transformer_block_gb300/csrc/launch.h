@@ -25,14 +25,17 @@ cudaError_t launch_pool(const uint16_t* x0, const uint16_t* x1, const uint16_t* 
                         int ntensors, int BH, int S, int D, int block, const PoolSplit& split, int* status,
                         cudaStream_t stream);
 
-// Sol-Attn routing on the tensor cores (route_tc.cu): one CTA per head and 128
-// query blocks.  tkh / tkl: 3-D fp32 maps of the pooled keys' hi / lo (dims
+// Sol-Attn routing (route_tc.cu): on the tensor cores, one CTA per head and 128
+// query blocks, and a short last tile of up to 32 blocks per head on the CUDA
+// cores beside it.  tkh / tkl: 3-D fp32 maps of the pooled keys' hi / lo (dims
 // D, NKB, BH; box 32 x 128); tvh / tvl: of the transposed pooled values' hi /
-// lo (dims NKB, D, BH; box 32 x D); qp: pooled queries [BH][NQB][D].
+// lo (dims NKB, D, BH; box 32 x D); tq: of the pooled queries [BH][NQB][D]
+// (dims D, NQB, BH; box 32 x 128); qp / kp / vp: the pooled tensors in fp32.
 cudaError_t launch_route_tc(const CUtensorMap& tkh, const CUtensorMap& tkl, const CUtensorMap& tvh,
-                            const CUtensorMap& tvl, const float* qp, int BH, int NQB, int NKB, int S, int D,
-                            int block_k, float scale, float beta, int32_t* sel_idx, int32_t* sel_cnt, float* stats,
-                            float* taylor_t, int* status, unsigned launch_id, cudaStream_t stream);
+                            const CUtensorMap& tvl, const CUtensorMap& tq, const float* qp, const float* kp,
+                            const float* vp, int BH, int NQB, int NKB, int S, int D, int block_k, float scale,
+                            float beta, int32_t* sel_idx, int32_t* sel_cnt, float* stats, float* taylor_t, int* status,
+                            unsigned launch_id, cudaStream_t stream);
 
 // Exact log-sum-exp merge of n partials, rows = B*H*Sq.
 cudaError_t launch_merge(const float* o_part, const float* lse_part, uint16_t* out, float* lse, int n, long long rows,

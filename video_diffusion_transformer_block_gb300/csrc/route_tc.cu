@@ -9,7 +9,8 @@
 // and "Proxy-score reuse" (the rejected blocks' first-order Taylor term).
 //
 // CTA = one head and a tile of 128 query blocks; TMEM lane r holds query block
-// i0 + r.  Both products are tcgen05 GEMMs with fp32-grade accuracy from three
+// i0 + r.  (A short last tile of up to 32 blocks goes to the CUDA-core kernel
+// at the end of this file instead.)  Both products are tcgen05 GEMMs with fp32-grade accuracy from three
 // tf32 products: every operand x is split into hi = x with its 13 low mantissa
 // bits cleared (a tf32 value) and lo = x - hi (exact in fp32), and
 // X.Y = Xh.Yh + Xh.Yl + Xl.Yh; the dropped Xl.Yl and the tf32 rounding of the
@@ -30,8 +31,10 @@
 //
 // Warps 0-7: row threads, two per query block: warp w reads TMEM lanes
 // 32 (w % 4) .. + 32 (its lane = its row) and half h = w / 4 of every chunk's
-// 128 columns.  Warp 8, lane 0: TMA producer.  Warp 9, lane 0: MMA issuer (and
-// TMEM owner).  TMEM columns: Qbar hi [0, D), Qbar lo [D, 2D), S [256, 384),
+// 128 columns.  Warp 8, lane 0: TMA producer of the pooled-key ring.  Warp 9,
+// lane 0: MMA issuer (and TMEM owner).  Warp 10, lane 0: TMA producer of the
+// pooled-value ring (its own thread, so value loads start at once and never
+// wait behind a key slot).  TMEM columns: Qbar hi [0, D), Qbar lo [D, 2D), S [256, 384),
 // T [384, 384 + D).
 #include <math.h>
 #include <stdint.h>
@@ -45,7 +48,7 @@ constexpr int kRtRows = 128;      // query blocks per CTA
 constexpr int kRtChunk = 128;     // key blocks per proxy chunk (two halves of 64, one per row thread)
 constexpr int kRtKStages = 2;     // pooled-key ring: one 32-wide d-slice of a chunk (hi + lo) per stage
 constexpr int kRtVStages = 2;     // transposed pooled-value ring: one 32-wide key slice (hi + lo)
-constexpr int kRtThreads = 320;
+constexpr int kRtThreads = 352;
 constexpr int kRtRowThreads = 256;
 constexpr uint32_t kRtTmemCols = 512;
 constexpr uint32_t kColS = 256, kColT = 384;
@@ -168,7 +171,8 @@ template <int D>
 __global__ void __launch_bounds__(kRtThreads, 1)
     route_tc_kernel(const __grid_constant__ CUtensorMap tm_kh, const __grid_constant__ CUtensorMap tm_kl,
                     const __grid_constant__ CUtensorMap tm_vh, const __grid_constant__ CUtensorMap tm_vl,
-                    const float* __restrict__ qp, int NQB, int NKB, int S, int block_k, float scale, float beta,
+                    const __grid_constant__ CUtensorMap tm_q, int n_tiles, int NQB, int NKB, int S, int block_k,
+                    float scale, float beta,
                     int32_t* __restrict__ sel_idx, int32_t* __restrict__ sel_cnt, float* __restrict__ stats,
                     float* __restrict__ taylor_t, int* status, unsigned launch_id) {
   using Cfg = RtCfg<D>;
@@ -180,7 +184,7 @@ __global__ void __launch_bounds__(kRtThreads, 1)
   uint8_t* sW = sV + kRtVStages * Cfg::kVStageBytes;
   __shared__ uint64_t kfull[kRtKStages], kempty[kRtKStages], vfull[kRtVStages], vempty[kRtVStages];
   __shared__ uint64_t wfull[2], wfree[2];
-  __shared__ uint64_t q_ready, s_full, s_free, t_done, mma_done;
+  __shared__ uint64_t q_ready, q_full, s_full, s_free, t_done, mma_done;
   __shared__ uint32_t tmem_base_sh;
   __shared__ WaitState wstate;
   __shared__ int skip_cta;
@@ -191,8 +195,7 @@ __global__ void __launch_bounds__(kRtThreads, 1)
   WaitState* const wc = &wstate;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int n_tiles = (NQB + kRtRows - 1) / kRtRows;
-  const long long bh = blockIdx.x / n_tiles;
+  const long long bh = blockIdx.x / n_tiles;   // n_tiles: tiles of this head in the grid
   const int i0 = (blockIdx.x % n_tiles) * kRtRows;
   [[maybe_unused]] const long long nrows = (long long)(gridDim.x / n_tiles) * NQB;   // B * H * NQB
   const int nch = (NKB + kRtChunk - 1) / kRtChunk;
@@ -211,6 +214,7 @@ __global__ void __launch_bounds__(kRtThreads, 1)
       mbar_init(&wfree[b], 1);
     }
     mbar_init(&q_ready, kRtRowThreads);
+    mbar_init(&q_full, 1);
     mbar_init(&s_full, 1);
     mbar_init(&s_free, kRtRowThreads);
     mbar_init(&t_done, 1);
@@ -223,16 +227,20 @@ __global__ void __launch_bounds__(kRtThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_base_sh;
+  // a tail-rows kernel launched after this one may start on the SMs this grid leaves idle
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   if (!skip_cta) {
-    if (warp == 8) {
-      // ======================= TMA producer =======================
-      if (lane == 0) {
+    if (warp == 8 || warp == 10) {
+      // ======================= TMA producers (8: pooled keys, 10: transposed pooled values) =======================
+      if (lane == 0 && warp == 8) {
+        // the tile's pooled queries (fp32) into the weight buffers, which stay idle until pass 2
+        mbar_expect_tx(&q_full, D * kRtRows * 4);
+#pragma unroll
+        for (int b = 0; b < D / 32; ++b) tma_load_3d(sW + b * (kRtRows * 128), &tm_q, &q_full, 32 * b, i0, (int)bh);
         tma_prefetch_desc(&tm_kh);
         tma_prefetch_desc(&tm_kl);
-        tma_prefetch_desc(&tm_vh);
-        tma_prefetch_desc(&tm_vl);
-        int kl = 0, vl = 0;   // loads issued into each ring
+        int kl = 0;   // loads issued into the ring
         auto load_k = [&](int c) -> bool {
           for (int s = 0; s < kDS; ++s, ++kl) {
             const int st = kl % kRtKStages;
@@ -244,34 +252,37 @@ __global__ void __launch_bounds__(kRtThreads, 1)
           }
           return true;
         };
-        auto load_v = [&](int c) -> bool {
+        // the order the MMA issuer consumes them: every chunk in pass 1, then again in pass 2
+        bool ok = true;
+        for (int c = 0; ok && c < nch; ++c) ok = load_k(c);
+        for (int c = 0; ok && c < nch; ++c) ok = load_k(c);
+        // drain: no copy may still be landing when the CTA exits
+        for (int j = (kl > kRtKStages ? kl - kRtKStages : 0); j < kl; ++j)
+          drain_wait(&kfull[j % kRtKStages], (j / kRtKStages) & 1, wc);
+        drain_wait(&q_full, 0, wc);
+      } else if (lane == 0) {
+        tma_prefetch_desc(&tm_vh);
+        tma_prefetch_desc(&tm_vl);
+        int vl = 0;
+        bool ok = true;
+        for (int c = 0; ok && c < nch; ++c) {
           const int nj = min(kRtChunk, NKB - kRtChunk * c);
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
             const int js = rt_slice_js(k);
-            if (32 * js >= nj) continue;
+            if (!ok || 32 * js >= nj) continue;
             const int st = vl % kRtVStages;
-            if (vl >= kRtVStages && !bounded_wait(&vempty[st], ((vl / kRtVStages) - 1) & 1, wc)) return false;
+            if (vl >= kRtVStages && !bounded_wait(&vempty[st], ((vl / kRtVStages) - 1) & 1, wc)) {
+              ok = false;
+              continue;
+            }
             uint8_t* dst = sV + st * Cfg::kVStageBytes;
             mbar_expect_tx(&vfull[st], Cfg::kVStageBytes);
             tma_load_3d(dst, &tm_vh, &vfull[st], kRtChunk * c + 32 * js, 0, (int)bh);
             tma_load_3d(dst + Cfg::kVHalf, &tm_vl, &vfull[st], kRtChunk * c + 32 * js, 0, (int)bh);
             ++vl;
           }
-          return true;
-        };
-        // the order the MMA issuer consumes them: pass 1 every key chunk; pass 2 chunk 0, then
-        // per chunk c the keys of chunk c + 1 and the values of chunk c
-        bool ok = true;
-        for (int c = 0; ok && c < nch; ++c) ok = load_k(c);
-        if (ok) ok = load_k(0);
-        for (int c = 0; ok && c < nch; ++c) {
-          if (c + 1 < nch) ok = load_k(c + 1);
-          if (ok) ok = load_v(c);
         }
-        // drain: no copy may still be landing when the CTA exits
-        for (int j = (kl > kRtKStages ? kl - kRtKStages : 0); j < kl; ++j)
-          drain_wait(&kfull[j % kRtKStages], (j / kRtKStages) & 1, wc);
         for (int j = (vl > kRtVStages ? vl - kRtVStages : 0); j < vl; ++j)
           drain_wait(&vfull[j % kRtVStages], (j / kRtVStages) & 1, wc);
       }
@@ -357,21 +368,24 @@ __global__ void __launch_bounds__(kRtThreads, 1)
       const int i = i0 + r;
       const bool valid = i < NQB;
       const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-      // Qbar_i * scale, split into tf32 hi / lo, into this row's TMEM lane: half 0 stores hi, half 1 lo
+      // Qbar_i * scale, split into tf32 hi / lo, into this row's TMEM lane: half 0 stores hi, half 1 lo.
+      // The tile arrives by TMA (128B-swizzled boxes of 32 columns), so each thread reads its row from
+      // shared memory without bank conflicts.
       {
-        const float* qrow = qp + (bh * NQB + (valid ? i : 0)) * D;
+        bool qok = __all_sync(0xffffffffu, bounded_wait(&q_full, 0, wc));
 #pragma unroll
         for (int c0 = 0; c0 < D; c0 += 32) {
+          const uint8_t* box = sW + (c0 / 32) * (kRtRows * 128) + r * 128;
           uint32_t part[32];
 #pragma unroll
-          for (int e = 0; e < 32; e += 4) {
-            const float4 q4 =
-                valid ? __ldg(reinterpret_cast<const float4*>(qrow + c0 + e)) : make_float4(0.f, 0.f, 0.f, 0.f);
-            const float qs[4] = {q4.x * scale, q4.y * scale, q4.z * scale, q4.w * scale};
+          for (int c = 0; c < 8; ++c) {
+            const float4 v4 = qok ? *reinterpret_cast<const float4*>(box + ((c ^ (r & 7)) << 4))
+                                  : make_float4(0.f, 0.f, 0.f, 0.f);
+            const float qs[4] = {v4.x * scale, v4.y * scale, v4.z * scale, v4.w * scale};
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
               const float h = tf32_hi(qs[u]);
-              part[e + u] = __float_as_uint(half == 0 ? h : qs[u] - h);
+              part[4 * c + u] = __float_as_uint(half == 0 ? h : qs[u] - h);
             }
           }
           tmem_st32(tmem + lane_base + half * D + c0, part);
@@ -533,7 +547,13 @@ __global__ void __launch_bounds__(kRtThreads, 1)
         if (ATTN_CHECKED((bh * NQB + i) * 4 + 3, 1, nrows * 4, status)) stats[(bh * NQB + i) * 4 + 3] = W;
         if (ATTN_CHECKED(bh * NQB + i, 1, nrows, status)) sel_cnt[bh * NQB + i] = cnt;
       }
-      if (ok && __all_sync(0xffffffffu, bounded_wait(&t_done, 0, wc))) {
+      // T: out of TMEM into the idle key ring (row r's 16-byte chunk c at position c ^ (r & 31), so
+      // that both the row-wise writes and the later chunk-wise reads are free of bank conflicts), then
+      // each warp stores whole rows to global memory with coalesced 512-byte writes
+      const bool tok = ok && __all_sync(0xffffffffu, bounded_wait(&t_done, 0, wc)) && !wstate.abort;
+      constexpr int kChunks = D / 4;   // 16-byte chunks per T row
+      float* sT = reinterpret_cast<float*>(sK);
+      if (tok) {
         tc_fence_after();
         constexpr int kHalfD = D / 2;
         const uint32_t tT = tmem + lane_base + kColT + half * kHalfD;
@@ -543,14 +563,24 @@ __global__ void __launch_bounds__(kRtThreads, 1)
           tmem_ld32(tT + c0, rr);
           tmem_ld_wait();
           tmem_reg_fence(rr);
-          if (valid) {
-            const long long off = (bh * NQB + i) * D + half * kHalfD + c0;
-            float* dst = taylor_t + off;
 #pragma unroll
-            for (int e = 0; e < 32; e += 4)
-              if (ATTN_CHECKED(off + e, 4, nrows * D, status))
-                *reinterpret_cast<float4*>(dst + e) = make_float4(__uint_as_float(rr[e]), __uint_as_float(rr[e + 1]),
-                                                                  __uint_as_float(rr[e + 2]), __uint_as_float(rr[e + 3]));
+          for (int e = 0; e < 32; e += 4) {
+            const int chunk = (half * kHalfD + c0 + e) / 4;
+            *reinterpret_cast<float4*>(sT + r * D + 4 * (chunk ^ (r & (kChunks - 1)))) =
+                make_float4(__uint_as_float(rr[e]), __uint_as_float(rr[e + 1]), __uint_as_float(rr[e + 2]),
+                            __uint_as_float(rr[e + 3]));
+          }
+        }
+      }
+      rows_sync();
+      if (tok) {
+        for (int row = warp; row < kRtRows; row += 8) {
+          const int ig = i0 + row;
+          if (ig >= NQB) break;
+          for (int chunk = lane; chunk < kChunks; chunk += 32) {
+            const float4 v4 = *reinterpret_cast<const float4*>(sT + row * D + 4 * (chunk ^ (row & (kChunks - 1))));
+            const long long off = (bh * NQB + ig) * D + 4 * chunk;
+            if (ATTN_CHECKED(off, 4, nrows * D, status)) *reinterpret_cast<float4*>(taylor_t + off) = v4;
           }
         }
       }
@@ -565,27 +595,254 @@ __global__ void __launch_bounds__(kRtThreads, 1)
   }
 }
 
+// ============================================================ tail rows on the CUDA cores
+// The tensor-core kernel works on tiles of 128 query blocks, one CTA per SM.
+// A head whose query-block count leaves a short last tile (the Stage-2
+// sequence: 513 blocks = 4 x 128 + 1) would spend a whole CTA, with all of its
+// key and value traffic, on a few rows, and push the grid into a second wave.
+// Those rows go to this kernel instead, one CTA per (head, row), which runs
+// beside the tensor-core kernel on the SMs it leaves idle (programmatic
+// dependent launch).  Same definitions in fp32 on the CUDA cores: the row's
+// proxies s_j = (scale Qbar_i) . Kbar_j, one warp per key block (coalesced
+// 512-byte row loads, shuffle reduction), are kept in shared memory (so the
+// selection pass needs no recomputation); mean, population std and argmax
+// (lowest j on ties) by block reductions; selection s_j >= tau or the argmax,
+// compacted in ascending j with ballot/popc; Taylor weights w_j = n_j max(0,
+// 1 + s_j - mu) of the rejected blocks; W = sum w_j and T = sum w_j Vbar_j with
+// every thread holding a float4 of columns for one residue class of j.
+constexpr int kTailThreads = 256;
+constexpr int kTailWarps = kTailThreads / 32;
+
+__device__ __forceinline__ float tail_block_sum(float v, float* red) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+  __syncthreads();
+  float t = 0.f;
+#pragma unroll
+  for (int w = 0; w < kTailWarps; ++w) t += red[w];
+  return t;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kTailThreads) route_tail_kernel(
+    const float* __restrict__ qp, const float* __restrict__ kp, const float* __restrict__ vp, int NQB, int NKB, int S,
+    int block_k, float scale, float beta, int32_t* __restrict__ sel_idx, int32_t* __restrict__ sel_cnt,
+    float* __restrict__ stats, float* __restrict__ taylor_t, int row_lo, int* status) {
+  extern __shared__ __align__(16) float srow[];   // NKB proxies, then Taylor weights
+  __shared__ float qs[D];
+  __shared__ float red[kTailWarps];
+  __shared__ int redi[kTailWarps];
+  __shared__ float tred[kTailThreads / (D / 4)][D];
+  const int nrow = NQB - row_lo;
+  const long long bh = blockIdx.x / nrow;
+  const int i = row_lo + blockIdx.x % nrow;
+  [[maybe_unused]] const long long nrows = (long long)(gridDim.x / nrow) * NQB;   // B * H * NQB
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const float* kh = kp + bh * NKB * D;
+  const float* vh = vp + bh * NKB * D;
+  if (tid < D) qs[tid] = scale * __ldg(qp + (bh * NQB + i) * D + tid);
+  __syncthreads();
+
+  // proxies: warp per key block, lanes across the row (float4 for d = 128, float2 for d = 64)
+  constexpr int PER = D / 32;
+  float q[PER];
+#pragma unroll
+  for (int e = 0; e < PER; ++e) q[e] = qs[lane * PER + e];
+  for (int j0 = warp; j0 < NKB; j0 += 4 * kTailWarps) {
+    float part[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int j = j0 + u * kTailWarps;
+      float a = 0.f;
+      if (j < NKB) {
+        const float* kr = kh + (long long)j * D + lane * PER;
+        if constexpr (PER == 4) {
+          const float4 k4 = __ldg(reinterpret_cast<const float4*>(kr));
+          a = fmaf(q[0], k4.x, fmaf(q[1], k4.y, fmaf(q[2], k4.z, q[3] * k4.w)));
+        } else {
+          const float2 k2 = __ldg(reinterpret_cast<const float2*>(kr));
+          a = fmaf(q[0], k2.x, q[1] * k2.y);
+        }
+      }
+      part[u] = a;
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) part[u] += __shfl_xor_sync(0xffffffffu, part[u], o);
+      const int j = j0 + u * kTailWarps;
+      if (lane == 0 && j < NKB) srow[j] = part[u];
+    }
+  }
+  __syncthreads();
+
+  // mean, then the population variance about it (two passes), and the argmax
+  float sum = 0.f, best = -INFINITY;
+  int bidx = INT_MAX;
+  for (int j = tid; j < NKB; j += kTailThreads) {
+    const float v = srow[j];
+    sum += v;
+    if (v > best) {   // j increases within a thread: strict > keeps the lowest j
+      best = v;
+      bidx = j;
+    }
+  }
+  const float mu = tail_block_sum(sum, red) / (float)NKB;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float ob = __shfl_xor_sync(0xffffffffu, best, o);
+    const int oi = __shfl_xor_sync(0xffffffffu, bidx, o);
+    if (ob > best || (ob == best && oi < bidx)) {
+      best = ob;
+      bidx = oi;
+    }
+  }
+  __syncthreads();
+  if (lane == 0) {
+    red[warp] = best;
+    redi[warp] = bidx;
+  }
+  __syncthreads();
+  best = red[0];
+  bidx = redi[0];
+#pragma unroll
+  for (int w = 1; w < kTailWarps; ++w)
+    if (red[w] > best || (red[w] == best && redi[w] < bidx)) {
+      best = red[w];
+      bidx = redi[w];
+    }
+  float sq = 0.f;
+  for (int j = tid; j < NKB; j += kTailThreads) {
+    const float dv = srow[j] - mu;
+    sq = fmaf(dv, dv, sq);
+  }
+  const float sigma = sqrtf(tail_block_sum(sq, red) / (float)NKB);
+  const float tau = (beta == -INFINITY) ? -INFINITY : fmaf(beta, sigma, mu);
+
+  // selection in ascending j (ballot / popc within a warp, warp counts through shared memory),
+  // Taylor weights over the proxies
+  int32_t* list = sel_idx + (bh * NQB + i) * NKB;
+  int cnt = 0;
+  float wsum = 0.f;
+  for (int j0 = 0; j0 < NKB; j0 += kTailThreads) {
+    const int j = j0 + tid;
+    const bool in = j < NKB;
+    const float v = in ? srow[j] : 0.f;
+    const bool keep = in && (v >= tau || j == bidx);
+    const unsigned m = __ballot_sync(0xffffffffu, keep);
+    __syncthreads();
+    if (lane == 0) redi[warp] = __popc(m);
+    __syncthreads();
+    int before = cnt, total = 0;
+#pragma unroll
+    for (int w = 0; w < kTailWarps; ++w) {
+      if (w < warp) before += redi[w];
+      total += redi[w];
+    }
+    const int slot = before + __popc(m & ((1u << lane) - 1u));
+    if (keep && ATTN_CHECKED((bh * NQB + i) * NKB + slot, 1, nrows * NKB, status)) list[slot] = j;
+    cnt += total;
+    if (in) {
+      const float w = keep ? 0.f : (float)min(block_k, S - j * block_k) * fmaxf(0.f, 1.f + v - mu);
+      srow[j] = w;
+      wsum += w;
+    }
+  }
+  const float W = tail_block_sum(wsum, red);
+
+  // T = sum_j w_j Vbar_j: thread = (column quad, residue class of j)
+  constexpr int NQ = D / 4, NG = kTailThreads / NQ;
+  const int cq = tid % NQ, g = tid / NQ;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int j = g; j < NKB; j += NG) {
+    const float w = srow[j];
+    if (w != 0.f) {
+      const float4 v4 = __ldg(reinterpret_cast<const float4*>(vh + (long long)j * D) + cq);
+      acc.x = fmaf(w, v4.x, acc.x);
+      acc.y = fmaf(w, v4.y, acc.y);
+      acc.z = fmaf(w, v4.z, acc.z);
+      acc.w = fmaf(w, v4.w, acc.w);
+    }
+  }
+  *reinterpret_cast<float4*>(&tred[g][4 * cq]) = acc;
+  __syncthreads();
+  if (tid < D) {
+    float t = 0.f;
+#pragma unroll
+    for (int gg = 0; gg < NG; ++gg) t += tred[gg][tid];
+    if (ATTN_CHECKED((bh * NQB + i) * D + tid, 1, nrows * D, status)) taylor_t[(bh * NQB + i) * D + tid] = t;
+  }
+  if (tid == 0) {
+    if (ATTN_CHECKED((bh * NQB + i) * 4, 4, nrows * 4, status)) {
+      float* st = stats + (bh * NQB + i) * 4;
+      st[0] = mu;
+      st[1] = sigma;
+      st[2] = tau;
+      st[3] = W;
+    }
+    if (ATTN_CHECKED(bh * NQB + i, 1, nrows, status)) sel_cnt[bh * NQB + i] = cnt;
+  }
+  // launched beside the tensor-core kernel (programmatic dependent launch): do not complete before it
+  // has, so that work queued after this kernel sees both kernels' results
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 }  // namespace
 
+// Largest short last tile (query blocks) that goes to the CUDA-core kernel.
+constexpr int kTailRowsMax = 32;
+
 cudaError_t launch_route_tc(const CUtensorMap& tkh, const CUtensorMap& tkl, const CUtensorMap& tvh,
-                            const CUtensorMap& tvl, const float* qp, int BH, int NQB, int NKB, int S, int D,
-                            int block_k, float scale, float beta, int32_t* sel_idx, int32_t* sel_cnt, float* stats,
-                            float* taylor_t, int* status, unsigned launch_id, cudaStream_t stream) {
-  const long long grid = (long long)BH * ((NQB + kRtRows - 1) / kRtRows);
-  if (grid <= 0 || grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+                            const CUtensorMap& tvl, const CUtensorMap& tq, const float* qp, const float* kp,
+                            const float* vp, int BH, int NQB, int NKB, int S, int D, int block_k, float scale,
+                            float beta, int32_t* sel_idx, int32_t* sel_cnt, float* stats, float* taylor_t, int* status,
+                            unsigned launch_id, cudaStream_t stream) {
+  const int rem = NQB % kRtRows;
+  const bool tail = rem != 0 && rem <= kTailRowsMax;
+  const int tc_tiles = tail ? NQB / kRtRows : (NQB + kRtRows - 1) / kRtRows;
+  const long long grid = (long long)BH * tc_tiles;
+  if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   cudaError_t e;
-  if (D == 128) {
-    e = cudaFuncSetAttribute(route_tc_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, RtCfg<128>::kSmemBytes);
+  if (grid > 0) {
+    if (D == 128) {
+      e = cudaFuncSetAttribute(route_tc_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               RtCfg<128>::kSmemBytes);
+      if (e != cudaSuccess) return e;
+      route_tc_kernel<128><<<(unsigned)grid, kRtThreads, RtCfg<128>::kSmemBytes, stream>>>(
+          tkh, tkl, tvh, tvl, tq, tc_tiles, NQB, NKB, S, block_k, scale, beta, sel_idx, sel_cnt, stats, taylor_t,
+          status, launch_id);
+    } else {
+      e = cudaFuncSetAttribute(route_tc_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               RtCfg<64>::kSmemBytes);
+      if (e != cudaSuccess) return e;
+      route_tc_kernel<64><<<(unsigned)grid, kRtThreads, RtCfg<64>::kSmemBytes, stream>>>(
+          tkh, tkl, tvh, tvl, tq, tc_tiles, NQB, NKB, S, block_k, scale, beta, sel_idx, sel_cnt, stats, taylor_t,
+          status, launch_id);
+    }
+    e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    route_tc_kernel<128><<<(unsigned)grid, kRtThreads, RtCfg<128>::kSmemBytes, stream>>>(
-        tkh, tkl, tvh, tvl, qp, NQB, NKB, S, block_k, scale, beta, sel_idx, sel_cnt, stats, taylor_t, status, launch_id);
-  } else {
-    e = cudaFuncSetAttribute(route_tc_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, RtCfg<64>::kSmemBytes);
-    if (e != cudaSuccess) return e;
-    route_tc_kernel<64><<<(unsigned)grid, kRtThreads, RtCfg<64>::kSmemBytes, stream>>>(
-        tkh, tkl, tvh, tvl, qp, NQB, NKB, S, block_k, scale, beta, sel_idx, sel_cnt, stats, taylor_t, status, launch_id);
   }
-  return cudaGetLastError();
+  if (!tail) return cudaSuccess;
+  const int row_lo = tc_tiles * kRtRows;
+  const long long tgrid = (long long)BH * (NQB - row_lo);
+  if (tgrid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)tgrid);
+  cfg.blockDim = dim3(kTailThreads);
+  cfg.dynamicSmemBytes = (size_t)NKB * 4;   // NKB <= 8192: at most 32 KB
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = grid > 0 ? 1 : 0;
+  if (D == 128)
+    return cudaLaunchKernelEx(&cfg, route_tail_kernel<128>, qp, kp, vp, NQB, NKB, S, block_k, scale, beta, sel_idx,
+                              sel_cnt, stats, taylor_t, row_lo, status);
+  return cudaLaunchKernelEx(&cfg, route_tail_kernel<64>, qp, kp, vp, NQB, NKB, S, block_k, scale, beta, sel_idx,
+                            sel_cnt, stats, taylor_t, row_lo, status);
 }
 
 }  // namespace vdtb
