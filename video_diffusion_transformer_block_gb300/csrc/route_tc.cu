@@ -650,10 +650,10 @@ __global__ void __launch_bounds__(kTailThreads) route_tail_kernel(
   float q[PER];
 #pragma unroll
   for (int e = 0; e < PER; ++e) q[e] = qs[lane * PER + e];
-  for (int j0 = warp; j0 < NKB; j0 += 4 * kTailWarps) {
-    float part[4];
+  for (int j0 = warp; j0 < NKB; j0 += 8 * kTailWarps) {
+    float part[8];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
+    for (int u = 0; u < 8; ++u) {
       const int j = j0 + u * kTailWarps;
       float a = 0.f;
       if (j < NKB) {
@@ -669,7 +669,7 @@ __global__ void __launch_bounds__(kTailThreads) route_tail_kernel(
       part[u] = a;
     }
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
+    for (int u = 0; u < 8; ++u) {
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) part[u] += __shfl_xor_sync(0xffffffffu, part[u], o);
       const int j = j0 + u * kTailWarps;
@@ -756,14 +756,23 @@ __global__ void __launch_bounds__(kTailThreads) route_tail_kernel(
   constexpr int NQ = D / 4, NG = kTailThreads / NQ;
   const int cq = tid % NQ, g = tid / NQ;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int j = g; j < NKB; j += NG) {
-    const float w = srow[j];
-    if (w != 0.f) {
-      const float4 v4 = __ldg(reinterpret_cast<const float4*>(vh + (long long)j * D) + cq);
-      acc.x = fmaf(w, v4.x, acc.x);
-      acc.y = fmaf(w, v4.y, acc.y);
-      acc.z = fmaf(w, v4.z, acc.z);
-      acc.w = fmaf(w, v4.w, acc.w);
+  constexpr int kU = 8;   // loads in flight per thread
+  for (int j0 = g; j0 < NKB; j0 += kU * NG) {
+    float4 v4[kU];
+    float w[kU];
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const int j = j0 + u * NG;
+      w[u] = j < NKB ? srow[j] : 0.f;
+      v4[u] = w[u] != 0.f ? __ldg(reinterpret_cast<const float4*>(vh + (long long)j * D) + cq)
+                          : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      acc.x = fmaf(w[u], v4[u].x, acc.x);
+      acc.y = fmaf(w[u], v4[u].y, acc.y);
+      acc.z = fmaf(w[u], v4[u].z, acc.z);
+      acc.w = fmaf(w[u], v4[u].w, acc.w);
     }
   }
   *reinterpret_cast<float4*>(&tred[g][4 * cq]) = acc;
