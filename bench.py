@@ -549,7 +549,10 @@ def run_native_kernel(args, world, rank, local):
         kern = w0.extra["kernel"]
         brick, pair, boxes = vd.attn_na3d_plan(w.grid, kern)
         flops = 4.0 * B * H * Sq * math.prod(kern) * d                 # the windows' own work
-        exec_flops = 4.0 * B * H * boxes * 128 * 128 * d               # what the tensor cores run
+        # what the tensor cores run: per key box S = Q K^T and O += P V, and on the
+        # persistent plan one (4x4x8 bricks) or two K = 16 steps that add the window
+        window_k = (16 if brick == 3 else 32) if pair == 4 else 0
+        exec_flops = 2.0 * B * H * boxes * 128 * 128 * (2 * d + window_k)
 
         def step():
             vd.attn_na3d_fwd(q, k, v, w.grid, kern, out=out, lse=lse)
@@ -588,7 +591,9 @@ def run_native_kernel(args, world, rank, local):
     if args.workload == "na3d":
         peak = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
         ach = exec_flops / (ms * 1e-3) / 1e12
-        roof = {"bound": "tensor", "kernel": f"attn_fwd_kernel (3D neighbourhood, brick {brick}, pair {pair}, d={d})",
+        kname = (f"attn_na_persist_kernel (3D neighbourhood, persistent one-brick tiles, brick {brick}, d={d})"
+                 if pair == 4 else f"attn_fwd_kernel (3D neighbourhood, brick {brick}, pair {pair}, d={d})")
+        roof = {"bound": "tensor", "kernel": kname,
                 "achieved": round(ach, 2), "peak": peak, "unit": "TFLOP/s", "frac": round(ach / peak, 4),
                 "peak_source": f"{peaks_src} bf16_tflops (burst: one kernel per timed step, L2 flushed between)",
                 "traffic": None}

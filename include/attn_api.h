@@ -255,15 +255,22 @@ attn_status_t attn_cross_fwd(const attn_bf16* q, const attn_bf16* k, const attn_
  *   scale         softmax scale, finite and > 0.
  *   brick         query/key tile shape, frames x rows x columns of 128 tokens:
  *                 1 = 1x8x16, 2 = 2x8x8, 3 = 4x4x8, 0 = chosen by the library.
- *   pair_axis     axis along which a CTA's two query bricks are neighbours:
- *                 0 = frames, 1 = rows, 2 = columns; 3 = one brick per CTA
- *                 (two CTAs share an SM); -1 = chosen by the library (one
- *                 brick per CTA, the fastest on GB300 for every window
- *                 measured; an open brick takes the shape with the least
- *                 key boxes plus two per CTA).
+ *   pair_axis     the CTA layout: 0 / 1 / 2 = a CTA takes two query bricks
+ *                 that are neighbours along frames / rows / columns (one walk
+ *                 of the union of their windows); 3 = one brick per CTA, two
+ *                 CTAs per SM; 4 = persistent CTAs, one per SM, whose two
+ *                 query tiles each run a sequence of bricks (one brick's
+ *                 epilogue overlaps the other tile's MMAs) and whose tensor
+ *                 cores add the window to the scores (0 inside, -2^120
+ *                 outside; for scale * log2(e) < 2^-80, where that would not
+ *                 vanish in the exponent, plan 3 runs instead, with the same
+ *                 results); -1 = chosen by the library: plan 4, the fastest on
+ *                 GB300 for every volume and window measured.  An open brick
+ *                 minimises a measured cost model of key boxes and bricks (see
+ *                 attn_na3d_plan).
  *   The choice only changes speed, never results beyond fp32 rounding order.
  *   Errors: ATTN_ERR_INVALID_ARG (null or misaligned pointer, a window outside
- *   [1, L], S > 2^30, non-positive scale, bad brick/pair code),
+ *   [1, L], S > 2^30, non-positive scale, bad brick/pair code (0..3 / -1..4)),
  *   ATTN_ERR_UNSUPPORTED (d), ATTN_ERR_CUDA (launch).  Asynchronous on stream.
  */
 attn_status_t attn_na3d_fwd(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v, attn_bf16* out, float* lse,
@@ -271,11 +278,16 @@ attn_status_t attn_na3d_fwd(const attn_bf16* q, const attn_bf16* k, const attn_b
                             int pair_axis, cudaStream_t stream);
 
 /*
- * The tile plan attn_na3d_fwd uses for a volume and window.  On entry *brick
- * and *pair_axis hold the caller's request (0 / -1 = open); on return the
- * plan.  *key_boxes (nullable) receives the number of 128-key boxes the query
- * tiles of one head multiply: the executed work of one head is
- * key_boxes * 4 * 128 * 128 * d floating-point operations.  Host only.
+ * The tile plan attn_na3d_fwd uses for a volume and window (at a scale with
+ * scale * log2(e) >= 2^-80).  On entry *brick and *pair_axis hold the
+ * caller's request (0 / -1 = open); on return the plan.  An open brick
+ * minimises, in twentieths of a key box, for plan 4: 20 per box of a 4x4x8
+ * brick and 23 per box of the others (their window step is 32 columns wide)
+ * plus 34 per brick; for the other plans: 20 per box plus 40 per CTA.
+ * *key_boxes (nullable) receives the number of 128-key boxes the query tiles
+ * of one head multiply: the executed work of one head is
+ * key_boxes * 4 * 128 * 128 * d floating-point operations (plan 4 adds one or
+ * two K = 16 steps per box for the window).  Host only.
  */
 attn_status_t attn_na3d_plan(int T, int Y, int X, int Kt, int Ky, int Kx, int* brick, int* pair_axis,
                              long long* key_boxes);

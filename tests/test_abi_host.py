@@ -135,8 +135,9 @@ def na_start(p, K, L):
 
 def na_walk(grid, kernel, brick, pair):
     """Python restatement of the kernel's box walk: yields, per CTA, its query
-    bricks (two neighbours along ``pair``, or one when pair == 3) and the boxes
-    with their tile flags."""
+    bricks (two neighbours along ``pair``, or one when pair is 3 or 4: plan 4
+    runs the one-brick tiles on persistent CTAs, with the same boxes per brick)
+    and the boxes with their tile flags."""
     B = BRICKS[brick]
     nq = [-(-grid[a] // B[a]) for a in range(3)]
     np_ = [(-(-nq[a] // 2) if a == pair else nq[a]) for a in range(3)]
@@ -170,7 +171,7 @@ def na_walk(grid, kernel, brick, pair):
 @pytest.mark.parametrize("grid,kernel", [((3, 13, 21), (3, 5, 7)), ((5, 11, 19), (3, 5, 4)), ((1, 20, 24), (1, 9, 9)),
                                          ((4, 16, 32), (2, 16, 1)), ((2, 5, 6), (2, 5, 6))])
 @pytest.mark.parametrize("brick", [1, 2, 3])
-@pytest.mark.parametrize("pair", [0, 1, 2, 3])
+@pytest.mark.parametrize("pair", [0, 1, 2, 3, 4])
 def test_na3d_walk_covers_every_window_and_plan_counts_it(lib, grid, kernel, brick, pair):
     B = BRICKS[brick]
     work = 0
@@ -202,26 +203,35 @@ def test_na3d_walk_covers_every_window_and_plan_counts_it(lib, grid, kernel, bri
 
 
 def test_na3d_plan_picks_the_least_work(lib):
-    # an open pair axis means one brick per CTA; an open brick minimises key boxes + 2 per CTA
+    # an open pair axis means the persistent one-brick tiles (plan 4); an open brick minimises
+    # 20 (4x4x8) or 23 (the others) per key box + 34 per brick there, 20 per box + 40 per CTA elsewhere
     for grid, kernel in [((4, 128, 128), (3, 7, 7)), ((4, 64, 64), (3, 31, 31)), ((1, 96, 160), (1, 13, 13)),
-                         ((5, 11, 19), (3, 5, 4))]:
-        costs = {}
-        for brick in (1, 2, 3):
-            b, pa, nbox = vd.attn_na3d_plan(grid, kernel, brick, 3)
-            assert (b, pa) == (brick, 3)
-            ctas = np.prod([-(-grid[a] // BRICKS[brick][a]) for a in range(3)])
-            costs[brick] = nbox + 2 * ctas
-            assert nbox * 128 * 128 >= np.prod(grid) * np.prod(kernel)   # the boxes hold every window
+                         ((5, 11, 19), (3, 5, 4)), ((8, 64, 64), (3, 7, 7))]:
+        for pair in (3, 4):
+            costs = {}
+            for brick in (1, 2, 3):
+                b, pa, nbox = vd.attn_na3d_plan(grid, kernel, brick, pair)
+                assert (b, pa) == (brick, pair)
+                ctas = np.prod([-(-grid[a] // BRICKS[brick][a]) for a in range(3)])
+                costs[brick] = ((20 if brick == 3 else 23) * nbox + 34 * ctas) if pair == 4 else 20 * nbox + 40 * ctas
+                assert nbox * 128 * 128 >= np.prod(grid) * np.prod(kernel)   # the boxes hold every window
+            b, pa, nb = vd.attn_na3d_plan(grid, kernel, 0, pair)
+            assert pa == pair and costs[b] == min(costs.values())
         b, pa, nb = vd.attn_na3d_plan(grid, kernel)
-        assert pa == 3 and costs[b] == min(costs.values())
+        assert pa == 4 and (b, pa, nb) == vd.attn_na3d_plan(grid, kernel, 0, 4)
         # a fixed brick with an open pair axis keeps the brick
-        assert vd.attn_na3d_plan(grid, kernel, 2)[:2] == (2, 3)
+        assert vd.attn_na3d_plan(grid, kernel, 2)[:2] == (2, 4)
+    # the volumes timed on GB300 take their fastest brick
+    assert vd.attn_na3d_plan((4, 128, 128), (3, 7, 7))[0] == 3
+    assert vd.attn_na3d_plan((4, 64, 64), (3, 31, 31))[0] == 3
+    assert vd.attn_na3d_plan((1, 96, 160), (1, 13, 13))[0] == 1
+    assert vd.attn_na3d_plan((8, 64, 64), (3, 7, 7))[0] == 2
 
 
 def test_na3d_rejections(lib):
     base = [P, P, P, P, P, 1, 2, 4, 16, 16, 128, 3, 5, 5, 0.088, 0, -1, None]
     for i, bad in [(11, 0), (11, 5), (12, 17), (13, 0), (7, 0), (14, 0.0), (14, math.nan), (15, 4), (15, -1),
-                   (16, 4), (16, -2)]:
+                   (16, 5), (16, -2)]:
         args = list(base)
         args[i] = bad
         assert lib.attn_na3d_fwd(*args) == 1, (i, bad)

@@ -172,6 +172,15 @@ def _p(t):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
 
+def fresh(*shape, dtype=torch.float32, device=DEV):
+    """An output buffer filled with the byte 0xA5: both libraries get the same
+    contents wherever a call writes nothing (the entries of a selected-block
+    row past its count, for one)."""
+    t = torch.empty(*shape, dtype=dtype, device=device)
+    t.view(torch.uint8).fill_(0xA5)
+    return t
+
+
 def test_bounds_checked_build_reports_nothing_and_matches(dbg):
     lib = vd.load_library()
     stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
@@ -193,17 +202,17 @@ def test_bounds_checked_build_reports_nothing_and_matches(dbg):
     # dense, ragged query and key tails
     B, H, Sq, Skv, d = 1, 2, 300, 517, 64
     q, k, v = rnd_qkv(B, H, Sq, Skv, d, seed=5)
-    both("attn_dense_fwd", lambda: [torch.empty(B, H, Sq, d, dtype=torch.bfloat16, device=DEV),
-                                    torch.empty(B, H, Sq, device=DEV)],
+    both("attn_dense_fwd", lambda: [fresh(B, H, Sq, d, dtype=torch.bfloat16, device=DEV),
+                                    fresh(B, H, Sq, device=DEV)],
          lambda o: [q, k, v, o[0], o[1], B, H, Sq, Skv, d, ctypes.c_float(1 / math.sqrt(d))])
     # split-KV partials of an odd key count, then the merge
     H, Sq, Skv, d, n = 2, 130, 2001, 128, 3
     q, k, v = rnd_qkv(1, H, Sq, Skv, d, seed=6)
-    op, lp = both("attn_cross_splitkv_fwd", lambda: [torch.empty(n, 1, H, Sq, d, device=DEV),
-                                                     torch.empty(n, 1, H, Sq, device=DEV)],
+    op, lp = both("attn_cross_splitkv_fwd", lambda: [fresh(n, 1, H, Sq, d, device=DEV),
+                                                     fresh(n, 1, H, Sq, device=DEV)],
                   lambda o: [q, k, v, o[0], o[1], 1, H, Sq, Skv, d, n, ctypes.c_float(1 / math.sqrt(d))])
-    both("attn_lse_merge", lambda: [torch.empty(1, H, Sq, d, dtype=torch.bfloat16, device=DEV),
-                                    torch.empty(1, H, Sq, device=DEV)],
+    both("attn_lse_merge", lambda: [fresh(1, H, Sq, d, dtype=torch.bfloat16, device=DEV),
+                                    fresh(1, H, Sq, device=DEV)],
          lambda o: [op, lp, o[0], o[1], n, 1, H, Sq, d])
     # pool + route + block-sparse forward, ragged last block, with the routing outputs
     B, H, S, d, blk = 1, 2, 1000, 128, 128
@@ -211,25 +220,25 @@ def test_bounds_checked_build_reports_nothing_and_matches(dbg):
     nq = (S + blk - 1) // blk
     nbytes = lib.attn_sparse_workspace_bytes(B, H, S, d, blk, blk)
     both("attn_sparse_route_fwd",
-         lambda: [torch.empty(B, H, S, d, dtype=torch.bfloat16, device=DEV), torch.empty(B, H, S, device=DEV),
+         lambda: [fresh(B, H, S, d, dtype=torch.bfloat16, device=DEV), fresh(B, H, S, device=DEV),
                   torch.zeros(nbytes, dtype=torch.uint8, device=DEV),
-                  torch.empty(B, H, nq, nq, dtype=torch.int32, device=DEV),
-                  torch.empty(B, H, nq, dtype=torch.int32, device=DEV), torch.empty(B, H, nq, 4, device=DEV),
-                  torch.empty(B, H, nq, d, device=DEV)],
+                  fresh(B, H, nq, nq, dtype=torch.int32, device=DEV),
+                  fresh(B, H, nq, dtype=torch.int32, device=DEV), fresh(B, H, nq, 4, device=DEV),
+                  fresh(B, H, nq, d, device=DEV)],
          lambda o: [q, k, v, o[0], o[1], B, H, S, d, ctypes.c_float(1 / math.sqrt(d)), ctypes.c_float(0.5), blk, blk,
                     o[2], ctypes.c_size_t(nbytes), o[3], o[4], o[5], o[6]])
     # neighbourhood attention on a ragged volume
     T, Y, X = 3, 13, 21
     S = T * Y * X
     q, k, v = make_qkv(Workload("dna", B=1, H=2, Sq=S, Skv=S, d=128, seed=8, grid=(T, Y, X), pe=True), device=DEV)
-    both("attn_na3d_fwd", lambda: [torch.empty(1, 2, S, 128, dtype=torch.bfloat16, device=DEV),
-                                   torch.empty(1, 2, S, device=DEV)],
+    both("attn_na3d_fwd", lambda: [fresh(1, 2, S, 128, dtype=torch.bfloat16, device=DEV),
+                                   fresh(1, 2, S, device=DEV)],
          lambda o: [q, k, v, o[0], o[1], 1, 2, T, Y, X, 128, 3, 5, 7, ctypes.c_float(1 / math.sqrt(128)), 0, -1])
     # FP8 quantiser and scaled product, ragged M and N, K not a multiple of 128
     M, N, K = 129, 264, 144
     x, W = make_linear(LinearWorkload("dfp8", M=M, K=K, N=N, seed=9), device=DEV)
-    aq, sa = both("fp8_quantize_rows", lambda: [torch.empty(M, K, dtype=torch.uint8, device=DEV),
-                                                torch.empty(M, device=DEV)], lambda o: [x, o[0], o[1], M, K])
+    aq, sa = both("fp8_quantize_rows", lambda: [fresh(M, K, dtype=torch.uint8, device=DEV),
+                                                fresh(M, device=DEV)], lambda o: [x, o[0], o[1], M, K])
     wq, sw = vd.fp8_quantize_rows(W)
-    both("fp8_scaled_gemm", lambda: [torch.empty(M, N, dtype=torch.bfloat16, device=DEV)],
+    both("fp8_scaled_gemm", lambda: [fresh(M, N, dtype=torch.bfloat16, device=DEV)],
          lambda o: [aq, sa, wq, sw, o[0], M, N, K])

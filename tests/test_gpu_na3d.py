@@ -1,8 +1,9 @@
 """GPU parity of 3D neighbourhood attention against the fp64 oracle, through the C ABI.
 
 Every output element of small volumes is compared: ragged volumes (bricks cut
-by the borders), every brick shape and pair axis (and one brick per CTA), d = 64/128, B > 1, a single
-frame, even windows, windows of one token and of the whole volume.
+by the borders), every brick shape and pair axis (and one brick per CTA, and
+the persistent one-brick tiles, also with several bricks per tile), d = 64/128,
+B > 1, a single frame, even windows, windows of one token and of the whole volume.
 Tolerances as for dense attention (max-abs 2e-2, relative L2 5e-3).
 """
 import math
@@ -45,7 +46,7 @@ def check(B, H, grid, kernel, d, brick=0, pair=-1, seed=7, scale=None):
 
 
 @pytest.mark.parametrize("brick", [1, 2, 3])
-@pytest.mark.parametrize("pair", [0, 1, 2, 3])
+@pytest.mark.parametrize("pair", [0, 1, 2, 3, 4])
 def test_na3d_every_plan_ragged_volume(brick, pair):
     check(1, 2, (5, 11, 19), (3, 5, 4), 64, brick, pair, seed=brick * 3 + pair)
 
@@ -81,6 +82,61 @@ def test_na3d_single_token_window_returns_v():
     torch.testing.assert_close(lse, expect, atol=1e-3, rtol=1e-4)
 
 
-def test_na3d_peaked_scores_rescale():
+@pytest.mark.parametrize("pair", [-1, 3, 4])
+def test_na3d_peaked_scores_rescale(pair):
     # large scores: the running max moves by more than the lazy-rescale threshold between boxes
-    check(1, 2, (4, 16, 32), (3, 9, 9), 128, scale=0.6, seed=5)
+    check(1, 2, (4, 16, 32), (3, 9, 9), 128, pair=pair, scale=0.6, seed=5)
+
+
+def test_na3d_persistent_plan_tiny_scale_same_bits():
+    # below scale * log2(e) = 2^-80 the window bias of the persistent plan could leave
+    # masked keys a weight; the library then runs the one-brick CTAs, whose bits are the same
+    grid, kernel = (3, 13, 21), (3, 5, 7)
+    q, k, v = na_inputs(1, 2, grid, 128, seed=13)
+    scale = 2.0 ** -90
+    o4, l4 = vd.attn_na3d_fwd(q, k, v, grid, kernel, scale=scale, brick=3, pair_axis=4)
+    o3, l3 = vd.attn_na3d_fwd(q, k, v, grid, kernel, scale=scale, brick=3, pair_axis=3)
+    torch.cuda.synchronize()
+    assert torch.equal(o4, o3) and torch.equal(l4, l3)
+    ro, rl = oracle.na3d_attention(host(q), host(k), host(v), grid, kernel, scale)
+    assert_close(host(o4), ro, "na3d tiny scale out")
+    assert_close(host(l4), rl, "na3d tiny scale lse")
+
+
+@pytest.mark.parametrize("brick,grid,kernel,H,d", [
+    (3, (5, 37, 45), (3, 7, 7), 12, 128),   # 1440 bricks of 4x4x8, ragged in every axis
+    (1, (3, 40, 50), (3, 5, 9), 16, 64),    # 960 bricks of 1x8x16
+])
+def test_na3d_persistent_tiles_walk_several_bricks(brick, grid, kernel, H, d):
+    # plan 4: each tile of a persistent CTA runs bricks one after another (the
+    # epilogue of one brick, the Q load of the next); enough bricks that every
+    # tile takes several
+    B = {1: (1, 8, 16), 2: (2, 8, 8), 3: (4, 4, 8)}[brick]
+    units = H * int(np.prod([-(-grid[a] // B[a]) for a in range(3)]))
+    assert units > 2 * 2 * torch.cuda.get_device_properties(0).multi_processor_count
+    q, k, v = na_inputs(1, H, grid, d, seed=31 + brick)
+    scale = 1 / math.sqrt(d)
+    out4, lse4 = vd.attn_na3d_fwd(q, k, v, grid, kernel, scale=scale, brick=brick, pair_axis=4)
+    out3, lse3 = vd.attn_na3d_fwd(q, k, v, grid, kernel, scale=scale, brick=brick, pair_axis=3)
+    torch.cuda.synchronize()
+    # the same boxes in the same order through the same arithmetic as the one-brick CTAs: identical bits
+    assert torch.equal(out4, out3)
+    assert torch.equal(lse4, lse3)
+    ro, rl = oracle.na3d_attention(host(q), host(k), host(v), grid, kernel, scale)
+    assert_close(host(out4), ro, f"na3d persistent out (grid {grid} brick {brick})")
+    assert_close(host(lse4), rl, f"na3d persistent lse (grid {grid} brick {brick})")
+
+
+def test_na3d_persistent_output_16_byte_aligned():
+    # the persistent plan writes whole 32-byte sectors when the output starts on a 32-byte
+    # boundary and 16-byte pieces otherwise: an output 16 bytes past a boundary takes the second path
+    grid, kernel, H, d = (3, 13, 21), (3, 5, 7), 2, 128
+    S = int(np.prod(grid))
+    q, k, v = na_inputs(1, H, grid, d, seed=17)
+    buf = torch.empty(H * S * d + 8, dtype=torch.bfloat16, device="cuda")
+    out = buf[8:].view(1, H, S, d)
+    assert out.data_ptr() % 32 == 16
+    vd.attn_na3d_fwd(q, k, v, grid, kernel, brick=3, pair_axis=4, out=out)
+    o3, _ = vd.attn_na3d_fwd(q, k, v, grid, kernel, brick=3, pair_axis=3)
+    torch.cuda.synchronize()
+    assert torch.equal(out, o3)

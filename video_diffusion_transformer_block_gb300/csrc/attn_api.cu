@@ -181,12 +181,15 @@ void na_plan_cost(const int L[3], const int K[3], int brick, int pair, long long
 }
 
 // Picks the plan left open by the caller (brick 0, pair -1).  An open pair
-// axis means one brick per CTA (pair 3): two such CTAs share an SM, so one
-// CTA's prologue and epilogue overlap the other's main loop, which measured
-// faster than every paired plan on GB300.  An open brick takes the least
-// work, counting a CTA's fixed cost as two key boxes.
+// axis means the persistent one-brick tiles (pair 4), the fastest plan on
+// GB300 for every volume and window measured.  An open brick minimises a cost
+// in twentieths of a key box: for pair 4, 20 per box of a brick whose window
+// step is 16 columns wide (4x4x8), 23 per box where it is 32 (the other
+// bricks: a wider MMA step and one window buffer), plus 34 per brick (its
+// epilogue); for the other plans 20 per box plus 40 per CTA (a CTA's fixed
+// cost counted as two boxes).  The weights are fits to GB300 timings.
 void na_choose(const int L[3], const int K[3], int* brick, int* pair, long long* boxes) {
-  if (*pair < 0) *pair = 3;
+  if (*pair < 0) *pair = 4;
   long long best = -1;
   int bb = 1;
   long long bboxes = 0;
@@ -194,7 +197,7 @@ void na_choose(const int L[3], const int K[3], int* brick, int* pair, long long*
     if (*brick != 0 && b != *brick) continue;
     long long nbox, ncta;
     na_plan_cost(L, K, b, *pair, &nbox, &ncta);
-    const long long cost = nbox + 2 * ncta;
+    const long long cost = *pair == 4 ? (b == 3 ? 20 : 23) * nbox + 34 * ncta : 20 * nbox + 40 * ncta;
     if (best < 0 || cost < best) {
       best = cost;
       bb = b;
@@ -325,7 +328,7 @@ attn_status_t attn_dense_fwd(const attn_bf16* q, const attn_bf16* k, const attn_
 attn_status_t attn_na3d_plan(int T, int Y, int X, int Kt, int Ky, int Kx, int* brick, int* pair_axis,
                              long long* key_boxes) {
   if (!brick || !pair_axis || !na_args_ok(1, 1, T, Y, X, Kt, Ky, Kx)) return ATTN_ERR_INVALID_ARG;
-  if (*brick < 0 || *brick > 3 || *pair_axis < -1 || *pair_axis > 3) return ATTN_ERR_INVALID_ARG;
+  if (*brick < 0 || *brick > 3 || *pair_axis < -1 || *pair_axis > 4) return ATTN_ERR_INVALID_ARG;
   const int L[3] = {T, Y, X}, K[3] = {Kt, Ky, Kx};
   long long boxes = 0;
   na_choose(L, K, brick, pair_axis, &boxes);
@@ -341,11 +344,16 @@ attn_status_t attn_na3d_fwd(const attn_bf16* q, const attn_bf16* k, const attn_b
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || (lse && ((uintptr_t)lse & 3u)))
     return ATTN_ERR_INVALID_ARG;
   if (!na_args_ok(B, H, T, Y, X, Kt, Ky, Kx) || !(isfinite(scale) && scale > 0.f)) return ATTN_ERR_INVALID_ARG;
-  if (brick < 0 || brick > 3 || pair_axis < -1 || pair_axis > 3) return ATTN_ERR_INVALID_ARG;
+  if (brick < 0 || brick > 3 || pair_axis < -1 || pair_axis > 4) return ATTN_ERR_INVALID_ARG;
   if (!valid_d(d)) return ATTN_ERR_UNSUPPORTED;
   const int L[3] = {T, Y, X}, K[3] = {Kt, Ky, Kx};
   long long boxes = 0;
   na_choose(L, K, &brick, &pair_axis, &boxes);
+  // the persistent plan adds the window to the scores on the tensor core (-2^120
+  // outside it), which an exponent turns into an exact 0 only for scale * log2(e)
+  // >= 2^-80; below that the one-brick CTAs (the same boxes and arithmetic, the
+  // window applied as -inf by the softmax threads) give the same results
+  if (pair_axis == 4 && !(scale * 1.4426950408889634f >= 0x1p-80f)) pair_axis = 3;
   const int mode = na_mode_of(brick);
   const int Bv[3] = {na_brick_t(mode), na_brick_y(mode), na_brick_x(mode)};
   int* status = nullptr;
@@ -370,6 +378,9 @@ attn_status_t attn_na3d_fwd(const attn_bf16* q, const attn_bf16* k, const attn_b
   p.na_pair_axis = pair_axis;
   p.out = out;
   p.lse = lse;
+  if (pair_axis == 4)
+    return cuda_status(d == 128 ? launch_na_persist_d128(mode, tq, tk, tv, p, stream)
+                                : launch_na_persist_d64(mode, tq, tk, tv, p, stream));
   return cuda_status(launch_fwd(d, 128, mode, tq, tk, tv, p, stream));
 }
 

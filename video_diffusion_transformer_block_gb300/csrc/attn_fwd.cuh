@@ -391,6 +391,153 @@ __device__ __forceinline__ void named_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
+// 3D neighbourhood attention: the scores of one query row against a key box
+// (origin `box`, shape BT x BY x BX, x fastest) keep the keys inside the row's
+// window (start `ws`, extent K per axis) and become -inf elsewhere.
+template <int BT, int BY, int BX, int BK>
+__device__ __forceinline__ void na_mask_scores(float (&x)[BK], const int (&ws)[3], const int (&box)[3],
+                                               const int (&K)[3]) {
+  int lo[3], hi[3];
+  const int Bd[3] = {BT, BY, BX};
+#pragma unroll
+  for (int a = 0; a < 3; ++a) {
+    lo[a] = min(max(ws[a] - box[a], 0), Bd[a]);
+    hi[a] = min(max(ws[a] + K[a] - box[a], 0), Bd[a]);
+  }
+  const bool full = lo[0] == 0 && hi[0] == BT && lo[1] == 0 && hi[1] == BY && lo[2] == 0 && hi[2] == BX;
+  if (full) return;
+  const bool any = lo[0] < hi[0] && lo[1] < hi[1] && lo[2] < hi[2];
+  const uint32_t xm = any ? (((1u << hi[2]) - 1u) & ~((1u << lo[2]) - 1u)) : 0u;
+  const uint32_t ym = ((1u << hi[1]) - 1u) & ~((1u << lo[1]) - 1u);
+  uint32_t lm = 0;   // bit (frame * BY + row) of the box: that line is in the window
+#pragma unroll
+  for (int ct = 0; ct < BT; ++ct)
+    if (ct >= lo[0] && ct < hi[0]) lm |= ym << (ct * BY);
+  constexpr int LPW = 32 / BX;   // lines per 32-column word
+#pragma unroll
+  for (int w = 0; w < BK / 32; ++w) {
+    uint32_t wd = 0;
+#pragma unroll
+    for (int j = 0; j < LPW; ++j)
+      if ((lm >> (w * LPW + j)) & 1u) wd |= xm << (j * BX);
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      if (!((wd >> j) & 1u)) x[w * 32 + j] = -INFINITY;
+  }
+}
+
+// One online-softmax step of the query row a thread owns (TMEM lane), on its
+// raw scores x of one key tile: moves the running max (lazily, see
+// kRescaleLog2) and rescales O in TMEM at tO when `o_live` (O holds earlier
+// steps), then writes P = 2^(x scale_log2 - m) as bf16 pairs over the first
+// BK/2 columns of S at tS and adds its row sum to l_run.  Returns after the
+// TMEM stores have completed; the caller fences and signals P ready.
+//
+// kBiasMasked: keys outside the row's window carry a score of -2^120 or less
+// instead of -inf (the window added by the tensor core, see NABiasMMA); a
+// maximum below -2^119 means no key of the tile is in the window and counts as
+// -inf, so such a tile moves nothing, as a tile of -inf scores would.
+template <int BK, int D, bool kBiasMasked = false>
+__device__ __forceinline__ void softmax_step(float (&x)[BK], float scale_log2, float& m_run, float& l_run, bool o_live,
+                                             uint32_t tS, uint32_t tO) {
+  // row max: two chains of three-input maxima (max is exact, so the order is free)
+  float mx0 = fmaxf(x[0], x[1]), mx1 = fmaxf(x[2], x[3]);
+#pragma unroll
+  for (int c = 4; c < BK; c += 4) {
+    mx0 = fmax3(mx0, x[c], x[c + 1]);
+    mx1 = fmax3(mx1, x[c + 2], x[c + 3]);
+  }
+  float raw = fmaxf(mx0, mx1);
+  if constexpr (kBiasMasked) raw = raw < -0x1p119f ? -INFINITY : raw;
+  const float mt = raw * scale_log2;
+  // lazy rescale of the running max
+  float alpha = 1.f;
+  bool need = mt > m_run + kRescaleLog2 || (m_run == -INFINITY && mt > -INFINITY);
+  if (need) {
+    alpha = (m_run == -INFINITY) ? 0.f : ex2_approx(m_run - mt);
+    l_run *= alpha;
+    m_run = mt;
+  }
+  if (__any_sync(0xffffffffu, need && alpha != 0.f && o_live)) {
+    // O holds the sum over earlier steps; rescale it in TMEM.  No wait is
+    // needed: the issuer committed the barrier of this step's S after issuing
+    // the previous PV of this tile, and a commit tracks every earlier MMA of
+    // the issuing thread, so that PV has completed as well.
+    const float a = (need && o_live) ? alpha : 1.f;
+#pragma unroll
+    for (int c0 = 0; c0 < D; c0 += 32) {
+      uint32_t rr[32];
+      tmem_ld32(tO + c0, rr);
+      tmem_ld_wait();
+      tmem_reg_fence(rr);
+#pragma unroll
+      for (int j = 0; j < 32; j += 2) {
+        const float2 v = __fmul2_rn(make_float2(__uint_as_float(rr[j]), __uint_as_float(rr[j + 1])),
+                                    make_float2(a, a));
+        rr[j] = __float_as_uint(v.x);
+        rr[j + 1] = __float_as_uint(v.y);
+      }
+      tmem_st32(tO + c0, rr);
+    }
+  }
+  const float nbase = (m_run == -INFINITY) ? 0.f : -m_run;
+  // pairs of columns through the packed fp32 pipe: the same fused multiply-add
+  // and the same two (even / odd) row-sum chains as scalar code, half the instructions
+  const float2 sc2 = make_float2(scale_log2, scale_log2), nb2 = make_float2(nbase, nbase);
+  float2 ls = make_float2(0.f, 0.f);
+#pragma unroll
+  for (int c0 = 0; c0 < BK; c0 += 64) {
+    uint32_t pk[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      const float2 arg = __ffma2_rn(make_float2(x[c0 + 2 * j], x[c0 + 2 * j + 1]), sc2, nb2);
+      const float p0 = ex2_approx(arg.x);
+      const float p1 = ex2_approx(arg.y);
+      ls = __fadd2_rn(ls, make_float2(p0, p1));
+      pk[j] = pack_bf16x2(p0, p1);
+    }
+    tmem_st32(tS + c0 / 2, pk);
+  }
+  l_run += ls.x + ls.y;
+  tmem_st_wait();
+}
+
+// Epilogue of the query row a thread owns: (O + f T) * inv from TMEM at tO
+// (zero when !have_o; T optional) as bf16 into dst[0, D), element offset `off`
+// of an output of `total` elements (bounds-checked in the debug build).
+template <int D>
+__device__ __forceinline__ void store_row_bf16(uint32_t tO, bool have_o, float inv, float f, const float* tt,
+                                               bool row_valid, uint16_t* dst, [[maybe_unused]] long long off,
+                                               [[maybe_unused]] long long total, [[maybe_unused]] int* status) {
+#pragma unroll
+  for (int c0 = 0; c0 < D; c0 += 32) {
+    uint32_t rr[32];
+    if (have_o) {
+      tmem_ld32(tO + c0, rr);
+      tmem_ld_wait();
+      tmem_reg_fence(rr);
+    }
+    if (row_valid) {
+#pragma unroll
+      for (int j = 0; j < 32; j += 8) {
+        uint4 pk;
+        float o[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          float val = have_o ? __uint_as_float(rr[j + e]) : 0.f;
+          if (tt != nullptr) val = fmaf(f, tt[c0 + j + e], val);
+          o[e] = val * inv;
+        }
+        pk.x = pack_bf16x2(o[0], o[1]);
+        pk.y = pack_bf16x2(o[2], o[3]);
+        pk.z = pack_bf16x2(o[4], o[5]);
+        pk.w = pack_bf16x2(o[6], o[7]);
+        if (ATTN_CHECKED(off + c0 + j, 8, total, status)) *reinterpret_cast<uint4*>(dst + c0 + j) = pk;
+      }
+    }
+  }
+}
+
 // Split-KV tail with the merge fused in (one-tile CTA, run by its 128 softmax
 // threads after they stored this chunk's partials): the partials are made
 // visible device-wide, the (head, query tile) counter counts this chunk, and
@@ -685,6 +832,40 @@ __device__ __forceinline__ void fused_route(const FwdParams& p, int bh, int qb0,
   // the ring is handed over to TMA (async proxy) after these generic accesses
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   named_sync(1, TH);
+}
+
+// store_row_bf16 without the Taylor term, for an output whose rows start on
+// 32-byte boundaries: each lane writes whole 32-byte sectors (256-bit stores),
+// half the store instructions and sector writes of 16-byte stores, with two
+// TMEM loads in flight.
+template <int D>
+__device__ __forceinline__ void store_row_bf16_wide(uint32_t tO, float inv, bool row_valid, uint16_t* dst,
+                                                    [[maybe_unused]] long long off, [[maybe_unused]] long long total,
+                                                    [[maybe_unused]] int* status) {
+#pragma unroll
+  for (int c0 = 0; c0 < D; c0 += 64) {
+    uint32_t rr[2][32];
+    tmem_ld32(tO + c0, rr[0]);
+    tmem_ld32(tO + c0 + 32, rr[1]);
+    tmem_ld_wait();
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      tmem_reg_fence(rr[h]);
+      if (!row_valid) continue;
+#pragma unroll
+      for (int j = 0; j < 32; j += 16) {
+        uint32_t pk[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+          pk[e] = pack_bf16x2(__uint_as_float(rr[h][j + 2 * e]) * inv, __uint_as_float(rr[h][j + 2 * e + 1]) * inv);
+        const int col = c0 + 32 * h + j;
+        if (ATTN_CHECKED(off + col, 16, total, status))
+          asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst + col), "r"(pk[0]),
+                       "r"(pk[1]), "r"(pk[2]), "r"(pk[3]), "r"(pk[4]), "r"(pk[5]), "r"(pk[6]), "r"(pk[7])
+                       : "memory");
+      }
+    }
+  }
 }
 
 template <int D, int BK, int MODE, int NQT, int NSTAGE>
@@ -1162,99 +1343,13 @@ __global__ void __launch_bounds__(NQT * 128 + 128, (NQT == 1) ? 2 : 1)
       // raw scores stay unscaled: the softmax scale is positive, so the max
       // commutes with it and the scaling folds into the exponent's FFMA
       if constexpr (kNA) {
-        // keys of the box inside this row's window: a [lo, hi) range per axis
-        constexpr int BT = Cfg::kNaT, BY = Cfg::kNaY, BX = Cfg::kNaX;
-        int lo[3], hi[3];
-        const int Bd[3] = {BT, BY, BX};
-#pragma unroll
-        for (int a = 0; a < 3; ++a) {
-          lo[a] = min(max(na_ws[a] - na_box[a], 0), Bd[a]);
-          hi[a] = min(max(na_ws[a] + p.na_K[a] - na_box[a], 0), Bd[a]);
-        }
-        const bool full = lo[0] == 0 && hi[0] == BT && lo[1] == 0 && hi[1] == BY && lo[2] == 0 && hi[2] == BX;
-        if (!full) {
-          const bool any = lo[0] < hi[0] && lo[1] < hi[1] && lo[2] < hi[2];
-          const uint32_t xm = any ? (((1u << hi[2]) - 1u) & ~((1u << lo[2]) - 1u)) : 0u;
-          const uint32_t ym = ((1u << hi[1]) - 1u) & ~((1u << lo[1]) - 1u);
-          uint32_t lm = 0;   // bit (frame * BY + row) of the box: that line is in the window
-#pragma unroll
-          for (int ct = 0; ct < BT; ++ct)
-            if (ct >= lo[0] && ct < hi[0]) lm |= ym << (ct * BY);
-          constexpr int LPW = 32 / BX;   // lines per 32-column word
-#pragma unroll
-          for (int w = 0; w < BK / 32; ++w) {
-            uint32_t wd = 0;
-#pragma unroll
-            for (int j = 0; j < LPW; ++j)
-              if ((lm >> (w * LPW + j)) & 1u) wd |= xm << (j * BX);
-#pragma unroll
-            for (int j = 0; j < 32; ++j)
-              if (!((wd >> j) & 1u)) x[w * 32 + j] = -INFINITY;
-          }
-        }
+        na_mask_scores<Cfg::kNaT, Cfg::kNaY, Cfg::kNaX, BK>(x, na_ws, na_box, p.na_K);
       } else if (!(mine && n_valid == BK)) {
 #pragma unroll
         for (int c = 0; c < BK; ++c)
           if (!mine || c >= n_valid) x[c] = -INFINITY;
       }
-      // row max: two chains of three-input maxima (max is exact, so the order is free)
-      float mx0 = fmaxf(x[0], x[1]), mx1 = fmaxf(x[2], x[3]);
-#pragma unroll
-      for (int c = 4; c < BK; c += 4) {
-        mx0 = fmax3(mx0, x[c], x[c + 1]);
-        mx1 = fmax3(mx1, x[c + 2], x[c + 3]);
-      }
-      const float mt = fmaxf(mx0, mx1) * p.scale_log2;
-      // lazy rescale of the running max
-      float alpha = 1.f;
-      bool need = mt > m_run + kRescaleLog2 || (m_run == -INFINITY && mt > -INFINITY);
-      if (need) {
-        alpha = (m_run == -INFINITY) ? 0.f : ex2_approx(m_run - mt);
-        l_run *= alpha;
-        m_run = mt;
-      }
-      if (__any_sync(0xffffffffu, need && alpha != 0.f && it > 0)) {
-        // O_t holds the sum over earlier steps; rescale it in TMEM.  No wait is
-        // needed: the issuer committed bar_s for this step's S after issuing the
-        // previous PV of this tile, and a commit tracks every earlier MMA of the
-        // issuing thread, so that PV has completed as well.
-        const float a = (need && it > 0) ? alpha : 1.f;
-#pragma unroll
-        for (int c0 = 0; c0 < D; c0 += 32) {
-          uint32_t rr[32];
-          tmem_ld32(tO + c0, rr);
-          tmem_ld_wait();
-          tmem_reg_fence(rr);
-#pragma unroll
-          for (int j = 0; j < 32; j += 2) {
-            const float2 v = __fmul2_rn(make_float2(__uint_as_float(rr[j]), __uint_as_float(rr[j + 1])),
-                                        make_float2(a, a));
-            rr[j] = __float_as_uint(v.x);
-            rr[j + 1] = __float_as_uint(v.y);
-          }
-          tmem_st32(tO + c0, rr);
-        }
-      }
-      const float nbase = (m_run == -INFINITY) ? 0.f : -m_run;
-      // pairs of columns through the packed fp32 pipe: the same fused multiply-add
-      // and the same two (even / odd) row-sum chains as scalar code, half the instructions
-      const float2 sc2 = make_float2(p.scale_log2, p.scale_log2), nb2 = make_float2(nbase, nbase);
-      float2 ls = make_float2(0.f, 0.f);
-#pragma unroll
-      for (int c0 = 0; c0 < BK; c0 += 64) {
-        uint32_t pk[32];
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const float2 arg = __ffma2_rn(make_float2(x[c0 + 2 * j], x[c0 + 2 * j + 1]), sc2, nb2);
-          const float p0 = ex2_approx(arg.x);
-          const float p1 = ex2_approx(arg.y);
-          ls = __fadd2_rn(ls, make_float2(p0, p1));
-          pk[j] = pack_bf16x2(p0, p1);
-        }
-        tmem_st32(tS + c0 / 2, pk);
-      }
-      l_run += ls.x + ls.y;
-      tmem_st_wait();
+      softmax_step<BK, D>(x, p.scale_log2, m_run, l_run, it > 0, tS, tO);
       tc_fence_before();
       mbar_arrive(&bar_p[t]);
       ++it;
@@ -1322,35 +1417,8 @@ __global__ void __launch_bounds__(NQT * 128 + 128, (NQT == 1) ? 2 : 1)
         const bool empty = !have_o || !(l_run > 0.f);
         if (empty && row_valid && it == 0 && Cfg::kSparseLike) atomicOr(p.status, ATTN_DEVICE_BAD_LIST);
         const float inv = empty ? 0.f : 1.f / l_run;
-        uint16_t* dst = p.out + ((long long)bh * p.Sq + grow) * D;
-#pragma unroll
-        for (int c0 = 0; c0 < D; c0 += 32) {
-          uint32_t rr[32];
-          if (have_o) {
-            tmem_ld32(tO + c0, rr);
-            tmem_ld_wait();
-            tmem_reg_fence(rr);
-          }
-          if (row_valid) {
-#pragma unroll
-            for (int j = 0; j < 32; j += 8) {
-              uint4 pk;
-              float o[8];
-#pragma unroll
-              for (int e = 0; e < 8; ++e) {
-                float val = have_o ? __uint_as_float(rr[j + e]) : 0.f;
-                if (tt != nullptr) val = fmaf(f, tt[c0 + j + e], val);
-                o[e] = val * inv;
-              }
-              pk.x = pack_bf16x2(o[0], o[1]);
-              pk.y = pack_bf16x2(o[2], o[3]);
-              pk.z = pack_bf16x2(o[4], o[5]);
-              pk.w = pack_bf16x2(o[6], o[7]);
-              if (ATTN_CHECKED(((long long)bh * p.Sq + grow) * D + c0 + j, 8, (long long)p.BH * p.Sq * D, p.status))
-                *reinterpret_cast<uint4*>(dst + c0 + j) = pk;
-            }
-          }
-        }
+        store_row_bf16<D>(tO, have_o, inv, f, tt, row_valid, p.out + ((long long)bh * p.Sq + grow) * D,
+                          ((long long)bh * p.Sq + grow) * D, (long long)p.BH * p.Sq * D, p.status);
         if (row_valid && p.lse != nullptr && ATTN_CHECKED((long long)bh * p.Sq + grow, 1, (long long)p.BH * p.Sq, p.status))
           p.lse[(long long)bh * p.Sq + grow] = empty ? -INFINITY : (m_run + __log2f(l_run)) * kLn2;
       }

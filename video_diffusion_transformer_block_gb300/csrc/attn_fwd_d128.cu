@@ -1,4 +1,4 @@
-// attn_fwd_kernel instantiations for head dim 128.
+// attn_fwd_kernel and attn_na_persist_kernel instantiations for head dim 128.
 #include "attn_fwd_inst.cuh"
 
 namespace vdtb {
@@ -17,6 +17,14 @@ cudaError_t launch_attn_fwd_d128(int BK, int mode, const CUtensorMap& tq, const 
   if (mode == kModeNA1x8x16 && BK == 128) return launch_fwd_cfg<128, 128, kModeNA1x8x16, 2, 4>(tq, tk, tv, p, stream);
   if (mode == kModeNA2x8x8 && BK == 128) return launch_fwd_cfg<128, 128, kModeNA2x8x8, 2, 4>(tq, tk, tv, p, stream);
   if (mode == kModeNA4x4x8 && BK == 128) return launch_fwd_cfg<128, 128, kModeNA4x4x8, 2, 4>(tq, tk, tv, p, stream);
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_na_persist_d128(int mode, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                                  const FwdParams& p, cudaStream_t stream) {
+  if (mode == kModeNA1x8x16) return launch_na_persist_cfg<128, kModeNA1x8x16>(tq, tk, tv, p, stream);
+  if (mode == kModeNA2x8x8) return launch_na_persist_cfg<128, kModeNA2x8x8>(tq, tk, tv, p, stream);
+  if (mode == kModeNA4x4x8) return launch_na_persist_cfg<128, kModeNA4x4x8>(tq, tk, tv, p, stream);
   return cudaErrorInvalidValue;
 }
 

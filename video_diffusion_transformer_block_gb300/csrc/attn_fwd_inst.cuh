@@ -1,6 +1,7 @@
 // Launch helper for one attn_fwd_kernel instantiation.
 #pragma once
 #include "launch.h"
+#include "na_persist.cuh"
 
 namespace vdtb {
 
@@ -20,6 +21,29 @@ cudaError_t launch_fwd_cfg(const CUtensorMap& tq, const CUtensorMap& tk, const C
   if (attr.numRegs != Cfg::kRegsLaunch) return cudaErrorInvalidDeviceFunction;
   long long grid = (long long)p.BH * p.n_qg * (MODE == kModeSplit ? p.n_split : 1);
   if (grid <= 0 || grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  kernel<<<(unsigned)grid, Cfg::kThreads, Cfg::kSmemBytes, stream>>>(tq, tk, tv, p);
+  return cudaGetLastError();
+}
+
+// The persistent neighbourhood kernel: one CTA per SM (fewer when there are
+// fewer than two bricks per SM), each of its two tiles walking its own bricks.
+template <int D, int MODE>
+cudaError_t launch_na_persist_cfg(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                                  const FwdParams& p, cudaStream_t stream) {
+  using Cfg = NAPersistCfg<D, MODE>;
+  auto kernel = attn_na_persist_kernel<D, MODE>;
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  cudaFuncAttributes attr;
+  e = cudaFuncGetAttributes(&attr, kernel);
+  if (e != cudaSuccess) return e;
+  if (attr.numRegs != Cfg::kRegsLaunch) return cudaErrorInvalidDeviceFunction;
+  int dev = 0, sms = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+  const long long units = (long long)p.BH * p.na_nq[0] * p.na_nq[1] * p.na_nq[2];
+  if (units <= 0 || units > 0x7fffffffLL || sms <= 0) return cudaErrorInvalidConfiguration;
+  const long long grid = (units + 1) / 2 < sms ? (units + 1) / 2 : sms;
   kernel<<<(unsigned)grid, Cfg::kThreads, Cfg::kSmemBytes, stream>>>(tq, tk, tv, p);
   return cudaGetLastError();
 }

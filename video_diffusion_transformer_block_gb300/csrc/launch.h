@@ -47,6 +47,14 @@ cudaError_t launch_attn_fwd_d64(int BK, int mode, const CUtensorMap& tq, const C
 cudaError_t launch_attn_fwd_d128(int BK, int mode, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                                  const FwdParams& p, cudaStream_t stream);
 
+// The persistent neighbourhood kernel (na_persist.cuh), mode kModeNA*: tq, tk,
+// tv are 5-D maps (channels, x, y, t, head) of q, k, v with
+// a brick-shaped box of 64 channels; the grid is one CTA per SM at most.
+cudaError_t launch_na_persist_d64(int mode, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                                  const FwdParams& p, cudaStream_t stream);
+cudaError_t launch_na_persist_d128(int mode, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                                   const FwdParams& p, cudaStream_t stream);
+
 // Query tiles of 128 rows per CTA for a mode (the grid is BH * ceil(Sq / (128 * tiles)) [* n_split]).
 // Dense and sparse CTAs take two tiles, each with its own list walk, K/V ring,
 // TMA producer and MMA issuer, and one CTA per SM; the issuers take turns on
