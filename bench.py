@@ -52,15 +52,16 @@ def load_peaks():
 
 def kernel_fingerprint() -> str:
     h = hashlib.sha256()
-    for name in ("attn_fwd.cuh", "ptx.cuh", "attn_fwd_d128.cu"):
+    for name in ("attn_fwd.cuh", "ptx.cuh", "attn_fwd_d128.cu", "na_persist.cuh"):
         with open(os.path.join(ROOT, "video_diffusion_transformer_block_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
 def profiled_counters(workload: str):
-    """Per-launch DRAM bytes and tensor-pipe activity of the sparse forward from the committed ncu
-    summary, if they were taken on the current kernel source (else None for both)."""
+    """Per-launch DRAM bytes and tensor-pipe activity of a workload's dominant kernel (sparse64k:
+    the sparse forward; na3d: the neighbourhood kernel) from the committed ncu summary, if they
+    were taken on the current kernel source (else None for both)."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None, None
@@ -593,10 +594,11 @@ def run_native_kernel(args, world, rank, local):
         ach = exec_flops / (ms * 1e-3) / 1e12
         kname = (f"attn_na_persist_kernel (3D neighbourhood, persistent one-brick tiles, brick {brick}, d={d})"
                  if pair == 4 else f"attn_fwd_kernel (3D neighbourhood, brick {brick}, pair {pair}, d={d})")
+        traffic, tpipe = profiled_counters("na3d") if H == 32 else (None, None)
         roof = {"bound": "tensor", "kernel": kname,
                 "achieved": round(ach, 2), "peak": peak, "unit": "TFLOP/s", "frac": round(ach / peak, 4),
                 "peak_source": f"{peaks_src} bf16_tflops (burst: one kernel per timed step, L2 flushed between)",
-                "traffic": None}
+                "traffic": traffic, "tensor_pipe_active_pct_ncu": tpipe}
         extra = {"executed_tflops": round(world * ach, 2), "window_fraction_of_executed": round(flops / exec_flops, 4)}
     elif args.workload == "dense16k":
         peak = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
