@@ -184,6 +184,21 @@ __global__ void __launch_bounds__(256) lse_merge_reg_kernel(const float* __restr
   // launch now, and wait until the kernel before this one (which may have
   // produced the partials) has completed and its writes are visible
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  // Meanwhile thread c asks L2 for this block's 8 rows of partial c and their
+  // lse values, so that the loads after the wait find them there instead of
+  // waiting on DRAM.  A prefetch returns no data and L2 is where every write
+  // of the kernel before lands, so a line it is still writing cannot be read
+  // stale: the loads come after the wait.
+  {
+    const long long row0 = (long long)blockIdx.x * 8;
+    const int c = threadIdx.x;
+    if (c < n && row0 < rows) {
+      const long long nr = rows - row0 < 8 ? rows - row0 : 8;
+      const float* src = o_part + ((long long)c * rows + row0) * D;   // 16-byte aligned, nr * D * 4 bytes
+      asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"((unsigned)(nr * D * 4)) : "memory");
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(lse_part + (long long)c * rows + row0) : "memory");
+    }
+  }
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
