@@ -103,6 +103,20 @@ def test_sparse64k_full_size():
     assert 0.0 < density < 1.0
 
 
+@pytest.mark.parametrize("H,S,d,beta", [(8, 128 * 301 - 37, 128, 0.5), (12, 128 * 201 - 5, 64, 1.0)])
+def test_fused_routing_odd_block_count_mid_size(H, S, d, beta):
+    # routing folded into the forward at a size between the small cases and the benchmark: an odd
+    # query-block count leaves the second tile of the last CTA of every head without a block, and
+    # the last key block is short
+    nqb = -(-S // 128)
+    assert nqb % 2 == 1
+    w0 = WORKLOADS["sparse64k"]
+    w = Workload("fp", B=1, H=H, Sq=S, Skv=S, d=d, seed=43 + d, q_std=0.5, k_std=0.5, grid=w0.grid,
+                 audio_per_frame=8, pe=True, block=128, beta=beta)
+    flips, density = sparse_full_size(w, beta, n_rows=2048, n_heads=3, seed=108 + d, fn=vd.attn_sparse_fused_fwd)
+    assert 0.0 < density < 1.0
+
+
 def test_sparse64k_full_size_fused_routing():
     w = WORKLOADS["sparse64k"]
     flips, density = sparse_full_size(w, w.beta, n_rows=4096, n_heads=4, seed=106, fn=vd.attn_sparse_fused_fwd)
