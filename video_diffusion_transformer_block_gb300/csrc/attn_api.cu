@@ -529,7 +529,7 @@ attn_status_t sparse_common_checks(const SparseArgs& a) {
 attn_status_t run_route(const SparseArgs& a, float beta, void* workspace, size_t workspace_bytes, int32_t* si,
                         int32_t* sc, float* stt, float* tt, cudaStream_t stream) {
   SparseLayout L;
-  sparse_layout(a.B, a.H, a.S, a.d, a.block_q, a.block_k, &L);
+  if (!sparse_layout(a.B, a.H, a.S, a.d, a.block_q, a.block_k, &L)) return ATTN_ERR_UNSUPPORTED;
   if (!workspace || ((uintptr_t)workspace & 255u) || workspace_bytes < L.total) return ATTN_ERR_WORKSPACE;
   uint8_t* ws = (uint8_t*)workspace;
   float* qp = (float*)(ws + L.qp);
@@ -632,7 +632,7 @@ attn_status_t attn_sparse_route_fwd(const attn_bf16* q, const attn_bf16* k, cons
     return ATTN_ERR_INVALID_ARG;
   if (isnan(beta) || beta == INFINITY) return ATTN_ERR_INVALID_ARG;
   SparseLayout L;
-  sparse_layout(B, H, S, d, block_q, block_k, &L);
+  if (!sparse_layout(B, H, S, d, block_q, block_k, &L)) return ATTN_ERR_UNSUPPORTED;
   if (!workspace || ((uintptr_t)workspace & 255u) || workspace_bytes < L.total) return ATTN_ERR_WORKSPACE;
   uint8_t* ws = (uint8_t*)workspace;
   int32_t* si = sel_idx ? sel_idx : (int32_t*)(ws + L.sel_idx);
@@ -657,7 +657,7 @@ attn_status_t attn_sparse_fused_fwd(const attn_bf16* q, const attn_bf16* k, cons
   const int NQB = (S + block_q - 1) / block_q, NKB = (S + block_k - 1) / block_k;
   if (NKB > kFusedMaxNKB) return ATTN_ERR_UNSUPPORTED;
   SparseLayout L;
-  sparse_layout(B, H, S, d, block_q, block_k, &L);
+  if (!sparse_layout(B, H, S, d, block_q, block_k, &L)) return ATTN_ERR_UNSUPPORTED;
   if (!workspace || ((uintptr_t)workspace & 255u) || workspace_bytes < L.total) return ATTN_ERR_WORKSPACE;
   int* status = nullptr;
   if ((st = status_ptr(&status)) != ATTN_OK) return st;

@@ -12,18 +12,22 @@
 //   - group g of the tile's producer loads the K box of stream element g and
 //     the V box of element g-1 (and, when g starts a brick, that brick's Q
 //     tile, whose slot the last score MMA of the previous brick has freed);
-//   - batch g of the tile's issuer is PV(g-1) then S(g), under the issue lock
-//     that alternates the two tiles' batches on the tensor pipe, with one
-//     commit that tells the softmax (S ready) and the producer (slots free);
-//     the first PV of a brick overwrites O;
-//   - the tile's softmax warpgroup, on the batch that starts a brick, first
+//   - batch g of the tile's issuer is PV(g-1) then S(g) with the window step
+//     (see NABiasLayout), under the issue lock that alternates the two tiles'
+//     batches on the tensor pipe, with one commit that tells the softmax (S
+//     ready) and the producer (slots free); the first PV of a brick
+//     overwrites O;
+//   - the tile's softmax warpgroup writes the window rows of element g+1
+//     while S(g) is computed, and on the batch that starts a brick first
 //     stores the previous brick's rows (that batch held its last PV), then
 //     runs the softmax of the new brick's first scores.
 // So one tile's epilogue and Q load overlap the other tile's MMAs.  The
-// arithmetic of every row (mask, online softmax, normalisation) is that of
-// attn_fwd_kernel's neighbourhood modes; the key boxes of a brick are those
-// of its one-brick walk (a box grid from the corner of the union of the
-// brick's windows), so results are identical to that kernel's one-brick plan.
+// online softmax and normalisation are those of attn_fwd_kernel's
+// neighbourhood modes and the key boxes of a brick those of its one-brick
+// walk (a box grid from the corner of the union of the brick's windows); the
+// window, added by the tensor core instead of masked by the softmax threads,
+// leaves every in-window score unchanged, so results are bit-identical to
+// that kernel's one-brick plan.
 #pragma once
 #include "attn_fwd.cuh"
 
