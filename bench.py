@@ -21,6 +21,7 @@ import hashlib
 import json
 import math
 import os
+import re
 import subprocess
 import sys
 import time
@@ -51,10 +52,15 @@ def load_peaks():
 
 
 def kernel_fingerprint() -> str:
+    """Hash of the profiled kernels' source with comments and layout removed, so that counters
+    taken on a kernel stay attached to it across edits of its comments only."""
     h = hashlib.sha256()
     for name in ("attn_fwd.cuh", "ptx.cuh", "attn_fwd_d128.cu", "na_persist.cuh"):
-        with open(os.path.join(ROOT, "video_diffusion_transformer_block_gb300", "csrc", name), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, "video_diffusion_transformer_block_gb300", "csrc", name)) as f:
+            src = f.read()
+        src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)
+        src = re.sub(r"//[^\n]*", " ", src)
+        h.update(" ".join(src.split()).encode())
     return h.hexdigest()[:16]
 
 
