@@ -178,7 +178,8 @@ attn_status_t attn_sparse_route(const attn_bf16* q, const attn_bf16* k, const at
  * (sel_idx/sel_cnt ascending lists, stats[..][0] = mu, stats[..][3] = W,
  * taylor_t = T).  Lets a caller reuse one routing for several calls.  A list
  * entry outside [0, NKB) is clamped and reported by attn_last_device_status
- * as ATTN_ERR_INVALID_ARG.
+ * as ATTN_ERR_INVALID_ARG; so is an empty list (sel_cnt 0), whose query rows
+ * are written as zeros with lse -inf.
  */
 attn_status_t attn_sparse_fwd(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v, attn_bf16* out, float* lse,
                               int B, int H, int S, int d, float scale, int block_q, int block_k,

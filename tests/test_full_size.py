@@ -117,6 +117,18 @@ def test_fused_routing_odd_block_count_mid_size(H, S, d, beta):
     assert 0.0 < density < 1.0
 
 
+@pytest.mark.parametrize("H,S,d,beta", [(8, 128 * 301 - 37, 128, 0.5), (12, 128 * 201 - 5, 64, 1.0)])
+def test_sparse_two_launch_mid_size_odd_block_count(H, S, d, beta):
+    # pool + route + forward at a size between the small cases and the benchmark (the sizes of the
+    # folded-routing case above): an odd query-block count leaves the second tile of the last CTA
+    # of every head without a block, and the last key block is short
+    w0 = WORKLOADS["sparse64k"]
+    w = Workload("tp", B=1, H=H, Sq=S, Skv=S, d=d, seed=47 + d, q_std=0.5, k_std=0.5, grid=w0.grid,
+                 audio_per_frame=8, pe=True, block=128, beta=beta)
+    flips, density = sparse_full_size(w, beta, n_rows=2048, n_heads=3, seed=112 + d)
+    assert 0.0 < density < 1.0
+
+
 def test_sparse64k_full_size_fused_routing():
     w = WORKLOADS["sparse64k"]
     flips, density = sparse_full_size(w, w.beta, n_rows=4096, n_heads=4, seed=106, fn=vd.attn_sparse_fused_fwd)

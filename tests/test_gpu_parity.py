@@ -176,6 +176,49 @@ def test_sparse_beta_minus_inf_equals_dense():
             assert_close(host(out_s), host(out_d), "sparse(-inf) vs dense")
 
 
+@pytest.mark.parametrize("d", [128, 64])
+def test_sparse_all_blocks_equals_dense_over_many_ctas(d):
+    # 6 heads x 52 two-tile CTAs (more than two waves of CTAs), each head ending in a short query
+    # block and a short key block; with every key block selected the sparse walk does the dense
+    # kernel's arithmetic in the same order, bit for bit
+    S = 128 * 103 - 11
+    q, k, v = rnd_qkv(1, 6, S, S, d, seed=53)
+    out_s, lse_s = vd.attn_sparse_route_fwd(q, k, v, -math.inf, block=128)
+    out_d, lse_d = vd.attn_dense_fwd(q, k, v)
+    torch.cuda.synchronize()
+    assert torch.equal(out_s, out_d) and torch.equal(lse_s, lse_d)
+
+
+def test_sparse_forward_reports_corrupt_lists_and_keeps_other_rows():
+    # an empty list and an entry past the last key block: the forward reports both; the empty
+    # list's rows become zeros (lse -inf), the bad entry is clamped to the last key block, and every
+    # other query block's rows are exactly those of the intact routing
+    B, H, S, d, block = 1, 2, 1000, 128, 128
+    q, k, v = rnd_qkv(B, H, S, S, d, seed=57)
+    rt = vd.attn_sparse_route(q, k, v, 1.0, block=block)
+    ref_o, ref_l = vd.attn_sparse_fwd(q, k, v, rt, block=block)
+    assert vd.attn_last_device_status() == 0
+    nkb = rt["sel_idx"].shape[-1]
+    bad = {key: val.clone() for key, val in rt.items()}
+    bad["sel_cnt"][0, 0, 3] = 0
+    bad["sel_idx"][0, 1, 2, 0] = nkb + 5
+    out, lse = vd.attn_sparse_fwd(q, k, v, bad, block=block)
+    assert vd.attn_last_device_status() == 1     # ATTN_ERR_INVALID_ARG
+    rows3 = slice(3 * block, 4 * block)
+    assert torch.all(out[0, 0, rows3] == 0) and torch.all(torch.isneginf(lse[0, 0, rows3]))
+    # the clamped list now holds the last key block where it held its first entry
+    fixed = {key: val.clone() for key, val in rt.items()}
+    fixed["sel_idx"][0, 1, 2, 0] = nkb - 1
+    fo, fl = vd.attn_sparse_fwd(q, k, v, fixed, block=block)
+    assert vd.attn_last_device_status() == 0
+    rows2 = slice(2 * block, 3 * block)
+    assert torch.equal(out[0, 1, rows2], fo[0, 1, rows2]) and torch.equal(lse[0, 1, rows2], fl[0, 1, rows2])
+    keep = torch.ones(H, S, dtype=torch.bool, device=out.device)
+    keep[0, rows3] = False
+    keep[1, rows2] = False
+    assert torch.equal(out[0][keep], ref_o[0][keep]) and torch.equal(lse[0][keep], ref_l[0][keep])
+
+
 @pytest.mark.parametrize("d,block,beta", [(128, 128, 1.0), (128, 64, 0.5), (64, 128, 1.5)])
 def test_sparse_local_workload_ragged(d, block, beta):
     # the Stage-2 generator (noise + 3D position code, interleaved audio) truncated to two frames: S = 8208

@@ -834,14 +834,15 @@ __device__ __forceinline__ void fused_route(const FwdParams& p, int bh, int qb0,
   named_sync(1, TH);
 }
 
-// store_row_bf16 without the Taylor term, for an output whose rows start on
-// 32-byte boundaries: each lane writes whole 32-byte sectors (256-bit stores),
-// half the store instructions and sector writes of 16-byte stores, with two
-// TMEM loads in flight.
+// store_row_bf16 for an output whose rows start on 32-byte boundaries: each
+// lane writes whole 32-byte sectors (256-bit stores), half the store
+// instructions and sector writes of 16-byte stores, with two TMEM loads in
+// flight.  Same arithmetic per element: (O + f T) * inv, T optional (16-byte
+// aligned, in global or shared memory).
 template <int D>
-__device__ __forceinline__ void store_row_bf16_wide(uint32_t tO, float inv, bool row_valid, uint16_t* dst,
-                                                    [[maybe_unused]] long long off, [[maybe_unused]] long long total,
-                                                    [[maybe_unused]] int* status) {
+__device__ __forceinline__ void store_row_bf16_wide(uint32_t tO, float inv, float f, const float* tt, bool row_valid,
+                                                    uint16_t* dst, [[maybe_unused]] long long off,
+                                                    [[maybe_unused]] long long total, [[maybe_unused]] int* status) {
 #pragma unroll
   for (int c0 = 0; c0 < D; c0 += 64) {
     uint32_t rr[2][32];
@@ -854,11 +855,24 @@ __device__ __forceinline__ void store_row_bf16_wide(uint32_t tO, float inv, bool
       if (!row_valid) continue;
 #pragma unroll
       for (int j = 0; j < 32; j += 16) {
+        const int col = c0 + 32 * h + j;
+        float o[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) o[e] = __uint_as_float(rr[h][j + e]);
+        if (tt != nullptr) {
+#pragma unroll
+          for (int e4 = 0; e4 < 4; ++e4) {
+            // a generic load: T lives in global memory or (folded routing) in shared memory
+            const float4 t4 = reinterpret_cast<const float4*>(tt + col)[e4];
+            o[4 * e4 + 0] = fmaf(f, t4.x, o[4 * e4 + 0]);
+            o[4 * e4 + 1] = fmaf(f, t4.y, o[4 * e4 + 1]);
+            o[4 * e4 + 2] = fmaf(f, t4.z, o[4 * e4 + 2]);
+            o[4 * e4 + 3] = fmaf(f, t4.w, o[4 * e4 + 3]);
+          }
+        }
         uint32_t pk[8];
 #pragma unroll
-        for (int e = 0; e < 8; ++e)
-          pk[e] = pack_bf16x2(__uint_as_float(rr[h][j + 2 * e]) * inv, __uint_as_float(rr[h][j + 2 * e + 1]) * inv);
-        const int col = c0 + 32 * h + j;
+        for (int e = 0; e < 8; ++e) pk[e] = pack_bf16x2(o[2 * e] * inv, o[2 * e + 1] * inv);
         if (ATTN_CHECKED(off + col, 16, total, status))
           asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst + col), "r"(pk[0]),
                        "r"(pk[1]), "r"(pk[2]), "r"(pk[3]), "r"(pk[4]), "r"(pk[5]), "r"(pk[6]), "r"(pk[7])
@@ -1389,10 +1403,11 @@ __global__ void __launch_bounds__(NQT * 128 + 128, (NQT == 1) ? 2 : 1)
         if (row_valid && ATTN_CHECKED(orow, 1, (long long)p.n_split * p.BH * p.Sq, p.status))
           p.lse_part[orow] = empty ? -INFINITY : (m_run + __log2f(l_run)) * kLn2;
       } else {
-        // Taylor term for the rejected blocks of this row's query block
+        // Taylor term for the rejected blocks of this row's query block (none
+        // when the row met no key: an empty, i.e. corrupt, list; its row becomes zeros)
         float f = 0.f;
         const float* tt = nullptr;
-        if (MODE == kModeSparseFused) {
+        if (MODE == kModeSparseFused && m_run > -INFINITY) {
           const int l = t * QB + qb;
           if (qg * NQT * QB + l < p.NQB && f_cnt[l] < p.NKB) {
             f = ex2_approx(f_mu[l] * kLog2e - m_run);
@@ -1400,7 +1415,7 @@ __global__ void __launch_bounds__(NQT * 128 + 128, (NQT == 1) ? 2 : 1)
             tt = f_T + l * D;
           }
         }
-        if (MODE == kModeSparse) {
+        if (MODE == kModeSparse && m_run > -INFINITY) {
           const long long qbi = (long long)(qg * NQT + t) * QB + qb;
           if (qbi < p.NQB) {
             const long long srow = (long long)bh * p.NQB + qbi;
@@ -1417,8 +1432,13 @@ __global__ void __launch_bounds__(NQT * 128 + 128, (NQT == 1) ? 2 : 1)
         const bool empty = !have_o || !(l_run > 0.f);
         if (empty && row_valid && it == 0 && Cfg::kSparseLike) atomicOr(p.status, ATTN_DEVICE_BAD_LIST);
         const float inv = empty ? 0.f : 1.f / l_run;
-        store_row_bf16<D>(tO, have_o, inv, f, tt, row_valid, p.out + ((long long)bh * p.Sq + grow) * D,
-                          ((long long)bh * p.Sq + grow) * D, (long long)p.BH * p.Sq * D, p.status);
+        // rows of D bf16 start on 32-byte boundaries when the output does: whole 32-byte sectors per lane
+        if (have_o && ((uintptr_t)p.out & 31u) == 0)
+          store_row_bf16_wide<D>(tO, inv, f, tt, row_valid, p.out + ((long long)bh * p.Sq + grow) * D,
+                                 ((long long)bh * p.Sq + grow) * D, (long long)p.BH * p.Sq * D, p.status);
+        else
+          store_row_bf16<D>(tO, have_o, inv, f, tt, row_valid, p.out + ((long long)bh * p.Sq + grow) * D,
+                            ((long long)bh * p.Sq + grow) * D, (long long)p.BH * p.Sq * D, p.status);
         if (row_valid && p.lse != nullptr && ATTN_CHECKED((long long)bh * p.Sq + grow, 1, (long long)p.BH * p.Sq, p.status))
           p.lse[(long long)bh * p.Sq + grow] = empty ? -INFINITY : (m_run + __log2f(l_run)) * kLn2;
       }

@@ -380,7 +380,7 @@ __global__ void __launch_bounds__(384, 1)
         const float inv = empty ? 0.f : 1.f / l_run;
         const bool row_valid = orow >= 0;
         if (out_wide)
-          store_row_bf16_wide<D>(tO, inv, row_valid, p.out + orow * D, orow * D, (long long)p.BH * p.Sq * D, p.status);
+          store_row_bf16_wide<D>(tO, inv, 0.f, nullptr, row_valid, p.out + orow * D, orow * D, (long long)p.BH * p.Sq * D, p.status);
         else
           store_row_bf16<D>(tO, true, inv, 0.f, nullptr, row_valid, p.out + orow * D, orow * D,
                             (long long)p.BH * p.Sq * D, p.status);
