@@ -557,8 +557,8 @@ def run_native_kernel(args, world, rank, local):
         brick, pair, boxes = vd.attn_na3d_plan(w.grid, kern)
         flops = 4.0 * B * H * Sq * math.prod(kern) * d                 # the windows' own work
         # what the tensor cores run: per key box S = Q K^T and O += P V, and on the
-        # persistent plan one (4x4x8 bricks) or two K = 16 steps that add the window
-        window_k = (16 if brick == 3 else 32) if pair == 4 else 0
+        # persistent plans one (plan 4, 4x4x8 bricks) or two K = 16 steps that add the window
+        window_k = (16 if (brick == 3 and pair == 4) else 32) if pair in (4, 5) else 0
         exec_flops = 2.0 * B * H * boxes * 128 * 128 * (2 * d + window_k)
 
         def step():
@@ -598,8 +598,9 @@ def run_native_kernel(args, world, rank, local):
     if args.workload == "na3d":
         peak = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
         ach = exec_flops / (ms * 1e-3) / 1e12
-        kname = (f"attn_na_persist_kernel (3D neighbourhood, persistent one-brick tiles, brick {brick}, d={d})"
-                 if pair == 4 else f"attn_fwd_kernel (3D neighbourhood, brick {brick}, pair {pair}, d={d})")
+        kname = (f"attn_na_persist_kernel (3D neighbourhood, persistent one-brick tiles, brick {brick}"
+                 f"{', key boxes 4x2x16' if pair == 5 else ''}, d={d})"
+                 if pair in (4, 5) else f"attn_fwd_kernel (3D neighbourhood, brick {brick}, pair {pair}, d={d})")
         traffic, tpipe = profiled_counters("na3d") if H == 32 else (None, None)
         roof = {"bound": "tensor", "kernel": kname,
                 "achieved": round(ach, 2), "peak": peak, "unit": "TFLOP/s", "frac": round(ach / peak, 4),

@@ -127,6 +127,11 @@ def test_fused_sparse_rejections(lib):
 # ---------------------------------------------------------------- 3D neighbourhood attention (host logic)
 
 BRICKS = {1: (1, 8, 16), 2: (2, 8, 8), 3: (4, 4, 8)}
+WIDE_KEYS = (4, 2, 16)   # the key boxes of plan 5 (with the 4x4x8 brick)
+
+
+def key_box(brick, pair):
+    return WIDE_KEYS if pair == 5 else BRICKS[brick]
 
 
 def na_start(p, K, L):
@@ -135,10 +140,12 @@ def na_start(p, K, L):
 
 def na_walk(grid, kernel, brick, pair):
     """Python restatement of the kernel's box walk: yields, per CTA, its query
-    bricks (two neighbours along ``pair``, or one when pair is 3 or 4: plan 4
-    runs the one-brick tiles on persistent CTAs, with the same boxes per brick)
-    and the boxes with their tile flags."""
+    bricks (two neighbours along ``pair``, or one when pair is 3, 4 or 5: plans
+    4 and 5 run the one-brick tiles on persistent CTAs, plan 4 with the same
+    boxes per brick, plan 5 with 4x2x16 key boxes) and the boxes with their
+    tile flags."""
     B = BRICKS[brick]
+    KB = key_box(brick, pair)
     nq = [-(-grid[a] // B[a]) for a in range(3)]
     np_ = [(-(-nq[a] // 2) if a == pair else nq[a]) for a in range(3)]
     for it in range(np_[0]):
@@ -155,13 +162,13 @@ def na_walk(grid, kernel, brick, pair):
                     hi = [na_start(min(org[a] + B[a], grid[a]) - 1, kernel[a], grid[a]) + kernel[a] for a in range(3)]
                     tiles.append((org, lo, hi))
                 cu = [min(tl[1][a] for tl in tiles) for a in range(3)]
-                nk = [-(-(max(tl[2][a] for tl in tiles) - cu[a]) // B[a]) for a in range(3)]
+                nk = [-(-(max(tl[2][a] for tl in tiles) - cu[a]) // KB[a]) for a in range(3)]
                 boxes = []
                 for ut in range(nk[0]):
                     for uy in range(nk[1]):
                         for ux in range(nk[2]):
-                            box = [cu[0] + ut * B[0], cu[1] + uy * B[1], cu[2] + ux * B[2]]
-                            flags = [all(box[a] < tl[2][a] and box[a] + B[a] > tl[1][a] for a in range(3))
+                            box = [cu[0] + ut * KB[0], cu[1] + uy * KB[1], cu[2] + ux * KB[2]]
+                            flags = [all(box[a] < tl[2][a] and box[a] + KB[a] > tl[1][a] for a in range(3))
                                      for tl in tiles]
                             if any(flags):
                                 boxes.append((box, flags))
@@ -171,9 +178,12 @@ def na_walk(grid, kernel, brick, pair):
 @pytest.mark.parametrize("grid,kernel", [((3, 13, 21), (3, 5, 7)), ((5, 11, 19), (3, 5, 4)), ((1, 20, 24), (1, 9, 9)),
                                          ((4, 16, 32), (2, 16, 1)), ((2, 5, 6), (2, 5, 6))])
 @pytest.mark.parametrize("brick", [1, 2, 3])
-@pytest.mark.parametrize("pair", [0, 1, 2, 3, 4])
+@pytest.mark.parametrize("pair", [0, 1, 2, 3, 4, 5])
 def test_na3d_walk_covers_every_window_and_plan_counts_it(lib, grid, kernel, brick, pair):
+    if pair == 5 and brick != 3:
+        pytest.skip("plan 5 takes the 4x4x8 brick only")
     B = BRICKS[brick]
+    KB = key_box(brick, pair)
     work = 0
     for tiles, boxes in na_walk(grid, kernel, brick, pair):
         for t, (org, lo, hi) in enumerate(tiles):
@@ -190,12 +200,12 @@ def test_na3d_walk_covers_every_window_and_plan_counts_it(lib, grid, kernel, bri
                         for a in range(3):
                             covered = set()
                             for box in mine:
-                                covered.update(range(box[a], box[a] + B[a]))
+                                covered.update(range(box[a], box[a] + KB[a]))
                             assert set(range(ws[a], ws[a] + kernel[a])) <= covered
                         corners = [(ws[0] + e0 * (kernel[0] - 1), ws[1] + e1 * (kernel[1] - 1), ws[2] + e2 * (kernel[2] - 1))
                                    for e0 in (0, 1) for e1 in (0, 1) for e2 in (0, 1)]
                         for kc in corners:
-                            assert any(all(box[a] <= kc[a] < box[a] + B[a] for a in range(3)) for box in mine)
+                            assert any(all(box[a] <= kc[a] < box[a] + KB[a] for a in range(3)) for box in mine)
     b, pa, nb = ctypes.c_int(brick), ctypes.c_int(pair), ctypes.c_longlong(0)
     assert lib.attn_na3d_plan(*grid, *kernel, ctypes.byref(b), ctypes.byref(pa), ctypes.byref(nb)) == 0
     assert (b.value, pa.value) == (brick, pair)
@@ -203,26 +213,36 @@ def test_na3d_walk_covers_every_window_and_plan_counts_it(lib, grid, kernel, bri
 
 
 def test_na3d_plan_picks_the_least_work(lib):
-    # an open pair axis means the persistent one-brick tiles (plan 4); an open brick minimises
-    # 20 (4x4x8) or 23 (the others) per key box + 34 per brick there, 20 per box + 40 per CTA elsewhere
+    # an open pair axis means the persistent one-brick tiles (plan 4, or plan 5 with the 4x4x8 brick);
+    # an open brick minimises 20 (plan 4, 4x4x8) or 23 (plan 4 with the others, plan 5) per key box +
+    # 34 per brick there, 20 per box + 40 per CTA elsewhere
     for grid, kernel in [((4, 128, 128), (3, 7, 7)), ((4, 64, 64), (3, 31, 31)), ((1, 96, 160), (1, 13, 13)),
                          ((5, 11, 19), (3, 5, 4)), ((8, 64, 64), (3, 7, 7))]:
-        for pair in (3, 4):
+        persistent = {}
+        for pair in (3, 4, 5):
             costs = {}
             for brick in (1, 2, 3):
+                if pair == 5 and brick != 3:
+                    continue
                 b, pa, nbox = vd.attn_na3d_plan(grid, kernel, brick, pair)
                 assert (b, pa) == (brick, pair)
                 ctas = np.prod([-(-grid[a] // BRICKS[brick][a]) for a in range(3)])
-                costs[brick] = ((20 if brick == 3 else 23) * nbox + 34 * ctas) if pair == 4 else 20 * nbox + 40 * ctas
+                if pair == 3:
+                    costs[brick] = 20 * nbox + 40 * ctas
+                else:
+                    costs[brick] = (20 if (brick == 3 and pair == 4) else 23) * nbox + 34 * ctas
+                    persistent[(brick, pair)] = costs[brick]
                 assert nbox * 128 * 128 >= np.prod(grid) * np.prod(kernel)   # the boxes hold every window
             b, pa, nb = vd.attn_na3d_plan(grid, kernel, 0, pair)
             assert pa == pair and costs[b] == min(costs.values())
         b, pa, nb = vd.attn_na3d_plan(grid, kernel)
-        assert pa == 4 and (b, pa, nb) == vd.attn_na3d_plan(grid, kernel, 0, 4)
-        # a fixed brick with an open pair axis keeps the brick
+        assert pa in (4, 5) and persistent[(b, pa)] == min(persistent.values())
+        assert (b, pa, nb) == vd.attn_na3d_plan(grid, kernel, b, pa)
+        # a fixed brick with an open pair axis keeps the brick (plan 5 only with the 4x4x8 brick)
         assert vd.attn_na3d_plan(grid, kernel, 2)[:2] == (2, 4)
-    # the volumes timed on GB300 take their fastest brick
-    assert vd.attn_na3d_plan((4, 128, 128), (3, 7, 7))[0] == 3
+        assert vd.attn_na3d_plan(grid, kernel, 3)[1] in (4, 5)
+    # the volumes timed on GB300 take their fastest plan
+    assert vd.attn_na3d_plan((4, 128, 128), (3, 7, 7))[:2] == (3, 5)
     assert vd.attn_na3d_plan((4, 64, 64), (3, 31, 31))[0] == 3
     assert vd.attn_na3d_plan((1, 96, 160), (1, 13, 13))[0] == 1
     assert vd.attn_na3d_plan((8, 64, 64), (3, 7, 7))[0] == 2
@@ -231,10 +251,14 @@ def test_na3d_plan_picks_the_least_work(lib):
 def test_na3d_rejections(lib):
     base = [P, P, P, P, P, 1, 2, 4, 16, 16, 128, 3, 5, 5, 0.088, 0, -1, None]
     for i, bad in [(11, 0), (11, 5), (12, 17), (13, 0), (7, 0), (14, 0.0), (14, math.nan), (15, 4), (15, -1),
-                   (16, 5), (16, -2)]:
+                   (16, 6), (16, -2)]:
         args = list(base)
         args[i] = bad
         assert lib.attn_na3d_fwd(*args) == 1, (i, bad)
+    for brick in (1, 2):   # plan 5 takes the 4x4x8 brick only
+        args = list(base)
+        args[15], args[16] = brick, 5
+        assert lib.attn_na3d_fwd(*args) == 1, brick
     args = list(base)
     args[10] = 96
     assert lib.attn_na3d_fwd(*args) == 2

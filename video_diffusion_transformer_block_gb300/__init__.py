@@ -151,8 +151,8 @@ def attn_na3d_fwd(q, k, v, grid, kernel, scale=None, brick=0, pair_axis=-1, out=
     """3D neighbourhood attention over a (T, Y, X) volume of raster-ordered tokens;
     returns (out bf16 [B,H,S,d], lse fp32 [B,H,S]).  brick / pair_axis: 0 / -1 let
     the library choose the tile plan (attn_na3d_plan); pair_axis 4 is the
-    persistent one-brick plan, 3 one brick per CTA, 0-2 two neighbouring bricks
-    per CTA."""
+    persistent one-brick plan, 5 the same with 4x2x16 key boxes (4x4x8 brick
+    only), 3 one brick per CTA, 0-2 two neighbouring bricks per CTA."""
     lib = load_library()
     B, H, S, d = _bhsd(q, "q")
     if _bhsd(k, "k") != q.shape or _bhsd(v, "v") != q.shape:

@@ -150,21 +150,26 @@ int na_start(int p, int K, int L) {
 }
 int na_mode_of(int brick) { return brick == 1 ? kModeNA1x8x16 : brick == 2 ? kModeNA2x8x8 : kModeNA4x4x8; }
 
+// The key boxes of a plan: the brick's own shape, or (plan 5) the wide boxes.
+int na_keys_of(int pair) { return pair == 5 ? kNAKeysWide : kNAKeysBrick; }
+
 // Key boxes a (brick, pair axis) plan makes the CTAs multiply, summed over
-// every query tile of one head, and the number of CTAs per head.  The count
-// separates over the axes: along a non-pair axis a tile's boxes depend only on
-// its own coordinate, along the pair axis on the pair it belongs to.
+// every query tile of one head, and the number of CTAs per head (for the
+// persistent plans 4 and 5, of bricks).  The count separates over the axes:
+// along a non-pair axis a tile's boxes depend only on its own coordinate,
+// along the pair axis on the pair it belongs to.
 void na_plan_cost(const int L[3], const int K[3], int brick, int pair, long long* boxes, long long* ctas) {
-  const int mode = na_mode_of(brick);
+  const int mode = na_mode_of(brick), keys = na_keys_of(pair);
   const int B[3] = {na_brick_t(mode), na_brick_y(mode), na_brick_x(mode)};
+  const int KB[3] = {na_keys_t(mode, keys), na_keys_y(mode, keys), na_keys_x(mode, keys)};
   long long prod = 1, n = 1;
   for (int a = 0; a < 3; ++a) {
     const int nq = (L[a] + B[a] - 1) / B[a];
     auto lo_of = [&](int i) { return na_start(i * B[a], K[a], L[a]); };
     auto hi_of = [&](int i) { return na_start((i + 1) * B[a] < L[a] ? (i + 1) * B[a] - 1 : L[a] - 1, K[a], L[a]) + K[a]; };
     long long sum = 0;
-    if (a != pair) {   // (pair 3: no axis is paired)
-      for (int i = 0; i < nq; ++i) sum += (hi_of(i) - lo_of(i) + B[a] - 1) / B[a];
+    if (a != pair) {   // (pairs 3, 4, 5: no axis is paired)
+      for (int i = 0; i < nq; ++i) sum += (hi_of(i) - lo_of(i) + KB[a] - 1) / KB[a];
       n *= nq;
     } else {
       for (int j = 0; 2 * j < nq; ++j) {
@@ -181,31 +186,42 @@ void na_plan_cost(const int L[3], const int K[3], int brick, int pair, long long
 }
 
 // Picks the plan left open by the caller (brick 0, pair -1).  An open pair
-// axis means the persistent one-brick tiles (pair 4), the fastest plan on
-// GB300 for every volume and window measured.  An open brick minimises a cost
-// in twentieths of a key box: for pair 4, 20 per box of a brick whose window
-// step is 16 columns wide (4x4x8), 23 per box where it is 32 (the other
-// bricks: a wider MMA step and one window buffer), plus 34 per brick (its
-// epilogue); for the other plans 20 per box plus 40 per CTA (a CTA's fixed
-// cost counted as two boxes).  The weights are fits to GB300 timings.
-void na_choose(const int L[3], const int K[3], int* brick, int* pair, long long* boxes) {
-  if (*pair < 0) *pair = 4;
+// axis means the persistent one-brick tiles: plan 4 (key boxes of the brick's
+// shape) or, for the 4x4x8 brick, plan 5 (4x2x16 key boxes), the fastest plans
+// on GB300 for every volume and window measured.  The choice minimises a cost
+// in twentieths of a key box: 20 per box whose window step is 16 columns wide
+// (plan 4 with the 4x4x8 brick), 23 where it is 32 (a wider MMA step and, at
+// d = 128, one window buffer instead of two), plus 34 per brick (its epilogue);
+// for the other plans 20 per box plus 40 per CTA (a CTA's fixed cost counted as
+// two boxes).  The weights are fits to GB300 timings.  Plan 5 exists for the
+// 4x4x8 brick only: asked for with another brick, it is refused (false).
+bool na_choose(const int L[3], const int K[3], int* brick, int* pair, long long* boxes) {
+  if (*pair == 5 && *brick != 0 && *brick != 3) return false;
   long long best = -1;
-  int bb = 1;
+  int bb = 1, bp = *pair;
   long long bboxes = 0;
   for (int b = 1; b <= 3; ++b) {
     if (*brick != 0 && b != *brick) continue;
-    long long nbox, ncta;
-    na_plan_cost(L, K, b, *pair, &nbox, &ncta);
-    const long long cost = *pair == 4 ? (b == 3 ? 20 : 23) * nbox + 34 * ncta : 20 * nbox + 40 * ncta;
-    if (best < 0 || cost < best) {
-      best = cost;
-      bb = b;
-      bboxes = nbox;
+    // the caller's pair axis, or (left open) the persistent plans 4 and 5
+    const int first = *pair >= 0 ? *pair : 4, last = *pair >= 0 ? *pair : 5;
+    for (int cand = first; cand <= last; ++cand) {
+      if (cand == 5 && b != 3) continue;
+      long long nbox, ncta;
+      na_plan_cost(L, K, b, cand, &nbox, &ncta);
+      const bool wide_step = cand == 5 || (cand == 4 && b != 3);
+      const long long cost = cand >= 4 ? (wide_step ? 23 : 20) * nbox + 34 * ncta : 20 * nbox + 40 * ncta;
+      if (best < 0 || cost < best) {
+        best = cost;
+        bb = b;
+        bp = cand;
+        bboxes = nbox;
+      }
     }
   }
   *brick = bb;
+  *pair = bp;
   *boxes = bboxes;
+  return true;
 }
 
 attn_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA; }
@@ -328,10 +344,10 @@ attn_status_t attn_dense_fwd(const attn_bf16* q, const attn_bf16* k, const attn_
 attn_status_t attn_na3d_plan(int T, int Y, int X, int Kt, int Ky, int Kx, int* brick, int* pair_axis,
                              long long* key_boxes) {
   if (!brick || !pair_axis || !na_args_ok(1, 1, T, Y, X, Kt, Ky, Kx)) return ATTN_ERR_INVALID_ARG;
-  if (*brick < 0 || *brick > 3 || *pair_axis < -1 || *pair_axis > 4) return ATTN_ERR_INVALID_ARG;
+  if (*brick < 0 || *brick > 3 || *pair_axis < -1 || *pair_axis > 5) return ATTN_ERR_INVALID_ARG;
   const int L[3] = {T, Y, X}, K[3] = {Kt, Ky, Kx};
   long long boxes = 0;
-  na_choose(L, K, brick, pair_axis, &boxes);
+  if (!na_choose(L, K, brick, pair_axis, &boxes)) return ATTN_ERR_INVALID_ARG;
   if (key_boxes) *key_boxes = boxes;
   return ATTN_OK;
 }
@@ -344,26 +360,28 @@ attn_status_t attn_na3d_fwd(const attn_bf16* q, const attn_bf16* k, const attn_b
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || (lse && ((uintptr_t)lse & 3u)))
     return ATTN_ERR_INVALID_ARG;
   if (!na_args_ok(B, H, T, Y, X, Kt, Ky, Kx) || !(isfinite(scale) && scale > 0.f)) return ATTN_ERR_INVALID_ARG;
-  if (brick < 0 || brick > 3 || pair_axis < -1 || pair_axis > 4) return ATTN_ERR_INVALID_ARG;
+  if (brick < 0 || brick > 3 || pair_axis < -1 || pair_axis > 5) return ATTN_ERR_INVALID_ARG;
   if (!valid_d(d)) return ATTN_ERR_UNSUPPORTED;
   const int L[3] = {T, Y, X}, K[3] = {Kt, Ky, Kx};
   long long boxes = 0;
-  na_choose(L, K, &brick, &pair_axis, &boxes);
-  // the persistent plan adds the window to the scores on the tensor core (-2^120
+  if (!na_choose(L, K, &brick, &pair_axis, &boxes)) return ATTN_ERR_INVALID_ARG;
+  // the persistent plans add the window to the scores on the tensor core (-2^120
   // outside it), which an exponent turns into an exact 0 only for scale * log2(e)
-  // >= 2^-80; below that the one-brick CTAs (the same boxes and arithmetic, the
-  // window applied as -inf by the softmax threads) give the same results
-  if (pair_axis == 4 && !(scale * 1.4426950408889634f >= 0x1p-80f)) pair_axis = 3;
-  const int mode = na_mode_of(brick);
+  // >= 2^-80; below that the one-brick CTAs (the window applied as -inf by the
+  // softmax threads) give the same results as plan 4 (the same boxes and
+  // arithmetic) and plan 5's results up to rounding (other key boxes)
+  if (pair_axis >= 4 && !(scale * 1.4426950408889634f >= 0x1p-80f)) pair_axis = 3;
+  const int mode = na_mode_of(brick), keys = na_keys_of(pair_axis);
   const int Bv[3] = {na_brick_t(mode), na_brick_y(mode), na_brick_x(mode)};
+  const int KBv[3] = {na_keys_t(mode, keys), na_keys_y(mode, keys), na_keys_x(mode, keys)};
   int* status = nullptr;
   attn_status_t st = status_ptr(&status);
   if (st != ATTN_OK) return st;
   const int S = T * Y * X;
   CUtensorMap tq, tk, tv;
   if ((st = make_map_5d(&tq, q, d, T, Y, X, B * H, Bv[0], Bv[1], Bv[2])) != ATTN_OK) return st;
-  if ((st = make_map_5d(&tk, k, d, T, Y, X, B * H, Bv[0], Bv[1], Bv[2])) != ATTN_OK) return st;
-  if ((st = make_map_5d(&tv, v, d, T, Y, X, B * H, Bv[0], Bv[1], Bv[2])) != ATTN_OK) return st;
+  if ((st = make_map_5d(&tk, k, d, T, Y, X, B * H, KBv[0], KBv[1], KBv[2])) != ATTN_OK) return st;
+  if ((st = make_map_5d(&tv, v, d, T, Y, X, B * H, KBv[0], KBv[1], KBv[2])) != ATTN_OK) return st;
   FwdParams p = base_params(B, H, S, S, scale, mode, status);
   long long n_qg = 1;
   for (int a = 0; a < 3; ++a) {
@@ -378,9 +396,9 @@ attn_status_t attn_na3d_fwd(const attn_bf16* q, const attn_bf16* k, const attn_b
   p.na_pair_axis = pair_axis;
   p.out = out;
   p.lse = lse;
-  if (pair_axis == 4)
-    return cuda_status(d == 128 ? launch_na_persist_d128(mode, tq, tk, tv, p, stream)
-                                : launch_na_persist_d64(mode, tq, tk, tv, p, stream));
+  if (pair_axis >= 4)
+    return cuda_status(d == 128 ? launch_na_persist_d128(mode, keys, tq, tk, tv, p, stream)
+                                : launch_na_persist_d64(mode, keys, tq, tk, tv, p, stream));
   return cuda_status(launch_fwd(d, 128, mode, tq, tk, tv, p, stream));
 }
 

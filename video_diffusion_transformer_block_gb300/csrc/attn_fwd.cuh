@@ -64,6 +64,13 @@ __host__ __device__ constexpr bool is_na_mode(int m) { return m >= kModeNA1x8x16
 __host__ __device__ constexpr int na_brick_t(int m) { return m == kModeNA4x4x8 ? 4 : (m == kModeNA2x8x8 ? 2 : 1); }
 __host__ __device__ constexpr int na_brick_y(int m) { return m == kModeNA4x4x8 ? 4 : 8; }
 __host__ __device__ constexpr int na_brick_x(int m) { return m == kModeNA1x8x16 ? 16 : 8; }
+// Key boxes of the persistent neighbourhood kernel: kNAKeysBrick takes the
+// brick's own shape, kNAKeysWide 4 x 2 x 16 (which covers the window union of a
+// 4 x 4 x 8 brick under small windows with fewer boxes).
+constexpr int kNAKeysBrick = 0, kNAKeysWide = 1;
+__host__ __device__ constexpr int na_keys_t(int m, int keys) { return keys == kNAKeysWide ? 4 : na_brick_t(m); }
+__host__ __device__ constexpr int na_keys_y(int m, int keys) { return keys == kNAKeysWide ? 2 : na_brick_y(m); }
+__host__ __device__ constexpr int na_keys_x(int m, int keys) { return keys == kNAKeysWide ? 16 : na_brick_x(m); }
 
 constexpr float kRescaleLog2 = 8.0f;
 constexpr float kLog2e = 1.4426950408889634f;

@@ -27,11 +27,11 @@ cudaError_t launch_fwd_cfg(const CUtensorMap& tq, const CUtensorMap& tk, const C
 
 // The persistent neighbourhood kernel: one CTA per SM (fewer when there are
 // fewer than two bricks per SM), each of its two tiles walking its own bricks.
-template <int D, int MODE>
+template <int D, int MODE, int KEYS>
 cudaError_t launch_na_persist_cfg(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                                   const FwdParams& p, cudaStream_t stream) {
-  using Cfg = NAPersistCfg<D, MODE>;
-  auto kernel = attn_na_persist_kernel<D, MODE>;
+  using Cfg = NAPersistCfg<D, MODE, KEYS>;
+  auto kernel = attn_na_persist_kernel<D, MODE, KEYS>;
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes);
   if (e != cudaSuccess) return e;
   cudaFuncAttributes attr;

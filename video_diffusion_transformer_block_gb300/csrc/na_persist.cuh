@@ -35,11 +35,13 @@ namespace vdtb {
 
 // The bricks of one tile and their key boxes, in visiting order.  Unit w =
 // head * bricks per head + brick (bricks x fastest); the tile takes units
-// first, first + 2 * grid, ... below BH * bricks per head.  Only what the
-// next box needs is kept; a brick's head and origin are handed out when it
-// starts (so they hold no registers between bricks).  Within a brick the box
-// index steps like an odometer (x fastest), without divisions.
-template <int BT, int BY, int BX>
+// first, first + 2 * grid, ... below BH * bricks per head.  A brick is BT x
+// BY x BX queries, a key box KT x KY x KX keys (128 each; the key boxes tile
+// the union of the brick's windows from its corner).  Only what the next box
+// needs is kept; a brick's head and origin are handed out when it starts (so
+// they hold no registers between bricks).  Within a brick the box index steps
+// like an odometer (x fastest), without divisions.
+template <int BT, int BY, int BX, int KT, int KY, int KX>
 struct NABrickStream {
   int w;          // next unit
   int lo[3];      // origin of the current brick's box grid (corner of the union of its rows' windows)
@@ -52,7 +54,7 @@ struct NABrickStream {
     ix[1] = ix[2] = nk[1] = nk[2] = 1;
   }
   // Next key box of the stream: its origin `box` and its index `bi` in the
-  // brick's box grid (box = lo + bi * brick).  When it starts a brick,
+  // brick's box grid (box = lo + bi * key box).  When it starts a brick,
   // `starts` is set and bh / org / glo receive the brick's head, origin and
   // box-grid origin.  False at the end.
   __device__ __forceinline__ bool next(const FwdParams& p, int (&box)[3], int (&bi)[3], bool& starts, int& bh,
@@ -68,14 +70,14 @@ struct NABrickStream {
       b /= p.na_nq[2];
       id[1] = b % p.na_nq[1];
       id[0] = b / p.na_nq[1];
-      const int B[3] = {BT, BY, BX};
+      const int B[3] = {BT, BY, BX}, KB[3] = {KT, KY, KX};
 #pragma unroll
       for (int a = 0; a < 3; ++a) {
         org[a] = id[a] * B[a];
         const int last = min(org[a] + B[a], p.na_L[a]) - 1;
         lo[a] = na_window_start(org[a], p.na_K[a], p.na_L[a]);
         const int hi = na_window_start(last, p.na_K[a], p.na_L[a]) + p.na_K[a];
-        nk[a] = (hi - lo[a] + B[a] - 1) / B[a];
+        nk[a] = (hi - lo[a] + KB[a] - 1) / KB[a];
         glo[a] = lo[a];
         ix[a] = 0;
       }
@@ -83,9 +85,9 @@ struct NABrickStream {
     }
 #pragma unroll
     for (int a = 0; a < 3; ++a) bi[a] = ix[a];
-    box[0] = lo[0] + bi[0] * BT;
-    box[1] = lo[1] + bi[1] * BY;
-    box[2] = lo[2] + bi[2] * BX;
+    box[0] = lo[0] + bi[0] * KT;
+    box[1] = lo[1] + bi[1] * KY;
+    box[2] = lo[2] + bi[2] * KX;
     if (++ix[2] == nk[2]) {
       ix[2] = 0;
       if (++ix[1] == nk[1]) {
@@ -108,14 +110,15 @@ struct NABrickStream {
 // so a key in the window gets x + 0 = x (its score unchanged, bit for bit)
 // and a key outside gets -2^120 or less, which the softmax's exponent turns
 // into an exact 0 whenever scale * log2(e) >= 2^-80 (|x| < 2^96 leaves
-// x - 2^120 = -2^120).  A frame one-hot is only needed when the brick has
-// several frames (a one-frame brick's boxes all lie in its frame window).
-template <int BT, int BY, int BX>
+// x - 2^120 = -2^120).  Frame one-hots are only needed when the brick or the
+// key box has several frames (a one-frame brick's one-frame boxes all lie in
+// its frame window).  KT x KY x KX: the key box; kFrames: frame one-hots kept.
+template <int KT, int KY, int KX, bool kFrames>
 struct NABiasLayout {
   static constexpr int kT0 = 0;                        // first frame column
-  static constexpr int kY0 = BT > 1 ? BT : 0;          // first row column
-  static constexpr int kX0 = kY0 + BY;                 // first column column
-  static constexpr int kUsed = kX0 + BX;
+  static constexpr int kY0 = kFrames ? KT : 0;         // first row column
+  static constexpr int kX0 = kY0 + KY;                 // first column column
+  static constexpr int kUsed = kX0 + KX;
   static constexpr int kCols = (kUsed + 15) / 16 * 16;   // K of the bias step (16 or 32)
   static constexpr int kBytes = 128 * kCols * 2;         // one operand (128 rows)
   // no-swizzle K-major layout: 8 x 8 core matrices (128 bytes each); the
@@ -127,11 +130,13 @@ struct NABiasLayout {
   }
 };
 
-template <int D, int MODE>
+template <int D, int MODE, int KEYS>
 struct NAPersistCfg {
   static constexpr int BT = na_brick_t(MODE), BY = na_brick_y(MODE), BX = na_brick_x(MODE);
+  static constexpr int KT = na_keys_t(MODE, KEYS), KY = na_keys_y(MODE, KEYS), KX = na_keys_x(MODE, KEYS);
   static constexpr int BK = 128;
-  using Bias = NABiasLayout<BT, BY, BX>;
+  static constexpr bool kFrames = BT > 1 || KT > 1;
+  using Bias = NABiasLayout<KT, KY, KX, kFrames>;
   // two softmax warpgroups (one per tile) + one control warpgroup: warps 8, 9
   // are tile 0's producer and issuer, 10, 11 tile 1's
   static constexpr int kThreads = 384;
@@ -155,7 +160,7 @@ struct NAPersistCfg {
   static constexpr uint32_t kIdescS = idesc_bf16_f32(128, BK, 0, 0);
   static constexpr uint32_t kIdescPV = idesc_bf16_f32(128, D, 0, 1);
   static_assert(D == 64 || D == 128, "head dim");
-  static_assert(is_na_mode(MODE) && BT * BY * BX == 128, "neighbourhood bricks");
+  static_assert(is_na_mode(MODE) && BT * BY * BX == 128 && KT * KY * KX == BK, "neighbourhood bricks and key boxes");
   static_assert(kSmemRaw <= 227 * 1024, "shared memory");
 };
 
@@ -163,12 +168,12 @@ struct NAPersistCfg {
 constexpr uint16_t kBf16One = 0x3F80;        // 1.0
 constexpr uint16_t kBf16MaskBias = 0xFB80;   // -2^120
 
-// Row `row` of the window operand for one box: per axis, 0 for the box
-// coordinates inside the window (rel_ws: the window start minus the box
-// origin, extent K), -2^120 for the others; unused columns 0.
-template <int BT, int BY, int BX>
+// Row `row` of the window operand for one key box (KT x KY x KX, layout L):
+// per axis, 0 for the box coordinates inside the window (rel_ws: the window
+// start minus the box origin, extent K), -2^120 for the others; unused
+// columns 0.
+template <class L, int KT, int KY, int KX>
 __device__ __forceinline__ void write_window_row(uint8_t* qm, int row, const int (&rel_ws)[3], const int (&K)[3]) {
-  using L = NABiasLayout<BT, BY, BX>;
   uint32_t w[L::kCols / 2];
 #pragma unroll
   for (int i = 0; i < L::kCols / 2; ++i) w[i] = 0;
@@ -176,28 +181,28 @@ __device__ __forceinline__ void write_window_row(uint8_t* qm, int row, const int
     const uint32_t v = in ? 0u : (uint32_t)kBf16MaskBias;
     w[col >> 1] |= v << ((col & 1) * 16);
   };
-  if constexpr (BT > 1) {
+  if constexpr (L::kY0 > 0) {
 #pragma unroll
-    for (int c = 0; c < BT; ++c) put(L::kT0 + c, c >= rel_ws[0] && c < rel_ws[0] + K[0]);
+    for (int c = 0; c < KT; ++c) put(L::kT0 + c, c >= rel_ws[0] && c < rel_ws[0] + K[0]);
   }
 #pragma unroll
-  for (int c = 0; c < BY; ++c) put(L::kY0 + c, c >= rel_ws[1] && c < rel_ws[1] + K[1]);
+  for (int c = 0; c < KY; ++c) put(L::kY0 + c, c >= rel_ws[1] && c < rel_ws[1] + K[1]);
 #pragma unroll
-  for (int c = 0; c < BX; ++c) put(L::kX0 + c, c >= rel_ws[2] && c < rel_ws[2] + K[2]);
+  for (int c = 0; c < KX; ++c) put(L::kX0 + c, c >= rel_ws[2] && c < rel_ws[2] + K[2]);
 #pragma unroll
   for (int c8 = 0; c8 < L::kCols / 8; ++c8)
     *reinterpret_cast<uint4*>(qm + L::offset(row, 8 * c8)) =
         make_uint4(w[4 * c8], w[4 * c8 + 1], w[4 * c8 + 2], w[4 * c8 + 3]);
 }
 
-template <int D, int MODE>
+template <int D, int MODE, int KEYS>
 __global__ void __launch_bounds__(384, 1)
     attn_na_persist_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                            const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
-  using Cfg = NAPersistCfg<D, MODE>;
+  using Cfg = NAPersistCfg<D, MODE, KEYS>;
   using Bias = typename Cfg::Bias;
   constexpr int BK = Cfg::BK;
-  using Stream = NABrickStream<Cfg::BT, Cfg::BY, Cfg::BX>;
+  using Stream = NABrickStream<Cfg::BT, Cfg::BY, Cfg::BX, Cfg::KT, Cfg::KY, Cfg::KX>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint8_t* sQ = smem;                              // tile t's Q at t * kQTileBytes
@@ -232,8 +237,8 @@ __global__ void __launch_bounds__(384, 1)
     uint32_t w[Bias::kCols / 2];
 #pragma unroll
     for (int i = 0; i < Bias::kCols / 2; ++i) w[i] = 0;
-    const int tk = tid / (Cfg::BY * Cfg::BX), yk = (tid / Cfg::BX) % Cfg::BY, xk = tid % Cfg::BX;
-    const int cols[3] = {Cfg::BT > 1 ? Bias::kT0 + tk : -1, Bias::kY0 + yk, Bias::kX0 + xk};
+    const int tk = tid / (Cfg::KY * Cfg::KX), yk = (tid / Cfg::KX) % Cfg::KY, xk = tid % Cfg::KX;
+    const int cols[3] = {Cfg::kFrames ? Bias::kT0 + tk : -1, Bias::kY0 + yk, Bias::kX0 + xk};
 #pragma unroll
     for (int a = 0; a < 3; ++a)
       if (cols[a] >= 0) w[cols[a] >> 1] |= (uint32_t)kBf16One << ((cols[a] & 1) * 16);
@@ -402,9 +407,9 @@ __global__ void __launch_bounds__(384, 1)
           for (int a = 0; a < 3; ++a)
             ws_rel |= (uint32_t)(na_window_start(min(rc[a], p.na_L[a] - 1), p.na_K[a], p.na_L[a]) - glo[a]) << (8 * a);
         }
-        const int rel[3] = {(int)(ws_rel & 0xffu) - bi[0] * Cfg::BT, (int)((ws_rel >> 8) & 0xffu) - bi[1] * Cfg::BY,
-                            (int)(ws_rel >> 16) - bi[2] * Cfg::BX};
-        write_window_row<Cfg::BT, Cfg::BY, Cfg::BX>(qm + (la % Cfg::kQmBufs) * Bias::kBytes, r, rel, p.na_K);
+        const int rel[3] = {(int)(ws_rel & 0xffu) - bi[0] * Cfg::KT, (int)((ws_rel >> 8) & 0xffu) - bi[1] * Cfg::KY,
+                            (int)(ws_rel >> 16) - bi[2] * Cfg::KX};
+        write_window_row<Bias, Cfg::KT, Cfg::KY, Cfg::KX>(qm + (la % Cfg::kQmBufs) * Bias::kBytes, r, rel, p.na_K);
         ++la;
         return true;
       };
