@@ -23,11 +23,14 @@
 //     runs the softmax of the new brick's first scores.
 // So one tile's epilogue and Q load overlap the other tile's MMAs.  The
 // online softmax and normalisation are those of attn_fwd_kernel's
-// neighbourhood modes and the key boxes of a brick those of its one-brick
-// walk (a box grid from the corner of the union of the brick's windows); the
-// window, added by the tensor core instead of masked by the softmax threads,
-// leaves every in-window score unchanged, so results are bit-identical to
-// that kernel's one-brick plan.
+// neighbourhood modes; the key boxes tile the union of the brick's windows
+// from its corner, in the brick's own shape (KEYS = kNAKeysBrick: the boxes of
+// that kernel's one-brick walk) or as 4 x 2 x 16 boxes (kNAKeysWide, fewer
+// boxes per 4 x 4 x 8 brick under small windows).  The window, added by the
+// tensor core instead of masked by the softmax threads, leaves every
+// in-window score unchanged, so with the brick-shaped boxes results are
+// bit-identical to that kernel's one-brick plan (with the wide boxes, equal
+// up to the rounding of another key order).
 #pragma once
 #include "attn_fwd.cuh"
 
