@@ -139,11 +139,13 @@ def test_na3d_persistent_plan_tiny_scale_same_bits():
 @pytest.mark.parametrize("brick,grid,kernel,H,d", [
     (3, (5, 37, 45), (3, 7, 7), 12, 128),   # 1440 bricks of 4x4x8, ragged in every axis
     (1, (3, 40, 50), (3, 5, 9), 16, 64),    # 960 bricks of 1x8x16
+    (2, (6, 37, 45), (3, 7, 7), 8, 128),    # 720 bricks of 2x8x8; one window buffer per tile at d = 128
 ])
 def test_na3d_persistent_tiles_walk_several_bricks(brick, grid, kernel, H, d):
     # plan 4: each tile of a persistent CTA runs bricks one after another (the
     # epilogue of one brick, the Q load of the next); enough bricks that every
-    # tile takes several
+    # tile takes several.  With one window buffer (2x8x8 at d = 128) the window
+    # step runs first in each score MMA, which must not change a bit either
     B = {1: (1, 8, 16), 2: (2, 8, 8), 3: (4, 4, 8)}[brick]
     units = H * int(np.prod([-(-grid[a] // B[a]) for a in range(3)]))
     assert units > 2 * 2 * torch.cuda.get_device_properties(0).multi_processor_count
