@@ -118,6 +118,20 @@ def test_splitkv_and_merge(H, Sq, Skv, d, n):
     assert_close(host(lse), rl, "merged lse")
 
 
+def test_splitkv_partials_16_byte_aligned():
+    # the partial rows are written as whole 32-byte sectors when they start on a 32-byte boundary
+    # and as 16-byte pieces otherwise: partials 16 bytes past a boundary take the second path
+    H, Sq, Skv, d, n = 2, 130, 2000, 128, 4
+    q, k, v = rnd_qkv(1, H, Sq, Skv, d, seed=61)
+    op, lp = vd.attn_cross_splitkv_fwd(q, k, v, n)
+    buf = torch.empty(n * H * Sq * d + 4, dtype=torch.float32, device=q.device)
+    op16 = buf[4:].view(n, 1, H, Sq, d)
+    assert op16.data_ptr() % 32 == 16
+    _, lp16 = vd.attn_cross_splitkv_fwd(q, k, v, n, out_part=op16)
+    torch.cuda.synchronize()
+    assert torch.equal(op16, op) and torch.equal(lp16, lp)
+
+
 # ---------------------------------------------------------------- block-sparse
 
 def sparse_check(q, k, v, block, beta, scale=None, rows=None, heads_idx=None, fn=None):

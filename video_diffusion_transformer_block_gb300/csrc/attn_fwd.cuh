@@ -1386,6 +1386,9 @@ __global__ void __launch_bounds__(NQT * 128 + 128, (NQT == 1) ? 2 : 1)
         const float inv = empty ? 0.f : 1.f / l_run;
         const long long orow = ((long long)chunk * p.BH + bh) * p.Sq + grow;
         float* dst = p.out_part + orow * D;
+        // rows of D floats start on 32-byte boundaries when the partials do: whole
+        // 32-byte sectors per lane then (half the store instructions)
+        const bool wide = ((uintptr_t)p.out_part & 31u) == 0;
 #pragma unroll
         for (int c0 = 0; c0 < D; c0 += 32) {
           uint32_t rr[32];
@@ -1396,14 +1399,22 @@ __global__ void __launch_bounds__(NQT * 128 + 128, (NQT == 1) ? 2 : 1)
           }
           if (row_valid) {
 #pragma unroll
-            for (int j = 0; j < 32; j += 4) {
-              float4 o4;
-              o4.x = have_o ? __uint_as_float(rr[j]) * inv : 0.f;
-              o4.y = have_o ? __uint_as_float(rr[j + 1]) * inv : 0.f;
-              o4.z = have_o ? __uint_as_float(rr[j + 2]) * inv : 0.f;
-              o4.w = have_o ? __uint_as_float(rr[j + 3]) * inv : 0.f;
-              if (ATTN_CHECKED(orow * D + c0 + j, 4, (long long)p.n_split * p.BH * p.Sq * D, p.status))
-                *reinterpret_cast<float4*>(dst + c0 + j) = o4;
+            for (int j = 0; j < 32; j += 8) {
+              uint32_t o[8];
+#pragma unroll
+              for (int e = 0; e < 8; ++e) o[e] = __float_as_uint(have_o ? __uint_as_float(rr[j + e]) * inv : 0.f);
+              if (wide) {
+                if (ATTN_CHECKED(orow * D + c0 + j, 8, (long long)p.n_split * p.BH * p.Sq * D, p.status))
+                  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst + c0 + j),
+                               "r"(o[0]), "r"(o[1]), "r"(o[2]), "r"(o[3]), "r"(o[4]), "r"(o[5]), "r"(o[6]), "r"(o[7])
+                               : "memory");
+              } else {
+#pragma unroll
+                for (int h = 0; h < 2; ++h)
+                  if (ATTN_CHECKED(orow * D + c0 + j + 4 * h, 4, (long long)p.n_split * p.BH * p.Sq * D, p.status))
+                    *reinterpret_cast<uint4*>(dst + c0 + j + 4 * h) =
+                        make_uint4(o[4 * h], o[4 * h + 1], o[4 * h + 2], o[4 * h + 3]);
+              }
             }
           }
         }
