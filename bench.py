@@ -215,7 +215,7 @@ def run_native(args, world, rank, local):
     B, H, S, d, block = w.B, w.H, w.Sq, w.d, w.block
     dev = q.device
     ws = torch.empty(vd.attn_sparse_workspace_bytes(B, H, S, d, block, block), dtype=torch.uint8, device=dev)
-    rt = vd.sparse_route_buffers(B, H, S, d, block, dev)
+    rt = vd.sparse_route_buffers(B, H, S, d, block, dev, order=True)
     out = torch.empty_like(q)
     lse = torch.empty((B, H, S), dtype=torch.float32, device=dev)
     op = torch.empty((CROSS_N_SPLIT, B, H, CROSS_SQ, d), dtype=torch.float32, device=dev)
@@ -473,7 +473,7 @@ def run_sweep(args, world, rank, local):
     q, k, v = make_qkv(w, device="cuda")
     B, H, S, d, block = w.B, w.H, w.Sq, w.d, w.block
     ws = torch.empty(vd.attn_sparse_workspace_bytes(B, H, S, d, block, block), dtype=torch.uint8, device=q.device)
-    rt = vd.sparse_route_buffers(B, H, S, d, block, q.device)
+    rt = vd.sparse_route_buffers(B, H, S, d, block, q.device, order=True)
     out = torch.empty_like(q)
     lse = torch.empty((B, H, S), dtype=torch.float32, device=q.device)
     stream = torch.cuda.current_stream()

@@ -155,6 +155,8 @@ size_t attn_sparse_workspace_bytes(int B, int H, int S, int d, int block_q, int 
  *   stats      [B][H][NQB][4] fp32 (nullable): mu, sigma, tau, W
  *   taylor_t   [B][H][NQB][d] fp32 (nullable): T
  * Null outputs are kept inside the workspace.  S is limited to NKB <= 8192.
+ * With 128-token blocks the workspace also holds the query-block order
+ * (attn_sparse_route's qb_order) the forward pairs its query tiles by.
  */
 attn_status_t attn_sparse_route_fwd(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v, attn_bf16* out,
                                     float* lse, int B, int H, int S, int d, float scale, float beta, int block_q,
@@ -166,11 +168,19 @@ attn_status_t attn_sparse_route_fwd(const attn_bf16* q, const attn_bf16* k, cons
  * Sol-Attn selection with its Taylor aggregates (same definitions as
  * attn_sparse_route_fwd).  Here sel_idx, sel_cnt, stats and taylor_t are
  * required (non-null); the workspace holds the pooled tensors.
+ *   qb_order   [B][H][NQB] int32 (nullable; 128-token blocks only, else
+ *              ATTN_ERR_INVALID_ARG): per head, within each run of 128
+ *              consecutive query blocks, the blocks sorted by sel_cnt,
+ *              longest list first (ties: lower index first).  The forward
+ *              runs the blocks in places 2s and 2s + 1 of this order on one
+ *              CTA, whose time is that of the longer list, so neighbours of
+ *              nearly equal length waste little; any order gives the same
+ *              results bit for bit.
  */
 attn_status_t attn_sparse_route(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v, int B, int H, int S,
                                 int d, float scale, float beta, int block_q, int block_k, void* workspace,
                                 size_t workspace_bytes, int32_t* sel_idx, int32_t* sel_cnt, float* stats,
-                                float* taylor_t, cudaStream_t stream);
+                                float* taylor_t, int32_t* qb_order, cudaStream_t stream);
 
 /*
  * Forward half of attn_sparse_route_fwd: block-sparse attention with the
@@ -179,12 +189,16 @@ attn_status_t attn_sparse_route(const attn_bf16* q, const attn_bf16* k, const at
  * taylor_t = T).  Lets a caller reuse one routing for several calls.  A list
  * entry outside [0, NKB) is clamped and reported by attn_last_device_status
  * as ATTN_ERR_INVALID_ARG; so is an empty list (sel_cnt 0), whose query rows
- * are written as zeros with lse -inf.
+ * are written as zeros with lse -inf.  qb_order (nullable; 128-token blocks
+ * only): the order attn_sparse_route writes, i.e. per head a permutation of
+ * the query blocks; null pairs blocks 2s and 2s + 1.  An entry outside
+ * [0, NQB) is clamped and reported like a bad list entry; an order that is not
+ * a permutation leaves some query rows unwritten.
  */
 attn_status_t attn_sparse_fwd(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v, attn_bf16* out, float* lse,
                               int B, int H, int S, int d, float scale, int block_q, int block_k,
                               const int32_t* sel_idx, const int32_t* sel_cnt, const float* stats,
-                              const float* taylor_t, cudaStream_t stream);
+                              const float* taylor_t, const int32_t* qb_order, cudaStream_t stream);
 
 /*
  * attn_sparse_route_fwd with the routing folded into the forward kernel: after

@@ -91,11 +91,11 @@ def test_sparse_workspace_and_rejections(lib):
     n = lib.attn_sparse_workspace_bytes(1, 32, 65664, 128, 128, 128)
     nq = 513
     nqp = (nq + 3) // 4 * 4
-    # pooled q, k, v; lists; counts + stats; Taylor T; tf32 hi / lo of the pooled keys and of the transposed
-    # pooled values (rows padded to a multiple of 4)
-    expect_min = (32 * nq * 128 * 4 * 3 + 32 * nq * nq * 4 + 32 * nq * 4 * 5 + 32 * nq * 128 * 4
+    # pooled q, k, v; lists; counts + stats; Taylor T; the query-block order; tf32 hi / lo of the pooled
+    # keys and of the transposed pooled values (rows padded to a multiple of 4)
+    expect_min = (32 * nq * 128 * 4 * 3 + 32 * nq * nq * 4 + 32 * nq * 4 * 5 + 32 * nq * 128 * 4 + 32 * nq * 4
                   + 2 * 32 * nq * 128 * 4 + 2 * 32 * 128 * nqp * 4)
-    assert expect_min <= n <= expect_min + 11 * 256
+    assert expect_min <= n <= expect_min + 12 * 256
     assert lib.attn_sparse_workspace_bytes(1, 1, 1000, 128, 64, 128) == 0      # block_q != block_k
     assert lib.attn_sparse_workspace_bytes(1, 1, 1000, 96, 64, 64) == 0        # bad d
     ws = ctypes.c_void_p(0x100000)
@@ -105,6 +105,21 @@ def test_sparse_workspace_and_rejections(lib):
     assert lib.attn_sparse_route_fwd(*args) == 1                              # NaN beta
     args[10], args[11] = 0.5, 32
     assert lib.attn_sparse_route_fwd(*args) == 2                              # unsupported block
+
+
+def test_sparse_query_block_order_rejections(lib):
+    # the order is for 128-token blocks only, and 4-byte aligned
+    odd = ctypes.c_void_p(0x1002)
+    ws = ctypes.c_void_p(0x100000)
+    big = 1 << 40
+    route = [P, P, P, 1, 2, 1024, 64, 0.125, 0.5, 64, 64, ws, big, P, P, P, P]
+    assert lib.attn_sparse_route(*route, P, None) == 1                      # order with 64-token blocks
+    route[9], route[10] = 128, 128
+    assert lib.attn_sparse_route(*route, odd, None) == 1                    # misaligned order
+    fwd = [P, P, P, P, P, 1, 2, 1024, 64, 0.125, 64, 64, P, P, P, P]
+    assert lib.attn_sparse_fwd(*fwd, P, None) == 1
+    fwd[10], fwd[11] = 128, 128
+    assert lib.attn_sparse_fwd(*fwd, odd, None) == 1
 
 
 def test_selftest_rejects_bad_limit(lib):

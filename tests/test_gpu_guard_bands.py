@@ -81,6 +81,8 @@ def test_sparse_guard_bands(S, d, block, beta):
     nq = (S + block - 1) // block
     rt = {"sel_idx": Guarded((B, H, nq, nq), torch.int32), "sel_cnt": Guarded((B, H, nq), torch.int32),
           "stats": Guarded((B, H, nq, 4), torch.float32), "taylor_t": Guarded((B, H, nq, d), torch.float32)}
+    if block == 128:
+        rt["qb_order"] = Guarded((B, H, nq), torch.int32)   # the query-block order the forward pairs tiles by
     ws = Guarded((vd.attn_sparse_workspace_bytes(B, H, S, d, block, block),), torch.uint8)
     out, lse = Guarded((B, H, S, d), torch.bfloat16), Guarded((B, H, S), torch.float32)
     route = {name: g.t for name, g in rt.items()}

@@ -203,6 +203,39 @@ def test_sparse_all_blocks_equals_dense_over_many_ctas(d):
     assert torch.equal(out_s, out_d) and torch.equal(lse_s, lse_d)
 
 
+def test_sparse_query_block_order_balances_pairs_and_changes_no_bits():
+    # the routing's query-block order: per head a permutation, sorted by list length (longest
+    # first) within each run of 128 blocks; the forward runs neighbours in it on one CTA, which
+    # changes which CTA computes a row but not a bit of any row
+    B, H, S, d, block = 1, 4, 128 * 300 - 11, 128, 128
+    w0 = WORKLOADS["sparse64k"]
+    w = Workload("ord", B=B, H=H, Sq=S, Skv=S, d=d, seed=59, q_std=0.5, k_std=0.5, grid=w0.grid,
+                 audio_per_frame=8, pe=True, block=block, beta=1.0)
+    q, k, v = make_qkv(w, device=DEV)
+    rt = vd.attn_sparse_route(q, k, v, 1.0, block=block)
+    out, lse = vd.attn_sparse_fwd(q, k, v, rt, block=block)
+    plain = {key: val for key, val in rt.items() if key != "qb_order"}
+    out0, lse0 = vd.attn_sparse_fwd(q, k, v, plain, block=block)
+    torch.cuda.synchronize()
+    assert torch.equal(out, out0) and torch.equal(lse, lse0)
+    order = rt["qb_order"].cpu().numpy().reshape(H, -1)
+    cnt = rt["sel_cnt"].cpu().numpy().reshape(H, -1)
+    nqb = order.shape[1]
+    for h in range(H):
+        assert sorted(order[h]) == list(range(nqb))
+        for c0 in range(0, nqb, 128):
+            chunk = order[h, c0:c0 + 128]
+            assert set(chunk) == set(range(c0, min(c0 + 128, nqb)))
+            lens = cnt[h, chunk]
+            assert np.all(np.diff(lens) <= 0)
+            ties = np.diff(lens) == 0
+            assert np.all(np.diff(chunk)[ties] > 0)
+    # the pairs' longer lists: never more than the plain pairing's
+    def pair_max(o):
+        return sum(int(max(cnt[h, o[h, i:i + 2]])) for h in range(H) for i in range(0, nqb, 2))
+    assert pair_max(order) <= pair_max(np.tile(np.arange(nqb), (H, 1)))
+
+
 def test_sparse_forward_reports_corrupt_lists_and_keeps_other_rows():
     # an empty list and an entry past the last key block: the forward reports both; the empty
     # list's rows become zeros (lse -inf), the bad entry is clamped to the last key block, and every

@@ -70,8 +70,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         lib.attn_sparse_workspace_bytes.argtypes = [i, i, i, i, i, i]
         lib.attn_sparse_workspace_bytes.restype = sz
         lib.attn_sparse_route_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, f, i, i, vp, sz, vp, vp, vp, vp, vp]
-        lib.attn_sparse_route.argtypes = [vp, vp, vp, i, i, i, i, f, f, i, i, vp, sz, vp, vp, vp, vp, vp]
-        lib.attn_sparse_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, i, vp, vp, vp, vp, vp]
+        lib.attn_sparse_route.argtypes = [vp, vp, vp, i, i, i, i, f, f, i, i, vp, sz, vp, vp, vp, vp, vp, vp]
+        lib.attn_sparse_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, i, vp, vp, vp, vp, vp, vp]
         lib.attn_sparse_route_fwd_noalloc.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, f, i, i, vp]
         lib.attn_sparse_fused_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, f, i, i, vp, sz, vp, vp, vp, vp, vp]
         lib.attn_na3d_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, i, f, i, i, vp]
@@ -302,23 +302,29 @@ def attn_sparse_route_fwd(q, k, v, beta, block=128, scale=None, out=None, lse=No
     return (out, lse, extra) if route else (out, lse)
 
 
-def sparse_route_buffers(B, H, S, d, block, device):
-    """Allocates (with torch) the routing outputs of attn_sparse_route for these sizes."""
+def sparse_route_buffers(B, H, S, d, block, device, order=False):
+    """Allocates (with torch) the routing outputs of attn_sparse_route for these sizes (with
+    ``order`` and 128-token blocks also the query-block order the forward pairs its tiles by,
+    which only attn_sparse_route writes: leave it out of a routing built by other means)."""
     nq = (S + block - 1) // block
-    return dict(sel_idx=torch.empty((B, H, nq, nq), dtype=torch.int32, device=device),
+    bufs = dict(sel_idx=torch.empty((B, H, nq, nq), dtype=torch.int32, device=device),
                 sel_cnt=torch.empty((B, H, nq), dtype=torch.int32, device=device),
                 stats=torch.empty((B, H, nq, 4), dtype=torch.float32, device=device),
                 taylor_t=torch.empty((B, H, nq, d), dtype=torch.float32, device=device))
+    if order and block == 128:
+        bufs["qb_order"] = torch.empty((B, H, nq), dtype=torch.int32, device=device)
+    return bufs
 
 
 def attn_sparse_route(q, k, v, beta, block=128, scale=None, route=None, workspace=None, stream=None):
-    """Pool + route only; returns the routing dict (sel_idx, sel_cnt, stats, taylor_t)."""
+    """Pool + route only; returns the routing dict (sel_idx, sel_cnt, stats, taylor_t and, with
+    128-token blocks, qb_order)."""
     lib = load_library()
     B, H, S, d = _bhsd(q, "q")
     _bhsd(k, "k")
     _bhsd(v, "v")
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
-    route = sparse_route_buffers(B, H, S, d, block, q.device) if route is None else route
+    route = sparse_route_buffers(B, H, S, d, block, q.device, order=True) if route is None else route
     nbytes = attn_sparse_workspace_bytes(B, H, S, d, block, block)
     if nbytes == 0:
         raise AttnError("attn_sparse_workspace_bytes", 2)
@@ -327,7 +333,8 @@ def attn_sparse_route(q, k, v, beta, block=128, scale=None, route=None, workspac
     _check("attn_sparse_route",
            lib.attn_sparse_route(_ptr(q), _ptr(k), _ptr(v), B, H, S, d, scale, float(beta), block, block,
                                  _ptr(workspace), workspace.numel(), _ptr(route["sel_idx"]), _ptr(route["sel_cnt"]),
-                                 _ptr(route["stats"]), _ptr(route["taylor_t"]), _stream(stream)))
+                                 _ptr(route["stats"]), _ptr(route["taylor_t"]), _ptr(route.get("qb_order")),
+                                 _stream(stream)))
     return route
 
 
@@ -343,7 +350,7 @@ def attn_sparse_fwd(q, k, v, route, block=128, scale=None, out=None, lse=None, s
     _check("attn_sparse_fwd",
            lib.attn_sparse_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, S, d, scale, block, block,
                                _ptr(route["sel_idx"]), _ptr(route["sel_cnt"]), _ptr(route["stats"]),
-                               _ptr(route["taylor_t"]), _stream(stream)))
+                               _ptr(route["taylor_t"]), _ptr(route.get("qb_order")), _stream(stream)))
     return out, lse
 
 

@@ -261,7 +261,7 @@ bool na_args_ok(int B, int H, int T, int Y, int X, int Kt, int Ky, int Kx) {
 }
 
 struct SparseLayout {
-  size_t qp, kp, vp, sel_idx, sel_cnt, stats, taylor, kh, kl, vth, vtl, total;
+  size_t qp, kp, vp, sel_idx, sel_cnt, stats, taylor, order, kh, kl, vth, vtl, total;
   int NKBp;   // row pitch (floats) of the transposed pooled values
 };
 
@@ -287,6 +287,8 @@ bool sparse_layout(int B, int H, int S, int d, int block_q, int block_k, SparseL
   off = align256(off + BH * NQB * 4 * 4);
   L->taylor = off;
   off = align256(off + BH * NQB * d * 4);
+  L->order = off;   // the query-block order of the forward (128-row blocks)
+  off = align256(off + BH * NQB * 4);
   // tf32 hi / lo copies of the pooled keys and of the transposed pooled values (tensor-core routing)
   L->NKBp = (int)((NKB + 3) & ~(size_t)3);
   L->kh = off;
@@ -545,7 +547,7 @@ attn_status_t sparse_common_checks(const SparseArgs& a) {
 }
 
 attn_status_t run_route(const SparseArgs& a, float beta, void* workspace, size_t workspace_bytes, int32_t* si,
-                        int32_t* sc, float* stt, float* tt, cudaStream_t stream) {
+                        int32_t* sc, float* stt, float* tt, int32_t* order, cudaStream_t stream) {
   SparseLayout L;
   if (!sparse_layout(a.B, a.H, a.S, a.d, a.block_q, a.block_k, &L)) return ATTN_ERR_UNSUPPORTED;
   if (!workspace || ((uintptr_t)workspace & 255u) || workspace_bytes < L.total) return ATTN_ERR_WORKSPACE;
@@ -578,11 +580,12 @@ attn_status_t run_route(const SparseArgs& a, float beta, void* workspace, size_t
   if (launch_route_tc(tkh, tkl, tvh, tvl, tqp, qp, kp, vp, BH, NQB, NKB, a.S, a.d, a.block_k, a.scale, beta, si, sc,
                       stt, tt, status, next_launch_id(), stream) != cudaSuccess)
     return ATTN_ERR_CUDA;
+  if (order != nullptr && launch_qb_order(sc, order, BH, NQB, NKB, stream) != cudaSuccess) return ATTN_ERR_CUDA;
   return ATTN_OK;
 }
 
 attn_status_t run_sparse_fwd(const SparseArgs& a, attn_bf16* out, float* lse, const int32_t* si, const int32_t* sc,
-                             const float* stt, const float* tt, cudaStream_t stream) {
+                             const float* stt, const float* tt, const int32_t* order, cudaStream_t stream) {
   int* status = nullptr;
   attn_status_t st = status_ptr(&status);
   if (st != ATTN_OK) return st;
@@ -600,7 +603,13 @@ attn_status_t run_sparse_fwd(const SparseArgs& a, attn_bf16* out, float* lse, co
   p.taylor_t = tt;
   p.NQB = (a.S + a.block_q - 1) / a.block_q;
   p.NKB = (a.S + a.block_k - 1) / a.block_k;
+  p.qb_order = a.block_q == 128 ? order : nullptr;
   return cuda_status(launch_fwd(a.d, a.block_k, kModeSparse, tq, tk, tv, p, stream));
+}
+
+// A query-block order is for 128-row blocks only and must be 4-byte aligned.
+bool bad_order(const int32_t* order, int block_q) {
+  return order != nullptr && (block_q != 128 || ((uintptr_t)order & 3u));
 }
 
 bool bad_opt_ptrs(const int32_t* si, const int32_t* sc, const float* stt, const float* tt) {
@@ -613,29 +622,30 @@ bool bad_opt_ptrs(const int32_t* si, const int32_t* sc, const float* stt, const 
 attn_status_t attn_sparse_route(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v, int B, int H, int S,
                                 int d, float scale, float beta, int block_q, int block_k, void* workspace,
                                 size_t workspace_bytes, int32_t* sel_idx, int32_t* sel_cnt, float* stats,
-                                float* taylor_t, cudaStream_t stream) {
+                                float* taylor_t, int32_t* qb_order, cudaStream_t stream) {
   const NvtxRange nvtx_range("attn_sparse_route");
   SparseArgs a{q, k, v, B, H, S, d, block_q, block_k, scale};
   attn_status_t st = sparse_common_checks(a);
   if (st != ATTN_OK) return st;
   if (!sel_idx || !sel_cnt || !stats || !taylor_t || bad_opt_ptrs(sel_idx, sel_cnt, stats, taylor_t) || isnan(beta) ||
-      beta == INFINITY)
+      beta == INFINITY || bad_order(qb_order, block_q))
     return ATTN_ERR_INVALID_ARG;
-  return run_route(a, beta, workspace, workspace_bytes, sel_idx, sel_cnt, stats, taylor_t, stream);
+  return run_route(a, beta, workspace, workspace_bytes, sel_idx, sel_cnt, stats, taylor_t, qb_order, stream);
 }
 
 attn_status_t attn_sparse_fwd(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v, attn_bf16* out, float* lse,
                               int B, int H, int S, int d, float scale, int block_q, int block_k,
                               const int32_t* sel_idx, const int32_t* sel_cnt, const float* stats,
-                              const float* taylor_t, cudaStream_t stream) {
+                              const float* taylor_t, const int32_t* qb_order, cudaStream_t stream) {
   const NvtxRange nvtx_range("attn_sparse_fwd");
   SparseArgs a{q, k, v, B, H, S, d, block_q, block_k, scale};
   attn_status_t st = sparse_common_checks(a);
   if (st != ATTN_OK) return st;
   if (!out || !aligned16(out) || (lse && ((uintptr_t)lse & 3u))) return ATTN_ERR_INVALID_ARG;
-  if (!sel_idx || !sel_cnt || !stats || !taylor_t || bad_opt_ptrs(sel_idx, sel_cnt, stats, taylor_t))
+  if (!sel_idx || !sel_cnt || !stats || !taylor_t || bad_opt_ptrs(sel_idx, sel_cnt, stats, taylor_t) ||
+      bad_order(qb_order, block_q))
     return ATTN_ERR_INVALID_ARG;
-  return run_sparse_fwd(a, out, lse, sel_idx, sel_cnt, stats, taylor_t, stream);
+  return run_sparse_fwd(a, out, lse, sel_idx, sel_cnt, stats, taylor_t, qb_order, stream);
 }
 
 attn_status_t attn_sparse_route_fwd(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v, attn_bf16* out,
@@ -657,8 +667,9 @@ attn_status_t attn_sparse_route_fwd(const attn_bf16* q, const attn_bf16* k, cons
   int32_t* sc = sel_cnt ? sel_cnt : (int32_t*)(ws + L.sel_cnt);
   float* stt = stats ? stats : (float*)(ws + L.stats);
   float* tt = taylor_t ? taylor_t : (float*)(ws + L.taylor);
-  if ((st = run_route(a, beta, workspace, workspace_bytes, si, sc, stt, tt, stream)) != ATTN_OK) return st;
-  return run_sparse_fwd(a, out, lse, si, sc, stt, tt, stream);
+  int32_t* order = block_q == 128 ? (int32_t*)(ws + L.order) : nullptr;
+  if ((st = run_route(a, beta, workspace, workspace_bytes, si, sc, stt, tt, order, stream)) != ATTN_OK) return st;
+  return run_sparse_fwd(a, out, lse, si, sc, stt, tt, order, stream);
 }
 
 attn_status_t attn_sparse_fused_fwd(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v, attn_bf16* out,

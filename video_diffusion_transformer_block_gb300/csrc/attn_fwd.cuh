@@ -92,6 +92,10 @@ struct FwdParams {
   const int32_t* sel_cnt;  // sparse: [BH][NQB]
   const float* stats;      // sparse: [BH][NQB][4] = mu, sigma, tau, W
   const float* taylor_t;   // sparse: [BH][NQB][D]
+  // sparse with 128-row blocks, nullable: [BH][NQB], per head a permutation of
+  // the query blocks; the two tiles of CTA qg take blocks qb_order[2qg] and
+  // qb_order[2qg + 1] (null: blocks 2qg and 2qg + 1)
+  const int32_t* qb_order;
   int NQB, NKB;
   int* status;             // device status words (status bits, id of the last launch that timed out)
   unsigned launch_id;      // this launch (never 0)
@@ -941,6 +945,23 @@ __global__ void __launch_bounds__(NQT * 128 + 128, (NQT == 1) ? 2 : 1)
 #pragma unroll
   for (int t = 0; t < NQT; ++t)
     if (q_row0 + t * 128 < p.Sq) n_valid_tiles = t + 1;
+  // The query tile (of 128 rows) that tile t runs: its slot qg * NQT + t, or
+  // the block a query-block order puts in that slot (independent sparse tiles
+  // of 128-row blocks; an entry outside [0, NQB) is clamped and reported).
+  auto tile_of = [&](int t) -> int {
+    const int slot = qg * NQT + t;
+    if constexpr (MODE == kModeSparse && NQT == 2 && QB == 1) {
+      if (p.qb_order != nullptr && slot < p.NQB) {
+        int v = __ldg(p.qb_order + (long long)bh * p.NQB + slot);
+        if ((unsigned)v >= (unsigned)p.NQB) {
+          atomicOr(p.status, ATTN_DEVICE_BAD_LIST);
+          v = v < 0 ? 0 : p.NQB - 1;
+        }
+        return v;
+      }
+    }
+    return slot;
+  };
   constexpr bool kNA = Cfg::kNA;
   NAWalk<Cfg::kNaT, Cfg::kNaY, Cfg::kNaX> naw;
   int na_box[3] = {0, 0, 0};
@@ -1043,8 +1064,9 @@ __global__ void __launch_bounds__(NQT * 128 + 128, (NQT == 1) ? 2 : 1)
     const int t = role >> 1;
     if (lane == 0 && t < NQT) {
       TileMerge<QB> w;
+      const int qtile = tile_of(t);
       if constexpr (Cfg::kDual)
-        tile_walk_init<QB, Cfg::kSparseLike>(w, p, bh, qg * 2 + t, t < n_valid_tiles, (kv_hi - kv_lo + BK - 1) / BK);
+        tile_walk_init<QB, Cfg::kSparseLike>(w, p, bh, qtile, t < n_valid_tiles, (kv_hi - kv_lo + BK - 1) / BK);
       uint32_t fl;
       int u;
       if ((role & 1) == 0) {
@@ -1059,7 +1081,7 @@ __global__ void __launch_bounds__(NQT * 128 + 128, (NQT == 1) ? 2 : 1)
             if constexpr (kNA)
               tma_load_5d(sQ + h * 16384, &tm_q, &bar_qt[t], h * 64, naw.org[0][2], naw.org[0][1], naw.org[0][0], bh);
             else
-              tma_load_3d(sQ + t * Cfg::kQTileBytes + h * 16384, &tm_q, &bar_qt[t], h * 64, q_row0 + t * 128, bh);
+              tma_load_3d(sQ + t * Cfg::kQTileBytes + h * 16384, &tm_q, &bar_qt[t], h * 64, qtile * 128, bh);
           }
         }
         // group g: K of key tile g into slot 2t, V of key tile g-1 into slot 2t+1, both on
@@ -1304,7 +1326,8 @@ __global__ void __launch_bounds__(NQT * 128 + 128, (NQT == 1) ? 2 : 1)
     const int t = warp >> 2;
     const int w4 = warp & 3;
     const int r = w4 * 32 + lane;                  // row within the tile = TMEM lane
-    int grow = q_row0 + t * 128 + r;               // row within the head
+    const int qtile = tile_of(t);
+    int grow = qtile * 128 + r;                    // row within the head
     bool row_valid = grow < p.Sq;
     int na_ws[3] = {0, 0, 0};                      // this row's window start per axis
     if constexpr (kNA) {
@@ -1323,7 +1346,7 @@ __global__ void __launch_bounds__(NQT * 128 + 128, (NQT == 1) ? 2 : 1)
     const uint32_t tile_mask = Cfg::kDual ? ((1u << QB) - 1u) : (((1u << QB) - 1u) << (t * QB));
     TileMerge<QB> wk;
     if constexpr (Cfg::kDual)
-      tile_walk_init<QB, Cfg::kSparseLike>(wk, p, bh, qg * 2 + t, t < n_valid_tiles, (kv_hi - kv_lo + BK - 1) / BK);
+      tile_walk_init<QB, Cfg::kSparseLike>(wk, p, bh, qtile, t < n_valid_tiles, (kv_hi - kv_lo + BK - 1) / BK);
     const uint32_t lane_base = (uint32_t)(w4 * 32) << 16;
     const uint32_t tS = tmem + lane_base + t * 256;
     const uint32_t tO = tS + 128;
@@ -1434,7 +1457,7 @@ __global__ void __launch_bounds__(NQT * 128 + 128, (NQT == 1) ? 2 : 1)
           }
         }
         if (MODE == kModeSparse && m_run > -INFINITY) {
-          const long long qbi = (long long)(qg * NQT + t) * QB + qb;
+          const long long qbi = (long long)qtile * QB + qb;
           if (qbi < p.NQB) {
             const long long srow = (long long)bh * p.NQB + qbi;
             const int cnt = __ldg(p.sel_cnt + srow);

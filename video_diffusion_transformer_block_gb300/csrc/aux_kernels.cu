@@ -317,4 +317,56 @@ cudaError_t launch_wait_selftest(int limit_us, int n_ctas, int smem_bytes, int* 
   return cudaGetLastError();
 }
 
+// ---------------------------------------------------------------- query-block order
+// Per head and chunk of 128 query blocks, the blocks sorted by their selected-
+// block count, longest first (ties: lower index first), written to order[bh][...]
+// at the chunk's positions.  The sparse forward pairs the blocks in slots 2s
+// and 2s + 1 in one CTA, whose time is that of the longer list: neighbours in
+// this order have nearly equal lists.  A chunk keeps the blocks of 128
+// consecutive query positions together (their keys overlap, as in the order
+// of positions).  One CTA of 128 threads per (chunk, head); a count outside
+// [0, NKB] sorts as its clamp.
+__global__ void __launch_bounds__(128) qb_order_kernel(const int32_t* __restrict__ sel_cnt,
+                                                       int32_t* __restrict__ order, int NQB, int NKB) {
+  __shared__ uint32_t key[128];
+  const int i = threadIdx.x;
+  const int base = blockIdx.x * 128;
+  const long long row = (long long)blockIdx.y * NQB;
+  const int n = min(128, NQB - base);
+  // key: (count + 1) above the local index's complement, so that a descending
+  // sort puts longer lists first and, among equal ones, lower indices first;
+  // padding (past the last block) gets 0 and sorts last
+  uint32_t k = 0;
+  if (i < n) {
+    int c = __ldg(sel_cnt + row + base + i);
+    c = c < 0 ? 0 : (c > NKB ? NKB : c);
+    k = ((uint32_t)(c + 1) << 8) | (uint32_t)(127 - i);
+  }
+  key[i] = k;
+  __syncthreads();
+  // bitonic sort, descending
+  for (int size = 2; size <= 128; size <<= 1) {
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      const int j = i ^ stride;
+      if (j > i) {
+        const uint32_t a = key[i], b = key[j];
+        const bool desc = (i & size) == 0;
+        if (desc ? a < b : a > b) {
+          key[i] = b;
+          key[j] = a;
+        }
+      }
+      __syncthreads();
+    }
+  }
+  if (i < n) order[row + base + i] = base + (127 - (int)(key[i] & 0xFFu));
+}
+
+cudaError_t launch_qb_order(const int32_t* sel_cnt, int32_t* order, int BH, int NQB, int NKB, cudaStream_t stream) {
+  if (BH <= 0 || NQB <= 0 || BH > 65535 || NKB >= (1 << 23)) return cudaErrorInvalidValue;
+  const dim3 grid((unsigned)((NQB + 127) / 128), (unsigned)BH);
+  qb_order_kernel<<<grid, 128, 0, stream>>>(sel_cnt, order, NQB, NKB);
+  return cudaGetLastError();
+}
+
 }  // namespace vdtb

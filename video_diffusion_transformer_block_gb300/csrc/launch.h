@@ -37,6 +37,11 @@ cudaError_t launch_route_tc(const CUtensorMap& tkh, const CUtensorMap& tkl, cons
                             float beta, int32_t* sel_idx, int32_t* sel_cnt, float* stats, float* taylor_t, int* status,
                             unsigned launch_id, cudaStream_t stream);
 
+// Query-block order for the sparse forward (FwdParams::qb_order): per head and
+// chunk of 128 query blocks, the blocks sorted by sel_cnt, longest first, into
+// order [BH][NQB] (BH <= 65535, NKB < 2^23).
+cudaError_t launch_qb_order(const int32_t* sel_cnt, int32_t* order, int BH, int NQB, int NKB, cudaStream_t stream);
+
 // Exact log-sum-exp merge of n partials, rows = B*H*Sq.
 cudaError_t launch_merge(const float* o_part, const float* lse_part, uint16_t* out, float* lse, int n, long long rows,
                          int D, int* status, cudaStream_t stream);
