@@ -226,7 +226,9 @@ def run_native(args, world, rank, local):
     # the audio->video cross attention needs none of the self-attention's results: it runs on a
     # second stream, beside pool/route (HBM- and shared-memory-bound) and the sparse forward
     xstream = stream if args.serial_cross else torch.cuda.Stream()
-    kernels_per_step = 5  # pool, route, sparse forward, split-KV forward, merge
+    # pool, routing (the tensor-core tiles and, for 513 query blocks a head, the last block's
+    # tail kernel), the query-block order, sparse forward, split-KV forward, merge
+    kernels_per_step = 7
 
     def step(ev=None, xev=None):
         start = ev[0] if ev is not None else torch.cuda.Event()
@@ -521,7 +523,8 @@ def run_sweep(args, world, rank, local):
             "roofline": {"bound": "tensor", "kernel": "attn_fwd_kernel (sparse, d=128, block 128)",
                          "achieved": round(fwd, 2), "peak": peak, "unit": "TFLOP/s", "frac": round(fwd / peak, 4),
                          "peak_source": f"{peaks_src} bf16_tflops (burst)", "traffic": None},
-            "gpu_launches": 3 * args.steps, "clocks": clocks.summary()}
+            # pool, routing (1024 query blocks a head: tensor-core tiles only), query-block order, forward
+            "gpu_launches": 4 * args.steps, "clocks": clocks.summary()}
 
 
 def run_native_kernel(args, world, rank, local):
