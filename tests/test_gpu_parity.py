@@ -203,11 +203,12 @@ def test_sparse_all_blocks_equals_dense_over_many_ctas(d):
     assert torch.equal(out_s, out_d) and torch.equal(lse_s, lse_d)
 
 
-def test_sparse_query_block_order_balances_pairs_and_changes_no_bits():
+@pytest.mark.parametrize("d", [128, 64])
+def test_sparse_query_block_order_balances_pairs_and_changes_no_bits(d):
     # the routing's query-block order: per head a permutation, sorted by list length (longest
     # first) within each run of 128 blocks; the forward runs neighbours in it on one CTA, which
     # changes which CTA computes a row but not a bit of any row
-    B, H, S, d, block = 1, 4, 128 * 300 - 11, 128, 128
+    B, H, S, block = 1, 4, 128 * 300 - 11, 128
     w0 = WORKLOADS["sparse64k"]
     w = Workload("ord", B=B, H=H, Sq=S, Skv=S, d=d, seed=59, q_std=0.5, k_std=0.5, grid=w0.grid,
                  audio_per_frame=8, pe=True, block=block, beta=1.0)
