@@ -265,6 +265,18 @@ def test_sparse_forward_reports_corrupt_lists_and_keeps_other_rows():
     keep[0, rows3] = False
     keep[1, rows2] = False
     assert torch.equal(out[0][keep], ref_o[0][keep]) and torch.equal(lse[0][keep], ref_l[0][keep])
+    # an order entry past the last query block is clamped and reported too; the blocks the
+    # order still names come out as with the intact routing
+    odd = {key: val.clone() for key, val in rt.items()}
+    nqb = odd["qb_order"].shape[-1]
+    lost = int(odd["qb_order"][0, 1, 0])
+    odd["qb_order"][0, 1, 0] = nqb + 3
+    o2, l2 = vd.attn_sparse_fwd(q, k, v, odd, block=block)
+    assert vd.attn_last_device_status() == 1
+    named = [b for b in range(nqb) if b != lost]
+    for b in named:
+        rows = slice(b * block, min((b + 1) * block, S))
+        assert torch.equal(o2[0, 1, rows], ref_o[0, 1, rows]) and torch.equal(l2[0, 1, rows], ref_l[0, 1, rows])
 
 
 @pytest.mark.parametrize("d,block,beta", [(128, 128, 1.0), (128, 64, 0.5), (64, 128, 1.5)])
