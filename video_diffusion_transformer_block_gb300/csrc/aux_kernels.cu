@@ -324,14 +324,14 @@ cudaError_t launch_wait_selftest(int limit_us, int n_ctas, int smem_bytes, int* 
 // and 2s + 1 in one CTA, whose time is that of the longer list: neighbours in
 // this order have nearly equal lists.  A chunk keeps the blocks of 128
 // consecutive query positions together (their keys overlap, as in the order
-// of positions).  One CTA of 128 threads per (chunk, head); a count outside
+// of positions).  One CTA of 128 threads per (head, chunk); a count outside
 // [0, NKB] sorts as its clamp.
 __global__ void __launch_bounds__(128) qb_order_kernel(const int32_t* __restrict__ sel_cnt,
                                                        int32_t* __restrict__ order, int NQB, int NKB) {
   __shared__ uint32_t key[128];
   const int i = threadIdx.x;
-  const int base = blockIdx.x * 128;
-  const long long row = (long long)blockIdx.y * NQB;
+  const int base = blockIdx.y * 128;
+  const long long row = (long long)blockIdx.x * NQB;
   const int n = min(128, NQB - base);
   // key: (count + 1) above the local index's complement, so that a descending
   // sort puts longer lists first and, among equal ones, lower indices first;
@@ -363,8 +363,8 @@ __global__ void __launch_bounds__(128) qb_order_kernel(const int32_t* __restrict
 }
 
 cudaError_t launch_qb_order(const int32_t* sel_cnt, int32_t* order, int BH, int NQB, int NKB, cudaStream_t stream) {
-  if (BH <= 0 || NQB <= 0 || BH > 65535 || NKB >= (1 << 23)) return cudaErrorInvalidValue;
-  const dim3 grid((unsigned)((NQB + 127) / 128), (unsigned)BH);
+  if (BH <= 0 || NQB <= 0 || (NQB + 127) / 128 > 65535 || NKB >= (1 << 23)) return cudaErrorInvalidValue;
+  const dim3 grid((unsigned)BH, (unsigned)((NQB + 127) / 128));
   qb_order_kernel<<<grid, 128, 0, stream>>>(sel_cnt, order, NQB, NKB);
   return cudaGetLastError();
 }

@@ -39,7 +39,7 @@ cudaError_t launch_route_tc(const CUtensorMap& tkh, const CUtensorMap& tkl, cons
 
 // Query-block order for the sparse forward (FwdParams::qb_order): per head and
 // chunk of 128 query blocks, the blocks sorted by sel_cnt, longest first, into
-// order [BH][NQB] (BH <= 65535, NKB < 2^23).
+// order [BH][NQB] (NKB < 2^23).
 cudaError_t launch_qb_order(const int32_t* sel_cnt, int32_t* order, int BH, int NQB, int NKB, cudaStream_t stream);
 
 // Exact log-sum-exp merge of n partials, rows = B*H*Sq.
