@@ -513,6 +513,100 @@ __device__ __forceinline__ void softmax_step(float (&x)[BK], float scale_log2, f
   tmem_st_wait();
 }
 
+// softmax_step reading its scores from TMEM twice instead of holding all BK
+// of them in registers: pass 1 takes the row maximum 64 columns at a time,
+// pass 2 reloads each 64 columns, exponentiates them and writes their P (which
+// lands on columns pass 2 has already read).  The same maxima, the same
+// fused multiply-adds in the same order and the same row-sum chains as
+// softmax_step, so the same bits, with 64 score registers live instead of BK.
+// `between()` runs while the first loads are in flight.
+template <int BK, int D, bool kBiasMasked, class Between>
+__device__ __forceinline__ void softmax_step_tmem(uint32_t tS, float scale_log2, float& m_run, float& l_run,
+                                                  bool o_live, uint32_t tO, Between&& between) {
+  static_assert(BK % 64 == 0, "key tile");
+  // pass 1: the row max, in softmax_step's two chains of three-input maxima
+  float mx0 = 0.f, mx1 = 0.f;
+#pragma unroll
+  for (int c0 = 0; c0 < BK; c0 += 64) {
+    uint32_t ra[32], rb[32];
+    tmem_ld32(tS + c0, ra);
+    tmem_ld32(tS + c0 + 32, rb);
+    if (c0 == 0) between();
+    tmem_ld_wait();
+    tmem_reg_fence(ra);
+    tmem_reg_fence(rb);
+#pragma unroll
+    for (int c = 0; c < 64; c += 4) {
+      const uint32_t* r = c < 32 ? ra : rb;
+      const int e = c & 31;
+      const float x0 = __uint_as_float(r[e]), x1 = __uint_as_float(r[e + 1]);
+      const float x2 = __uint_as_float(r[e + 2]), x3 = __uint_as_float(r[e + 3]);
+      if (c0 == 0 && c == 0) {
+        mx0 = fmaxf(x0, x1);
+        mx1 = fmaxf(x2, x3);
+      } else {
+        mx0 = fmax3(mx0, x0, x1);
+        mx1 = fmax3(mx1, x2, x3);
+      }
+    }
+  }
+  float raw = fmaxf(mx0, mx1);
+  if constexpr (kBiasMasked) raw = raw < -0x1p119f ? -INFINITY : raw;
+  const float mt = raw * scale_log2;
+  float alpha = 1.f;
+  bool need = mt > m_run + kRescaleLog2 || (m_run == -INFINITY && mt > -INFINITY);
+  if (need) {
+    alpha = (m_run == -INFINITY) ? 0.f : ex2_approx(m_run - mt);
+    l_run *= alpha;
+    m_run = mt;
+  }
+  if (__any_sync(0xffffffffu, need && alpha != 0.f && o_live)) {
+    const float a = (need && o_live) ? alpha : 1.f;
+#pragma unroll
+    for (int c0 = 0; c0 < D; c0 += 32) {
+      uint32_t rr[32];
+      tmem_ld32(tO + c0, rr);
+      tmem_ld_wait();
+      tmem_reg_fence(rr);
+#pragma unroll
+      for (int j = 0; j < 32; j += 2) {
+        const float2 v = __fmul2_rn(make_float2(__uint_as_float(rr[j]), __uint_as_float(rr[j + 1])),
+                                    make_float2(a, a));
+        rr[j] = __float_as_uint(v.x);
+        rr[j + 1] = __float_as_uint(v.y);
+      }
+      tmem_st32(tO + c0, rr);
+    }
+  }
+  // pass 2: P = 2^(x scale_log2 - m), 64 columns at a time, as in softmax_step
+  const float nbase = (m_run == -INFINITY) ? 0.f : -m_run;
+  const float2 sc2 = make_float2(scale_log2, scale_log2), nb2 = make_float2(nbase, nbase);
+  float2 ls = make_float2(0.f, 0.f);
+#pragma unroll
+  for (int c0 = 0; c0 < BK; c0 += 64) {
+    uint32_t ra[32], rb[32];
+    tmem_ld32(tS + c0, ra);
+    tmem_ld32(tS + c0 + 32, rb);
+    tmem_ld_wait();
+    tmem_reg_fence(ra);
+    tmem_reg_fence(rb);
+    uint32_t pk[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      const uint32_t* r = j < 16 ? ra : rb;
+      const int e = (2 * j) & 31;
+      const float2 arg = __ffma2_rn(make_float2(__uint_as_float(r[e]), __uint_as_float(r[e + 1])), sc2, nb2);
+      const float p0 = ex2_approx(arg.x);
+      const float p1 = ex2_approx(arg.y);
+      ls = __fadd2_rn(ls, make_float2(p0, p1));
+      pk[j] = pack_bf16x2(p0, p1);
+    }
+    tmem_st32(tS + c0 / 2, pk);
+  }
+  l_run += ls.x + ls.y;
+  tmem_st_wait();
+}
+
 // Epilogue of the query row a thread owns: (O + f T) * inv from TMEM at tO
 // (zero when !have_o; T optional) as bf16 into dst[0, D), element offset `off`
 // of an output of `total` elements (bounds-checked in the debug build).

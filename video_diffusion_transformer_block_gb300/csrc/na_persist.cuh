@@ -439,23 +439,12 @@ __global__ void __launch_bounds__(384, 1)
           m_run = -INFINITY;
           l_run = 0.f;
         }
-        float x[BK];
-        {
-          uint32_t rr[BK / 32][32];
-#pragma unroll
-          for (int c = 0; c < BK / 32; ++c) tmem_ld32(tS + c * 32, rr[c]);
-          // one buffer: the next element's window rows now that S is done, while the loads are in flight
+        // O holds earlier boxes of this brick unless this box starts it.  One
+        // buffer: the next element's window rows now that S is done, while the
+        // first score loads are in flight
+        softmax_step_tmem<BK, D, true>(tS, p.scale_log2, m_run, l_run, !cur_starts, tO, [&]() {
           if constexpr (Cfg::kQmBufs == 1) have = look_ahead(next_starts);
-          tmem_ld_wait();
-#pragma unroll
-          for (int c = 0; c < BK / 32; ++c) {
-            tmem_reg_fence(rr[c]);
-#pragma unroll
-            for (int j = 0; j < 32; ++j) x[c * 32 + j] = __uint_as_float(rr[c][j]);
-          }
-        }
-        // O holds earlier boxes of this brick unless this box starts it
-        softmax_step<BK, D, true>(x, p.scale_log2, m_run, l_run, !cur_starts, tS, tO);
+        });
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         tc_fence_before();
         mbar_arrive(&bar_p[t]);
