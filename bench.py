@@ -557,15 +557,17 @@ def run_native_kernel(args, world, rank, local):
     elif args.workload == "na3d":
         launches = 1
         kern = w0.extra["kernel"]
-        brick, pair, boxes = vd.attn_na3d_plan(w.grid, kern)
+        brick, pair, boxes = vd.attn_na3d_plan(w.grid, kern, 0, args.na_plan)
         flops = 4.0 * B * H * Sq * math.prod(kern) * d                 # the windows' own work
         # what the tensor cores run: per key box S = Q K^T and O += P V, and on the
-        # persistent plans one (plan 4, 4x4x8 bricks) or two K = 16 steps that add the window
-        window_k = (16 if (brick == 3 and pair == 4) else 32) if pair in (4, 5) else 0
+        # persistent plans one (plan 4, 4x4x8 bricks) or two K = 16 steps that add the window;
+        # plan 6's one K = 32 step of E5M2 operands takes the tensor pipe as long as one bf16
+        # K = 16 step, and is counted as one
+        window_k = (16 if (brick == 3 and pair == 4) or pair == 6 else 32) if pair in (4, 5, 6) else 0
         exec_flops = 2.0 * B * H * boxes * 128 * 128 * (2 * d + window_k)
 
         def step():
-            vd.attn_na3d_fwd(q, k, v, w.grid, kern, out=out, lse=lse)
+            vd.attn_na3d_fwd(q, k, v, w.grid, kern, brick=brick, pair_axis=pair, out=out, lse=lse)
     else:
         n = w.n_split
         op = torch.empty((n, B, H, Sq, d), dtype=torch.float32, device=q.device)
@@ -602,9 +604,12 @@ def run_native_kernel(args, world, rank, local):
         peak = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
         ach = exec_flops / (ms * 1e-3) / 1e12
         kname = (f"attn_na_persist_kernel (3D neighbourhood, persistent one-brick tiles, brick {brick}"
-                 f"{', key boxes 4x2x16' if pair == 5 else ''}, d={d})"
-                 if pair in (4, 5) else f"attn_fwd_kernel (3D neighbourhood, brick {brick}, pair {pair}, d={d})")
-        traffic, tpipe = profiled_counters("na3d") if H == 32 else (None, None)
+                 f"{', key boxes 4x2x16' if pair in (5, 6) else ''}{', E5M2 window operands' if pair == 6 else ''}"
+                 f", d={d})"
+                 if pair in (4, 5, 6) else f"attn_fwd_kernel (3D neighbourhood, brick {brick}, pair {pair}, d={d})")
+        # counters of the library's own plan under "na3d", of an explicit plan under "na3d_plan<n>"
+        traffic, tpipe = (profiled_counters("na3d" if args.na_plan == -1 else f"na3d_plan{args.na_plan}")
+                          if H == 32 else (None, None))
         roof = {"bound": "tensor", "kernel": kname,
                 "achieved": round(ach, 2), "peak": peak, "unit": "TFLOP/s", "frac": round(ach / peak, 4),
                 "peak_source": f"{peaks_src} bf16_tflops (burst: one kernel per timed step, L2 flushed between)",
@@ -626,7 +631,8 @@ def run_native_kernel(args, world, rank, local):
             "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": f"{args.workload}: B={B} H={H} Sq={Sq} Skv={Skv} d={d}"
-                       + (f" volume {w.grid} window {w0.extra['kernel']}" if args.workload == "na3d" else ""),
+                       + (f" volume {w.grid} window {w0.extra['kernel']} plan {pair}" if args.workload == "na3d"
+                          else ""),
                        "seq_len": Skv, "l2": "256 MB buffer written between timed steps (L2 flush)"},
             **extra, "roofline": roof, "gpu_launches": launches * args.steps, "clocks": clocks.summary()}
 
@@ -911,6 +917,9 @@ def main():
                                            "sweep128k"],
                     default="sparse64k",
                     help="sparse64k = the benchmark step; dense16k / cross / na3d / fp8_proj time one path each")
+    ap.add_argument("--na-plan", type=int, default=-1, choices=[-1, 3, 4, 5, 6],
+                    help="na3d only: the pair axis / plan (-1 = the library's choice; 6 = E5M2 window operands, "
+                         "exact for raw scores |q.k| < 2^30)")
     ap.add_argument("--tokens", type=int, default=None,
                     help="fp8_proj only: activation rows (default 65664; fewer only for profiling)")
     ap.add_argument("--no-e2e", action="store_true")

@@ -282,15 +282,23 @@ attn_status_t attn_cross_fwd(const attn_bf16* q, const attn_bf16* k, const attn_
  *                 results); 5 = plan 4 with key boxes of 4x2x16 tokens instead
  *                 of the brick's shape (brick 3, i.e. 4x4x8 queries, only),
  *                 which cover a brick's window union with fewer boxes under
- *                 small windows (3x7x7: 5 boxes per brick instead of 6); -1 =
- *                 chosen by the library: plan 4 or 5, the fastest on GB300 for
- *                 every volume and window measured.  An open brick minimises a
- *                 measured cost model of key boxes and bricks (see
- *                 attn_na3d_plan).
- *   The choice only changes speed, never results beyond fp32 rounding order.
+ *                 small windows (3x7x7: 5 boxes per brick instead of 6); 6 =
+ *                 plan 5 with the window's operands in E5M2 (-57344 outside
+ *                 against one-hots of 57344: -49 * 2^26 per missed axis), half
+ *                 the shared memory of plan 5's bf16 ones, so each tile keeps
+ *                 two window buffers at d = 128; it gives plan 5's results
+ *                 bit for bit when every raw score |q.k| < 2^30, and is not
+ *                 exact beyond that, so the library never picks it (for
+ *                 scale * log2(e) < 2^-22 plan 5 runs instead); -1 = chosen
+ *                 by the library: plan 4 or 5, the fastest on GB300 for every
+ *                 volume and window measured among the plans exact for all
+ *                 inputs.  An open brick minimises a measured cost model of
+ *                 key boxes and bricks (see attn_na3d_plan).
+ *   The choice only changes speed, never results beyond fp32 rounding order
+ *   (plan 6: within its score range).
  *   Errors: ATTN_ERR_INVALID_ARG (null or misaligned pointer, a window outside
- *   [1, L], S > 2^30, non-positive scale, bad brick/pair code (0..3 / -1..5),
- *   pair 5 with brick 1 or 2), ATTN_ERR_UNSUPPORTED (d), ATTN_ERR_CUDA
+ *   [1, L], S > 2^30, non-positive scale, bad brick/pair code (0..3 / -1..6),
+ *   pair 5 or 6 with brick 1 or 2), ATTN_ERR_UNSUPPORTED (d), ATTN_ERR_CUDA
  *   (launch).  Asynchronous on stream.
  */
 attn_status_t attn_na3d_fwd(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v, attn_bf16* out, float* lse,
@@ -301,14 +309,16 @@ attn_status_t attn_na3d_fwd(const attn_bf16* q, const attn_bf16* k, const attn_b
  * The tile plan attn_na3d_fwd uses for a volume and window (at a scale with
  * scale * log2(e) >= 2^-80).  On entry *brick and *pair_axis hold the
  * caller's request (0 / -1 = open); on return the plan.  An open pair axis
- * takes plan 4 or (brick 3) plan 5, an open brick any brick; the choice
+ * takes plan 4 or (brick 3) plan 5 (plan 6 only when asked for, with brick 3
+ * or an open brick), an open brick any brick; the choice
  * minimises, in twentieths of a key box, for plans 4 and 5: 20 per box of
  * plan 4 with a 4x4x8 brick and 23 per box otherwise (their window step is 32
  * columns wide) plus 34 per brick; for the other plans: 20 per box plus 40
  * per CTA.  *key_boxes (nullable) receives the number of 128-key boxes the
  * query tiles of one head multiply: the executed work of one head is
  * key_boxes * 4 * 128 * 128 * d floating-point operations (plans 4 and 5 add
- * one or two K = 16 steps per box for the window).  Host only.
+ * one or two K = 16 steps per box for the window, plan 6 one K = 32 step of
+ * 8-bit operands).  Host only.
  * ATTN_ERR_INVALID_ARG as for attn_na3d_fwd.
  */
 attn_status_t attn_na3d_plan(int T, int Y, int X, int Kt, int Ky, int Kx, int* brick, int* pair_axis,

@@ -142,11 +142,11 @@ def test_fused_sparse_rejections(lib):
 # ---------------------------------------------------------------- 3D neighbourhood attention (host logic)
 
 BRICKS = {1: (1, 8, 16), 2: (2, 8, 8), 3: (4, 4, 8)}
-WIDE_KEYS = (4, 2, 16)   # the key boxes of plan 5 (with the 4x4x8 brick)
+WIDE_KEYS = (4, 2, 16)   # the key boxes of plans 5 and 6 (with the 4x4x8 brick)
 
 
 def key_box(brick, pair):
-    return WIDE_KEYS if pair == 5 else BRICKS[brick]
+    return WIDE_KEYS if pair in (5, 6) else BRICKS[brick]
 
 
 def na_start(p, K, L):
@@ -155,10 +155,10 @@ def na_start(p, K, L):
 
 def na_walk(grid, kernel, brick, pair):
     """Python restatement of the kernel's box walk: yields, per CTA, its query
-    bricks (two neighbours along ``pair``, or one when pair is 3, 4 or 5: plans
-    4 and 5 run the one-brick tiles on persistent CTAs, plan 4 with the same
-    boxes per brick, plan 5 with 4x2x16 key boxes) and the boxes with their
-    tile flags."""
+    bricks (two neighbours along ``pair``, or one when pair is 3 to 6: plans
+    4 to 6 run the one-brick tiles on persistent CTAs, plan 4 with the same
+    boxes per brick, plans 5 and 6 with 4x2x16 key boxes) and the boxes with
+    their tile flags."""
     B = BRICKS[brick]
     KB = key_box(brick, pair)
     nq = [-(-grid[a] // B[a]) for a in range(3)]
@@ -193,10 +193,10 @@ def na_walk(grid, kernel, brick, pair):
 @pytest.mark.parametrize("grid,kernel", [((3, 13, 21), (3, 5, 7)), ((5, 11, 19), (3, 5, 4)), ((1, 20, 24), (1, 9, 9)),
                                          ((4, 16, 32), (2, 16, 1)), ((2, 5, 6), (2, 5, 6))])
 @pytest.mark.parametrize("brick", [1, 2, 3])
-@pytest.mark.parametrize("pair", [0, 1, 2, 3, 4, 5])
+@pytest.mark.parametrize("pair", [0, 1, 2, 3, 4, 5, 6])
 def test_na3d_walk_covers_every_window_and_plan_counts_it(lib, grid, kernel, brick, pair):
-    if pair == 5 and brick != 3:
-        pytest.skip("plan 5 takes the 4x4x8 brick only")
+    if pair in (5, 6) and brick != 3:
+        pytest.skip("plans 5 and 6 take the 4x4x8 brick only")
     B = BRICKS[brick]
     KB = key_box(brick, pair)
     work = 0
@@ -256,6 +256,9 @@ def test_na3d_plan_picks_the_least_work(lib):
         # a fixed brick with an open pair axis keeps the brick (plan 5 only with the 4x4x8 brick)
         assert vd.attn_na3d_plan(grid, kernel, 2)[:2] == (2, 4)
         assert vd.attn_na3d_plan(grid, kernel, 3)[1] in (4, 5)
+        # plan 6 (E5M2 window operands) is never chosen, only taken when asked for
+        assert vd.attn_na3d_plan(grid, kernel, 0, 6)[:2] == (3, 6)
+        assert vd.attn_na3d_plan(grid, kernel, 3, 6)[2] == vd.attn_na3d_plan(grid, kernel, 3, 5)[2]
     # the volumes timed on GB300 take their fastest plan
     assert vd.attn_na3d_plan((4, 128, 128), (3, 7, 7))[:2] == (3, 5)
     assert vd.attn_na3d_plan((4, 64, 64), (3, 31, 31))[0] == 3
@@ -266,14 +269,17 @@ def test_na3d_plan_picks_the_least_work(lib):
 def test_na3d_rejections(lib):
     base = [P, P, P, P, P, 1, 2, 4, 16, 16, 128, 3, 5, 5, 0.088, 0, -1, None]
     for i, bad in [(11, 0), (11, 5), (12, 17), (13, 0), (7, 0), (14, 0.0), (14, math.nan), (15, 4), (15, -1),
-                   (16, 6), (16, -2)]:
+                   (16, 7), (16, -2)]:
         args = list(base)
         args[i] = bad
         assert lib.attn_na3d_fwd(*args) == 1, (i, bad)
-    for brick in (1, 2):   # plan 5 takes the 4x4x8 brick only
-        args = list(base)
-        args[15], args[16] = brick, 5
-        assert lib.attn_na3d_fwd(*args) == 1, brick
+    for brick in (1, 2):   # plans 5 and 6 take the 4x4x8 brick only
+        for pair in (5, 6):
+            args = list(base)
+            args[15], args[16] = brick, pair
+            assert lib.attn_na3d_fwd(*args) == 1, (brick, pair)
+            b, pa = ctypes.c_int(brick), ctypes.c_int(pair)
+            assert lib.attn_na3d_plan(4, 16, 16, 3, 5, 5, ctypes.byref(b), ctypes.byref(pa), None) == 1
     args = list(base)
     args[10] = 96
     assert lib.attn_na3d_fwd(*args) == 2

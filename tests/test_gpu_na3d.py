@@ -56,10 +56,10 @@ def check(B, H, grid, kernel, d, brick=0, pair=-1, seed=7, scale=None, out_max_a
 
 
 @pytest.mark.parametrize("brick", [1, 2, 3])
-@pytest.mark.parametrize("pair", [0, 1, 2, 3, 4, 5])
+@pytest.mark.parametrize("pair", [0, 1, 2, 3, 4, 5, 6])
 def test_na3d_every_plan_ragged_volume(brick, pair):
-    if pair == 5 and brick != 3:
-        pytest.skip("plan 5 takes the 4x4x8 brick only")
+    if pair in (5, 6) and brick != 3:
+        pytest.skip("plans 5 and 6 take the 4x4x8 brick only")
     check(1, 2, (5, 11, 19), (3, 5, 4), 64, brick, pair, seed=brick * 3 + pair)
 
 
@@ -106,7 +106,7 @@ def test_na3d_single_token_window_returns_v():
     torch.testing.assert_close(lse, expect, atol=1e-3, rtol=1e-4)
 
 
-@pytest.mark.parametrize("pair", [-1, 3, 4, 5])
+@pytest.mark.parametrize("pair", [-1, 3, 4, 5, 6])
 def test_na3d_peaked_scores_rescale(pair):
     # large scores: the running max moves by more than the lazy-rescale threshold between boxes.
     # Each output is then close to one value row (|out| up to ~5), so the bf16 rounding of the
@@ -197,3 +197,74 @@ def test_na3d_persistent_output_16_byte_aligned():
     o5, _ = vd.attn_na3d_fwd(q, k, v, grid, kernel, brick=3, pair_axis=5)
     torch.cuda.synchronize()
     assert torch.equal(out, o5)
+
+
+# Plan 6: plan 5's key boxes with the window added through E5M2 operands (-57344 per missed
+# coordinate against one-hots of 57344).  Wherever both encodings are exact (raw scores
+# |q.k| < 2^30, scale * log2(e) >= 2^-22) every in-window score is left unchanged and every
+# other key gets an exact zero weight, with the same boxes in the same order: the bits of plan 5.
+
+@pytest.mark.parametrize("grid,kernel,d,H", [
+    ((1, 20, 24), (1, 9, 9), 128, 2),     # one frame: 4-frame key boxes mostly outside the volume
+    ((3, 13, 21), (3, 5, 7), 128, 2),     # ragged in y and x
+    ((6, 9, 10), (4, 2, 6), 64, 2),       # even windows, d = 64
+    ((4, 32, 32), (3, 31, 31), 128, 2),   # a window wider than two key boxes
+    ((5, 37, 45), (3, 7, 7), 128, 12),    # 1440 bricks: every tile of a persistent CTA takes several
+])
+def test_na3d_e5m2_window_same_bits_as_plan5(grid, kernel, d, H):
+    q, k, v = na_inputs(1, H, grid, d, seed=41)
+    scale = 1 / math.sqrt(d)
+    o6, l6 = vd.attn_na3d_fwd(q, k, v, grid, kernel, scale=scale, brick=3, pair_axis=6)
+    o5, l5 = vd.attn_na3d_fwd(q, k, v, grid, kernel, scale=scale, brick=3, pair_axis=5)
+    torch.cuda.synchronize()
+    assert torch.equal(o6, o5) and torch.equal(l6, l5)
+    ro, rl = oracle.na3d_attention(host(q), host(k), host(v), grid, kernel, scale)
+    assert_close(host(o6), ro, f"na3d plan 6 out (grid {grid})")
+    np.testing.assert_allclose(host(l6), rl, atol=LSE_ATOL, rtol=0, err_msg=f"na3d plan 6 lse (grid {grid})")
+
+
+def test_na3d_e5m2_window_large_scores_same_bits():
+    # raw scores of ~1e5 (inputs scaled by 40, softmax scale divided by 1600): still far inside
+    # the E5M2 window's exact range, so plan 6 keeps plan 5's bits and both match the oracle
+    grid, kernel, d = (4, 16, 32), (3, 9, 9), 128
+    q, k, v = na_inputs(1, 2, grid, d, seed=43)
+    q, k = (q.float() * 40).bfloat16(), (k.float() * 40).bfloat16()
+    scale = 1 / (1600 * math.sqrt(d))
+    raw = (q[0, 0].float() @ k[0, 0].float().T).abs().max().item()
+    assert 1e4 < raw < 2.0 ** 30
+    o6, l6 = vd.attn_na3d_fwd(q, k, v, grid, kernel, scale=scale, brick=3, pair_axis=6)
+    o5, l5 = vd.attn_na3d_fwd(q, k, v, grid, kernel, scale=scale, brick=3, pair_axis=5)
+    torch.cuda.synchronize()
+    assert torch.equal(o6, o5) and torch.equal(l6, l5)
+    ro, rl = oracle.na3d_attention(host(q), host(k), host(v), grid, kernel, scale)
+    assert_close(host(o6), ro, "na3d plan 6 large scores out")
+    np.testing.assert_allclose(host(l6), rl, atol=LSE_ATOL, rtol=0, err_msg="na3d plan 6 large scores lse")
+
+
+def test_na3d_e5m2_window_small_scale_falls_back():
+    # below scale * log2(e) = 2^-22 the E5M2 bias no longer zeroes a key's weight for certain:
+    # the library runs plan 5 (bf16 window) instead, below 2^-80 the one-brick CTAs
+    grid, kernel = (3, 13, 21), (3, 5, 7)
+    q, k, v = na_inputs(1, 2, grid, 128, seed=47)
+    for scale, fallback in [(2.0 ** -30, 5), (2.0 ** -90, 3)]:
+        o6, l6 = vd.attn_na3d_fwd(q, k, v, grid, kernel, scale=scale, brick=3, pair_axis=6)
+        of, lf = vd.attn_na3d_fwd(q, k, v, grid, kernel, scale=scale, brick=3, pair_axis=fallback)
+        torch.cuda.synchronize()
+        assert torch.equal(o6, of) and torch.equal(l6, lf), scale
+        ro, rl = oracle.na3d_attention(host(q), host(k), host(v), grid, kernel, scale)
+        assert_close(host(o6), ro, f"na3d plan 6 scale {scale} out")
+        assert_close(host(l6), rl, f"na3d plan 6 scale {scale} lse")
+
+
+def test_na3d_e5m2_window_output_16_byte_aligned():
+    # plan 6 through the 16-byte store path: the same bits as through the 32-byte one
+    grid, kernel, H, d = (3, 13, 21), (3, 5, 7), 2, 128
+    S = int(np.prod(grid))
+    q, k, v = na_inputs(1, H, grid, d, seed=17)
+    buf = torch.empty(H * S * d + 8, dtype=torch.bfloat16, device="cuda")
+    out = buf[8:].view(1, H, S, d)
+    assert out.data_ptr() % 32 == 16
+    vd.attn_na3d_fwd(q, k, v, grid, kernel, brick=3, pair_axis=6, out=out)
+    o6, _ = vd.attn_na3d_fwd(q, k, v, grid, kernel, brick=3, pair_axis=6)
+    torch.cuda.synchronize()
+    assert torch.equal(out, o6)

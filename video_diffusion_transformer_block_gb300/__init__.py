@@ -152,7 +152,9 @@ def attn_na3d_fwd(q, k, v, grid, kernel, scale=None, brick=0, pair_axis=-1, out=
     returns (out bf16 [B,H,S,d], lse fp32 [B,H,S]).  brick / pair_axis: 0 / -1 let
     the library choose the tile plan (attn_na3d_plan); pair_axis 4 is the
     persistent one-brick plan, 5 the same with 4x2x16 key boxes (4x4x8 brick
-    only), 3 one brick per CTA, 0-2 two neighbouring bricks per CTA."""
+    only), 6 plan 5 with E5M2 window operands (never chosen by the library:
+    exact for raw scores |q.k| < 2^30, and run as plan 5 when scale * log2(e)
+    < 2^-22), 3 one brick per CTA, 0-2 two neighbouring bricks per CTA."""
     lib = load_library()
     B, H, S, d = _bhsd(q, "q")
     if _bhsd(k, "k") != q.shape or _bhsd(v, "v") != q.shape:

@@ -150,12 +150,13 @@ int na_start(int p, int K, int L) {
 }
 int na_mode_of(int brick) { return brick == 1 ? kModeNA1x8x16 : brick == 2 ? kModeNA2x8x8 : kModeNA4x4x8; }
 
-// The key boxes of a plan: the brick's own shape, or (plan 5) the wide boxes.
-int na_keys_of(int pair) { return pair == 5 ? kNAKeysWide : kNAKeysBrick; }
+// The key boxes of a plan: the brick's own shape, or the wide boxes (plan 5;
+// plan 6 with E5M2 window operands).
+int na_keys_of(int pair) { return pair == 5 ? kNAKeysWide : pair == 6 ? kNAKeysWideF8 : kNAKeysBrick; }
 
 // Key boxes a (brick, pair axis) plan makes the CTAs multiply, summed over
 // every query tile of one head, and the number of CTAs per head (for the
-// persistent plans 4 and 5, of bricks).  The count separates over the axes:
+// persistent plans 4, 5 and 6, of bricks).  The count separates over the axes:
 // along a non-pair axis a tile's boxes depend only on its own coordinate,
 // along the pair axis on the pair it belongs to.
 void na_plan_cost(const int L[3], const int K[3], int brick, int pair, long long* boxes, long long* ctas) {
@@ -168,7 +169,7 @@ void na_plan_cost(const int L[3], const int K[3], int brick, int pair, long long
     auto lo_of = [&](int i) { return na_start(i * B[a], K[a], L[a]); };
     auto hi_of = [&](int i) { return na_start((i + 1) * B[a] < L[a] ? (i + 1) * B[a] - 1 : L[a] - 1, K[a], L[a]) + K[a]; };
     long long sum = 0;
-    if (a != pair) {   // (pairs 3, 4, 5: no axis is paired)
+    if (a != pair) {   // (pairs 3 to 6: no axis is paired)
       for (int i = 0; i < nq; ++i) sum += (hi_of(i) - lo_of(i) + KB[a] - 1) / KB[a];
       n *= nq;
     } else {
@@ -193,10 +194,12 @@ void na_plan_cost(const int L[3], const int K[3], int brick, int pair, long long
 // (plan 4 with the 4x4x8 brick), 23 where it is 32 (a wider MMA step and, at
 // d = 128, one window buffer instead of two), plus 34 per brick (its epilogue);
 // for the other plans 20 per box plus 40 per CTA (a CTA's fixed cost counted as
-// two boxes).  The weights are fits to GB300 timings.  Plan 5 exists for the
-// 4x4x8 brick only: asked for with another brick, it is refused (false).
+// two boxes).  The weights are fits to GB300 timings.  Plans 5 and 6 exist for
+// the 4x4x8 brick only: asked for with another brick, they are refused (false).
+// Plan 6 (plan 5's boxes with E5M2 window operands: two window buffers per
+// tile, exact for raw scores |q.k| < 2^30) is taken only when asked for.
 bool na_choose(const int L[3], const int K[3], int* brick, int* pair, long long* boxes) {
-  if (*pair == 5 && *brick != 0 && *brick != 3) return false;
+  if ((*pair == 5 || *pair == 6) && *brick != 0 && *brick != 3) return false;
   long long best = -1;
   int bb = 1, bp = *pair;
   long long bboxes = 0;
@@ -205,7 +208,7 @@ bool na_choose(const int L[3], const int K[3], int* brick, int* pair, long long*
     // the caller's pair axis, or (left open) the persistent plans 4 and 5
     const int first = *pair >= 0 ? *pair : 4, last = *pair >= 0 ? *pair : 5;
     for (int cand = first; cand <= last; ++cand) {
-      if (cand == 5 && b != 3) continue;
+      if (cand >= 5 && b != 3) continue;
       long long nbox, ncta;
       na_plan_cost(L, K, b, cand, &nbox, &ncta);
       const bool wide_step = cand == 5 || (cand == 4 && b != 3);
@@ -346,7 +349,7 @@ attn_status_t attn_dense_fwd(const attn_bf16* q, const attn_bf16* k, const attn_
 attn_status_t attn_na3d_plan(int T, int Y, int X, int Kt, int Ky, int Kx, int* brick, int* pair_axis,
                              long long* key_boxes) {
   if (!brick || !pair_axis || !na_args_ok(1, 1, T, Y, X, Kt, Ky, Kx)) return ATTN_ERR_INVALID_ARG;
-  if (*brick < 0 || *brick > 3 || *pair_axis < -1 || *pair_axis > 5) return ATTN_ERR_INVALID_ARG;
+  if (*brick < 0 || *brick > 3 || *pair_axis < -1 || *pair_axis > 6) return ATTN_ERR_INVALID_ARG;
   const int L[3] = {T, Y, X}, K[3] = {Kt, Ky, Kx};
   long long boxes = 0;
   if (!na_choose(L, K, brick, pair_axis, &boxes)) return ATTN_ERR_INVALID_ARG;
@@ -362,7 +365,7 @@ attn_status_t attn_na3d_fwd(const attn_bf16* q, const attn_bf16* k, const attn_b
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || (lse && ((uintptr_t)lse & 3u)))
     return ATTN_ERR_INVALID_ARG;
   if (!na_args_ok(B, H, T, Y, X, Kt, Ky, Kx) || !(isfinite(scale) && scale > 0.f)) return ATTN_ERR_INVALID_ARG;
-  if (brick < 0 || brick > 3 || pair_axis < -1 || pair_axis > 5) return ATTN_ERR_INVALID_ARG;
+  if (brick < 0 || brick > 3 || pair_axis < -1 || pair_axis > 6) return ATTN_ERR_INVALID_ARG;
   if (!valid_d(d)) return ATTN_ERR_UNSUPPORTED;
   const int L[3] = {T, Y, X}, K[3] = {Kt, Ky, Kx};
   long long boxes = 0;
@@ -371,7 +374,10 @@ attn_status_t attn_na3d_fwd(const attn_bf16* q, const attn_bf16* k, const attn_b
   // outside it), which an exponent turns into an exact 0 only for scale * log2(e)
   // >= 2^-80; below that the one-brick CTAs (the window applied as -inf by the
   // softmax threads) give the same results as plan 4 (the same boxes and
-  // arithmetic) and plan 5's results up to rounding (other key boxes)
+  // arithmetic) and plan 5's results up to rounding (other key boxes).  Plan 6's
+  // E5M2 window (-49 * 2^26 outside) needs scale * log2(e) >= 2^-22; below that
+  // plan 5 gives its results.
+  if (pair_axis == 6 && !(scale * 1.4426950408889634f >= 0x1p-22f)) pair_axis = 5;
   if (pair_axis >= 4 && !(scale * 1.4426950408889634f >= 0x1p-80f)) pair_axis = 3;
   const int mode = na_mode_of(brick), keys = na_keys_of(pair_axis);
   const int Bv[3] = {na_brick_t(mode), na_brick_y(mode), na_brick_x(mode)};

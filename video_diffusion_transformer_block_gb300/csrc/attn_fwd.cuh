@@ -66,11 +66,21 @@ __host__ __device__ constexpr int na_brick_y(int m) { return m == kModeNA4x4x8 ?
 __host__ __device__ constexpr int na_brick_x(int m) { return m == kModeNA1x8x16 ? 16 : 8; }
 // Key boxes of the persistent neighbourhood kernel: kNAKeysBrick takes the
 // brick's own shape, kNAKeysWide 4 x 2 x 16 (which covers the window union of a
-// 4 x 4 x 8 brick under small windows with fewer boxes).
-constexpr int kNAKeysBrick = 0, kNAKeysWide = 1;
-__host__ __device__ constexpr int na_keys_t(int m, int keys) { return keys == kNAKeysWide ? 4 : na_brick_t(m); }
-__host__ __device__ constexpr int na_keys_y(int m, int keys) { return keys == kNAKeysWide ? 2 : na_brick_y(m); }
-__host__ __device__ constexpr int na_keys_x(int m, int keys) { return keys == kNAKeysWide ? 16 : na_brick_x(m); }
+// 4 x 4 x 8 brick under small windows with fewer boxes); kNAKeysWideF8 the same
+// boxes with the window operand in E5M2 instead of bf16 (half the bytes, so two
+// window buffers per tile fit at d = 128; exact for a narrower score range).
+constexpr int kNAKeysBrick = 0, kNAKeysWide = 1, kNAKeysWideF8 = 2;
+__host__ __device__ constexpr int na_keys_t(int m, int keys) { return keys != kNAKeysBrick ? 4 : na_brick_t(m); }
+__host__ __device__ constexpr int na_keys_y(int m, int keys) { return keys != kNAKeysBrick ? 2 : na_brick_y(m); }
+__host__ __device__ constexpr int na_keys_x(int m, int keys) { return keys != kNAKeysBrick ? 16 : na_brick_x(m); }
+// How a key tile's scores mark keys outside the row's window: not at all (the
+// caller masks them), or by a bias the tensor core added (NABiasLayout): -2^120
+// per missed coordinate with a bf16 window operand, -57344^2 = -49 * 2^26 with an
+// E5M2 one.  kWinMaskBelow: a tile maximum below it means no key of the tile is
+// in the window (with |raw score| < 2^96, resp. 2^30, every biased score lies
+// below it and every other above).
+constexpr int kWinNone = 0, kWinBf16 = 1, kWinF8 = 2;
+__host__ __device__ constexpr float win_mask_below(int win) { return win == kWinF8 ? -0x1p31f : -0x1p119f; }
 
 constexpr float kRescaleLog2 = 8.0f;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -444,11 +454,12 @@ __device__ __forceinline__ void na_mask_scores(float (&x)[BK], const int (&ws)[3
 // BK/2 columns of S at tS and adds its row sum to l_run.  Returns after the
 // TMEM stores have completed; the caller fences and signals P ready.
 //
-// kBiasMasked: keys outside the row's window carry a score of -2^120 or less
-// instead of -inf (the window added by the tensor core, see NABiasMMA); a
-// maximum below -2^119 means no key of the tile is in the window and counts as
-// -inf, so such a tile moves nothing, as a tile of -inf scores would.
-template <int BK, int D, bool kBiasMasked = false>
+// kWin (kWinBf16, kWinF8): keys outside the row's window carry a large
+// negative bias instead of -inf (the window added by the tensor core, see
+// NABiasLayout); a maximum below win_mask_below(kWin) means no key of the tile
+// is in the window and counts as -inf, so such a tile moves nothing, as a tile
+// of -inf scores would.
+template <int BK, int D, int kWin = kWinNone>
 __device__ __forceinline__ void softmax_step(float (&x)[BK], float scale_log2, float& m_run, float& l_run, bool o_live,
                                              uint32_t tS, uint32_t tO) {
   // row max: two chains of three-input maxima (max is exact, so the order is free)
@@ -459,7 +470,7 @@ __device__ __forceinline__ void softmax_step(float (&x)[BK], float scale_log2, f
     mx1 = fmax3(mx1, x[c + 2], x[c + 3]);
   }
   float raw = fmaxf(mx0, mx1);
-  if constexpr (kBiasMasked) raw = raw < -0x1p119f ? -INFINITY : raw;
+  if constexpr (kWin != kWinNone) raw = raw < win_mask_below(kWin) ? -INFINITY : raw;
   const float mt = raw * scale_log2;
   // lazy rescale of the running max
   float alpha = 1.f;
@@ -520,7 +531,7 @@ __device__ __forceinline__ void softmax_step(float (&x)[BK], float scale_log2, f
 // fused multiply-adds in the same order and the same row-sum chains as
 // softmax_step, so the same bits, with 64 score registers live instead of BK.
 // `between()` runs while the first loads are in flight.
-template <int BK, int D, bool kBiasMasked, class Between>
+template <int BK, int D, int kWin, class Between>
 __device__ __forceinline__ void softmax_step_tmem(uint32_t tS, float scale_log2, float& m_run, float& l_run,
                                                   bool o_live, uint32_t tO, Between&& between) {
   static_assert(BK % 64 == 0, "key tile");
@@ -551,7 +562,7 @@ __device__ __forceinline__ void softmax_step_tmem(uint32_t tS, float scale_log2,
     }
   }
   float raw = fmaxf(mx0, mx1);
-  if constexpr (kBiasMasked) raw = raw < -0x1p119f ? -INFINITY : raw;
+  if constexpr (kWin != kWinNone) raw = raw < win_mask_below(kWin) ? -INFINITY : raw;
   const float mt = raw * scale_log2;
   float alpha = 1.f;
   bool need = mt > m_run + kRescaleLog2 || (m_run == -INFINITY && mt > -INFINITY);

@@ -25,6 +25,9 @@ cudaError_t launch_na_persist_d128(int mode, int keys, const CUtensorMap& tq, co
   if (keys == kNAKeysWide)
     return mode == kModeNA4x4x8 ? launch_na_persist_cfg<128, kModeNA4x4x8, kNAKeysWide>(tq, tk, tv, p, stream)
                                 : cudaErrorInvalidValue;
+  if (keys == kNAKeysWideF8)
+    return mode == kModeNA4x4x8 ? launch_na_persist_cfg<128, kModeNA4x4x8, kNAKeysWideF8>(tq, tk, tv, p, stream)
+                                : cudaErrorInvalidValue;
   if (mode == kModeNA1x8x16) return launch_na_persist_cfg<128, kModeNA1x8x16, kNAKeysBrick>(tq, tk, tv, p, stream);
   if (mode == kModeNA2x8x8) return launch_na_persist_cfg<128, kModeNA2x8x8, kNAKeysBrick>(tq, tk, tv, p, stream);
   if (mode == kModeNA4x4x8) return launch_na_persist_cfg<128, kModeNA4x4x8, kNAKeysBrick>(tq, tk, tv, p, stream);

@@ -53,10 +53,11 @@ cudaError_t launch_attn_fwd_d128(int BK, int mode, const CUtensorMap& tq, const 
                                  const FwdParams& p, cudaStream_t stream);
 
 // The persistent neighbourhood kernel (na_persist.cuh), mode kModeNA* (the
-// query brick) and keys kNAKeysBrick / kNAKeysWide (the key box; the wide boxes
-// with the 4 x 4 x 8 brick only): tq, tk, tv are 5-D maps (channels, x, y, t,
-// head) of q, k, v with a box of 64 channels and the brick's (tq) or the key
-// box's (tk, tv) shape; the grid is one CTA per SM at most.
+// query brick) and keys kNAKeysBrick / kNAKeysWide / kNAKeysWideF8 (the key
+// box and the window operands' type; the wide boxes with the 4 x 4 x 8 brick
+// only): tq, tk, tv are 5-D maps (channels, x, y, t, head) of q, k, v with a
+// box of 64 channels and the brick's (tq) or the key box's (tk, tv) shape; the
+// grid is one CTA per SM at most.
 cudaError_t launch_na_persist_d64(int mode, int keys, const CUtensorMap& tq, const CUtensorMap& tk,
                                   const CUtensorMap& tv, const FwdParams& p, cudaStream_t stream);
 cudaError_t launch_na_persist_d128(int mode, int keys, const CUtensorMap& tq, const CUtensorMap& tk,

@@ -26,11 +26,13 @@
 // neighbourhood modes; the key boxes tile the union of the brick's windows
 // from its corner, in the brick's own shape (KEYS = kNAKeysBrick: the boxes of
 // that kernel's one-brick walk) or as 4 x 2 x 16 boxes (kNAKeysWide, fewer
-// boxes per 4 x 4 x 8 brick under small windows).  The window, added by the
+// boxes per 4 x 4 x 8 brick under small windows; kNAKeysWideF8: the same boxes
+// with E5M2 window operands, see NABiasLayout).  The window, added by the
 // tensor core instead of masked by the softmax threads, leaves every
 // in-window score unchanged, so with the brick-shaped boxes results are
 // bit-identical to that kernel's one-brick plan (with the wide boxes, equal
-// up to the rounding of another key order).
+// up to the rounding of another key order; the two encodings of the wide
+// boxes' window give the same bits wherever both are exact).
 #pragma once
 #include "attn_fwd.cuh"
 
@@ -107,29 +109,39 @@ struct NABrickStream {
 // within the box) is in the row's window when each coordinate lies in the
 // window's range on its axis.  One extra K-step of the score MMA contracts
 //   A = Qm [128 rows][KB]: per row and per axis coordinate, 0 when the
-//       coordinate is in the row's window, else -2^120 (written per box), with
+//       coordinate is in the row's window, else -b (written per box), with
 //   B = Km [128 keys][KB]: per key, a one-hot of each of its coordinates
-//       (constant);
+//       (value c, constant);
 // so a key in the window gets x + 0 = x (its score unchanged, bit for bit)
-// and a key outside gets -2^120 or less, which the softmax's exponent turns
-// into an exact 0 whenever scale * log2(e) >= 2^-80 (|x| < 2^96 leaves
-// x - 2^120 = -2^120).  Frame one-hots are only needed when the brick or the
-// key box has several frames (a one-frame brick's one-frame boxes all lie in
-// its frame window).  KT x KY x KX: the key box; kFrames: frame one-hots kept.
-template <int KT, int KY, int KX, bool kFrames>
+// and a key outside gets x - b c or less.  bf16 operands: b = 2^120, c = 1,
+// which the softmax's exponent turns into an exact 0 whenever scale * log2(e)
+// >= 2^-80 (|x| < 2^96 leaves x - 2^120 = -2^120).  E5M2 operands (F8): b = c =
+// 57344 (the largest finite E5M2 value), b c = 49 * 2^26 exactly in fp32, so
+// with |x| < 2^30 a key outside scores below -2^31 and its exponent is an exact
+// 0 whenever scale * log2(e) >= 2^-22; one f8f6f4 MMA of K = 32 takes the
+// window (two bf16 ones), in half the shared memory.  Frame one-hots are only
+// needed when the brick or the key box has several frames (a one-frame
+// brick's one-frame boxes all lie in its frame window).  KT x KY x KX: the key
+// box; kFrames: frame one-hots kept.
+template <int KT, int KY, int KX, bool kFrames, bool F8 = false>
 struct NABiasLayout {
   static constexpr int kT0 = 0;                        // first frame column
   static constexpr int kY0 = kFrames ? KT : 0;         // first row column
   static constexpr int kX0 = kY0 + KY;                 // first column column
   static constexpr int kUsed = kX0 + KX;
-  static constexpr int kCols = (kUsed + 15) / 16 * 16;   // K of the bias step (16 or 32)
-  static constexpr int kBytes = 128 * kCols * 2;         // one operand (128 rows)
-  // no-swizzle K-major layout: 8 x 8 core matrices (128 bytes each); the
-  // kCols / 8 core matrices of an 8-row group are adjacent
+  static constexpr int kElem = F8 ? 1 : 2;             // bytes per element
+  static constexpr int kKStep = F8 ? 32 : 16;          // K of one MMA
+  static constexpr int kCols = (kUsed + kKStep - 1) / kKStep * kKStep;   // K of the bias step
+  static constexpr int kBytes = 128 * kCols * kElem;   // one operand (128 rows)
+  // no-swizzle K-major layout: core matrices of 8 rows x 16 bytes (128 bytes
+  // each, kCore elements per row); the kCols / kCore core matrices of an
+  // 8-row group are adjacent; one MMA step spans two of them (256 bytes)
+  static constexpr int kCore = 16 / kElem;
   static constexpr uint32_t kLBO = 128;
-  static constexpr uint32_t kSBO = kCols / 8 * 128;
+  static constexpr uint32_t kSBO = kCols / kCore * 128;
+  static constexpr uint32_t kStepBytes = kKStep / kCore * 128;
   __device__ __forceinline__ static uint32_t offset(int row, int col) {
-    return (uint32_t)(((row >> 3) * (kCols / 8) + (col >> 3)) * 128 + (row & 7) * 16 + (col & 7) * 2);
+    return (uint32_t)(((row >> 3) * (kCols / kCore) + col / kCore) * 128 + (row & 7) * 16 + (col % kCore) * kElem);
   }
 };
 
@@ -139,7 +151,9 @@ struct NAPersistCfg {
   static constexpr int KT = na_keys_t(MODE, KEYS), KY = na_keys_y(MODE, KEYS), KX = na_keys_x(MODE, KEYS);
   static constexpr int BK = 128;
   static constexpr bool kFrames = BT > 1 || KT > 1;
-  using Bias = NABiasLayout<KT, KY, KX, kFrames>;
+  static constexpr bool kF8 = KEYS == kNAKeysWideF8;   // E5M2 window operands
+  using Bias = NABiasLayout<KT, KY, KX, kFrames, kF8>;
+  static constexpr int kWin = kF8 ? kWinF8 : kWinBf16;
   // two softmax warpgroups (one per tile) + one control warpgroup: warps 8, 9
   // are tile 0's producer and issuer, 10, 11 tile 1's
   static constexpr int kThreads = 384;
@@ -162,27 +176,34 @@ struct NAPersistCfg {
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kIdescS = idesc_bf16_f32(128, BK, 0, 0);
   static constexpr uint32_t kIdescPV = idesc_bf16_f32(128, D, 0, 1);
+  static constexpr uint32_t kIdescWin = kF8 ? idesc_e5m2_f32(128, BK) : kIdescS;
   static_assert(D == 64 || D == 128, "head dim");
+  static_assert(!kF8 || MODE == kModeNA4x4x8, "E5M2 window operands with the wide key boxes only");
   static_assert(is_na_mode(MODE) && BT * BY * BX == 128 && KT * KY * KX == BK, "neighbourhood bricks and key boxes");
   static_assert(kSmemRaw <= 227 * 1024, "shared memory");
 };
 
-// bf16 bit patterns
+// bf16 and E5M2 bit patterns
 constexpr uint16_t kBf16One = 0x3F80;        // 1.0
 constexpr uint16_t kBf16MaskBias = 0xFB80;   // -2^120
+constexpr uint8_t kE5M2Big = 0x7B;           // 57344
+constexpr uint8_t kE5M2MaskBias = 0xFB;      // -57344
 
 // Row `row` of the window operand for one key box (KT x KY x KX, layout L):
 // per axis, 0 for the box coordinates inside the window (rel_ws: the window
-// start minus the box origin, extent K), -2^120 for the others; unused
-// columns 0.
+// start minus the box origin, extent K), -b for the others (-2^120 in bf16,
+// -57344 in E5M2); unused columns 0.
 template <class L, int KT, int KY, int KX>
 __device__ __forceinline__ void write_window_row(uint8_t* qm, int row, const int (&rel_ws)[3], const int (&K)[3]) {
-  uint32_t w[L::kCols / 2];
+  constexpr int kWords = L::kCols * L::kElem / 4;
+  uint32_t w[kWords];
 #pragma unroll
-  for (int i = 0; i < L::kCols / 2; ++i) w[i] = 0;
+  for (int i = 0; i < kWords; ++i) w[i] = 0;
   auto put = [&](int col, bool in) {
-    const uint32_t v = in ? 0u : (uint32_t)kBf16MaskBias;
-    w[col >> 1] |= v << ((col & 1) * 16);
+    if constexpr (L::kElem == 1)
+      w[col >> 2] |= (in ? 0u : (uint32_t)kE5M2MaskBias) << ((col & 3) * 8);
+    else
+      w[col >> 1] |= (in ? 0u : (uint32_t)kBf16MaskBias) << ((col & 1) * 16);
   };
   if constexpr (L::kY0 > 0) {
 #pragma unroll
@@ -193,9 +214,9 @@ __device__ __forceinline__ void write_window_row(uint8_t* qm, int row, const int
 #pragma unroll
   for (int c = 0; c < KX; ++c) put(L::kX0 + c, c >= rel_ws[2] && c < rel_ws[2] + K[2]);
 #pragma unroll
-  for (int c8 = 0; c8 < L::kCols / 8; ++c8)
-    *reinterpret_cast<uint4*>(qm + L::offset(row, 8 * c8)) =
-        make_uint4(w[4 * c8], w[4 * c8 + 1], w[4 * c8 + 2], w[4 * c8 + 3]);
+  for (int c = 0; c < L::kCols; c += L::kCore)   // one core-matrix row (16 bytes) at a time
+    *reinterpret_cast<uint4*>(qm + L::offset(row, c)) =
+        make_uint4(w[c / L::kCore * 4], w[c / L::kCore * 4 + 1], w[c / L::kCore * 4 + 2], w[c / L::kCore * 4 + 3]);
 }
 
 template <int D, int MODE, int KEYS>
@@ -237,18 +258,25 @@ __global__ void __launch_bounds__(384, 1)
   }
   if (tid < 128) {
     // key tid of a box: frame, row, column one-hots
-    uint32_t w[Bias::kCols / 2];
+    constexpr int kWords = Bias::kCols * Bias::kElem / 4;
+    uint32_t w[kWords];
 #pragma unroll
-    for (int i = 0; i < Bias::kCols / 2; ++i) w[i] = 0;
+    for (int i = 0; i < kWords; ++i) w[i] = 0;
     const int tk = tid / (Cfg::KY * Cfg::KX), yk = (tid / Cfg::KX) % Cfg::KY, xk = tid % Cfg::KX;
     const int cols[3] = {Cfg::kFrames ? Bias::kT0 + tk : -1, Bias::kY0 + yk, Bias::kX0 + xk};
 #pragma unroll
     for (int a = 0; a < 3; ++a)
-      if (cols[a] >= 0) w[cols[a] >> 1] |= (uint32_t)kBf16One << ((cols[a] & 1) * 16);
+      if (cols[a] >= 0) {
+        if constexpr (Bias::kElem == 1)
+          w[cols[a] >> 2] |= (uint32_t)kE5M2Big << ((cols[a] & 3) * 8);
+        else
+          w[cols[a] >> 1] |= (uint32_t)kBf16One << ((cols[a] & 1) * 16);
+      }
 #pragma unroll
-    for (int c8 = 0; c8 < Bias::kCols / 8; ++c8)
-      *reinterpret_cast<uint4*>(sKm + Bias::offset(tid, 8 * c8)) =
-          make_uint4(w[4 * c8], w[4 * c8 + 1], w[4 * c8 + 2], w[4 * c8 + 3]);
+    for (int c = 0; c < Bias::kCols; c += Bias::kCore)
+      *reinterpret_cast<uint4*>(sKm + Bias::offset(tid, c)) =
+          make_uint4(w[c / Bias::kCore * 4], w[c / Bias::kCore * 4 + 1], w[c / Bias::kCore * 4 + 2],
+                     w[c / Bias::kCore * 4 + 3]);
     // the tensor core reads these through the async proxy
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
@@ -338,13 +366,16 @@ __global__ void __launch_bounds__(384, 1)
                 uint64_t bdesc = smem_desc_sw128(k_addr + (kk / 4) * (BK * 128) + (kk % 4) * 32, 16, 1024);
                 mma_ss(s_tmem, adesc, bdesc, Cfg::kIdescS, kk > 0 ? 1u : 0u);
               }
-              // the window: x + 0 inside, -2^120 outside
+              // the window: x + 0 inside, x - b c or less outside
 #pragma unroll
-              for (int kb = 0; kb < Bias::kCols / 16; ++kb) {
-                uint64_t adesc = smem_desc_noswz(qm_base + (g % Cfg::kQmBufs) * Bias::kBytes + kb * 256, Bias::kLBO,
-                                                 Bias::kSBO);
-                uint64_t bdesc = smem_desc_noswz(km_addr + kb * 256, Bias::kLBO, Bias::kSBO);
-                mma_ss(s_tmem, adesc, bdesc, Cfg::kIdescS, 1u);
+              for (int kb = 0; kb < Bias::kCols / Bias::kKStep; ++kb) {
+                uint64_t adesc = smem_desc_noswz(qm_base + (g % Cfg::kQmBufs) * Bias::kBytes + kb * Bias::kStepBytes,
+                                                 Bias::kLBO, Bias::kSBO);
+                uint64_t bdesc = smem_desc_noswz(km_addr + kb * Bias::kStepBytes, Bias::kLBO, Bias::kSBO);
+                if constexpr (Cfg::kF8)
+                  mma_ss_f8(s_tmem, adesc, bdesc, Cfg::kIdescWin, 1u);
+                else
+                  mma_ss(s_tmem, adesc, bdesc, Cfg::kIdescWin, 1u);
               }
             }
             if (locked) issue_unlock(&mma_lock);
@@ -442,7 +473,7 @@ __global__ void __launch_bounds__(384, 1)
         // O holds earlier boxes of this brick unless this box starts it.  One
         // buffer: the next element's window rows now that S is done, while the
         // first score loads are in flight
-        softmax_step_tmem<BK, D, true>(tS, p.scale_log2, m_run, l_run, !cur_starts, tO, [&]() {
+        softmax_step_tmem<BK, D, Cfg::kWin>(tS, p.scale_log2, m_run, l_run, !cur_starts, tO, [&]() {
           if constexpr (Cfg::kQmBufs == 1) have = look_ahead(next_starts);
         });
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
