@@ -426,6 +426,67 @@ __global__ void __launch_bounds__(384, 1)
         if (row_valid && p.lse != nullptr && ATTN_CHECKED(orow, 1, (long long)p.BH * p.Sq, p.status))
           p.lse[orow] = empty ? -INFINITY : (m_run + __log2f(l_run)) * kLn2;
       };
+      // A finished brick whose successor starts in the same stream: its rows
+      // leave TMEM as soon as the successor's first scores are ready (O is
+      // final then, and the successor's first PV, which overwrites it, waits
+      // for this tile's P).  The last 64 columns reach global memory only after
+      // that P is released, while the tensor core runs the next batch (32
+      // packed bf16 pairs per thread in between; holding all of d = 128 made
+      // the softmax spill); the columns before them are stored at once.  The
+      // same values as store_brick.
+      constexpr int kDeferCols = 64;
+      uint32_t pko[kDeferCols / 2];
+      long long pend_row = -1;
+      float pend_lse = 0.f;
+      auto put_cols = [&](uint16_t* dst, long long off, const uint32_t* pk, int ncols) {
+        [[maybe_unused]] const long long total = (long long)p.BH * p.Sq * D;
+        if (out_wide) {
+#pragma unroll
+          for (int c = 0; c < 64; c += 16)
+            if (c < ncols && ATTN_CHECKED(off + c, 16, total, p.status))
+              asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst + c), "r"(pk[c / 2]),
+                           "r"(pk[c / 2 + 1]), "r"(pk[c / 2 + 2]), "r"(pk[c / 2 + 3]), "r"(pk[c / 2 + 4]),
+                           "r"(pk[c / 2 + 5]), "r"(pk[c / 2 + 6]), "r"(pk[c / 2 + 7])
+                           : "memory");
+        } else {
+#pragma unroll
+          for (int c = 0; c < 64; c += 8)
+            if (c < ncols && ATTN_CHECKED(off + c, 8, total, p.status))
+              *reinterpret_cast<uint4*>(dst + c) = make_uint4(pk[c / 2], pk[c / 2 + 1], pk[c / 2 + 2], pk[c / 2 + 3]);
+        }
+      };
+      auto read_brick = [&]() {
+        const bool empty = !(l_run > 0.f);
+        const float inv = empty ? 0.f : 1.f / l_run;
+        pend_lse = empty ? -INFINITY : (m_run + __log2f(l_run)) * kLn2;
+        pend_row = orow;
+#pragma unroll
+        for (int c0 = 0; c0 < D; c0 += 64) {
+          uint32_t rr[2][32];
+          tmem_ld32(tO + c0, rr[0]);
+          tmem_ld32(tO + c0 + 32, rr[1]);
+          tmem_ld_wait();
+          uint32_t pk[32];
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            tmem_reg_fence(rr[h]);
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+              pk[16 * h + j] = pack_bf16x2(__uint_as_float(rr[h][2 * j]) * inv, __uint_as_float(rr[h][2 * j + 1]) * inv);
+          }
+          if (c0 + 64 < D) {
+            if (pend_row >= 0) put_cols(p.out + pend_row * D + c0, pend_row * D + c0, pk, 64);
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) pko[j] = pk[j];
+          }
+        }
+      };
+      auto write_brick = [&]() {
+        if (pend_row < 0) return;
+        put_cols(p.out + pend_row * D + (D - kDeferCols), pend_row * D + (D - kDeferCols), pko, kDeferCols);
+        if (p.lse != nullptr && ATTN_CHECKED(pend_row, 1, (long long)p.BH * p.Sq, p.status)) p.lse[pend_row] = pend_lse;
+      };
       // Looks at the next element of the stream and writes this row of its
       // window operand (into a buffer the scores in flight do not read).
       auto look_ahead = [&](bool& starts) -> bool {
@@ -463,9 +524,10 @@ __global__ void __launch_bounds__(384, 1)
         }
         ++it;
         tc_fence_after();
+        const bool pend = cur_starts && it > 1;
         if (cur_starts) {
-          // this batch held the previous brick's last PV: store its rows before O is reused
-          if (it > 1) store_brick();
+          // this batch held the previous brick's last PV: its rows leave TMEM before O is reused
+          if (pend) read_brick();
           orow = starts_orow;
           m_run = -INFINITY;
           l_run = 0.f;
@@ -479,6 +541,7 @@ __global__ void __launch_bounds__(384, 1)
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         tc_fence_before();
         mbar_arrive(&bar_p[t]);
+        if (pend) write_brick();
         cur_starts = next_starts;
       }
       // the last batch (the last brick's last PV alone); lane 0's view of the flag decides for the warp
