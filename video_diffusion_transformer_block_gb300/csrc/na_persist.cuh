@@ -19,8 +19,10 @@
 //     overwrites O;
 //   - the tile's softmax warpgroup writes the window rows of element g+1
 //     while S(g) is computed, and on the batch that starts a brick first
-//     stores the previous brick's rows (that batch held its last PV), then
-//     runs the softmax of the new brick's first scores.
+//     reads the previous brick's O out of TMEM (that batch held its last PV)
+//     and stores all but its last 64 columns, then runs the softmax of the
+//     new brick's first scores, and stores those 64 columns once it has
+//     released P.
 // So one tile's epilogue and Q load overlap the other tile's MMAs.  The
 // online softmax and normalisation are those of attn_fwd_kernel's
 // neighbourhood modes; the key boxes tile the union of the brick's windows
