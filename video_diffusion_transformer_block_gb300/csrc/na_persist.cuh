@@ -124,21 +124,26 @@ struct NABrickStream {
 // window (two bf16 ones), in half the shared memory.  Frame one-hots are only
 // needed when the brick or the key box has several frames (a one-frame
 // brick's one-frame boxes all lie in its frame window).  KT x KY x KX: the key
-// box; kFrames: frame one-hots kept.
+// box; kFrames: frame one-hots kept.  With E5M2 operands the column
+// one-hots start on a 16-byte chunk of their own, so a row whose column
+// window did not move between two boxes keeps that chunk (write_window_row;
+// measured faster there, slower with the bf16 brick-shaped boxes).
 template <int KT, int KY, int KX, bool kFrames, bool F8 = false>
 struct NABiasLayout {
-  static constexpr int kT0 = 0;                        // first frame column
-  static constexpr int kY0 = kFrames ? KT : 0;         // first row column
-  static constexpr int kX0 = kY0 + KY;                 // first column column
-  static constexpr int kUsed = kX0 + KX;
   static constexpr int kElem = F8 ? 1 : 2;             // bytes per element
   static constexpr int kKStep = F8 ? 32 : 16;          // K of one MMA
-  static constexpr int kCols = (kUsed + kKStep - 1) / kKStep * kKStep;   // K of the bias step
-  static constexpr int kBytes = 128 * kCols * kElem;   // one operand (128 rows)
   // no-swizzle K-major layout: core matrices of 8 rows x 16 bytes (128 bytes
   // each, kCore elements per row); the kCols / kCore core matrices of an
   // 8-row group are adjacent; one MMA step spans two of them (256 bytes)
   static constexpr int kCore = 16 / kElem;
+  static constexpr int kT0 = 0;                        // first frame column
+  static constexpr int kY0 = kFrames ? KT : 0;         // first row column
+  static constexpr bool kKeepChunks = F8;              // rows rewrite only the chunks that change
+  static constexpr int kX0 = kKeepChunks ? (kY0 + KY + kCore - 1) / kCore * kCore : kY0 + KY;   // first column column
+  static constexpr int kUsed = kX0 + KX;
+  static constexpr int kCols = (kUsed + kKStep - 1) / kKStep * kKStep;   // K of the bias step
+  static constexpr int kBytes = 128 * kCols * kElem;   // one operand (128 rows)
+  static constexpr int kChunks = kCols / kCore;        // 16-byte chunks of a row
   static constexpr uint32_t kLBO = 128;
   static constexpr uint32_t kSBO = kCols / kCore * 128;
   static constexpr uint32_t kStepBytes = kKStep / kCore * 128;
@@ -194,31 +199,54 @@ constexpr uint8_t kE5M2MaskBias = 0xFB;      // -57344
 // Row `row` of the window operand for one key box (KT x KY x KX, layout L):
 // per axis, 0 for the box coordinates inside the window (rel_ws: the window
 // start minus the box origin, extent K), -b for the others (-2^120 in bf16,
-// -57344 in E5M2); unused columns 0.
+// -57344 in E5M2); unused columns 0.  `key` describes what the buffer's row
+// holds (the rel_ws it was written for, 10 bits per axis; kNoWindowRow:
+// nothing yet): with L::kKeepChunks only the 16-byte chunks of axes whose
+// rel_ws changed are written (a brick's boxes mostly move along one axis),
+// else the whole row.  Returns the new key.
+constexpr uint32_t kNoWindowRow = 0xFFFFFFFFu;
 template <class L, int KT, int KY, int KX>
-__device__ __forceinline__ void write_window_row(uint8_t* qm, int row, const int (&rel_ws)[3], const int (&K)[3]) {
-  constexpr int kWords = L::kCols * L::kElem / 4;
-  uint32_t w[kWords];
-#pragma unroll
-  for (int i = 0; i < kWords; ++i) w[i] = 0;
-  auto put = [&](int col, bool in) {
-    if constexpr (L::kElem == 1)
-      w[col >> 2] |= (in ? 0u : (uint32_t)kE5M2MaskBias) << ((col & 3) * 8);
-    else
-      w[col >> 1] |= (in ? 0u : (uint32_t)kBf16MaskBias) << ((col & 1) * 16);
-  };
-  if constexpr (L::kY0 > 0) {
-#pragma unroll
-    for (int c = 0; c < KT; ++c) put(L::kT0 + c, c >= rel_ws[0] && c < rel_ws[0] + K[0]);
+__device__ __forceinline__ uint32_t write_window_row(uint8_t* qm, int row, const int (&rel_ws)[3], const int (&K)[3],
+                                                     uint32_t key) {
+  const uint32_t nkey = ((uint32_t)rel_ws[0] & 0x3FFu) | (((uint32_t)rel_ws[1] & 0x3FFu) << 10) |
+                        (((uint32_t)rel_ws[2] & 0x3FFu) << 20);
+  // the chunks each axis's columns occupy
+  constexpr uint32_t kTMask = L::kY0 > 0 ? ((2u << ((L::kT0 + KT - 1) / L::kCore)) - (1u << (L::kT0 / L::kCore))) : 0u;
+  constexpr uint32_t kYMask = (2u << ((L::kY0 + KY - 1) / L::kCore)) - (1u << (L::kY0 / L::kCore));
+  constexpr uint32_t kXMask = (2u << ((L::kX0 + KX - 1) / L::kCore)) - (1u << (L::kX0 / L::kCore));
+  uint32_t mask = (1u << L::kChunks) - 1u;
+  if (L::kKeepChunks && key != kNoWindowRow) {
+    mask = 0;
+    if (((key ^ nkey) & 0x3FFu) != 0) mask |= kTMask;
+    if (((key ^ nkey) & (0x3FFu << 10)) != 0) mask |= kYMask;
+    if (((key ^ nkey) & (0x3FFu << 20)) != 0) mask |= kXMask;
   }
 #pragma unroll
-  for (int c = 0; c < KY; ++c) put(L::kY0 + c, c >= rel_ws[1] && c < rel_ws[1] + K[1]);
+  for (int ch = 0; ch < L::kChunks; ++ch) {
+    if (!((mask >> ch) & 1u)) continue;
+    uint32_t w[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
-  for (int c = 0; c < KX; ++c) put(L::kX0 + c, c >= rel_ws[2] && c < rel_ws[2] + K[2]);
-#pragma unroll
-  for (int c = 0; c < L::kCols; c += L::kCore)   // one core-matrix row (16 bytes) at a time
-    *reinterpret_cast<uint4*>(qm + L::offset(row, c)) =
-        make_uint4(w[c / L::kCore * 4], w[c / L::kCore * 4 + 1], w[c / L::kCore * 4 + 2], w[c / L::kCore * 4 + 3]);
+    for (int j = 0; j < L::kCore; ++j) {
+      const int col = ch * L::kCore + j;
+      bool used = false, in = true;
+      if (L::kY0 > 0 && col >= L::kT0 && col < L::kT0 + KT) {
+        used = true;
+        in = col - L::kT0 >= rel_ws[0] && col - L::kT0 < rel_ws[0] + K[0];
+      } else if (col >= L::kY0 && col < L::kY0 + KY) {
+        used = true;
+        in = col - L::kY0 >= rel_ws[1] && col - L::kY0 < rel_ws[1] + K[1];
+      } else if (col >= L::kX0 && col < L::kX0 + KX) {
+        used = true;
+        in = col - L::kX0 >= rel_ws[2] && col - L::kX0 < rel_ws[2] + K[2];
+      }
+      if constexpr (L::kElem == 1)
+        w[j >> 2] |= (used && !in ? (uint32_t)kE5M2MaskBias : 0u) << ((j & 3) * 8);
+      else
+        w[j >> 1] |= (used && !in ? (uint32_t)kBf16MaskBias : 0u) << ((j & 1) * 16);
+    }
+    *reinterpret_cast<uint4*>(qm + L::offset(row, ch * L::kCore)) = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+  return nkey;
 }
 
 template <int D, int MODE, int KEYS>
@@ -412,6 +440,8 @@ __global__ void __launch_bounds__(384, 1)
       // window starts at most brick - 1 past the brick's first row's, and a
       // brick is at most 16 wide on every axis)
       uint32_t ws_rel = 0;
+      // what this row of each window buffer holds (write_window_row)
+      uint32_t wkey0 = kNoWindowRow, wkey1 = kNoWindowRow;
       // The finished brick: this row, O / l in bf16, and the lse.  Rows of D bf16
       // start on 32-byte boundaries when the output does: whole 32-byte sectors
       // per lane then (half the store instructions and sector writes).
@@ -506,7 +536,13 @@ __global__ void __launch_bounds__(384, 1)
         }
         const int rel[3] = {(int)(ws_rel & 0xffu) - bi[0] * Cfg::KT, (int)((ws_rel >> 8) & 0xffu) - bi[1] * Cfg::KY,
                             (int)(ws_rel >> 16) - bi[2] * Cfg::KX};
-        write_window_row<Bias, Cfg::KT, Cfg::KY, Cfg::KX>(qm + (la % Cfg::kQmBufs) * Bias::kBytes, r, rel, p.na_K);
+        const bool odd = Cfg::kQmBufs == 2 && (la & 1);
+        const uint32_t nk = write_window_row<Bias, Cfg::KT, Cfg::KY, Cfg::KX>(
+            qm + (la % Cfg::kQmBufs) * Bias::kBytes, r, rel, p.na_K, odd ? wkey1 : wkey0);
+        if (odd)
+          wkey1 = nk;
+        else
+          wkey0 = nk;
         ++la;
         return true;
       };
