@@ -241,6 +241,29 @@ def test_na3d_e5m2_window_large_scores_same_bits():
     np.testing.assert_allclose(host(l6), rl, atol=LSE_ATOL, rtol=0, err_msg="na3d plan 6 large scores lse")
 
 
+def test_na3d_e5m2_window_near_its_range_limit():
+    # raw scores above 1e8, within a factor ~4 of the 2^30 the E5M2 window is exact for, at a
+    # scale above its 2^-22 threshold (so plan 6 itself runs): keys outside a row's window still
+    # get an exact zero weight and every in-window score is unchanged, i.e. plan 5's bits
+    grid, kernel, d = (4, 16, 32), (3, 9, 9), 128
+    q, k, v = na_inputs(1, 2, grid, d, seed=53)
+    q, k = (q.float() * 1500).bfloat16(), (k.float() * 1500).bfloat16()
+    raw = max((q[0, h].float() @ k[0, h].float().T).abs().max().item() for h in range(2))
+    assert 1e8 < raw < 2.0 ** 30, raw
+    scale = 2.0 ** -21
+    assert scale * math.log2(math.e) >= 2.0 ** -22
+    o6, l6 = vd.attn_na3d_fwd(q, k, v, grid, kernel, scale=scale, brick=3, pair_axis=6)
+    o5, l5 = vd.attn_na3d_fwd(q, k, v, grid, kernel, scale=scale, brick=3, pair_axis=5)
+    torch.cuda.synchronize()
+    assert torch.equal(o6, o5) and torch.equal(l6, l5)
+    # peaked softmax: the bf16 bound of the peaked-scores case; the lse within the fp32 accumulation
+    # error of raw scores this large (128 products: ~128 * 2^-24 relative, ~1.2e-3 on logits up to 155)
+    ro, rl = oracle.na3d_attention(host(q), host(k), host(v), grid, kernel, scale)
+    bound = 2.0 ** -8 * (np.abs(ro).max() + np.abs(host(v)).max()) + 1e-3
+    assert np.abs(host(o6) - ro).max() <= bound
+    np.testing.assert_allclose(host(l6), rl, rtol=0, atol=4e-3, err_msg="na3d plan 6 near range lse")
+
+
 def test_na3d_e5m2_window_small_scale_falls_back():
     # below scale * log2(e) = 2^-22 the E5M2 bias no longer zeroes a key's weight for certain:
     # the library runs plan 5 (bf16 window) instead, below 2^-80 the one-brick CTAs
